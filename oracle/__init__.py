@@ -1,0 +1,171 @@
+"""fp64 CPU oracle of the sparse MoE layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  It shares
+no code with the CUDA library and never imports it.
+
+The arithmetic lives in ``moe_oracle.c`` (plain loops, fp64), built with gcc
+into ``oracle/_build/liboracle.so``.  This module only marshals numpy arrays.
+``bruteforce.py`` is a second, independent restatement (per-expert mask loop)
+used to pin the C oracle on tiny inputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+
+# statistics layout (see moe_oracle.c, OST_*)
+ST_AUX_LOSS, ST_AUX_SWITCH, ST_ENTROPY, ST_NONFINITE = 0, 1, 2, 3
+ST_DROPPED, ST_MAX_OVER_MEAN_KEPT, ST_COUNT_CV, ST_MAX_OVER_MEAN_COUNT = 4, 5, 6, 7
+ST_PBAR = 8
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C, OpenMP over independent loops)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("f", ctypes.c_int),
+                ("E", ctypes.c_int), ("k", ctypes.c_int),
+                ("capacity_factor", ctypes.c_double), ("swiglu", ctypes.c_int),
+                ("normalize_gates", ctypes.c_int), ("aux_coef", ctypes.c_double),
+                ("pad_m", ctypes.c_int)]
+
+
+@dataclass
+class OracleConfig:
+    T: int
+    d: int
+    f: int
+    E: int
+    k: int
+    capacity_factor: float = 0.0   # <= 0 : no limit; pass the fp32 value the GPU sees
+    swiglu: bool = False
+    normalize_gates: bool = True
+    aux_coef: float = 0.0
+    pad_m: int = 1
+
+    def c(self) -> _Cfg:
+        return _Cfg(self.T, self.d, self.f, self.E, self.k, float(self.capacity_factor),
+                    int(self.swiglu), int(self.normalize_gates), float(self.aux_coef),
+                    int(self.pad_m))
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        _lib.oracle_capacity.restype = ctypes.c_int
+        _lib.oracle_route.restype = ctypes.c_int
+        for name in ("oracle_router_logits", "oracle_permute", "oracle_combine", "oracle_stats",
+                     "oracle_forward", "oracle_backward", "oracle_expert_apply"):
+            getattr(_lib, name).restype = None
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _d(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def capacity(cfg: OracleConfig) -> int:
+    return lib().oracle_capacity(ctypes.byref(cfg.c()))
+
+
+def rows_bound(cfg: OracleConfig) -> int:
+    return cfg.T * cfg.k + cfg.E * (cfg.pad_m - 1)
+
+
+def router_logits(cfg, x, Wr, bias=None, noise=None):
+    x, Wr, bias, noise = _d(x), _d(Wr), _d(bias), _d(noise)
+    out = np.empty((cfg.T, cfg.E), np.float64)
+    lib().oracle_router_logits(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(bias), _p(noise), _p(out))
+    return out
+
+
+def route(cfg, logits):
+    logits = _d(logits)
+    probs = np.empty((cfg.T, cfg.E), np.float64)
+    topk = np.empty((cfg.T, cfg.k), np.int32)
+    gate = np.empty((cfg.T, cfg.k), np.float64)
+    counts = np.empty(cfg.E, np.int32)
+    nf = lib().oracle_route(ctypes.byref(cfg.c()), _p(logits), _p(probs), _p(topk), _p(gate), _p(counts))
+    return dict(probs=probs, topk_idx=topk, gate=gate, counts=counts, nonfinite=nf)
+
+
+def permute(cfg, topk_idx):
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    kept = np.empty(cfg.E, np.int32)
+    offsets = np.empty(cfg.E + 1, np.int32)
+    perm = np.empty(rows_bound(cfg), np.int32)
+    slot = np.empty((cfg.T, cfg.k), np.int32)
+    lib().oracle_permute(ctypes.byref(cfg.c()), _p(topk_idx), _p(kept), _p(offsets), _p(perm), _p(slot))
+    return dict(kept=kept, offsets=offsets, perm_token=perm[:offsets[-1]].copy(), slot_of=slot)
+
+
+def expert_apply(cfg, e, x_row, Wup, Wgate, Wdown):
+    y = np.empty(cfg.d, np.float64)
+    lib().oracle_expert_apply(ctypes.byref(cfg.c()), int(e), _p(_d(x_row)), _p(_d(Wup)),
+                              _p(_d(Wgate) if cfg.swiglu else None), _p(_d(Wdown)), _p(y))
+    return y
+
+
+def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in=None):
+    """Steps 1-9. ``logits_in`` (e.g. the GPU's fp32 logits) replaces step 1."""
+    x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
+    bias, noise, logits_in = _d(bias), _d(noise), _d(logits_in)
+    T, E, k, d = cfg.T, cfg.E, cfg.k, cfg.d
+    r = dict(logits=np.empty((T, E)), probs=np.empty((T, E)), topk_idx=np.empty((T, k), np.int32),
+             gate=np.empty((T, k)), counts=np.empty(E, np.int32), kept=np.empty(E, np.int32),
+             offsets=np.empty(E + 1, np.int32), perm_token=np.empty(rows_bound(cfg), np.int32),
+             slot_of=np.empty((T, k), np.int32), out=np.empty((T, d)), stats=np.empty(8 + E))
+    lib().oracle_forward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(bias), _p(noise), _p(Wup),
+                         _p(Wgate), _p(Wdown), _p(logits_in),
+                         *[_p(r[n]) for n in ("logits", "probs", "topk_idx", "gate", "counts", "kept",
+                                               "offsets", "perm_token", "slot_of", "out", "stats")])
+    r["perm_token"] = r["perm_token"][: r["offsets"][-1]].copy()
+    return r
+
+
+def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgate=None,
+             with_bias=False):
+    """Step 10: gradients of <dout, out> + aux loss (written, not accumulated)."""
+    x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
+    logits, gate, dout = _d(logits), _d(gate), _d(dout)
+    topk_idx = np.ascontiguousarray(topk_idx, np.int32)
+    slot_of = np.ascontiguousarray(slot_of, np.int32)
+    T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
+    g = dict(dx=np.empty((T, d)), dWr=np.empty((d, E)), db=np.empty(E) if with_bias else None,
+             dWup=np.empty((E, d, f)), dWgate=np.empty((E, d, f)) if cfg.swiglu else None,
+             dWdown=np.empty((E, f, d)), dgate=np.empty((T, k)), dlogits=np.empty((T, E)))
+    lib().oracle_backward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(Wup), _p(Wgate), _p(Wdown),
+                          _p(logits), _p(topk_idx), _p(gate), _p(slot_of), _p(dout),
+                          *[_p(g[n]) for n in ("dx", "dWr", "db", "dWup", "dWgate", "dWdown",
+                                               "dgate", "dlogits")])
+    return g

@@ -1,0 +1,83 @@
+"""Brute-force restatement of the MoE forward -- TEST INFRASTRUCTURE ONLY.
+
+Independent of ``moe_oracle.c``: written in the per-expert boolean-mask form
+("for each expert, take the tokens routed to it, run the expert, scatter the
+weighted result back") of the "Twinkle adapts DeepSeek-V4 training" notes,
+§3.2 (MoEBlock.forward), with numpy whole-array ops.  Used on tiny inputs to
+pin the C oracle; never fast, never used by the GPU path.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def capacity(T, k, E, capacity_factor):
+    if not capacity_factor > 0:
+        return T
+    return min(T, int(math.ceil(float(capacity_factor) * T * k / E)))
+
+
+def topk_by_sort(logits, k):
+    """Full stable sort per token: key (logit descending, NaN last, id ascending)."""
+    T, E = logits.shape
+    out = np.empty((T, k), np.int32)
+    for t in range(T):
+        row = logits[t]
+        key = np.where(np.isnan(row), -np.inf, row)
+        nan_rank = np.isnan(row).astype(np.int64)
+        order = np.lexsort((np.arange(E), -key, nan_rank))
+        out[t] = order[:k]
+    return out
+
+
+def forward(x, Wr, Wup, Wdown, k, capacity_factor=0.0, Wgate=None, bias=None, noise=None,
+            normalize_gates=True, logits=None):
+    """Returns (out, topk_idx, gate, kept_mask[T,k])."""
+    x = np.asarray(x, np.float64)
+    T, d = x.shape
+    E = Wr.shape[1]
+    if logits is None:
+        logits = x @ np.asarray(Wr, np.float64)
+        if bias is not None:
+            logits = logits + np.asarray(bias, np.float64)[None, :]
+        if noise is not None:
+            logits = logits + np.asarray(noise, np.float64)
+    logits = np.asarray(logits, np.float64)
+    probs = np.exp(logits - logits.max(axis=1, keepdims=True))
+    probs /= probs.sum(axis=1, keepdims=True)
+    topk = topk_by_sort(logits, k)
+    sel_logits = np.take_along_axis(logits, topk, axis=1)
+    if normalize_gates:
+        w = np.exp(sel_logits - sel_logits[:, :1])
+        gate = w / w.sum(axis=1, keepdims=True)
+    else:
+        gate = np.take_along_axis(probs, topk, axis=1)
+
+    # routing matrix [T, E] of slot indices (-1 = not selected), then capacity
+    C = capacity(T, k, E, capacity_factor)
+    kept = np.zeros((T, k), bool)
+    for e in range(E):
+        tok, slot = np.nonzero(topk == e)          # row-major => ascending token order
+        keep = np.arange(len(tok)) < C
+        kept[tok[keep], slot[keep]] = True
+
+    out = np.zeros((T, d))
+    for e in range(E):
+        mask = (topk == e) & kept                    # [T, k]
+        tok, slot = np.nonzero(mask)
+        if len(tok) == 0:
+            continue
+        xe = x[tok]
+        if Wgate is None:
+            a = _silu(xe @ np.asarray(Wup[e], np.float64))
+        else:
+            a = _silu(xe @ np.asarray(Wgate[e], np.float64)) * (xe @ np.asarray(Wup[e], np.float64))
+        ye = a @ np.asarray(Wdown[e], np.float64)
+        np.add.at(out, tok, gate[tok, slot][:, None] * ye)
+    return out, topk, gate, kept

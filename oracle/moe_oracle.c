@@ -1,0 +1,481 @@
+/*
+ * moe_oracle.c -- plain, slow, fp64 CPU definition of one sparse MoE layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this file's library.  It shares
+ * no code, header, table or constant with the CUDA library; neither includes
+ * or loads the other.
+ *
+ * Sources (the four web pages this layer is specified by):
+ *   [LLaMA4-MoE]  "Hand-building a LLaMA4-MoE" guide (nxmr.cn/news/140631)
+ *   [ZeRO3-MoE]   "DeepSpeed ZeRO-3 and MoE memory accounting" guide
+ *                 (nlpx.cn/news/237350)
+ *   [Twinkle]     "Twinkle adapts DeepSeek-V4 training" notes (wmrh.cn/news/44033)
+ *
+ * Every step is written as the plain definition, token by token, in the
+ * order the pages state the layer; no blocking, fusion or reordering.
+ * OpenMP is used only on loops whose iterations are independent (each
+ * writes its own output rows), so results do not depend on thread count.
+ *
+ * Readings taken where the pages are silent or inconsistent:
+ *   - top-k is taken on the logits (softmax is monotone), ties broken by the
+ *     lowest expert id; a NaN logit ranks below every number.
+ *   - gates are the softmax over the k selected logits (they sum to 1 before
+ *     capacity drops); normalize_gates = 0 keeps the raw softmax probability.
+ *   - capacity C = ceil(capacity_factor * T * k / E) evaluated in IEEE double
+ *     from the given (fp32) factor, clamped to T; assignments are kept in
+ *     ascending token order while an expert has fewer than C kept.
+ *   - dropped slots contribute nothing; surviving gates are not renormalised.
+ *   - aux loss = lambda * sum_i (pbar_i - 1/E)^2 with pbar the mean softmax
+ *     probability (the [ZeRO3-MoE] §3.2 form, its 1/k read as 1/E).
+ *   - each expert is a two-layer FFN without biases: SiLU-MLP, or SwiGLU.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int T, d, f, E, k;
+    double capacity_factor; /* <= 0 : no capacity limit */
+    int swiglu;             /* 0: y = Wd^T silu(Wu^T x); 1: y = Wd^T (silu(Wg^T x) * Wu^T x) */
+    int normalize_gates;    /* 1: softmax over the k selected logits; 0: raw probabilities */
+    double aux_coef;        /* lambda of the variance-form aux loss */
+    int pad_m;              /* segment padding of the expert-contiguous layout (>= 1) */
+} oracle_cfg;
+
+/* Layout of the statistics vector written by oracle_stats (length 8 + E). */
+enum {
+    OST_AUX_LOSS = 0,   /* lambda * sum_i (pbar_i - 1/E)^2                         */
+    OST_AUX_SWITCH = 1, /* E * sum_i f_i pbar_i, f_i = counts_i / (T k)             */
+    OST_ENTROPY = 2,    /* mean over tokens of -sum_e p log p                      */
+    OST_NONFINITE = 3,  /* number of tokens with a non-finite logit                */
+    OST_DROPPED = 4,    /* assignments dropped by the capacity limit               */
+    OST_MAX_OVER_MEAN_KEPT = 5, /* max_e kept_e / mean_e kept_e                   */
+    OST_COUNT_CV = 6,   /* std/mean of counts over experts                         */
+    OST_MAX_OVER_MEAN_COUNT = 7,
+    OST_PBAR = 8        /* pbar[0..E)                                              */
+};
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+/* d/dz silu(z) = s(z) (1 + z (1 - s(z))) */
+static double dsilu(double z) { double s = sigmoid(z); return s * (1.0 + z * (1.0 - s)); }
+
+/* ---- Step 1: router logits  [LLaMA4-MoE] §2.4; noise [LLaMA4-MoE] §3.2 ----
+ * logits[t,e] = sum_i x[t,i] W_r[i,e] + b[e] + noise[t,e]                      */
+void oracle_router_logits(const oracle_cfg* c, const double* x, const double* Wr,
+                          const double* bias, const double* noise, double* logits)
+{
+    const int T = c->T, d = c->d, E = c->E;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int i = 0; i < d; ++i) s += x[(size_t)t * d + i] * Wr[(size_t)i * E + e];
+            if (bias) s += bias[e];
+            if (noise) s += noise[(size_t)t * E + e];
+            logits[(size_t)t * E + e] = s;
+        }
+    }
+}
+
+/* a ranks above b in the top-k order: larger logit, NaN lowest, then lower id */
+static int ranks_above(double la, int a, double lb, int b)
+{
+    int na = isnan(la), nb = isnan(lb);
+    if (na != nb) return nb;          /* the number ranks above the NaN */
+    if (!na && la != lb) return la > lb;
+    return a < b;
+}
+
+/* ---- Steps 2-4: softmax, top-k, gates  [LLaMA4-MoE] §2.4; [Twinkle] §3.1 ----
+ * probs  [T,E] softmax of the logits (max subtracted)
+ * topk   [T,k] experts in rank order; gate [T,k]; counts [E] selections.
+ * Returns the number of tokens that had a non-finite logit.                   */
+int oracle_route(const oracle_cfg* c, const double* logits, double* probs,
+                 int* topk, double* gate, int* counts)
+{
+    const int T = c->T, E = c->E, k = c->k;
+    int nonfinite = 0;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int t = 0; t < T; ++t) {
+        const double* l = logits + (size_t)t * E;
+        double m = -INFINITY;
+        int bad = 0;
+        for (int e = 0; e < E; ++e) {
+            if (!isfinite(l[e])) bad = 1;
+            if (l[e] > m) m = l[e];
+        }
+        nonfinite += bad;
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+        for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = exp(l[e] - m) / z;
+
+        /* selection: k passes, each taking the best expert not yet taken */
+        int* sel = topk + (size_t)t * k;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                int taken = 0;
+                for (int q = 0; q < j; ++q) taken |= (sel[q] == e);
+                if (taken) continue;
+                if (best < 0 || ranks_above(l[e], e, l[best], best)) best = e;
+            }
+            sel[j] = best;
+            counts[best] += 1;
+        }
+        /* gates: softmax restricted to the selected logits, or raw probs */
+        double* g = gate + (size_t)t * k;
+        if (c->normalize_gates) {
+            double ms = l[sel[0]], zs = 0.0;
+            for (int j = 0; j < k; ++j) zs += exp(l[sel[j]] - ms);
+            for (int j = 0; j < k; ++j) g[j] = exp(l[sel[j]] - ms) / zs;
+        } else {
+            for (int j = 0; j < k; ++j) g[j] = probs[(size_t)t * E + sel[j]];
+        }
+    }
+    return nonfinite;
+}
+
+/* ---- Capacity C  [ZeRO3-MoE] §3.1, §3.4 (capacity_factor 1.2) ---- */
+int oracle_capacity(const oracle_cfg* c)
+{
+    if (!(c->capacity_factor > 0.0)) return c->T; /* no limit: an expert sees each token once at most */
+    double v = ceil(c->capacity_factor * (double)c->T * (double)c->k / (double)c->E);
+    if (v > (double)c->T) v = (double)c->T;
+    return (int)v;
+}
+
+/* ---- Steps 5-6: capacity dropping and the expert-contiguous permutation ----
+ * Sort-by-expert then split into per-expert intervals  [LLaMA4-MoE] §2.4.
+ * kept[E]; offsets[E+1] (segment e = rows offsets[e] .. offsets[e+1], its
+ * length kept[e] rounded up to pad_m); perm_token[rows] (-1 on padding rows);
+ * slot_of[T,k] (row of assignment (t,j), or -1 when dropped).
+ * perm_token must hold offsets[E] entries (at most T*k + E*(pad_m-1)).       */
+void oracle_permute(const oracle_cfg* c, const int* topk, int* kept, int* offsets,
+                    int* perm_token, int* slot_of)
+{
+    const int T = c->T, E = c->E, k = c->k, pm = c->pad_m;
+    const int C = oracle_capacity(c);
+    int* taken = (int*)calloc((size_t)E, sizeof(int));
+    int* rank = (int*)malloc(sizeof(int) * (size_t)T * k);
+    /* walk tokens in order; keep while the expert has room */
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int e = topk[(size_t)t * k + j];
+            if (taken[e] < C) { rank[(size_t)t * k + j] = taken[e]; taken[e]++; }
+            else rank[(size_t)t * k + j] = -1;
+        }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        kept[e] = taken[e];
+        int padded = (kept[e] + pm - 1) / pm * pm;
+        offsets[e + 1] = offsets[e] + padded;
+    }
+    for (int r = 0; r < offsets[E]; ++r) perm_token[r] = -1;
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int e = topk[(size_t)t * k + j];
+            int q = rank[(size_t)t * k + j];
+            if (q < 0) { slot_of[(size_t)t * k + j] = -1; continue; }
+            slot_of[(size_t)t * k + j] = offsets[e] + q;
+            perm_token[offsets[e] + q] = t;
+        }
+    free(taken);
+    free(rank);
+}
+
+/* ---- Step 7: one expert FFN on one token  [LLaMA4-MoE] §2.4 ("two-layer FFN") ----
+ * SiLU-MLP : h = Wu^T x, a = silu(h), y = Wd^T a
+ * SwiGLU   : g = Wg^T x, u = Wu^T x, a = silu(g) * u, y = Wd^T a
+ * Wu, Wg point at expert e's [d,f] block, Wd at its [f,d] block.
+ * h_out receives h (SiLU) or g (SwiGLU); u_out receives u (SwiGLU only).    */
+static void expert_ffn(const oracle_cfg* c, const double* x, const double* Wu,
+                       const double* Wg, const double* Wd, double* h_out,
+                       double* u_out, double* a_out, double* y)
+{
+    const int d = c->d, f = c->f;
+    for (int j = 0; j < f; ++j) { h_out[j] = 0.0; if (c->swiglu) u_out[j] = 0.0; }
+    for (int i = 0; i < d; ++i) {
+        const double xi = x[i];
+        const double* wu = Wu + (size_t)i * f;
+        if (c->swiglu) {
+            const double* wg = Wg + (size_t)i * f;
+            for (int j = 0; j < f; ++j) { h_out[j] += xi * wg[j]; u_out[j] += xi * wu[j]; }
+        } else {
+            for (int j = 0; j < f; ++j) h_out[j] += xi * wu[j];
+        }
+    }
+    for (int j = 0; j < f; ++j) a_out[j] = c->swiglu ? silu(h_out[j]) * u_out[j] : silu(h_out[j]);
+    for (int i = 0; i < d; ++i) y[i] = 0.0;
+    for (int j = 0; j < f; ++j) {
+        const double aj = a_out[j];
+        const double* wd = Wd + (size_t)j * d;
+        for (int i = 0; i < d; ++i) y[i] += aj * wd[i];
+    }
+}
+
+/* One expert's FFN output on one token (for sampled checks and special cases). */
+void oracle_expert_apply(const oracle_cfg* c, int e, const double* x, const double* Wup,
+                         const double* Wgate, const double* Wdown, double* y)
+{
+    const size_t df = (size_t)c->d * c->f;
+    double* h = (double*)malloc(sizeof(double) * 3 * (size_t)c->f);
+    expert_ffn(c, x, Wup + e * df, c->swiglu ? Wgate + e * df : NULL, Wdown + e * df,
+               h, h + c->f, h + 2 * (size_t)c->f, y);
+    free(h);
+}
+
+/* ---- Step 8: gate-weighted combine  [LLaMA4-MoE] §2.4 ----
+ * out[t] = sum over kept slots j (ascending) of gate[t,j] * FFN_{e_j}(x_t);
+ * a token whose slots were all dropped outputs zeros.                         */
+void oracle_combine(const oracle_cfg* c, const double* x, const int* topk,
+                    const double* gate, const int* slot_of, const double* Wup,
+                    const double* Wgate, const double* Wdown, double* out)
+{
+    const int T = c->T, d = c->d, f = c->f, k = c->k;
+    const size_t df = (size_t)d * f;
+#pragma omp parallel
+    {
+        double* h = (double*)malloc(sizeof(double) * (3 * (size_t)f + d));
+        double* y = h + 3 * (size_t)f;
+#pragma omp for schedule(dynamic, 4)
+        for (int t = 0; t < T; ++t) {
+            double* o = out + (size_t)t * d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            for (int j = 0; j < k; ++j) {
+                if (slot_of[(size_t)t * k + j] < 0) continue;
+                int e = topk[(size_t)t * k + j];
+                expert_ffn(c, x + (size_t)t * d, Wup + e * df, c->swiglu ? Wgate + e * df : NULL,
+                           Wdown + e * df, h, h + f, h + 2 * (size_t)f, y);
+                const double g = gate[(size_t)t * k + j];
+                for (int i = 0; i < d; ++i) o[i] += g * y[i];
+            }
+        }
+        free(h);
+    }
+}
+
+/* ---- Step 9: aux statistics  [ZeRO3-MoE] §3.2; [LLaMA4-MoE] §3.2, §3.3 ----
+ * stats has 8 + E entries (layout OST_*).                                     */
+void oracle_stats(const oracle_cfg* c, const double* probs, const int* counts,
+                  const int* kept, int nonfinite, double* stats)
+{
+    const int T = c->T, E = c->E, k = c->k;
+    double* pbar = stats + OST_PBAR;
+    for (int e = 0; e < E; ++e) pbar[e] = 0.0;
+    double ent = 0.0;
+    for (int t = 0; t < T; ++t) {
+        double h = 0.0;
+        for (int e = 0; e < E; ++e) {
+            double p = probs[(size_t)t * E + e];
+            pbar[e] += p;
+            if (p > 0.0) h -= p * log(p);
+        }
+        ent += h;
+    }
+    double aux = 0.0, sw = 0.0;
+    for (int e = 0; e < E; ++e) {
+        pbar[e] /= (double)T;
+        aux += (pbar[e] - 1.0 / E) * (pbar[e] - 1.0 / E);
+        sw += ((double)counts[e] / ((double)T * k)) * pbar[e];
+    }
+    stats[OST_AUX_LOSS] = c->aux_coef * aux;
+    stats[OST_AUX_SWITCH] = (double)E * sw;
+    stats[OST_ENTROPY] = ent / (double)T;
+    stats[OST_NONFINITE] = (double)nonfinite;
+    long dropped = 0, kmax = 0, ksum = 0, cmax = 0, csum = 0;
+    for (int e = 0; e < E; ++e) {
+        dropped += counts[e] - kept[e];
+        if (kept[e] > kmax) kmax = kept[e];
+        ksum += kept[e];
+        if (counts[e] > cmax) cmax = counts[e];
+        csum += counts[e];
+    }
+    double cmean = (double)csum / E, var = 0.0;
+    for (int e = 0; e < E; ++e) var += (counts[e] - cmean) * (counts[e] - cmean);
+    stats[OST_DROPPED] = (double)dropped;
+    stats[OST_MAX_OVER_MEAN_KEPT] = ksum > 0 ? (double)kmax / ((double)ksum / E) : 0.0;
+    stats[OST_COUNT_CV] = cmean > 0 ? sqrt(var / E) / cmean : 0.0;
+    stats[OST_MAX_OVER_MEAN_COUNT] = cmean > 0 ? (double)cmax / cmean : 0.0;
+}
+
+/* ---- Whole forward: steps 1-9.  If logits_in is given, step 1 is skipped and
+ * those logits are routed instead (the "conditioned" oracle).                 */
+void oracle_forward(const oracle_cfg* c, const double* x, const double* Wr, const double* bias,
+                    const double* noise, const double* Wup, const double* Wgate,
+                    const double* Wdown, const double* logits_in,
+                    double* logits, double* probs, int* topk, double* gate, int* counts,
+                    int* kept, int* offsets, int* perm_token, int* slot_of,
+                    double* out, double* stats)
+{
+    if (logits_in) memcpy(logits, logits_in, sizeof(double) * (size_t)c->T * c->E);
+    else oracle_router_logits(c, x, Wr, bias, noise, logits);
+    int nf = oracle_route(c, logits, probs, topk, gate, counts);
+    oracle_permute(c, topk, kept, offsets, perm_token, slot_of);
+    oracle_combine(c, x, topk, gate, slot_of, Wup, Wgate, Wdown, out);
+    oracle_stats(c, probs, counts, kept, nf, stats);
+}
+
+/* ---- Step 10: backward of L = <dout, out> + aux loss ----
+ * Gradients flow through the gate weights into the router; the selection
+ * itself is piecewise constant  ([LLaMA4-MoE] §2.4: do not detach the
+ * routing weights).  Outputs are written, not accumulated.
+ * dx[T,d], dWr[d,E], db[E] (may be NULL), dWup/dWgate[E,d,f], dWdown[E,f,d],
+ * dgate[T,k] and dlogits[T,E] (both may be NULL).                             */
+void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
+                     const double* Wup, const double* Wgate, const double* Wdown,
+                     const double* logits, const int* topk, const double* gate,
+                     const int* slot_of, const double* dout,
+                     double* dx, double* dWr, double* db, double* dWup, double* dWgate,
+                     double* dWdown, double* dgate_out, double* dlogits_out)
+{
+    const int T = c->T, d = c->d, f = c->f, E = c->E, k = c->k;
+    const size_t df = (size_t)d * f;
+    double* dgate = (double*)calloc((size_t)T * k, sizeof(double));
+    double* dxp = (double*)calloc((size_t)T * k * d, sizeof(double)); /* per-slot dx */
+    memset(dWup, 0, sizeof(double) * E * df);
+    memset(dWdown, 0, sizeof(double) * E * df);
+    if (c->swiglu) memset(dWgate, 0, sizeof(double) * E * df);
+
+    /* expert FFN backward, expert by expert, tokens ascending (each expert's
+     * weight gradients are its own; per-slot dx rows are disjoint)            */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int e = 0; e < E; ++e) {
+        double* h = (double*)malloc(sizeof(double) * (6 * (size_t)f + 2 * (size_t)d));
+        double *u = h + f, *a = h + 2 * (size_t)f, *da = h + 3 * (size_t)f;
+        double *dh = h + 4 * (size_t)f, *du = h + 5 * (size_t)f;
+        double *y = h + 6 * (size_t)f, *dy = y + d;
+        const double* Wu = Wup + e * df;
+        const double* Wg = c->swiglu ? Wgate + e * df : NULL;
+        const double* Wd = Wdown + e * df;
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j) {
+                if (topk[(size_t)t * k + j] != e || slot_of[(size_t)t * k + j] < 0) continue;
+                const double* xt = x + (size_t)t * d;
+                const double* go = dout + (size_t)t * d;
+                expert_ffn(c, xt, Wu, Wg, Wd, h, u, a, y);
+                /* out += gate * y  =>  dgate = <dout, y>, dy = gate * dout */
+                double s = 0.0;
+                for (int i = 0; i < d; ++i) s += go[i] * y[i];
+                dgate[(size_t)t * k + j] = s;
+                const double gt = gate[(size_t)t * k + j];
+                for (int i = 0; i < d; ++i) dy[i] = gt * go[i];
+                /* y = Wd^T a */
+                for (int q = 0; q < f; ++q) {
+                    const double* wd = Wd + (size_t)q * d;
+                    double acc = 0.0;
+                    for (int i = 0; i < d; ++i) acc += wd[i] * dy[i];
+                    da[q] = acc;
+                    double* gw = dWdown + e * df + (size_t)q * d;
+                    for (int i = 0; i < d; ++i) gw[i] += a[q] * dy[i];
+                }
+                /* activation */
+                for (int q = 0; q < f; ++q) {
+                    if (c->swiglu) {
+                        du[q] = da[q] * silu(h[q]);          /* d/du (silu(g) u) */
+                        dh[q] = da[q] * u[q] * dsilu(h[q]);  /* d/dg             */
+                    } else {
+                        dh[q] = da[q] * dsilu(h[q]);
+                    }
+                }
+                /* h = Wu^T x (SiLU) ; g = Wg^T x, u = Wu^T x (SwiGLU) */
+                double* dxr = dxp + ((size_t)t * k + j) * d;
+                for (int i = 0; i < d; ++i) {
+                    const double xi = xt[i];
+                    double acc = 0.0;
+                    if (c->swiglu) {
+                        double* gu = dWup + e * df + (size_t)i * f;
+                        double* gg = dWgate + e * df + (size_t)i * f;
+                        const double* wu = Wu + (size_t)i * f;
+                        const double* wg = Wg + (size_t)i * f;
+                        for (int q = 0; q < f; ++q) {
+                            gu[q] += xi * du[q];
+                            gg[q] += xi * dh[q];
+                            acc += wu[q] * du[q] + wg[q] * dh[q];
+                        }
+                    } else {
+                        double* gu = dWup + e * df + (size_t)i * f;
+                        const double* wu = Wu + (size_t)i * f;
+                        for (int q = 0; q < f; ++q) { gu[q] += xi * dh[q]; acc += wu[q] * dh[q]; }
+                    }
+                    dxr[i] = acc;
+                }
+            }
+        free(h);
+    }
+
+    /* router: dL/dlogits from the gates and from the aux loss */
+    double* probs = (double*)malloc(sizeof(double) * (size_t)T * E);
+    double* pbar = (double*)calloc((size_t)E, sizeof(double));
+    double* dl = (double*)malloc(sizeof(double) * (size_t)T * E);
+    for (int t = 0; t < T; ++t) {
+        const double* l = logits + (size_t)t * E;
+        double m = -INFINITY, z = 0.0;
+        for (int e = 0; e < E; ++e) if (l[e] > m) m = l[e];
+        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+        for (int e = 0; e < E; ++e) { probs[(size_t)t * E + e] = exp(l[e] - m) / z; pbar[e] += probs[(size_t)t * E + e]; }
+    }
+    for (int e = 0; e < E; ++e) pbar[e] /= (double)T;
+    double* cvec = (double*)malloc(sizeof(double) * (size_t)E); /* dL_aux / dp[t,e] */
+    for (int e = 0; e < E; ++e) cvec[e] = c->aux_coef * 2.0 * (pbar[e] - 1.0 / E) / (double)T;
+
+    for (int t = 0; t < T; ++t) {
+        const double* p = probs + (size_t)t * E;
+        const double* g = gate + (size_t)t * k;
+        const double* dg = dgate + (size_t)t * k;
+        const int* sel = topk + (size_t)t * k;
+        double* dlt = dl + (size_t)t * E;
+        for (int e = 0; e < E; ++e) dlt[e] = 0.0;
+        if (c->normalize_gates) {
+            /* gate_j = exp(l_j) / sum_sel exp: d gate_j / d l_i = gate_j (delta_ji - gate_i) */
+            double s = 0.0;
+            for (int j = 0; j < k; ++j) s += g[j] * dg[j];
+            for (int j = 0; j < k; ++j) dlt[sel[j]] += g[j] * (dg[j] - s);
+        } else {
+            /* gate_j = p_{e_j}: d p_a / d l_b = p_a (delta_ab - p_b) */
+            double s = 0.0;
+            for (int j = 0; j < k; ++j) s += dg[j] * p[sel[j]];
+            for (int j = 0; j < k; ++j) dlt[sel[j]] += dg[j] * p[sel[j]];
+            for (int e = 0; e < E; ++e) dlt[e] -= p[e] * s;
+        }
+        /* aux: dL/dp[t,e] = cvec[e], through the full softmax */
+        double s = 0.0;
+        for (int e = 0; e < E; ++e) s += p[e] * cvec[e];
+        for (int e = 0; e < E; ++e) dlt[e] += p[e] * (cvec[e] - s);
+    }
+
+    /* dx = sum over kept slots of the expert dx, plus the router term */
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        double* o = dx + (size_t)t * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            if (slot_of[(size_t)t * k + j] < 0) continue;
+            const double* r = dxp + ((size_t)t * k + j) * d;
+            for (int i = 0; i < d; ++i) o[i] += r[i];
+        }
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int e = 0; e < E; ++e) acc += dl[(size_t)t * E + e] * Wr[(size_t)i * E + e];
+            o[i] += acc;
+        }
+    }
+    /* dW_r = x^T dlogits ; db = sum_t dlogits */
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < d; ++i)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += x[(size_t)t * d + i] * dl[(size_t)t * E + e];
+            dWr[(size_t)i * E + e] = acc;
+        }
+    if (db)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += dl[(size_t)t * E + e];
+            db[e] = acc;
+        }
+    if (dgate_out) memcpy(dgate_out, dgate, sizeof(double) * (size_t)T * k);
+    if (dlogits_out) memcpy(dlogits_out, dl, sizeof(double) * (size_t)T * E);
+    free(dgate); free(dxp); free(probs); free(pbar); free(dl); free(cvec);
+}

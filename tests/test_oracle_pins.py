@@ -1,0 +1,259 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+* a hand-worked routing example (tests/golden/route_worked_example.json),
+* the independent brute-force mask-loop restatement (oracle/bruteforce.py),
+* closed forms: one expert = a plain FFN; k = E = a dense softmax mixture;
+  a uniform router gives zero variance-form aux loss and Switch form 1,
+* structural invariants of the routing,
+* central finite differences of <dout, out> + aux loss for every gradient.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import bruteforce
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _frac(s):
+    return float(Fraction(s))
+
+
+def _rand_case(rng, T, d, f, E, k, swiglu=False, bias=False, noise=False, scale=1.0):
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((d, E)) * scale
+    Wup = rng.standard_normal((E, d, f)) * 0.3
+    Wg = rng.standard_normal((E, d, f)) * 0.3 if swiglu else None
+    Wd = rng.standard_normal((E, f, d)) * 0.3
+    b = rng.standard_normal(E) * 0.5 if bias else None
+    nz = rng.standard_normal((T, E)) * 0.1 if noise else None
+    return x, Wr, Wup, Wg, Wd, b, nz
+
+
+# --------------------------------------------------------------------------- golden
+def test_worked_example_routing(oracle_lib):
+    g = json.load(open(os.path.join(GOLDEN, "route_worked_example.json")))
+    c = g["config"]
+    cfg = oracle.OracleConfig(T=c["T"], d=1, f=1, E=c["E"], k=c["k"],
+                              capacity_factor=c["capacity_factor"], pad_m=c["pad_m"],
+                              aux_coef=c["aux_coef"])
+    logits = np.log(np.array(g["logit_weights"], np.float64))
+    ex = g["expected"]
+    r = oracle.route(cfg, logits)
+    assert r["topk_idx"].tolist() == ex["topk_idx"]
+    assert r["counts"].tolist() == ex["counts"]
+    np.testing.assert_allclose(r["gate"], [[_frac(v) for v in row] for row in ex["gate"]], rtol=1e-14)
+    np.testing.assert_allclose(r["probs"], [[_frac(v) for v in row] for row in ex["probs"]], rtol=1e-14)
+    assert oracle.capacity(cfg) == ex["capacity"]
+    p = oracle.permute(cfg, r["topk_idx"])
+    assert p["kept"].tolist() == ex["kept"]
+    assert p["offsets"].tolist() == ex["offsets"]
+    assert p["perm_token"].tolist() == ex["perm_token"]
+    assert p["slot_of"].tolist() == ex["slot_of"]
+    x = np.zeros((cfg.T, 1))
+    W = np.zeros((cfg.E, 1, 1))
+    fw = oracle.forward(cfg, x, np.zeros((1, cfg.E)), W, W, logits_in=logits)
+    st = fw["stats"]
+    assert st[oracle.ST_DROPPED] == ex["dropped"]
+    np.testing.assert_allclose(st[oracle.ST_PBAR:], [_frac(v) for v in ex["pbar"]], rtol=1e-14)
+    assert st[oracle.ST_AUX_LOSS] == pytest.approx(_frac(ex["aux_loss"]), rel=1e-12)
+    assert st[oracle.ST_AUX_SWITCH] == pytest.approx(_frac(ex["aux_switch"]), rel=1e-12)
+    assert st[oracle.ST_MAX_OVER_MEAN_KEPT] == pytest.approx(_frac(ex["max_over_mean_kept"]))
+    assert st[oracle.ST_COUNT_CV] == pytest.approx(_frac(ex["count_cv"]))
+    assert st[oracle.ST_MAX_OVER_MEAN_COUNT] == pytest.approx(_frac(ex["max_over_mean_count"]))
+
+
+def test_capacity_values_of_the_workloads(oracle_lib):
+    # C = ceil(cf * T * k / E) with the fp32 factor 1.2f:
+    # 1.2*2048*2/4 = 1228.8 -> 1229; 1.2*16384*2/8 = 4915.2 -> 4916; 1.2*65536*2/16 = 9830.4 -> 9831
+    cf = float(np.float32(1.2))
+    for (T, E, want) in ((2048, 4, 1229), (16384, 8, 4916), (65536, 16, 9831)):
+        assert oracle.capacity(oracle.OracleConfig(T=T, d=1, f=1, E=E, k=2, capacity_factor=cf)) == want
+    # no factor -> each expert may see every token once
+    assert oracle.capacity(oracle.OracleConfig(T=77, d=1, f=1, E=4, k=2)) == 77
+    # clamped to T
+    assert oracle.capacity(oracle.OracleConfig(T=10, d=1, f=1, E=2, k=2, capacity_factor=50.0)) == 10
+
+
+# --------------------------------------------------------------------------- brute force
+@pytest.mark.parametrize("swiglu", [False, True])
+@pytest.mark.parametrize("cf", [0.0, 1.0, 0.5])
+@pytest.mark.parametrize("norm", [True, False])
+def test_matches_bruteforce_mask_loop(oracle_lib, swiglu, cf, norm):
+    rng = np.random.default_rng(1234 + int(swiglu) + int(cf * 10) + int(norm))
+    T, d, f, E, k = 37, 12, 20, 5, 2
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, swiglu, bias=True, noise=True)
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=cf, swiglu=swiglu,
+                              normalize_gates=norm, pad_m=4)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, Wgate=Wg, bias=b, noise=nz)
+    out, topk, gate, kept = bruteforce.forward(x, Wr, Wup, Wd, k, cf, Wgate=Wg, bias=b, noise=nz,
+                                               normalize_gates=norm)
+    assert (r["topk_idx"] == topk).all()
+    np.testing.assert_allclose(r["gate"], gate, rtol=1e-13, atol=0)
+    assert ((r["slot_of"] >= 0) == kept).all()
+    np.testing.assert_allclose(r["out"], out, rtol=1e-12, atol=1e-13)
+
+
+def test_topk_against_full_sort_with_ties_and_nan(oracle_lib):
+    rng = np.random.default_rng(7)
+    T, E = 300, 8
+    logits = rng.integers(-3, 4, size=(T, E)).astype(np.float64)  # many exact ties
+    logits[::17, 3] = np.nan
+    logits[::23, :] = 1.0                                          # all tied
+    for k in (1, 2, 3, 8):
+        cfg = oracle.OracleConfig(T=T, d=1, f=1, E=E, k=k)
+        r = oracle.route(cfg, logits)
+        assert (r["topk_idx"] == bruteforce.topk_by_sort(logits, k)).all()
+        assert r["nonfinite"] == int(np.isnan(logits).any(axis=1).sum())
+
+
+# --------------------------------------------------------------------------- closed forms
+def test_single_expert_is_a_plain_ffn(oracle_lib):
+    rng = np.random.default_rng(3)
+    T, d, f = 9, 7, 11
+    x = rng.standard_normal((T, d))
+    Wup = rng.standard_normal((1, d, f))
+    Wd = rng.standard_normal((1, f, d))
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=1, k=1)
+    r = oracle.forward(cfg, x, rng.standard_normal((d, 1)), Wup, Wd)
+    h = x @ Wup[0]
+    want = (h / (1 + np.exp(-h))) @ Wd[0]
+    np.testing.assert_allclose(r["out"], want, rtol=1e-12, atol=1e-12)
+    assert (r["gate"] == 1.0).all()
+
+
+def test_k_equals_E_is_a_dense_softmax_mixture(oracle_lib):
+    rng = np.random.default_rng(4)
+    T, d, f, E = 6, 5, 8, 3
+    x, Wr, Wup, Wg, Wd, _, _ = _rand_case(rng, T, d, f, E, E, swiglu=True)
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=E, swiglu=True)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, Wgate=Wg)
+    z = x @ Wr
+    p = np.exp(z - z.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    want = np.zeros((T, d))
+    for e in range(E):
+        g = x @ Wg[e]
+        want += p[:, e:e + 1] * (((g / (1 + np.exp(-g))) * (x @ Wup[e])) @ Wd[e])
+    np.testing.assert_allclose(r["out"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_uniform_router_aux_statistics(oracle_lib):
+    T, d, E, k = 64, 4, 8, 2
+    cfg = oracle.OracleConfig(T=T, d=d, f=2, E=E, k=k, aux_coef=0.01)
+    x = np.random.default_rng(5).standard_normal((T, d))
+    r = oracle.forward(cfg, x, np.zeros((d, E)), np.zeros((E, d, 2)), np.zeros((E, 2, d)))
+    st = r["stats"]
+    np.testing.assert_allclose(st[oracle.ST_PBAR:], 1.0 / E, rtol=1e-15)
+    assert st[oracle.ST_AUX_LOSS] == pytest.approx(0.0, abs=1e-18)
+    assert st[oracle.ST_AUX_SWITCH] == pytest.approx(1.0, rel=1e-14)
+    assert st[oracle.ST_ENTROPY] == pytest.approx(math.log(E), rel=1e-14)
+    # all logits tie -> every token picks experts 0 and 1
+    assert (r["topk_idx"] == [0, 1]).all()
+
+
+# --------------------------------------------------------------------------- invariants
+@pytest.mark.parametrize("cf", [0.0, 1.2, 0.7])
+def test_routing_invariants(oracle_lib, cf):
+    rng = np.random.default_rng(11)
+    T, E, k, pad = 500, 6, 2, 8
+    logits = rng.standard_normal((T, E)) + np.array([1.5, 0.8, 0, 0, -0.5, -1.0])
+    cfg = oracle.OracleConfig(T=T, d=1, f=1, E=E, k=k, capacity_factor=cf, pad_m=pad)
+    r = oracle.route(cfg, logits)
+    p = oracle.permute(cfg, r["topk_idx"])
+    topk, slot = r["topk_idx"], p["slot_of"]
+    C = oracle.capacity(cfg)
+    # k distinct experts per token; gates sum to one before drops
+    assert all(len(set(row)) == k for row in topk.tolist())
+    np.testing.assert_allclose(r["gate"].sum(1), 1.0, rtol=1e-14)
+    assert r["counts"].sum() == T * k
+    assert (p["kept"] == np.minimum(r["counts"], C)).all()
+    dropped = int((slot < 0).sum())
+    assert p["kept"].sum() == T * k - dropped
+    off = p["offsets"]
+    assert off[0] == 0 and ((np.diff(off) % pad) == 0).all()
+    assert (np.diff(off) - p["kept"] < pad).all() and (np.diff(off) >= p["kept"]).all()
+    perm = p["perm_token"]
+    for e in range(E):
+        seg = perm[off[e]:off[e + 1]]
+        real = seg[: p["kept"][e]]
+        assert (np.diff(real) > 0).all()                       # ascending token order
+        assert (seg[p["kept"][e]:] == -1).all()                # padding rows
+        want = [t for t in range(T) if e in topk[t]][:C]       # first C in token order
+        assert real.tolist() == want
+    for t in range(T):
+        for j in range(k):
+            if slot[t, j] >= 0:
+                assert perm[slot[t, j]] == t
+                assert off[topk[t, j]] <= slot[t, j] < off[topk[t, j] + 1]
+
+
+# --------------------------------------------------------------------------- gradients
+def _loss(cfg, x, Wr, Wup, Wd, Wg, b, nz, dout):
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, Wgate=Wg, bias=b, noise=nz)
+    return float((dout * r["out"]).sum() + r["stats"][oracle.ST_AUX_LOSS]), r
+
+
+@pytest.mark.parametrize("swiglu,cf,norm", [(False, 0.0, True), (False, 0.75, True),
+                                            (True, 0.0, True), (True, 0.75, False),
+                                            (False, 0.0, False)])
+def test_backward_matches_finite_differences(oracle_lib, swiglu, cf, norm):
+    rng = np.random.default_rng(100 + int(swiglu) * 10 + int(cf * 4) + int(norm))
+    T, d, f, E, k = 8, 8, 16, 4, 2
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, swiglu, bias=True, noise=True)
+    dout = rng.standard_normal((T, d))
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=cf, swiglu=swiglu,
+                              normalize_gates=norm, aux_coef=0.3)
+    L0, r0 = _loss(cfg, x, Wr, Wup, Wd, Wg, b, nz, dout)
+    g = oracle.backward(cfg, x, Wr, Wup, Wd, r0["logits"], r0["topk_idx"], r0["gate"],
+                        r0["slot_of"], dout, Wgate=Wg, with_bias=True)
+    h = 1e-6
+    params = {"x": (x, g["dx"]), "Wr": (Wr, g["dWr"]), "b": (b, g["db"]),
+              "Wup": (Wup, g["dWup"]), "Wd": (Wd, g["dWdown"])}
+    if swiglu:
+        params["Wg"] = (Wg, g["dWgate"])
+    checked = 0
+    for name, (arr, grad) in params.items():
+        idxs = [np.unravel_index(i, arr.shape) for i in
+                rng.choice(arr.size, size=min(arr.size, 40), replace=False)]
+        for ix in idxs:
+            vals = []
+            for s in (+h, -h):
+                a2 = arr.copy()
+                a2[ix] += s
+                kw = dict(x=x, Wr=Wr, Wup=Wup, Wd=Wd, Wg=Wg, b=b, nz=nz)
+                kw[name] = a2
+                L, r = _loss(cfg, kw["x"], kw["Wr"], kw["Wup"], kw["Wd"], kw["Wg"], kw["b"],
+                             kw["nz"], dout)
+                assert (r["topk_idx"] == r0["topk_idx"]).all(), "routing moved under +-h"
+                assert (r["slot_of"] == r0["slot_of"]).all()
+                vals.append(L)
+            fd = (vals[0] - vals[1]) / (2 * h)
+            assert grad[ix] == pytest.approx(fd, rel=2e-5, abs=2e-7), (name, ix)
+            checked += 1
+    assert checked > 150
+
+
+def test_backward_gate_gradient_is_dot_with_expert_output(oracle_lib):
+    """dL/dgate[t,j] = <dout_t, FFN_{e_j}(x_t)> for kept slots, 0 for dropped ones."""
+    rng = np.random.default_rng(9)
+    T, d, f, E, k = 10, 6, 9, 3, 2
+    x, Wr, Wup, Wg, Wd, _, _ = _rand_case(rng, T, d, f, E, k)
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=0.5)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd)
+    dout = rng.standard_normal((T, d))
+    g = oracle.backward(cfg, x, Wr, Wup, Wd, r["logits"], r["topk_idx"], r["gate"],
+                        r["slot_of"], dout)
+    for t in range(T):
+        for j in range(k):
+            if r["slot_of"][t, j] < 0:
+                assert g["dgate"][t, j] == 0.0
+            else:
+                y = oracle.expert_apply(cfg, r["topk_idx"][t, j], x[t], Wup, None, Wd)
+                assert g["dgate"][t, j] == pytest.approx(float(dout[t] @ y), rel=1e-12)
