@@ -1,0 +1,226 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse Mixture-of-Experts layer.
+ *
+ * One GPU, one layer: router GEMM -> softmax -> top-k gating with a capacity
+ * limit -> permutation into expert-contiguous rows -> grouped two-layer expert
+ * FFN -> gate-weighted combine -> aux load-balance statistics, and the
+ * backward pass of all of it.
+ *
+ * Sources (the web pages that state the layer):
+ *   [LLaMA4-MoE] "Hand-building a LLaMA4-MoE" guide, §2.4 (router + softmax,
+ *                top-K index [B,K], sort by expert id, per-expert split,
+ *                two-layer FFN experts, gate-weighted sum, gradients through
+ *                the routing weights), §3.2 (Switch aux loss, gate noise).
+ *   [ZeRO3-MoE]  "DeepSpeed ZeRO-3 and MoE memory accounting" guide, §3.1 and
+ *                §3.4 (per-expert capacity, capacity_factor 1.2, gate_noise),
+ *                §3.2 (variance aux loss), §5.3 (gating computed in fp32).
+ *   [Twinkle]    "Twinkle adapts DeepSeek-V4 training" notes, §3.1
+ *                (scores = W_router x, softmax, top-k with k = 2).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer unless stated, owned by the
+ *     caller; the library never allocates or frees device memory.  Scratch
+ *     space is the caller's workspace of moe_workspace_size() bytes.
+ *   - Row-major tensors.  Expert weights are stacked per expert:
+ *     W_up[E,d,f], W_gate[E,d,f], W_down[E,f,d]; router W_r[d,E].
+ *   - "act" tensors have the layer dtype (fp32 or bf16, bit pattern uint16);
+ *     logits, gates, probabilities, statistics, bias, noise and dgate/dlogits
+ *     are always fp32; indices are int32.
+ *   - All pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  No call synchronises the host on the hot path:
+ *     row counts decided on the device (offsets) are read by later kernels
+ *     on the device; buffers of permuted rows are sized for the worst case
+ *     returned by moe_rows_capacity().
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_*.  Host-side argument
+ *     checks run before anything is launched.  Conditions found on the
+ *     device (a bounded wait that ran out, non-finite logits) are recorded
+ *     in a device status word read by moe_last_device_status().
+ *   - Gradients are written, never accumulated into.
+ *   - Results are deterministic: no floating-point atomics; reruns on the
+ *     same inputs give identical bytes.
+ */
+#ifndef GB300_MOE_H
+#define GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same handle as cudaStream_t */
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* ---- status codes ---- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)   /* bad shape, null or misaligned pointer      */
+#define MOE_ERR_UNSUPPORTED (-2)   /* valid but not implemented (see moe_check_config) */
+#define MOE_ERR_CUDA (-3)          /* a CUDA runtime call failed                 */
+#define MOE_ERR_TIMEOUT (-4)       /* device: a bounded wait gave up             */
+#define MOE_ERR_NONFINITE (-5)     /* device: a router logit was NaN or infinite */
+#define MOE_ERR_DEVICE_BOUNDS (-6) /* device: an index read from memory was out of range */
+
+/* ---- configuration ---- */
+#define MOE_DTYPE_F32 0
+#define MOE_DTYPE_BF16 1
+#define MOE_FFN_SILU 0   /* y = W_down^T silu(W_up^T x)                        */
+#define MOE_FFN_SWIGLU 1 /* y = W_down^T (silu(W_gate^T x) * (W_up^T x))        */
+
+typedef struct {
+    int32_t T;               /* tokens                                          */
+    int32_t d;               /* model width                                     */
+    int32_t f;               /* expert hidden width                             */
+    int32_t E;               /* experts, 1..64                                  */
+    int32_t k;               /* experts per token, 1..min(E, 8)                 */
+    float capacity_factor;   /* <= 0: no limit; else C = ceil(cf*T*k/E), in IEEE
+                                double from this fp32 value, clamped to T        */
+    int32_t ffn;             /* MOE_FFN_SILU or MOE_FFN_SWIGLU                   */
+    int32_t dtype;           /* MOE_DTYPE_F32 or MOE_DTYPE_BF16                  */
+    int32_t normalize_gates; /* 1: gates = softmax over the k selected logits (sum
+                                to 1 before drops); 0: raw softmax probabilities */
+    float aux_coef;          /* lambda of L_aux = lambda * sum_e (pbar_e - 1/E)^2 */
+    int32_t pad_m;           /* rows of each expert segment are padded to a
+                                multiple of pad_m; bf16 needs a multiple of 128  */
+} moe_config;
+
+/* ---- statistics vector written by moe_route / moe_permute (fp32, 8 + E) ---- */
+#define MOE_STAT_AUX_LOSS 0      /* lambda * sum_e (pbar_e - 1/E)^2   [ZeRO3-MoE] §3.2 */
+#define MOE_STAT_AUX_SWITCH 1    /* E * sum_e f_e pbar_e, f = counts/(T k) [LLaMA4-MoE] §3.2 */
+#define MOE_STAT_ENTROPY 2       /* mean over tokens of -sum_e p log p  [LLaMA4-MoE] §3.3 */
+#define MOE_STAT_NONFINITE 3     /* tokens with a NaN/Inf logit                      */
+#define MOE_STAT_DROPPED 4       /* assignments dropped by capacity (moe_permute)    */
+#define MOE_STAT_MAX_OVER_MEAN_KEPT 5  /* max_e kept_e / mean_e kept_e (moe_permute) */
+#define MOE_STAT_COUNT_CV 6      /* std/mean of counts over experts                  */
+#define MOE_STAT_MAX_OVER_MEAN_COUNT 7
+#define MOE_STAT_PBAR 8          /* pbar[0..E): mean softmax probability per expert  */
+#define MOE_STATS_LEN(E) (8 + (E))
+
+/* Validate a configuration.  MOE_OK, MOE_ERR_INVALID_ARG (impossible shape)
+ * or MOE_ERR_UNSUPPORTED (bf16 needs d % 128 == 0, f % 128 == 0 and
+ * pad_m % 128 == 0; E <= 64; k <= 8).                                         */
+MOE_API int moe_check_config(const moe_config* cfg);
+
+/* Per-expert capacity C (T when there is no limit).  [ZeRO3-MoE] §3.1, §3.4  */
+MOE_API int moe_capacity(const moe_config* cfg, int32_t* capacity);
+
+/* Worst-case row count of the permuted buffers (x_perm, act, y_perm, ...):
+ * min(T*k, E*C) + E*(pad_m - 1).  Each buffer holds rows_cap rows.            */
+MOE_API int moe_rows_capacity(const moe_config* cfg, int64_t* rows_cap);
+
+/* Bytes of scratch `ws` that every entry point below may use (the maximum
+ * over all of them, including moe_backward's intermediate gradients).        */
+MOE_API int moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* ---- forward ---- */
+
+/* Router: logits = x W_r (+ bias) (+ noise) in fp32 accumulation; softmax;
+ * top-k (largest logits; ties to the lowest expert id; NaN ranks lowest),
+ * slot j = rank j; gates; per-expert selection counts; statistics.
+ *   x[T,d] act dtype; W_r[d,E] act dtype; bias[E] fp32 or NULL;
+ *   noise[T,E] fp32 or NULL (gate noise drawn by the caller, [LLaMA4-MoE] §3.2);
+ *   out: logits[T,E] fp32, topk_idx[T,k] int32, gate[T,k] fp32,
+ *        counts[E] int32, stats[8+E] fp32 (entries 4 and 5 by moe_permute).
+ * [LLaMA4-MoE] §2.4; [Twinkle] §3.1; [ZeRO3-MoE] §5.3.                         */
+MOE_API int moe_route(const moe_config* cfg, const void* x, const void* W_r, const float* bias,
+              const float* noise, float* logits, int32_t* topk_idx, float* gate,
+              int32_t* counts, float* stats, void* ws, moe_stream_t stream);
+
+/* Capacity + permutation: rank each assignment (t, j) among its expert's
+ * assignments in ascending token order; keep it iff rank < C; lay experts out
+ * contiguously (segment e = rows offsets[e]..offsets[e+1], kept[e] real rows
+ * then zero rows up to a multiple of pad_m) and gather x rows into x_perm.
+ *   in : x[T,d], topk_idx[T,k]
+ *   out: x_perm[rows_cap,d] (rows >= offsets[E] untouched), perm_token[rows_cap]
+ *        (token of each row, -1 on padding rows), slot_of[T,k] (row of (t,j),
+ *        -1 if dropped), kept[E], offsets[E+1]; stats (may be NULL) gets
+ *        MOE_STAT_DROPPED and MOE_STAT_MAX_OVER_MEAN_KEPT.
+ * [LLaMA4-MoE] §2.4 (sort by expert id, split by counts); [ZeRO3-MoE] §3.1.   */
+MOE_API int moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                void* x_perm, int32_t* perm_token, int32_t* slot_of, int32_t* kept,
+                int32_t* offsets, float* stats, void* ws, moe_stream_t stream);
+
+/* Grouped expert FFN over the segments given by offsets (read on the device).
+ *   SiLU  : h = x_perm W_up[e]; act = silu(h); y = act W_down[e]
+ *   SwiGLU: g = x_perm W_gate[e]; u = x_perm W_up[e]; act = silu(g)*u; y = act W_down[e]
+ *   h_saved[nh,rows_cap,f] (nh = 1: h; nh = 2: g then u), act[rows_cap,f],
+ *   y_perm[rows_cap,d]; all act dtype; W_gate may be NULL for SiLU.
+ * [LLaMA4-MoE] §2.4 (each expert a two-layer FFN).                            */
+MOE_API int moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                    const void* W_up, const void* W_gate, const void* W_down,
+                    void* h_saved, void* act, void* y_perm, void* ws, moe_stream_t stream);
+
+/* Combine: out[t] = sum over kept slots j (ascending) of gate[t,j] * y_perm[slot_of[t,j]],
+ * fp32 accumulation; a token whose slots were all dropped gets zeros.
+ * [LLaMA4-MoE] §2.4 (weighted by the post-softmax routing score).             */
+MOE_API int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_of,
+                const float* gate, void* out, moe_stream_t stream);
+
+/* ---- backward of  L = <dout, out> + L_aux  ---- */
+
+/* Combine backward: dy_perm[r] = gate[t,j] * dout[t] for r = slot_of[t,j],
+ * zero on padding rows; dgate[t,j] = <dout[t], y_perm[r]> (0 if dropped).     */
+MOE_API int moe_combine_backward(const moe_config* cfg, const void* dout, const void* y_perm,
+                         const float* gate, const int32_t* slot_of, const int32_t* perm_token,
+                         const int32_t* offsets, void* dy_perm, float* dgate,
+                         moe_stream_t stream);
+
+/* Grouped FFN backward.  dact = dy W_down[e]^T; dh = dact * silu'(h)
+ * (SwiGLU: du = dact * silu(g), dg = dact * u * silu'(g));
+ * dW_down[e] = act_e^T dy_e; dW_up[e] = x_e^T dh_e (dW_gate[e] = x_e^T dg_e),
+ * each summed over expert e's rows only (a variable-length reduction);
+ * dx_perm = dh W_up[e]^T (+ dg W_gate[e]^T).
+ *   dh[nh,rows_cap,f] act dtype is an output buffer of intermediate gradients
+ *   (nh as h_saved: dh, or dg then du); dx_perm[rows_cap,d];
+ *   dW_up/dW_gate[E,d,f], dW_down[E,f,d] act dtype.                           */
+MOE_API int moe_grouped_ffn_backward(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                             const void* W_up, const void* W_gate, const void* W_down,
+                             const void* h_saved, const void* act, const void* dy_perm,
+                             void* dh, void* dx_perm, void* dW_up, void* dW_gate, void* dW_down,
+                             void* ws, moe_stream_t stream);
+
+/* Router backward.  dlogits[t] = gate softmax Jacobian applied to dgate
+ * (selected logits only) + aux term lambda*2(pbar-1/E)/T through the full
+ * softmax; dx[t] = sum over kept slots of dx_perm[slot] + dlogits[t] W_r^T;
+ * dW_r = x^T dlogits; dbias = sum_t dlogits (if non-NULL).
+ *   stats: the moe_route statistics of the same forward (pbar is used).
+ *   dlogits[T,E] fp32 output (may be NULL: then ws is used).
+ * [LLaMA4-MoE] §2.4 (do not detach the routing weights).                      */
+MOE_API int moe_router_backward(const moe_config* cfg, const void* x, const void* W_r,
+                        const float* logits, const int32_t* topk_idx, const float* gate,
+                        const int32_t* slot_of, const float* dgate, const void* dx_perm,
+                        const float* stats, void* dx, void* dW_r, float* dbias, float* dlogits,
+                        void* ws, moe_stream_t stream);
+
+/* Whole backward: moe_combine_backward -> moe_grouped_ffn_backward ->
+ * moe_router_backward, intermediates in ws.  Saved forward tensors as above. */
+MOE_API int moe_backward(const moe_config* cfg, const void* x, const void* W_r, const void* W_up,
+                 const void* W_gate, const void* W_down, const float* logits,
+                 const int32_t* topk_idx, const float* gate, const int32_t* slot_of,
+                 const int32_t* perm_token, const int32_t* offsets, const void* x_perm,
+                 const void* h_saved, const void* act, const void* y_perm, const float* stats,
+                 const void* dout, void* dx, void* dW_r, float* dbias, void* dW_up,
+                 void* dW_gate, void* dW_down, void* ws, moe_stream_t stream);
+
+/* ---- status and bookkeeping ---- */
+
+/* Text of a status code (static storage). */
+MOE_API const char* moe_error_string(int code);
+
+/* Synchronise `stream`, then read and clear the device status word of the
+ * current device (*status = MOE_OK or a MOE_ERR_* recorded by a kernel).     */
+MOE_API int moe_last_device_status(moe_stream_t stream, int* status);
+
+/* Number of kernels this library has launched in this process (host counter). */
+MOE_API uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_MOE_H */

@@ -78,7 +78,8 @@ def lib():
         _lib.oracle_capacity.restype = ctypes.c_int
         _lib.oracle_route.restype = ctypes.c_int
         for name in ("oracle_router_logits", "oracle_permute", "oracle_combine", "oracle_stats",
-                     "oracle_forward", "oracle_backward", "oracle_expert_apply"):
+                     "oracle_forward", "oracle_backward", "oracle_expert_apply",
+                     "oracle_expert_forward"):
             getattr(_lib, name).restype = None
     return _lib
 
@@ -136,6 +137,17 @@ def expert_apply(cfg, e, x_row, Wup, Wgate, Wdown):
     return y
 
 
+def expert_forward(cfg, e, x_row, Wup, Wdown, Wgate=None):
+    """One expert on one token: dict(h, u, act, y) (h is g for SwiGLU; u None for SiLU)."""
+    f, d = cfg.f, cfg.d
+    h, act, y = np.empty(f), np.empty(f), np.empty(d)
+    u = np.empty(f) if cfg.swiglu else None
+    lib().oracle_expert_forward(ctypes.byref(cfg.c()), int(e), _p(_d(x_row)), _p(_d(Wup)),
+                                _p(_d(Wgate) if cfg.swiglu else None), _p(_d(Wdown)), _p(h),
+                                _p(u), _p(act), _p(y))
+    return dict(h=h, u=u, act=act, y=y)
+
+
 def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in=None):
     """Steps 1-9. ``logits_in`` (e.g. the GPU's fp32 logits) replaces step 1."""
     x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
@@ -154,7 +166,7 @@ def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in
 
 
 def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgate=None,
-             with_bias=False):
+             with_bias=False, per_slot=False):
     """Step 10: gradients of <dout, out> + aux loss (written, not accumulated)."""
     x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
     logits, gate, dout = _d(logits), _d(gate), _d(dout)
@@ -163,9 +175,11 @@ def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgat
     T, E, k, d, f = cfg.T, cfg.E, cfg.k, cfg.d, cfg.f
     g = dict(dx=np.empty((T, d)), dWr=np.empty((d, E)), db=np.empty(E) if with_bias else None,
              dWup=np.empty((E, d, f)), dWgate=np.empty((E, d, f)) if cfg.swiglu else None,
-             dWdown=np.empty((E, f, d)), dgate=np.empty((T, k)), dlogits=np.empty((T, E)))
+             dWdown=np.empty((E, f, d)), dgate=np.empty((T, k)), dlogits=np.empty((T, E)),
+             dh_slot=np.empty((T, k, 2 if cfg.swiglu else 1, f)) if per_slot else None,
+             dxp_slot=np.empty((T, k, d)) if per_slot else None)
     lib().oracle_backward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(Wup), _p(Wgate), _p(Wdown),
                           _p(logits), _p(topk_idx), _p(gate), _p(slot_of), _p(dout),
                           *[_p(g[n]) for n in ("dx", "dWr", "db", "dWup", "dWgate", "dWdown",
-                                               "dgate", "dlogits")])
+                                               "dgate", "dlogits", "dh_slot", "dxp_slot")])
     return g

@@ -215,6 +215,19 @@ static void expert_ffn(const oracle_cfg* c, const double* x, const double* Wu,
     }
 }
 
+/* One expert on one token with its intermediates: h (SiLU: W_up^T x; SwiGLU:
+ * g = W_gate^T x), u (SwiGLU only; may be NULL), act, y.                      */
+void oracle_expert_forward(const oracle_cfg* c, int e, const double* x, const double* Wup,
+                           const double* Wgate, const double* Wdown, double* h, double* u,
+                           double* act, double* y)
+{
+    const size_t df = (size_t)c->d * c->f;
+    double* tmp = NULL;
+    if (c->swiglu && !u) u = tmp = (double*)malloc(sizeof(double) * (size_t)c->f);
+    expert_ffn(c, x, Wup + e * df, c->swiglu ? Wgate + e * df : NULL, Wdown + e * df, h, u, act, y);
+    free(tmp);
+}
+
 /* One expert's FFN output on one token (for sampled checks and special cases). */
 void oracle_expert_apply(const oracle_cfg* c, int e, const double* x, const double* Wup,
                          const double* Wgate, const double* Wdown, double* y)
@@ -322,13 +335,16 @@ void oracle_forward(const oracle_cfg* c, const double* x, const double* Wr, cons
  * itself is piecewise constant  ([LLaMA4-MoE] §2.4: do not detach the
  * routing weights).  Outputs are written, not accumulated.
  * dx[T,d], dWr[d,E], db[E] (may be NULL), dWup/dWgate[E,d,f], dWdown[E,f,d],
- * dgate[T,k] and dlogits[T,E] (both may be NULL).                             */
+ * dgate[T,k] and dlogits[T,E] (both may be NULL).  Optional per-slot views of
+ * the expert path (NULL = not wanted): dh_slot[T,k,nh,f] holds dh (SiLU) or
+ * dg then du (SwiGLU); dxp_slot[T,k,d] holds the slot's dx contribution.      */
 void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
                      const double* Wup, const double* Wgate, const double* Wdown,
                      const double* logits, const int* topk, const double* gate,
                      const int* slot_of, const double* dout,
                      double* dx, double* dWr, double* db, double* dWup, double* dWgate,
-                     double* dWdown, double* dgate_out, double* dlogits_out)
+                     double* dWdown, double* dgate_out, double* dlogits_out,
+                     double* dh_slot_out, double* dxp_slot_out)
 {
     const int T = c->T, d = c->d, f = c->f, E = c->E, k = c->k;
     const size_t df = (size_t)d * f;
@@ -377,6 +393,14 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
                         dh[q] = da[q] * u[q] * dsilu(h[q]);  /* d/dg             */
                     } else {
                         dh[q] = da[q] * dsilu(h[q]);
+                    }
+                }
+                if (dh_slot_out) {
+                    const int nh = c->swiglu ? 2 : 1;
+                    double* o = dh_slot_out + ((size_t)t * k + j) * nh * f;
+                    for (int q = 0; q < f; ++q) {
+                        o[q] = dh[q];
+                        if (c->swiglu) o[f + q] = du[q];
                     }
                 }
                 /* h = Wu^T x (SiLU) ; g = Wg^T x, u = Wu^T x (SwiGLU) */
@@ -476,6 +500,7 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
             db[e] = acc;
         }
     if (dgate_out) memcpy(dgate_out, dgate, sizeof(double) * (size_t)T * k);
+    if (dxp_slot_out) memcpy(dxp_slot_out, dxp, sizeof(double) * (size_t)T * k * d);
     if (dlogits_out) memcpy(dlogits_out, dl, sizeof(double) * (size_t)T * E);
     free(dgate); free(dxp); free(probs); free(pbar); free(dl); free(cvec);
 }

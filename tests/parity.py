@@ -1,0 +1,227 @@
+"""Helpers for GPU-vs-oracle parity tests (imported by tests and the smoke check).
+
+The CUDA path runs through the C ABI (the ctypes binding); the oracle runs on
+the same seeded inputs in fp64.  Comparisons:
+  * routing indices, counts, offsets, permutation: bit-exact, with the oracle's
+    route stage fed the GPU's fp32 logits (the same values decide the top-k);
+  * floating-point tensors: relative Frobenius error within the tolerance of
+    the layer dtype (1e-5 fp32, 2e-2 bf16);
+  * independent routing (oracle logits in fp64): identical top-k except on
+    tokens whose k-th / (k+1)-th logit gap is below 1e-4, which are counted.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import moe_inputs
+import oracle
+import top_routing_expert_moe_gb300 as moe
+
+TOL = {"fp32": 1e-5, "bf16": 2e-2}
+NEAR_TIE = 1e-4
+
+
+def rel_fro(got, want) -> float:
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    den = float(np.linalg.norm(want))
+    num = float(np.linalg.norm(got - want))
+    return num / den if den > 0 else num
+
+
+def to_torch(a, dtype: str, device="cuda"):
+    if a is None:
+        return None
+    if dtype == "bf16" and a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def np64(t) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def gpu_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True) -> moe.MoEConfig:
+    return moe.MoEConfig(T=w.T, d=w.d, f=w.f, E=w.E, k=w.k,
+                         capacity_factor=w.capacity_factor,
+                         ffn=moe.SWIGLU if w.swiglu else moe.SILU,
+                         dtype=moe.BF16 if w.dtype == "bf16" else moe.F32,
+                         normalize_gates=1 if normalize else 0, aux_coef=w.aux_coef, pad_m=pad_m)
+
+
+def oracle_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True) -> oracle.OracleConfig:
+    return oracle.OracleConfig(T=w.T, d=w.d, f=w.f, E=w.E, k=w.k,
+                               capacity_factor=float(np.float32(w.capacity_factor)),
+                               swiglu=w.swiglu, normalize_gates=normalize,
+                               aux_coef=float(np.float32(w.aux_coef)), pad_m=pad_m)
+
+
+def f64_inputs(w, inp):
+    return {k: moe_inputs.as_f64(v, w.dtype if k not in ("bias", "noise") else "fp32")
+            for k, v in inp.items()}
+
+
+def run_gpu(w, inp, pad_m=128, normalize=True, backward=True):
+    """Forward (and the backward sub-steps with their intermediates) on the GPU."""
+    cfg = gpu_cfg(w, pad_m, normalize)
+    dt = w.dtype
+    x = to_torch(inp["x"], dt)
+    Wr = to_torch(inp["W_r"], dt)
+    Wu = to_torch(inp["W_up"], dt)
+    Wg = to_torch(inp.get("W_gate"), dt)
+    Wd = to_torch(inp["W_down"], dt)
+    b = to_torch(inp.get("bias"), "fp32")
+    nz = to_torch(inp.get("noise"), "fp32")
+    L = moe.MoELayer(cfg)
+    L.forward(x, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz)
+    res = dict(cfg=cfg, layer=L)
+    if backward:
+        dout = to_torch(inp["dout"], dt)
+        R, dev, tdt = L.rows_cap, x.device, cfg.torch_dtype
+        dy = torch.empty(R, w.d, dtype=tdt, device=dev)
+        dgate = torch.empty(w.T, w.k, dtype=torch.float32, device=dev)
+        dh = torch.empty(cfg.nh, R, w.f, dtype=tdt, device=dev)
+        dxp = torch.empty(R, w.d, dtype=tdt, device=dev)
+        dlogits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
+        g = L.grads()
+        moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token, L.offsets,
+                                 dy, dgate)
+        moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, dy,
+                                     dh, dxp, g["dW_up"], g["dW_gate"], g["dW_down"], L.ws)
+        moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of, dgate, dxp,
+                                L.stats, g["dx"], g["dW_r"], g["dbias"] if b is not None else None,
+                                dlogits, L.ws)
+        res.update(dy=dy, dgate=dgate, dh=dh, dxp=dxp, dlogits=dlogits, grads=g, dout=dout)
+    torch.cuda.synchronize()
+    res["status"] = moe.last_device_status()
+    return res
+
+
+def check_routing(w, ocfg, r, inp64, report):
+    """Route/permute parity.  Returns the conditioned oracle forward."""
+    L = r["layer"]
+    logits = np64(L.logits)
+    # logits vs fp64 oracle
+    ol = oracle.router_logits(ocfg, inp64["x"], inp64["W_r"], inp64.get("bias"), inp64.get("noise"))
+    report["logits_rel"] = rel_fro(logits, ol)
+    # conditioned oracle: route the GPU's fp32 logits
+    o = oracle.forward(ocfg, inp64["x"], inp64["W_r"], inp64["W_up"], inp64["W_down"],
+                       Wgate=inp64.get("W_gate"), logits_in=logits)
+    topk = L.topk_idx.cpu().numpy()
+    assert (topk == o["topk_idx"]).all(), "top-k differs from the oracle on the same logits"
+    assert (L.counts.cpu().numpy() == o["counts"]).all(), "counts differ"
+    assert (L.kept.cpu().numpy() == o["kept"]).all(), "kept differs"
+    assert (L.offsets.cpu().numpy() == o["offsets"]).all(), "offsets differ"
+    rows = int(o["offsets"][-1])
+    assert (L.perm_token.cpu().numpy()[:rows] == o["perm_token"]).all(), "perm_token differs"
+    assert (L.slot_of.cpu().numpy() == o["slot_of"]).all(), "slot_of differs"
+    report["gate_rel"] = rel_fro(np64(L.gate), o["gate"])
+    st = np64(L.stats)
+    report["pbar_rel"] = rel_fro(st[moe.STAT_PBAR:], o["stats"][oracle.ST_PBAR:])
+    report["aux_loss"] = (float(st[moe.STAT_AUX_LOSS]), float(o["stats"][oracle.ST_AUX_LOSS]))
+    for i in (moe.STAT_AUX_SWITCH, moe.STAT_ENTROPY):
+        assert abs(st[i] - o["stats"][i]) <= 1e-4 * max(1.0, abs(o["stats"][i])), (i, st[i], o["stats"][i])
+    assert abs(st[moe.STAT_AUX_LOSS] - o["stats"][oracle.ST_AUX_LOSS]) <= \
+        1e-3 * abs(o["stats"][oracle.ST_AUX_LOSS]) + 1e-9
+    for i in (moe.STAT_NONFINITE, moe.STAT_DROPPED):
+        assert st[i] == o["stats"][i], (i, st[i], o["stats"][i])
+    for i in (moe.STAT_MAX_OVER_MEAN_KEPT, moe.STAT_COUNT_CV, moe.STAT_MAX_OVER_MEAN_COUNT):
+        assert abs(st[i] - o["stats"][i]) <= 1e-5 * max(1.0, abs(o["stats"][i])), (i, st[i], o["stats"][i])
+    # independent routing (oracle's own fp64 logits)
+    oi = oracle.route(ocfg, ol)
+    srt = -np.sort(-ol, axis=1)
+    gap = srt[:, ocfg.k - 1] - srt[:, ocfg.k] if ocfg.k < ocfg.E else np.full(ocfg.T, np.inf)
+    near = gap < NEAR_TIE
+    same = (np.sort(oi["topk_idx"], 1) == np.sort(topk, 1)).all(1)
+    report["near_tie_tokens"] = int(near.sum())
+    report["independent_mismatch_excluded"] = int((~same & near).sum())
+    assert same[~near].all(), f"independent routing differs on {int((~same & ~near).sum())} clear tokens"
+    return o
+
+
+def check_forward(w, ocfg, r, o, inp64, report, sample_rows=None):
+    L = r["layer"]
+    tol = TOL[w.dtype]
+    rows = int(o["offsets"][-1])
+    # x_perm rows are exact copies; padding rows zero
+    xp = np64(L.x_perm)[:rows]
+    perm = o["perm_token"]
+    real = perm >= 0
+    assert np.array_equal(xp[real], inp64["x"][perm[real]]), "x_perm rows differ"
+    assert (xp[~real] == 0).all(), "padding rows of x_perm are not zero"
+    # per-row expert stage (sampled)
+    idx = np.nonzero(real)[0]
+    if sample_rows is not None and len(idx) > sample_rows:
+        idx = np.sort(np.random.default_rng(0).choice(idx, sample_rows, replace=False))
+    row_e = np.searchsorted(o["offsets"], idx, side="right") - 1
+    H = np64(L.h_saved)
+    A = np64(L.act)
+    Y = np64(L.y_perm)
+    want_h, want_u, want_a, want_y = [], [], [], []
+    for rr, e in zip(idx, row_e):
+        ef = oracle.expert_forward(ocfg, e, inp64["x"][perm[rr]], inp64["W_up"], inp64["W_down"],
+                                   inp64.get("W_gate"))
+        want_h.append(ef["h"]); want_a.append(ef["act"]); want_y.append(ef["y"])
+        if ocfg.swiglu:
+            want_u.append(ef["u"])
+    report["h_rel"] = rel_fro(H[0][idx], np.array(want_h))
+    if ocfg.swiglu:
+        report["u_rel"] = rel_fro(H[1][idx], np.array(want_u))
+    report["act_rel"] = rel_fro(A[idx], np.array(want_a))
+    report["y_rel"] = rel_fro(Y[idx], np.array(want_y))
+    report["out_rel"] = rel_fro(np64(L.out), o["out"])
+    for key in ("h_rel", "u_rel", "act_rel", "y_rel", "out_rel"):
+        if key in report:
+            assert report[key] <= tol, (key, report[key], tol)
+
+
+def check_backward(w, ocfg, r, o, inp64, report, with_bias):
+    L = r["layer"]
+    tol = TOL[w.dtype]
+    logits = np64(L.logits)
+    ob = oracle.backward(ocfg, inp64["x"], inp64["W_r"], inp64["W_up"], inp64["W_down"], logits,
+                         o["topk_idx"], o["gate"], o["slot_of"], inp64["dout"],
+                         Wgate=inp64.get("W_gate"), with_bias=with_bias, per_slot=True)
+    g = r["grads"]
+    slot = o["slot_of"]
+    kept = slot >= 0
+    # dgate and the per-slot intermediates
+    report["dgate_rel"] = rel_fro(np64(r["dgate"]), ob["dgate"])
+    tt, jj = np.nonzero(kept)
+    rows = slot[tt, jj]
+    dy = np64(r["dy"])
+    gate = o["gate"]
+    report["dy_rel"] = rel_fro(dy[rows], gate[tt, jj][:, None] * inp64["dout"][tt])
+    pad_rows = np.nonzero(o["perm_token"] < 0)[0]
+    assert (dy[pad_rows] == 0).all(), "padding rows of dy_perm are not zero"
+    dh = np64(r["dh"])
+    report["dh_rel"] = rel_fro(dh[0][rows], ob["dh_slot"][tt, jj, 0])
+    if ocfg.swiglu:
+        report["du_rel"] = rel_fro(dh[1][rows], ob["dh_slot"][tt, jj, 1])
+    report["dxp_rel"] = rel_fro(np64(r["dxp"])[rows], ob["dxp_slot"][tt, jj])
+    report["dlogits_rel"] = rel_fro(np64(r["dlogits"]), ob["dlogits"])
+    report["dx_rel"] = rel_fro(np64(g["dx"]), ob["dx"])
+    report["dWr_rel"] = rel_fro(np64(g["dW_r"]), ob["dWr"])
+    report["dWup_rel"] = rel_fro(np64(g["dW_up"]), ob["dWup"])
+    report["dWdown_rel"] = rel_fro(np64(g["dW_down"]), ob["dWdown"])
+    if ocfg.swiglu:
+        report["dWgate_rel"] = rel_fro(np64(g["dW_gate"]), ob["dWgate"])
+    if with_bias:
+        report["db_rel"] = rel_fro(np64(g["dbias"]), ob["db"])
+    for key, v in list(report.items()):
+        if key.startswith("d") and key.endswith("_rel"):
+            assert v <= tol, (key, v, tol)
+
+
+def full_check(w, inp, pad_m=128, normalize=True, backward=True, sample_rows=None):
+    report = {}
+    r = run_gpu(w, inp, pad_m=pad_m, normalize=normalize, backward=backward)
+    assert r["status"] == 0, f"device status {r['status']}"
+    ocfg = oracle_cfg(w, pad_m, normalize)
+    inp64 = f64_inputs(w, inp)
+    o = check_routing(w, ocfg, r, inp64, report)
+    check_forward(w, ocfg, r, o, inp64, report, sample_rows=sample_rows)
+    if backward:
+        check_backward(w, ocfg, r, o, inp64, report, with_bias=inp.get("bias") is not None)
+    return report, r

@@ -1,0 +1,682 @@
+// gemm_tc.cu -- persistent tcgen05 grouped GEMM over expert segments (sm_103a).
+//
+// Every expert-FFN contraction of the layer ([LLaMA4-MoE] §2.4: each expert a
+// two-layer FFN over the tokens routed to it) is one launch of this kernel:
+//   forward   h|g,u = x_perm W_up|W_gate  (activation fused in the epilogue)
+//             y     = act W_down
+//   backward  dact  = dy W_down^T          (silu' / SwiGLU derivative fused)
+//             dW    = x^T dh, act^T dy     (reduction over each expert's rows)
+//             dx    = dh W_up^T (+ dg W_gate^T)
+//
+// Design (one CTA per SM, 192 threads, warp-specialised):
+//   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
+//               (BN x 64) into a 4-stage shared-memory ring (mbarrier tx).
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (M=128, N=BN, K=16, bf16 in, fp32 accumulate) and commits to
+//               the ring's "empty" barriers and to a double-buffered TMEM
+//               accumulator's "full" barrier.
+//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time from TMEM, fused
+//               activation math, bf16 stores; frees the accumulator so the
+//               next tile's MMAs overlap this tile's epilogue.
+// Tiles come from a static persistent schedule whose per-expert tile counts
+// are read from the device-side segment offsets, so no host sync separates
+// routing from the GEMMs.  Within an expert, tiles are visited in groups of
+// 16 M-blocks so the A rows and B columns in flight stay L2-resident.
+//
+// Shared-memory operand layouts (canonical 128B-swizzle layouts):
+//   K-major   rows of 64 bf16 (128 B); 8-row groups 1024 B apart (SBO);
+//             the K=16 step advances the start address by 32 B.
+//   MN-major  boxes of 64 k-rows x 64 MN-elements (8 KB); 8-k-row groups
+//             1024 B apart (SBO); MN boxes 8 KB apart (LBO); the K=16 step
+//             advances the start address by 2048 B.
+//
+// Every mbarrier wait is bounded (globaltimer): on expiry the kernel records
+// MOE_ERR_TIMEOUT, tells the other roles to stop, drains its own TMA loads and
+// MMAs (again bounded), frees TMEM and returns.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm_tc.h"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + 256 * BK * 2;  // 48 KB
+constexpr int GUARD_BYTES = 16 * 1024;        // slack after the ring
+constexpr int CTRL_BYTES = 1024;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + GUARD_BYTES + CTRL_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int NTHREADS = 192;
+constexpr int RASTER_GM = 16;
+constexpr unsigned long long WAIT_NS = 4000000000ull;   // 4 s
+constexpr unsigned long long DRAIN_NS = 500000000ull;   // 0.5 s
+
+enum Epi { EPI_STORE = 0, EPI_SILU_FWD = 1, EPI_SWIGLU_FWD = 2, EPI_SILU_BWD = 3, EPI_SWIGLU_BWD = 4 };
+enum Sched { SCHED_ROWS = 0, SCHED_KSEG = 1 };
+
+struct TcParams {
+    CUtensorMap tmA0, tmB0, tmA1, tmB1;
+    const int32_t* offsets;
+    __nv_bfloat16* out0;
+    __nv_bfloat16* out1;
+    __nv_bfloat16* out2;
+    const __nv_bfloat16* in0;
+    const __nv_bfloat16* in1;
+    int* status;
+    long long out_estride;  // SCHED_KSEG: elements between experts' outputs
+    int sched, E;
+    int n_blocks;           // N / bn
+    int m_blocks;           // SCHED_KSEG: M / 128
+    int k_blocks;           // SCHED_ROWS: K / 64 (per operand pair)
+    int kconcat;            // SCHED_ROWS: 2 = K loop continues over (A1, B1)
+    int a_mn, b_mn;         // operand is MN-major in global memory
+    int bn;                 // 128 or 256
+    int dual;               // two accumulators (B0 -> cols 0..127, B1 -> 128..255)
+    int epi;
+    int ldo;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+// Bounded wait.  Returns false when the wait gave up (timeout or another
+// role's abort); the first to time out records the status and raises abort.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (*abort_flag) return false;
+            if (gtimer() - t0 > WAIT_NS) {
+                set_status(status, MOE_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+// Bounded wait used while draining (ignores the abort flag).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = gtimer();
+    while (!mbar_try(bar, parity))
+        if (gtimer() - t0 > DRAIN_NS) break;
+}
+
+__device__ __forceinline__ void tma_load3(const CUtensorMap* map, uint32_t dst, uint32_t bar, int c0,
+                                          int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;  // 128-byte swizzle
+    return d;
+}
+// kind::f16 instruction descriptor: bf16 x bf16 -> fp32, dense
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dtmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 fp32 -> 32 bf16 at p (64 bytes)
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float* v) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
+            w[j] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        q[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float* v) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 u = q[i];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+            v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- schedule
+struct Tile {
+    int e, m0, n0, krow0, nk;
+};
+
+// prefix[e] = first tile index of expert e; prefix[E] = total tiles
+__device__ __forceinline__ void decode_tile(const TcParams& p, const int* offs, const int* prefix,
+                                            int tix, Tile& t) {
+    int e = 0;
+    while (e + 1 < p.E && prefix[e + 1] <= tix) ++e;
+    const int local = tix - prefix[e];
+    const int mb_e = p.sched == SCHED_ROWS ? (offs[e + 1] - offs[e]) / BM : p.m_blocks;
+    const int gsz = RASTER_GM * p.n_blocks;
+    const int grp = local / gsz;
+    const int first = grp * RASTER_GM;
+    const int gm = min(RASTER_GM, mb_e - first);
+    const int r = local - grp * gsz;
+    const int mb = first + r % gm, nb = r / gm;
+    t.e = e;
+    t.n0 = nb * p.bn;
+    if (p.sched == SCHED_ROWS) {
+        t.m0 = offs[e] + mb * BM;
+        t.krow0 = 0;
+        t.nk = p.k_blocks * p.kconcat;
+    } else {
+        t.m0 = mb * BM;
+        t.krow0 = offs[e];
+        t.nk = (offs[e + 1] - offs[e]) / BK;
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ctrl = base + STAGES * STAGE_BYTES + GUARD_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* offs = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));  // [E+1]
+    int* prefix = offs + 66;                                                           // [E+1]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 4);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < p.E + 1) offs[tid] = p.offsets[tid];
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        int acc = 0;
+        for (int e = 0; e < p.E; ++e) {
+            prefix[e] = acc;
+            const int mb = p.sched == SCHED_ROWS ? (offs[e + 1] - offs[e]) / BM : p.m_blocks;
+            acc += mb * p.n_blocks;
+        }
+        prefix[p.E] = acc;
+    }
+    __syncthreads();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = prefix[p.E];
+    const uint32_t smem0 = smem_u32(base);
+    const uint32_t b_bytes = p.dual ? 2u * 128u * BK * 2u : (uint32_t)p.bn * BK * 2u;
+    const uint32_t stage_tx = (uint32_t)A_BYTES + b_bytes;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int it = 0;
+        bool ok = true;
+        for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x) {
+            Tile t;
+            decode_tile(p, offs, prefix, tix, t);
+            for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                const uint32_t bar = smem_u32(&full[s]);
+                const uint32_t sA = smem0 + s * STAGE_BYTES, sB = sA + A_BYTES;
+                mbar_expect_tx(bar, stage_tx);
+                if (p.sched == SCHED_KSEG) {
+                    const int kr = t.krow0 + kb * BK;
+                    tma_load3(&p.tmA0, sA, bar, t.m0, kr, 0);
+                    tma_load3(&p.tmA0, sA + 8192, bar, t.m0 + 64, kr, 0);
+                    for (int c = 0; c < p.bn / 64; ++c) tma_load3(&p.tmB0, sB + c * 8192, bar, t.n0 + 64 * c, kr, 0);
+                } else {
+                    const int phase = kb >= p.k_blocks ? 1 : 0;
+                    const int k0 = (kb - phase * p.k_blocks) * BK;
+                    tma_load3(phase ? &p.tmA1 : &p.tmA0, sA, bar, k0, t.m0, 0);
+                    if (p.dual) {
+                        tma_load3(&p.tmB0, sB, bar, t.n0, k0, t.e);
+                        tma_load3(&p.tmB0, sB + 8192, bar, t.n0 + 64, k0, t.e);
+                        tma_load3(&p.tmB1, sB + 16384, bar, t.n0, k0, t.e);
+                        tma_load3(&p.tmB1, sB + 24576, bar, t.n0 + 64, k0, t.e);
+                    } else if (p.b_mn) {
+                        for (int c = 0; c < p.bn / 64; ++c)
+                            tma_load3(&p.tmB0, sB + c * 8192, bar, t.n0 + 64 * c, k0, t.e);
+                    } else {
+                        tma_load3(phase ? &p.tmB1 : &p.tmB0, sB, bar, k0, t.n0, t.e);
+                    }
+                }
+            }
+        }
+        // drain: every load issued has landed before the CTA may exit
+        for (int i = max(0, it - STAGES); i < it; ++i)
+            mbar_drain(smem_u32(&full[i % STAGES]), (uint32_t)(i / STAGES) & 1u);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        const int nmma = p.dual ? 128 : p.bn;
+        const uint32_t idesc = idesc_bf16(BM, nmma, p.a_mn, p.b_mn);
+        int it = 0, tcount = 0;
+        bool ok = true;
+        for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x, ++tcount) {
+            Tile t;
+            decode_tile(p, offs, prefix, tix, t);
+            const int acc = tcount & 1;
+            const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
+            if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t dt = tmem_base + (uint32_t)(acc * 256);
+            uint32_t accum = 0;
+            for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sA = smem0 + s * STAGE_BYTES, sB = sA + A_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < BK / 16; ++ks) {
+                    const uint64_t ad = p.a_mn ? sdesc(sA + ks * 2048, 8192, 1024) : sdesc(sA + ks * 32, 16, 1024);
+                    if (p.dual) {
+                        mma_bf16(dt, ad, sdesc(sB + ks * 2048, 8192, 1024), idesc, accum);
+                        mma_bf16(dt + 128, ad, sdesc(sB + 16384 + ks * 2048, 8192, 1024), idesc, accum);
+                    } else {
+                        const uint64_t bd = p.b_mn ? sdesc(sB + ks * 2048, 8192, 1024) : sdesc(sB + ks * 32, 16, 1024);
+                        mma_bf16(dt, ad, bd, idesc, accum);
+                    }
+                    accum = 1;
+                }
+                mma_commit(smem_u32(&empty[s]));  // stage free once these MMAs finish
+            }
+            if (!ok) break;
+            mma_commit(smem_u32(&tfull[acc]));    // accumulator ready
+        }
+        mma_commit(smem_u32(drain));
+        mbar_drain(smem_u32(drain), 0);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        const int width = p.dual ? 128 : p.bn;
+        int tcount = 0;
+        for (int tix = blockIdx.x; tix < total; tix += gridDim.x, ++tcount) {
+            Tile t;
+            decode_tile(p, offs, prefix, tix, t);
+            const int acc = tcount & 1;
+            const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
+            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, p.status)) break;
+            tc_fence_after();
+            const long long row = (long long)t.m0 + row_in_tile;
+            const long long obase = (p.sched == SCHED_KSEG ? (long long)t.e * p.out_estride : 0) +
+                                    row * p.ldo + t.n0;
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(q * 32) << 16);
+            for (int c = 0; c < width / 32; ++c) {
+                float v[32];
+                if (t.nk == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    store32_bf16(p.out0 + obase + c * 32, v);
+                    continue;
+                }
+                tmem_ld32(taddr + c * 32, v);
+                if (p.epi == EPI_SWIGLU_FWD) {
+                    float u[32];
+                    tmem_ld32(taddr + 128 + c * 32, u);
+                    tmem_wait_ld();
+                    store32_bf16(p.out0 + obase + c * 32, v);
+                    store32_bf16(p.out1 + obase + c * 32, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * u[i];
+                    store32_bf16(p.out2 + obase + c * 32, v);
+                    continue;
+                }
+                tmem_wait_ld();
+                if (p.epi == EPI_STORE) {
+                    store32_bf16(p.out0 + obase + c * 32, v);
+                } else if (p.epi == EPI_SILU_FWD) {
+                    store32_bf16(p.out0 + obase + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]);
+                    store32_bf16(p.out1 + obase + c * 32, v);
+                } else if (p.epi == EPI_SILU_BWD) {
+                    float h[32];
+                    load32_bf16(p.in0 + obase + c * 32, h);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= dsilu_f(h[i]);
+                    store32_bf16(p.out0 + obase + c * 32, v);
+                } else {  // EPI_SWIGLU_BWD: v = dact
+                    float g[32], u[32], o[32];
+                    load32_bf16(p.in0 + obase + c * 32, g);
+                    load32_bf16(p.in1 + obase + c * 32, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = v[i] * u[i] * dsilu_f(g[i]);
+                    store32_bf16(p.out0 + obase + c * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = v[i] * silu_f(g[i]);
+                    store32_bf16(p.out1 + obase + c * 32, o);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 map: dims {d0 (contiguous), d1, d2}, byte strides {s1, s2}, box {b0, b1, 1}
+int make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+             uint64_t s2, uint32_t b0, uint32_t b1) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return MOE_ERR_CUDA;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// activations [rows_cap, cols]: K-major box {64, 128} or MN-major box {64, 64}
+int act_map(CUtensorMap* m, const void* ptr, int64_t rows_cap, int cols, bool mn_major) {
+    return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows_cap, 1, (uint64_t)cols * 2,
+                    (uint64_t)cols * 2 * rows_cap, 64, mn_major ? 64 : BM);
+}
+// expert weights [E, rows, cols]: MN-major box {64, 64} or K-major box {64, bn}
+int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool mn_major, int bn) {
+    return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)E, (uint64_t)cols * 2,
+                    (uint64_t)cols * 2 * rows, 64, mn_major ? 64 : (uint32_t)bn);
+}
+
+int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
+
+int launch_tc(TcParams& p, int64_t max_tiles, cudaStream_t st) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 64 && !attr_done[dev]) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(tc_grouped_gemm_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+        attr_done[dev] = true;
+    }
+    p.status = device_status_ptr();
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, num_sms()));
+    tc_grouped_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(p);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+TcParams base_params(const moe_config& c, const int32_t* offsets) {
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    p.offsets = offsets;
+    p.E = c.E;
+    p.kconcat = 1;
+    return p;
+}
+
+#define MOE_TRY(x)                \
+    do {                          \
+        int _r = (x);             \
+        if (_r != MOE_OK) return _r; \
+    } while (0)
+
+}  // namespace
+
+size_t tc_ws_bytes(const moe_config&) { return 0; }
+
+int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                   const void* W_up, const void* W_gate, const void* W_down, void* h_saved,
+                   void* act, void* y_perm, void*, cudaStream_t st)
+{
+    using bf = __nv_bfloat16;
+    const int64_t rc = rows_cap_of(c);
+    const int d = c.d, f = c.f, E = c.E;
+    const bool sw = c.ffn == MOE_FFN_SWIGLU;
+    // GEMM1 (+ activation)
+    {
+        TcParams p = base_params(c, offsets);
+        p.sched = SCHED_ROWS;
+        p.k_blocks = d / BK;
+        MOE_TRY(act_map(&p.tmA0, x_perm, rc, d, false));
+        if (sw) {
+            p.dual = 1;
+            p.bn = 128;
+            p.b_mn = 1;
+            MOE_TRY(weight_map(&p.tmB0, W_gate, E, d, f, true, 0));
+            MOE_TRY(weight_map(&p.tmB1, W_up, E, d, f, true, 0));
+            p.epi = EPI_SWIGLU_FWD;
+            p.out0 = static_cast<bf*>(h_saved);
+            p.out1 = static_cast<bf*>(h_saved) + rc * f;
+            p.out2 = static_cast<bf*>(act);
+        } else {
+            p.bn = pick_bn(f);
+            p.b_mn = 1;
+            MOE_TRY(weight_map(&p.tmB0, W_up, E, d, f, true, 0));
+            p.epi = EPI_SILU_FWD;
+            p.out0 = static_cast<bf*>(h_saved);
+            p.out1 = static_cast<bf*>(act);
+        }
+        p.n_blocks = f / p.bn;
+        p.ldo = f;
+        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
+    }
+    // GEMM2
+    {
+        TcParams p = base_params(c, offsets);
+        p.sched = SCHED_ROWS;
+        p.k_blocks = f / BK;
+        p.bn = pick_bn(d);
+        p.b_mn = 1;
+        MOE_TRY(act_map(&p.tmA0, act, rc, f, false));
+        MOE_TRY(weight_map(&p.tmB0, W_down, E, f, d, true, 0));
+        p.n_blocks = d / p.bn;
+        p.epi = EPI_STORE;
+        p.out0 = static_cast<bf*>(y_perm);
+        p.ldo = d;
+        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
+    }
+    return MOE_OK;
+}
+
+int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                    const void* W_up, const void* W_gate, const void* W_down,
+                    const void* h_saved, const void* act, const void* dy_perm, void* dh,
+                    void* dx_perm, void* dW_up, void* dW_gate, void* dW_down, void*, cudaStream_t st)
+{
+    using bf = __nv_bfloat16;
+    const int64_t rc = rows_cap_of(c);
+    const int d = c.d, f = c.f, E = c.E;
+    const bool sw = c.ffn == MOE_FFN_SWIGLU;
+    bf* dh0 = static_cast<bf*>(dh);                       // dh (SiLU) or dg (SwiGLU)
+    bf* dh1 = sw ? static_cast<bf*>(dh) + rc * f : nullptr;  // du (SwiGLU)
+    const bf* h0 = static_cast<const bf*>(h_saved);
+    const bf* h1 = sw ? h0 + rc * f : nullptr;
+    // dact = dy W_down^T, activation derivative fused
+    {
+        TcParams p = base_params(c, offsets);
+        p.sched = SCHED_ROWS;
+        p.k_blocks = d / BK;
+        p.bn = pick_bn(f);
+        MOE_TRY(act_map(&p.tmA0, dy_perm, rc, d, false));
+        MOE_TRY(weight_map(&p.tmB0, W_down, E, f, d, false, p.bn));
+        p.n_blocks = f / p.bn;
+        p.ldo = f;
+        p.in0 = h0;
+        p.out0 = dh0;
+        if (sw) {
+            p.epi = EPI_SWIGLU_BWD;
+            p.in1 = h1;
+            p.out1 = dh1;
+        } else {
+            p.epi = EPI_SILU_BWD;
+        }
+        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
+    }
+    // weight gradients: reductions over each expert's rows
+    auto wgrad = [&](const void* A, int M, const void* B, int N, void* out) -> int {
+        TcParams p = base_params(c, offsets);
+        p.sched = SCHED_KSEG;
+        p.a_mn = 1;
+        p.b_mn = 1;
+        p.bn = pick_bn(N);
+        p.m_blocks = M / BM;
+        p.n_blocks = N / p.bn;
+        MOE_TRY(act_map(&p.tmA0, A, rc, M, true));
+        MOE_TRY(act_map(&p.tmB0, B, rc, N, true));
+        p.epi = EPI_STORE;
+        p.out0 = static_cast<bf*>(out);
+        p.ldo = N;
+        p.out_estride = (long long)M * N;
+        return launch_tc(p, (int64_t)E * p.m_blocks * p.n_blocks, st);
+    };
+    MOE_TRY(wgrad(act, f, dy_perm, d, dW_down));
+    if (sw) {
+        MOE_TRY(wgrad(x_perm, d, dh1, f, dW_up));
+        MOE_TRY(wgrad(x_perm, d, dh0, f, dW_gate));
+    } else {
+        MOE_TRY(wgrad(x_perm, d, dh0, f, dW_up));
+    }
+    // dx_perm = dh W_up^T (+ dg W_gate^T)
+    {
+        TcParams p = base_params(c, offsets);
+        p.sched = SCHED_ROWS;
+        p.k_blocks = f / BK;
+        p.bn = pick_bn(d);
+        MOE_TRY(act_map(&p.tmA0, sw ? dh1 : dh0, rc, f, false));
+        MOE_TRY(weight_map(&p.tmB0, W_up, E, d, f, false, p.bn));
+        if (sw) {
+            p.kconcat = 2;
+            MOE_TRY(act_map(&p.tmA1, dh0, rc, f, false));
+            MOE_TRY(weight_map(&p.tmB1, W_gate, E, d, f, false, p.bn));
+        }
+        p.n_blocks = d / p.bn;
+        p.epi = EPI_STORE;
+        p.out0 = static_cast<bf*>(dx_perm);
+        p.ldo = d;
+        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
+    }
+    return MOE_OK;
+}
+
+}  // namespace moe
