@@ -1,0 +1,428 @@
+"""Benchmark of the sparse MoE layer (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = the whole hot path on one batch of synthetic tokens: router,
+permutation, grouped expert FFN, combine (forward) and the full backward
+(combine-bwd, grouped FFN backward, router backward), all through the C ABI.
+Inputs and weights are resident in HBM before the timed region; L2 is
+flushed (512 MB write) before every timed step, outside its event pair.
+Under torchrun each rank runs an independent replica on its own GPU (the
+layer has no exchange step on one GPU); rank 0 prints one JSON line with the
+whole-job tokens/s (max step time over ranks).
+
+--impl reference times the fp64 CPU oracle (the layer's plain definition) on
+the host cores, on a bounded token sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_inputs  # noqa: E402
+
+METRIC = "MoE layer tokens/sec fwd+bwd on 1 GB300 (grouped-GEMM % of bf16 peak in roofline)"
+DEFAULT_WORKLOAD = "small_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "tc_grouped_gemm_small_bf16.md")
+GEMM_SOURCE = os.path.join(ROOT, "top_routing_expert_moe_gb300", "csrc", "gemm_tc.cu")
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_work(w, A_kept: int):
+    """FLOPs of the grouped GEMMs and bytes of the HBM-bound kernels per step."""
+    s = 2 if w.dtype == "bf16" else 4
+    T, d, f, E, k = w.T, w.d, w.f, w.E, w.k
+    A = T * k
+    fwd = (6 if w.swiglu else 4) * A_kept * d * f
+    return dict(
+        gemm_fwd_flop=fwd, gemm_bwd_flop=2 * fwd,
+        route_bytes=T * d * s + d * E * s + T * (4 * E + 8 * k),
+        permute_bytes=2 * A_kept * d * s + 8 * A,
+        combine_bytes=A_kept * d * s + T * d * s + 8 * A)
+
+
+def gemm_traffic_from_profile():
+    """dram bytes per grouped-GEMM launch from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    if not os.path.exists(GEMM_PROFILE):
+        return None
+    txt = open(GEMM_PROFILE).read()
+    m = re.search(r"traffic_bytes_per_step:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"gemm_tc_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(GEMM_SOURCE, "rb").read()).hexdigest()
+    return float(m.group(1)) if cur == h.group(1) else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling around the timed region (SM clock, throttle reasons)."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[1]), float(parts[2]), parts[4:]))
+            except Exception:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed_region"
+        if not inside:
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+            window = "nearest_samples"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3][1:]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- oracle leg
+def oracle_step(w, T_s: int, seed: int = 0):
+    """One oracle forward + backward on a T_s-token batch of workload w (fp64)."""
+    import oracle
+    from dataclasses import replace
+    ws = replace(w, T=T_s)
+    inp = moe_inputs.make_inputs(ws, seed)
+    f64 = {k: moe_inputs.as_f64(v, ws.dtype if k not in ("bias", "noise") else "fp32")
+           for k, v in inp.items()}
+    cfg = oracle.OracleConfig(T=T_s, d=w.d, f=w.f, E=w.E, k=w.k,
+                              capacity_factor=float(np.float32(w.capacity_factor)),
+                              swiglu=w.swiglu, aux_coef=w.aux_coef, pad_m=128)
+    t0 = time.perf_counter()
+    o = oracle.forward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], Wgate=f64["W_gate"],
+                       bias=f64["bias"], noise=f64["noise"])
+    oracle.backward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], o["logits"],
+                    o["topk_idx"], o["gate"], o["slot_of"], f64["dout"], Wgate=f64["W_gate"],
+                    with_bias=f64["bias"] is not None)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_tokens(w, budget_s: float):
+    """Token count whose oracle fwd+bwd takes about budget_s on this host."""
+    pilot = min(64, w.T)
+    t = max(oracle_step(w, pilot), 1e-3)
+    return int(max(pilot, min(w.T, pilot * budget_s / t)))
+
+
+def oracle_cores():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
+
+
+def run_reference(args, w):
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    T_s = oracle_sample_tokens(w, args.ref_budget_s)
+    for _ in range(args.warmup):
+        oracle_step(w, T_s)
+    times = [oracle_step(w, T_s) for _ in range(args.steps)]
+    tok_s = T_s / statistics.mean(times)
+    sample = (f"oracle fp64 fwd+bwd on a {T_s}-token batch of {w.name} (same d, f, E, k, "
+              f"capacity factor), per step")
+    line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(times) * w.T / T_s,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, "n/a (CPU)"),
+            "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": oracle_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, l2):
+    return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E,
+            "top_k": w.k, "capacity_factor": w.capacity_factor,
+            "ffn": "swiglu" if w.swiglu else "silu", "gate_noise_std": w.noise_std,
+            "zipf_router_bias": w.zipf_bias, "aux_coef": w.aux_coef, "l2": l2,
+            "parallelism": "replicas (one independent layer per GPU)"}
+
+
+# ----------------------------------------------------------------------------- GPU leg
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import top_routing_expert_moe_gb300 as moe
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.load_library()
+
+    from tests.parity import gpu_cfg, to_torch   # seeded-input marshalling only
+    cfg = gpu_cfg(w)
+    inp = moe_inputs.make_inputs(w, args.seed + rank)
+    dt = w.dtype
+    x = to_torch(inp["x"], dt, dev)
+    Wr = to_torch(inp["W_r"], dt, dev)
+    Wu = to_torch(inp["W_up"], dt, dev)
+    Wg = to_torch(inp["W_gate"], dt, dev)
+    Wd = to_torch(inp["W_down"], dt, dev)
+    b = to_torch(inp["bias"], "fp32", dev)
+    nz = to_torch(inp["noise"], "fp32", dev)
+    dout = to_torch(inp["dout"], dt, dev)
+    L = moe.MoELayer(cfg, device=dev)
+    st = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # one step, with events around each C-ABI call (all on stream `st`)
+    def step(evs):
+        evs[0].record(st)
+        moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
+        evs[1].record(st)
+        moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept, L.offsets,
+                        L.stats, L.ws, st)
+        evs[2].record(st)
+        moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, L.y_perm,
+                            L.ws, st)
+        evs[3].record(st)
+        moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st)
+        evs[4].record(st)
+        g = L.grads()
+        moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token, L.offsets,
+                                 bw["dy"], bw["dgate"], st)
+        evs[5].record(st)
+        moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
+                                     bw["dy"], bw["dh"], bw["dxp"], g["dW_up"], g["dW_gate"],
+                                     g["dW_down"], L.ws, st)
+        evs[6].record(st)
+        moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of, bw["dgate"],
+                                bw["dxp"], L.stats, g["dx"], g["dW_r"],
+                                g["dbias"] if b is not None else None, bw["dlogits"], L.ws, st)
+        evs[7].record(st)
+
+    R = L.rows_cap
+    bw = dict(dy=torch.empty(R, w.d, dtype=cfg.torch_dtype, device=dev),
+              dgate=torch.empty(w.T, w.k, dtype=torch.float32, device=dev),
+              dh=torch.empty(cfg.nh, R, w.f, dtype=cfg.torch_dtype, device=dev),
+              dxp=torch.empty(R, w.d, dtype=cfg.torch_dtype, device=dev),
+              dlogits=torch.empty(w.T, w.E, dtype=torch.float32, device=dev))
+
+    with torch.cuda.stream(st):
+        for _ in range(max(3, args.warmup)):
+            step([ev() for _ in range(8)])
+        torch.cuda.synchronize(dev)
+        status = moe.last_device_status(st)
+        if status != 0:
+            raise RuntimeError(f"device status after warm-up: {moe.error_string(status)}")
+        A_kept = int(L.kept.sum().item())
+        work = algorithmic_work(w, A_kept)
+
+        sampler = ClockSampler(local)
+        time.sleep(0.3)
+        steps_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
+        launches0 = moe.launch_count()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.time()
+        for i in range(args.steps):
+            flush.zero_()                   # L2 flush, outside the step's events
+            step(steps_evs[i])
+        torch.cuda.synchronize(dev)
+        t_wall1 = time.time()
+        if world > 1:
+            dist.barrier()
+        launches = moe.launch_count() - launches0
+        clocks = sampler.stop(t_wall0, t_wall1)
+
+        per = np.array([[s[j].elapsed_time(s[j + 1]) for j in range(7)] for s in steps_evs])
+        step_ms = per.sum(1)
+        ms_local = float(step_ms.mean())
+        stage_ms = per.mean(0)
+
+        # forward-only throughput
+        fwd_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
+        fwd_ms = []
+        for i in range(args.steps):
+            flush.zero_()
+            e = fwd_evs[i]
+            e[0].record(st)
+            moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
+            moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept,
+                            L.offsets, L.stats, L.ws, st)
+            moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, L.y_perm,
+                                L.ws, st)
+            moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st)
+            e[1].record(st)
+        torch.cuda.synchronize(dev)
+        fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in fwd_evs]))
+
+        # end to end through the public API: pinned host inputs in, results out
+        x_h = x.cpu().pin_memory()
+        dout_h = dout.cpu().pin_memory()
+        out_h = torch.empty_like(L.out, device="cpu").pin_memory()
+        dx_h = torch.empty_like(L.out, device="cpu").pin_memory()
+        x_d = torch.empty_like(x)
+        dout_d = torch.empty_like(dout)
+        e2e = []
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e1 = ev(), ev()
+            e0.record(st)
+            x_d.copy_(x_h, non_blocking=True)
+            dout_d.copy_(dout_h, non_blocking=True)
+            L.forward(x_d, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, stream=st)
+            gg = L.backward(dout_d, stream=st)
+            out_h.copy_(L.out, non_blocking=True)
+            dx_h.copy_(gg["dx"], non_blocking=True)
+            e1.record(st)
+            e2e.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        e2e_ms = float(np.mean([a.elapsed_time(bb) for a, bb in e2e]))
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([ms_local, fwd_ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, fwd_ms, e2e_ms = (float(v) for v in t.tolist())
+    else:
+        ms = ms_local
+    if rank == 0:
+        peaks, src = load_peaks()
+        gemm_ms = float(stage_ms[2] + stage_ms[5])
+        gemm_flop = work["gemm_fwd_flop"] + work["gemm_bwd_flop"]
+        launches_gemm = 7 if w.swiglu else 6
+        achieved = gemm_flop / (gemm_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        traffic = gemm_traffic_from_profile()
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            T_s = oracle_sample_tokens(w, args.cpu_budget_s)
+            t_cpu = oracle_step(w, T_s)
+            cpu = {"value": T_s / t_cpu, "unit": "tokens/s", "cores": oracle_cores(),
+                   "kind": "oracle",
+                   "sample": f"oracle fp64 fwd+bwd on a {T_s}-token batch of {w.name} "
+                             f"(same d, f, E, k, capacity factor), {t_cpu:.1f} s"}
+        tok = w.T * world / (ms * 1e-3)
+        es = 2 if dt == "bf16" else 4
+        line = {
+            "metric": METRIC, "value": tok, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": dt, "data": "synthetic (seeded normals, random-init weights)",
+            "config": workload_config(w, "flushed before every step (512 MB write)"),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "traffic": None if traffic is None else traffic / launches_gemm,
+                         "kernel": "tc_grouped_gemm_kernel (all grouped-GEMM launches of a step)",
+                         "peak_source": f"{src} bf16 burst"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": w.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": (x.numel() + dout.numel()) * es,
+                    "d2h_bytes_per_step": 2 * L.out.numel() * es},
+            "clocks": clocks,
+            "gpu_launches": int(launches),
+            "fwd_tokens_per_s": w.T * world / (fwd_ms * 1e-3),
+            "stages_ms": {n: float(v) for n, v in zip(
+                ["route", "permute", "grouped_ffn", "combine", "combine_bwd", "grouped_ffn_bwd",
+                 "router_bwd"], stage_ms)},
+            "hbm_gbs": {"route": work["route_bytes"] / (stage_ms[0] * 1e-3) / 1e9,
+                        "permute": work["permute_bytes"] / (stage_ms[1] * 1e-3) / 1e9,
+                        "combine": work["combine_bytes"] / (stage_ms[3] * 1e-3) / 1e9,
+                        "peak": peaks["hbm_gbs"]},
+            "gemm_tflops": {"fwd": work["gemm_fwd_flop"] / (stage_ms[2] * 1e-3) / 1e12,
+                            "bwd": work["gemm_bwd_flop"] / (stage_ms[5] * 1e-3) / 1e12},
+            "kept_assignments": A_kept,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--ref-budget-s", type=float, default=4.0,
+                    help="CPU seconds per reference-arm step")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0,
+                    help="CPU seconds of the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = moe_inputs.get(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
