@@ -66,6 +66,8 @@ typedef struct CUstream_st* moe_stream_t; /* same handle as cudaStream_t */
 #define MOE_ERR_TIMEOUT (-4)       /* device: a bounded wait gave up             */
 #define MOE_ERR_NONFINITE (-5)     /* device: a router logit was NaN or infinite */
 #define MOE_ERR_DEVICE_BOUNDS (-6) /* device: an index read from memory was out of range */
+#define MOE_ERR_SCRATCH_LIMIT (-7) /* moe_route_noalloc: the configuration needs more scratch
+                                      than MOE_ROUTE_NOALLOC_SCRATCH_BYTES                */
 
 /* ---- configuration ---- */
 #define MOE_DTYPE_F32 0
@@ -131,6 +133,28 @@ MOE_API int moe_workspace_size(const moe_config* cfg, size_t* bytes);
 MOE_API int moe_route(const moe_config* cfg, const void* x, const void* W_r, const float* bias,
               const float* noise, float* logits, int32_t* topk_idx, float* gate,
               int32_t* counts, float* stats, void* ws, moe_stream_t stream);
+
+/* Router for callers that cannot allocate device memory (no counterpart in the
+ * pages: it exists for embedding).  Some hosts own all device memory through
+ * their own pool and forbid side allocations once running, and some latency
+ * paths cannot afford cudaMalloc's cost and implicit synchronisation; such
+ * callers cannot hand moe_route a workspace.  This entry point runs the same
+ * kernels as moe_route, with the same arguments minus `ws`; its scratch is a
+ * static device array of MOE_ROUTE_NOALLOC_SCRATCH_BYTES that every GPU loading
+ * the library holds until the process exits.  It calls no allocator.
+ *   - Configurations needing more scratch than that (moe_workspace_size's
+ *     router share: per-CTA partials plus E_pad*d bf16 transposed router
+ *     weights) return MOE_ERR_SCRATCH_LIMIT before anything is launched.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (every
+ *     word is written before it is read, so nothing needs clearing); calls
+ *     whose kernels overlap on the GPU race on it.                            */
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+MOE_API int moe_route_noalloc(const moe_config* cfg, const void* x, const void* W_r,
+                              const float* bias, const float* noise, float* logits,
+                              int32_t* topk_idx, float* gate, int32_t* counts, float* stats,
+                              moe_stream_t stream);
 
 /* Capacity + permutation: rank each assignment (t, j) among its expert's
  * assignments in ascending token order; keep it iff rank < C; lay experts out

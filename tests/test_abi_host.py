@@ -101,6 +101,6 @@ def test_null_and_misaligned_pointers_are_rejected_before_launch():
 
 
 def test_error_strings():
-    for code in range(-6, 1):
+    for code in range(-7, 1):
         assert moe.error_string(code)
     assert moe.error_string(-99) == "unknown status"

@@ -30,6 +30,8 @@ STAT_PBAR = 8
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE, ERR_DEVICE_BOUNDS = \
     0, -1, -2, -3, -4, -5, -6
+ERR_SCRATCH_LIMIT = -7
+ROUTE_NOALLOC_SCRATCH_BYTES = 2 * 1024 * 1024
 
 
 class MoEConfig(ctypes.Structure):
@@ -70,6 +72,7 @@ _SIGS = {
     "moe_rows_capacity": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_workspace_size": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_route": [ctypes.c_void_p] * 12,
+    "moe_route_noalloc": [ctypes.c_void_p] * 11,
     "moe_permute": [ctypes.c_void_p] * 11,
     "moe_grouped_ffn": [ctypes.c_void_p] * 11,
     "moe_combine": [ctypes.c_void_p] * 6,
@@ -169,6 +172,15 @@ def last_device_status(stream=None) -> int:
 def moe_route(cfg, x, W_r, bias, noise, logits, topk_idx, gate, counts, stats, ws, stream=None):
     _call("moe_route", ctypes.byref(cfg), _p(x), _p(W_r), _p(bias), _p(noise), _p(logits),
           _p(topk_idx), _p(gate), _p(counts), _p(stats), _p(ws), _s(stream))
+
+
+def moe_route_noalloc(cfg, x, W_r, bias, noise, logits, topk_idx, gate, counts, stats,
+                      stream=None):
+    """moe_route without a workspace, for callers that cannot allocate device
+    memory: scratch comes from the library's static device array (shared by all
+    calls; overlapping calls race)."""
+    _call("moe_route_noalloc", ctypes.byref(cfg), _p(x), _p(W_r), _p(bias), _p(noise),
+          _p(logits), _p(topk_idx), _p(gate), _p(counts), _p(stats), _s(stream))
 
 
 def moe_permute(cfg, x, topk_idx, x_perm, perm_token, slot_of, kept, offsets, stats, ws,

@@ -274,6 +274,7 @@ const char* moe_error_string(int code) {
         case MOE_ERR_TIMEOUT: return "device: a bounded wait timed out";
         case MOE_ERR_NONFINITE: return "device: non-finite router logits";
         case MOE_ERR_DEVICE_BOUNDS: return "device: index out of range";
+        case MOE_ERR_SCRATCH_LIMIT: return "configuration exceeds the no-allocation router's static scratch";
         default: return "unknown status";
     }
 }
