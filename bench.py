@@ -4,7 +4,10 @@
 
 One step = the whole hot path on one batch of synthetic tokens: router,
 permutation, grouped expert FFN, combine (forward) and the full backward
-(combine-bwd, grouped FFN backward, router backward), all through the C ABI.
+(combine-bwd, grouped FFN backward, router backward), all through the C ABI,
+replayed as one CUDA graph (the ABI does no host sync and no allocation, so
+the step is capturable).  An eager pass with events between the C-ABI calls
+gives the per-stage times and the grouped-GEMM roofline.
 Inputs and weights are resident in HBM before the timed region; L2 is
 flushed (512 MB write) before every timed step, outside its event pair.
 Under torchrun each rank runs an independent replica on its own GPU (the
@@ -230,48 +233,58 @@ def run_ours(args, w):
     nz = to_torch(inp["noise"], "fp32", dev)
     dout = to_torch(inp["dout"], dt, dev)
     L = moe.MoELayer(cfg, device=dev)
-    st = torch.cuda.current_stream(dev)
+    g = L.grads()
+    st = torch.cuda.Stream(dev)           # a side stream: graphs cannot capture the default one
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
-
-    def ev():
-        return torch.cuda.Event(enable_timing=True)
-
-    # one step, with events around each C-ABI call (all on stream `st`)
-    def step(evs):
-        evs[0].record(st)
-        moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
-        evs[1].record(st)
-        moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept, L.offsets,
-                        L.stats, L.ws, st)
-        evs[2].record(st)
-        moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, L.y_perm,
-                            L.ws, st)
-        evs[3].record(st)
-        moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st)
-        evs[4].record(st)
-        g = L.grads()
-        moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token, L.offsets,
-                                 bw["dy"], bw["dgate"], st)
-        evs[5].record(st)
-        moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
-                                     bw["dy"], bw["dh"], bw["dxp"], g["dW_up"], g["dW_gate"],
-                                     g["dW_down"], L.ws, st)
-        evs[6].record(st)
-        moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of, bw["dgate"],
-                                bw["dxp"], L.stats, g["dx"], g["dW_r"],
-                                g["dbias"] if b is not None else None, bw["dlogits"], L.ws, st)
-        evs[7].record(st)
-
     R = L.rows_cap
     bw = dict(dy=torch.empty(R, w.d, dtype=cfg.torch_dtype, device=dev),
               dgate=torch.empty(w.T, w.k, dtype=torch.float32, device=dev),
               dh=torch.empty(cfg.nh, R, w.f, dtype=cfg.torch_dtype, device=dev),
               dxp=torch.empty(R, w.d, dtype=cfg.torch_dtype, device=dev),
               dlogits=torch.empty(w.T, w.E, dtype=torch.float32, device=dev))
+    torch.cuda.synchronize(dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def rec(evs, i):
+        if evs is not None:
+            evs[i].record(st)
+
+    # one step through the C ABI; optional events around each call (all on `st`)
+    def forward(evs=None):
+        rec(evs, 0)
+        moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
+        rec(evs, 1)
+        moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept, L.offsets,
+                        L.stats, L.ws, st)
+        rec(evs, 2)
+        moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, L.y_perm,
+                            L.ws, st)
+        rec(evs, 3)
+        moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st)
+        rec(evs, 4)
+
+    def backward(evs=None):
+        moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token, L.offsets,
+                                 bw["dy"], bw["dgate"], st)
+        rec(evs, 5)
+        moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
+                                     bw["dy"], bw["dh"], bw["dxp"], g["dW_up"], g["dW_gate"],
+                                     g["dW_down"], L.ws, st)
+        rec(evs, 6)
+        moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of, bw["dgate"],
+                                bw["dxp"], L.stats, g["dx"], g["dW_r"],
+                                g["dbias"] if b is not None else None, bw["dlogits"], L.ws, st)
+        rec(evs, 7)
+
+    def step(evs=None):
+        forward(evs)
+        backward(evs)
 
     with torch.cuda.stream(st):
         for _ in range(max(3, args.warmup)):
-            step([ev() for _ in range(8)])
+            step()
         torch.cuda.synchronize(dev)
         status = moe.last_device_status(st)
         if status != 0:
@@ -279,45 +292,62 @@ def run_ours(args, w):
         A_kept = int(L.kept.sum().item())
         work = algorithmic_work(w, A_kept)
 
+        # the step and the forward as CUDA graphs (the C ABI is capturable: no host sync,
+        # no allocation); their kernel count per replay is the capture's launch count
+        graph, fgraph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        n0 = moe.launch_count()
+        with torch.cuda.graph(graph, stream=st):
+            step()
+        launches_per_step = moe.launch_count() - n0
+        with torch.cuda.graph(fgraph, stream=st):
+            forward()
+        torch.cuda.synchronize(dev)
+        for _ in range(3):
+            graph.replay()
+            fgraph.replay()
+        torch.cuda.synchronize(dev)
+
         sampler = ClockSampler(local)
         time.sleep(0.3)
-        steps_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
-        launches0 = moe.launch_count()
+        step_evs = [(ev(), ev()) for _ in range(args.steps)]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
         t_wall0 = time.time()
         for i in range(args.steps):
             flush.zero_()                   # L2 flush, outside the step's events
-            step(steps_evs[i])
+            step_evs[i][0].record(st)
+            graph.replay()
+            step_evs[i][1].record(st)
         torch.cuda.synchronize(dev)
         t_wall1 = time.time()
         if world > 1:
             dist.barrier()
-        launches = moe.launch_count() - launches0
         clocks = sampler.stop(t_wall0, t_wall1)
+        ms_local = float(np.mean([a.elapsed_time(c) for a, c in step_evs]))
+        status = moe.last_device_status(st)
+        if status != 0:
+            raise RuntimeError(f"device status after the timed steps: {moe.error_string(status)}")
 
-        per = np.array([[s[j].elapsed_time(s[j + 1]) for j in range(7)] for s in steps_evs])
-        step_ms = per.sum(1)
-        ms_local = float(step_ms.mean())
-        stage_ms = per.mean(0)
-
-        # forward-only throughput
-        fwd_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
-        fwd_ms = []
+        # forward only (graph)
+        fwd_evs = [(ev(), ev()) for _ in range(args.steps)]
         for i in range(args.steps):
             flush.zero_()
-            e = fwd_evs[i]
-            e[0].record(st)
-            moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
-            moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept,
-                            L.offsets, L.stats, L.ws, st)
-            moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, L.y_perm,
-                                L.ws, st)
-            moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st)
-            e[1].record(st)
+            fwd_evs[i][0].record(st)
+            fgraph.replay()
+            fwd_evs[i][1].record(st)
         torch.cuda.synchronize(dev)
-        fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in fwd_evs]))
+        fwd_ms = float(np.mean([a.elapsed_time(c) for a, c in fwd_evs]))
+
+        # per-stage breakdown (eager launches, events between C-ABI calls)
+        stage_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            step(stage_evs[i])
+        torch.cuda.synchronize(dev)
+        per = np.array([[s_[j].elapsed_time(s_[j + 1]) for j in range(7)] for s_ in stage_evs])
+        stage_ms = per.mean(0)
+        eager_ms = float(per.sum(1).mean())
 
         # end to end through the public API: pinned host inputs in, results out
         x_h = x.cpu().pin_memory()
@@ -326,6 +356,7 @@ def run_ours(args, w):
         dx_h = torch.empty_like(L.out, device="cpu").pin_memory()
         x_d = torch.empty_like(x)
         dout_d = torch.empty_like(dout)
+        torch.cuda.synchronize(dev)
         e2e = []
         for i in range(args.steps):
             flush.zero_()
@@ -340,7 +371,7 @@ def run_ours(args, w):
             e1.record(st)
             e2e.append((e0, e1))
         torch.cuda.synchronize(dev)
-        e2e_ms = float(np.mean([a.elapsed_time(bb) for a, bb in e2e]))
+        e2e_ms = float(np.mean([a.elapsed_time(c) for a, c in e2e]))
 
     # max over ranks
     if world > 1:
@@ -385,7 +416,9 @@ def run_ours(args, w):
                     "h2d_bytes_per_step": (x.numel() + dout.numel()) * es,
                     "d2h_bytes_per_step": 2 * L.out.numel() * es},
             "clocks": clocks,
-            "gpu_launches": int(launches),
+            "gpu_launches": int(launches_per_step * args.steps),
+            "launches_per_step": int(launches_per_step),
+            "eager_ms_per_step": eager_ms,
             "fwd_tokens_per_s": w.T * world / (fwd_ms * 1e-3),
             "stages_ms": {n: float(v) for n, v in zip(
                 ["route", "permute", "grouped_ffn", "combine", "combine_bwd", "grouped_ffn_bwd",

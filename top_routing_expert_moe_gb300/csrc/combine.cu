@@ -221,54 +221,66 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     }
 }
 
-// Partial dW_r over a token chunk: CTA = 64 columns of x x one token chunk.
-// part[s][i][e] = sum_{t in chunk s} x[t,i] dlogits[t,e]; part_db[s][e] likewise.
-template <typename T>
+// Partial dW_r over a token chunk: part[s][i][e] = sum_{t in chunk s} x[t,i] dlogits[t,e].
+// CTA = 32 column vectors (16 bytes each) x 8 token lanes; each thread keeps
+// V x EB accumulators (V columns of one vector, EB experts of this CTA's expert
+// group) while streaming its token lane's x rows with 16-byte loads; the 8 token
+// lanes are summed in a fixed order through shared memory.
+template <typename T, int EB>
 __global__ void __launch_bounds__(256) dwr_partial_kernel(const T* __restrict__ x,
                                                           const float* __restrict__ dlogits,
                                                           int Tn, int d, int E, int chunk,
                                                           float* __restrict__ part,
                                                           float* __restrict__ part_db)
 {
-    __shared__ float sx[32][65];
-    __shared__ float sl[32][65];
-    const int c0 = blockIdx.x * 64;
+    constexpr int V = 16 / sizeof(T);
+    extern __shared__ __align__(16) float red[];          // [8][32][V*EB]
+    const int tid = threadIdx.x, tl = tid >> 5, cv = tid & 31;
+    const int col0 = (blockIdx.x * 32 + cv) * V;
+    const int e0 = blockIdx.z * EB;
     const int s = blockIdx.y;
     const int tbeg = s * chunk, tend = min(Tn, tbeg + chunk);
-    const int tid = threadIdx.x;
-    const int col = tid & 63, eg = tid >> 6;  // 4 expert groups
-    const int ncol = min(64, d - c0);
-    float acc[16];
+    const bool colok = col0 < d;
+    float acc[V][EB];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-    float accb = 0.f;
-    for (int t0 = tbeg; t0 < tend; t0 += 32) {
-        const int nt = min(32, tend - t0);
-        for (int i = tid; i < 32 * 64; i += 256) {
-            int r = i >> 6, c = i & 63;
-            sx[r][c] = (r < nt && c < ncol) ? to_f<T>(x[(size_t)(t0 + r) * d + c0 + c]) : 0.f;
-        }
-        for (int i = tid; i < 32 * 64; i += 256) {
-            int r = i >> 6, c = i & 63;
-            sl[r][c] = (r < nt && c < E) ? dlogits[(size_t)(t0 + r) * E + c] : 0.f;
-        }
-        __syncthreads();
-        for (int r = 0; r < nt; ++r) {
-            const float xv = sx[r][col];
+    for (int v = 0; v < V; ++v)
 #pragma unroll
-            for (int q = 0; q < 16; ++q) acc[q] = fmaf(xv, sl[r][eg + 4 * q], acc[q]);
+        for (int e = 0; e < EB; ++e) acc[v][e] = 0.f;
+    for (int t = tbeg + tl; t < tend; t += 8) {
+        float xv[V];
+        if (colok) load16_f<T>(x + (size_t)t * d + col0, xv);
+        else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) xv[v] = 0.f;
         }
-        if (blockIdx.x == 0 && tid < E)
-            for (int r = 0; r < nt; ++r) accb += sl[r][tid];
-        __syncthreads();
+        float dl[EB];
+#pragma unroll
+        for (int e = 0; e < EB; ++e) dl[e] = (e0 + e < E) ? __ldg(dlogits + (size_t)t * E + e0 + e) : 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+#pragma unroll
+            for (int e = 0; e < EB; ++e) acc[v][e] = fmaf(xv[v], dl[e], acc[v][e]);
     }
-    if (col < ncol)
+    float* mine = red + ((size_t)tl * 32 + cv) * (V * EB);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const int e = eg + 4 * q;
-            if (e < E) part[((size_t)s * d + c0 + col) * E + e] = acc[q];
-        }
-    if (blockIdx.x == 0 && tid < E) part_db[(size_t)s * E + tid] = accb;
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int e = 0; e < EB; ++e) mine[v * EB + e] = acc[v][e];
+    __syncthreads();
+    for (int i = tid; i < 32 * V * EB; i += 256) {
+        const int c = i / (V * EB), r = i % (V * EB);
+        const int v = r / EB, e = r % EB;
+        float a = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a += red[((size_t)q * 32 + c) * (V * EB) + r];
+        const int col = (blockIdx.x * 32 + c) * V + v;
+        if (col < d && e0 + e < E) part[((size_t)s * d + col) * E + e0 + e] = a;
+    }
+    if (blockIdx.x == 0 && blockIdx.z == 0 && tid < E) {
+        float a = 0.f;
+        for (int t = tbeg; t < tend; ++t) a += dlogits[(size_t)t * E + tid];
+        part_db[(size_t)s * E + tid] = a;
+    }
 }
 
 template <typename T>
@@ -290,11 +302,19 @@ __global__ void dwr_reduce_kernel(const float* __restrict__ part, const float* _
     }
 }
 
+constexpr int DWR_EB = 8;  // experts per CTA of dwr_partial_kernel
+
+dim3 dwr_grid_xz(const moe_config& c) {
+    const int V = c.dtype == MOE_DTYPE_BF16 ? 8 : 4;
+    return dim3((c.d + 32 * V - 1) / (32 * V), 1, (c.E + DWR_EB - 1) / DWR_EB);
+}
+
+// token chunks: enough CTAs for about four per SM
 int dwr_nsplit(const moe_config& c) {
-    const int ncolb = (c.d + 63) / 64;
-    int ns = std::max(1, (2 * num_sms() + ncolb - 1) / ncolb);
-    ns = std::min(ns, std::max(1, (c.T + 255) / 256));
-    return ns;
+    const dim3 g = dwr_grid_xz(c);
+    const int per = (int)(g.x * g.z);
+    int ns = std::max(1, (4 * num_sms() + per - 1) / per);
+    return std::min(ns, std::max(1, (c.T + 63) / 64));
 }
 
 int row_grid(int64_t rows) {
@@ -359,7 +379,25 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
     if (!dlogits) dlogits = reinterpret_cast<float*>(w);
     const int chunk = (c.T + ns - 1) / ns;
     const int grid = row_grid(c.T);
-    const dim3 pgrid((c.d + 63) / 64, ns);
+    dim3 pgrid = dwr_grid_xz(c);
+    pgrid.y = ns;
+    // reduction buffer: 8 token lanes x 32 vectors x (V * EB) floats, V = 16 / sizeof(T)
+    const size_t dwr_smem = (size_t)8 * 32 * (c.dtype == MOE_DTYPE_BF16 ? 8 : 4) * DWR_EB * sizeof(float);
+    if (c.dtype == MOE_DTYPE_BF16) {
+        static bool attr = false;
+        if (!attr) {
+            MOE_CUDA_TRY(cudaFuncSetAttribute(dwr_partial_kernel<__nv_bfloat16, DWR_EB>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dwr_smem));
+            attr = true;
+        }
+    } else {
+        static bool attr = false;
+        if (!attr) {
+            MOE_CUDA_TRY(cudaFuncSetAttribute(dwr_partial_kernel<float, DWR_EB>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dwr_smem));
+            attr = true;
+        }
+    }
     if (c.dtype == MOE_DTYPE_BF16) {
         using T = __nv_bfloat16;
         transpose_wr_f32_kernel<T><<<64, 256, 0, st>>>(static_cast<const T*>(Wr), WrT, c.d, c.E);
@@ -368,8 +406,8 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
             logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), WrT, c.T,
             c.d, c.E, c.k, c.normalize_gates, c.aux_coef, dlogits, static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();
-        dwr_partial_kernel<T><<<pgrid, 256, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d,
-                                                     c.E, chunk, part, part_db);
+        dwr_partial_kernel<T, DWR_EB><<<pgrid, 256, dwr_smem, st>>>(static_cast<const T*>(x), dlogits,
+                                                                   c.T, c.d, c.E, chunk, part, part_db);
         MOE_LAUNCH_CHECK();
         dwr_reduce_kernel<T><<<std::min(1024, (c.d * c.E + 255) / 256), 256, 0, st>>>(
             part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);
@@ -382,8 +420,8 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
             logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), WrT, c.T,
             c.d, c.E, c.k, c.normalize_gates, c.aux_coef, dlogits, static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();
-        dwr_partial_kernel<T><<<pgrid, 256, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d,
-                                                     c.E, chunk, part, part_db);
+        dwr_partial_kernel<T, DWR_EB><<<pgrid, 256, dwr_smem, st>>>(static_cast<const T*>(x), dlogits,
+                                                                   c.T, c.d, c.E, chunk, part, part_db);
         MOE_LAUNCH_CHECK();
         dwr_reduce_kernel<T><<<std::min(1024, (c.d * c.E + 255) / 256), 256, 0, st>>>(
             part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);

@@ -8,16 +8,18 @@
 //             dW    = x^T dh, act^T dy     (reduction over each expert's rows)
 //             dx    = dh W_up^T (+ dg W_gate^T)
 //
-// Design (one CTA per SM, 192 threads, warp-specialised):
+// Design (one CTA per SM, 320 threads, warp-specialised):
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
 //               (BN x 64) into a 4-stage shared-memory ring (mbarrier tx).
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N=BN, K=16, bf16 in, fp32 accumulate) and commits to
 //               the ring's "empty" barriers and to a double-buffered TMEM
 //               accumulator's "full" barrier.
-//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time from TMEM, fused
-//               activation math, bf16 stores; frees the accumulator so the
-//               next tile's MMAs overlap this tile's epilogue.
+//   warps 2-9   epilogue: two warps per TMEM lane quarter, each taking half
+//               the tile's columns; tcgen05.ld 32 columns at a time, fused
+//               activation math (branch-free fast exp / divide so the 32
+//               elements of a chunk pipeline), bf16 stores; frees the
+//               accumulator so the next tile's MMAs overlap this epilogue.
 // Tiles come from a static persistent schedule whose per-expert tile counts
 // are read from the device-side segment offsets, so no host sync separates
 // routing from the GEMMs.  Within an expert, tiles are visited in groups of
@@ -53,7 +55,8 @@ constexpr int GUARD_BYTES = 16 * 1024;        // slack after the ring
 constexpr int CTRL_BYTES = 1024;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + GUARD_BYTES + CTRL_BYTES;
 constexpr int TMEM_COLS = 512;
-constexpr int NTHREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
+constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
 constexpr int RASTER_GM = 16;
 constexpr unsigned long long WAIT_NS = 4000000000ull;   // 4 s
 constexpr unsigned long long DRAIN_NS = 500000000ull;   // 0.5 s
@@ -219,6 +222,14 @@ __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float* v) {
     }
 }
 
+// bf16-path activations: fast exp and approximate divide (no slow-path
+// branches); errors of a few fp32 ulp vanish in the bf16 outputs.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float dsilu_fast(float z) {
+    const float s = __fdividef(1.0f, 1.0f + __expf(-z));
+    return s * (1.0f + z * (1.0f - s));
+}
+
 // ---------------------------------------------------------------- schedule
 struct Tile {
     int e, m0, n0, krow0, nk;
@@ -263,8 +274,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* offs = const_cast<int*>(reinterpret_cast<volatile int*>(abort_flag + 1));  // [E+1]
-    int* prefix = offs + 66;                                                           // [E+1]
+    int* offs = reinterpret_cast<int*>(tmem_slot + 2);  // [E+1] segment offsets
+    int* prefix = offs + 66;                            // [E+1] first tile of each expert
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -275,7 +286,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull[a]), 1);
-            mbar_init(smem_u32(&tempty[a]), 4);
+            mbar_init(smem_u32(&tempty[a]), NUM_EPI_WARPS);
         }
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
@@ -388,9 +399,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         mbar_drain(smem_u32(drain), 0);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int q = warp & 3;                   // TMEM lane quarter this warp may access
+        const int half = (warp - 2) / 4;          // which half of the tile's columns
         const int row_in_tile = q * 32 + lane;
         const int width = p.dual ? 128 : p.bn;
+        const int c_lo = half * (width / 64), c_hi = c_lo + width / 64;  // 32-column chunks
         int tcount = 0;
         for (int tix = blockIdx.x; tix < total; tix += gridDim.x, ++tcount) {
             Tile t;
@@ -403,7 +416,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const long long obase = (p.sched == SCHED_KSEG ? (long long)t.e * p.out_estride : 0) +
                                     row * p.ldo + t.n0;
             const uint32_t taddr = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(q * 32) << 16);
-            for (int c = 0; c < width / 32; ++c) {
+            for (int c = c_lo; c < c_hi; ++c) {
                 float v[32];
                 if (t.nk == 0) {
 #pragma unroll
@@ -419,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     store32_bf16(p.out0 + obase + c * 32, v);
                     store32_bf16(p.out1 + obase + c * 32, u);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * u[i];
+                    for (int i = 0; i < 32; ++i) v[i] = silu_fast(v[i]) * u[i];
                     store32_bf16(p.out2 + obase + c * 32, v);
                     continue;
                 }
@@ -429,23 +442,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                 } else if (p.epi == EPI_SILU_FWD) {
                     store32_bf16(p.out0 + obase + c * 32, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]);
+                    for (int i = 0; i < 32; ++i) v[i] = silu_fast(v[i]);
                     store32_bf16(p.out1 + obase + c * 32, v);
                 } else if (p.epi == EPI_SILU_BWD) {
                     float h[32];
                     load32_bf16(p.in0 + obase + c * 32, h);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= dsilu_f(h[i]);
+                    for (int i = 0; i < 32; ++i) v[i] *= dsilu_fast(h[i]);
                     store32_bf16(p.out0 + obase + c * 32, v);
                 } else {  // EPI_SWIGLU_BWD: v = dact
                     float g[32], u[32], o[32];
                     load32_bf16(p.in0 + obase + c * 32, g);
                     load32_bf16(p.in1 + obase + c * 32, u);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = v[i] * u[i] * dsilu_f(g[i]);
+                    for (int i = 0; i < 32; ++i) o[i] = v[i] * u[i] * dsilu_fast(g[i]);
                     store32_bf16(p.out0 + obase + c * 32, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = v[i] * silu_f(g[i]);
+                    for (int i = 0; i < 32; ++i) o[i] = v[i] * silu_fast(g[i]);
                     store32_bf16(p.out1 + obase + c * 32, o);
                 }
             }

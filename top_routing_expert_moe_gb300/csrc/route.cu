@@ -4,8 +4,9 @@
 // a [B,K] top-K index, outputs weighted by the post-softmax score.
 // [ZeRO3-MoE] §5.3: gating in fp32 even for half-precision models.
 //
-// bf16: one CTA per 128 tokens, 8 warps x 16 tokens; the x tile streams
-// through a 4-stage cp.async ring (the kernel is HBM-bound: x is read once);
+// bf16: one CTA per TT tokens (16..128, chosen so the grid covers the GPU),
+// 8 warps splitting each stage's 128 rows into (k-slice, 16 tokens); the x
+// tile streams through a 4-stage cp.async ring (HBM-bound: x is read once);
 // the router contraction runs on the tensor cores (mma.sync m16n8k16, fp32
 // accumulate) so that the E flops/byte never throttle the HBM stream.  The
 // logits tile lands in shared memory and one thread per token finishes the
@@ -142,49 +143,59 @@ __global__ void transpose_router_kernel(const __nv_bfloat16* __restrict__ Wr,
     }
 }
 
-template <int NT>  // NT = E_pad / 8 tensor-core n-tiles
+// One CTA = TT tokens.  The 8 warps split the 128 rows of each smem stage as
+// (k-slice, token): with NKS = 128 / TT k-slices, a stage holds NKS x 64 columns
+// of x for the CTA's TT tokens, so small token counts still spread over many
+// CTAs (split-K across warps); the k-slice partials are summed in a fixed order.
+template <int NT, int TT>  // NT = E_pad / 8 tensor-core n-tiles; TT tokens per CTA
 __global__ void __launch_bounds__(256) route_bf16_kernel(const __nv_bfloat16* __restrict__ x,
                                                          const __nv_bfloat16* __restrict__ WrT,
                                                          RouteOut o)
 {
     constexpr int E_PAD = NT * 8;
+    constexpr int NKS = RT_TOK / TT;            // k-slices per stage
     constexpr int LDL = E_PAD + 1;
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-    __nv_bfloat16* sW = sX + RT_STAGES * RT_TOK * RT_LDS;
-    float* sLog = reinterpret_cast<float*>(sW + RT_STAGES * E_PAD * RT_LDS);
-    int* sSel = reinterpret_cast<int*>(sLog + RT_TOK * LDL);
-    float* sEnt = reinterpret_cast<float*>(sSel + RT_TOK * 8);
-    int* sBad = reinterpret_cast<int*>(sEnt + RT_TOK);
+    __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(smem_raw);      // [S][128][LDS]
+    __nv_bfloat16* sW = sX + RT_STAGES * RT_TOK * RT_LDS;                // [S][NKS*E_PAD][LDS]
+    float* sLog = reinterpret_cast<float*>(sW + RT_STAGES * NKS * E_PAD * RT_LDS);  // [TT][LDL]
+    int* sSel = reinterpret_cast<int*>(sLog + TT * LDL);
+    float* sEnt = reinterpret_cast<float*>(sSel + TT * 8);
+    int* sBad = reinterpret_cast<int*>(sEnt + TT);
+    float* sRed = reinterpret_cast<float*>(smem_raw);                    // reuses the ring
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
-    const int t0 = blockIdx.x * RT_TOK;
-    const int ntok = min(RT_TOK, o.T - t0);
+    const int t0 = blockIdx.x * TT;
+    const int ntok = min(TT, o.T - t0);
     const int d = o.d;
-    const int nk = d / RT_BK;
+    const int kw = RT_BK * NKS;                  // columns per stage
+    const int nk = d / kw;
 
     auto load_stage = [&](int kc, int st) {
-        const int k0 = kc * RT_BK;
+        const int k0 = kc * kw;
         __nv_bfloat16* dX = sX + st * RT_TOK * RT_LDS;
 #pragma unroll
         for (int r = 0; r < (RT_TOK * RT_BK / 8) / 256; ++r) {
-            int s = tid + r * 256;
-            int row = s >> 3, c = s & 7;
-            bool ok = row < ntok;
-            const __nv_bfloat16* src = ok ? x + (size_t)(t0 + row) * d + k0 + c * 8 : x;
+            const int s = tid + r * 256;
+            const int row = s >> 3, c = s & 7;
+            const int ks = row / TT, tok = row % TT;
+            const bool ok = tok < ntok;
+            const __nv_bfloat16* src = ok ? x + (size_t)(t0 + tok) * d + k0 + ks * RT_BK + c * 8 : x;
             cp_async16(dX + row * RT_LDS + c * 8, src, ok);
         }
-        __nv_bfloat16* dW = sW + st * E_PAD * RT_LDS;
-        for (int s = tid; s < E_PAD * 8; s += 256) {
-            int row = s >> 3, c = s & 7;
-            cp_async16(dW + row * RT_LDS + c * 8, WrT + (size_t)row * d + k0 + c * 8, true);
+        __nv_bfloat16* dW = sW + st * NKS * E_PAD * RT_LDS;
+        for (int s = tid; s < NKS * E_PAD * 8; s += 256) {
+            const int row = s >> 3, c = s & 7;   // row = ks * E_PAD + e
+            const int ks = row / E_PAD, e = row % E_PAD;
+            cp_async16(dW + row * RT_LDS + c * 8, WrT + (size_t)e * d + k0 + ks * RT_BK + c * 8, true);
         }
     };
 
     float acc[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    const int my_ks = (warp * 16) / TT;
 
 #pragma unroll
     for (int s = 0; s < RT_STAGES - 1; ++s) {
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(256) route_bf16_kernel(const __nv_bfloat16* __
         __syncthreads();
         const int st = kc % RT_STAGES;
         const __nv_bfloat16* A = sX + st * RT_TOK * RT_LDS + (warp * 16) * RT_LDS;
-        const __nv_bfloat16* B = sW + st * E_PAD * RT_LDS;
+        const __nv_bfloat16* B = sW + (st * NKS + my_ks) * E_PAD * RT_LDS;
 #pragma unroll
         for (int ks = 0; ks < RT_BK / 16; ++ks) {
             const int kk = ks * 16 + 2 * tq;
@@ -220,13 +231,23 @@ __global__ void __launch_bounds__(256) route_bf16_kernel(const __nv_bfloat16* __
         cp_async_commit();
     }
     cp_async_wait<0>();
+    __syncthreads();                             // ring no longer read: reuse it
+    // partial sums of this warp's k-slice: sRed[ks][tok][E_PAD]
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        const int r0 = warp * 16 + g, c0 = n * 8 + 2 * tq;
-        sLog[r0 * LDL + c0] = acc[n][0];
-        sLog[r0 * LDL + c0 + 1] = acc[n][1];
-        sLog[(r0 + 8) * LDL + c0] = acc[n][2];
-        sLog[(r0 + 8) * LDL + c0 + 1] = acc[n][3];
+        const int r0 = warp * 16 + g, c0 = n * 8 + 2 * tq;   // r0 = ks * TT + tok
+        sRed[r0 * E_PAD + c0] = acc[n][0];
+        sRed[r0 * E_PAD + c0 + 1] = acc[n][1];
+        sRed[(r0 + 8) * E_PAD + c0] = acc[n][2];
+        sRed[(r0 + 8) * E_PAD + c0 + 1] = acc[n][3];
+    }
+    __syncthreads();
+    for (int i = tid; i < TT * E_PAD; i += 256) {
+        const int tok = i / E_PAD, e = i % E_PAD;
+        float v = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) v += sRed[(ks * TT + tok) * E_PAD + e];
+        sLog[tok * LDL + e] = v;
     }
     __syncthreads();
     finish_tile(sLog, LDL, sSel, sEnt, sBad, t0, ntok, o);
@@ -336,8 +357,25 @@ __global__ void route_finalize_kernel(int nblk, int T, int E, int k, float aux_c
 
 }  // namespace
 
+// Tokens per CTA of the bf16 router: the largest TT whose grid still covers two
+// waves of the GPU, else the smallest legal TT.  TT must keep a stage's router
+// columns within 64 rows (NKS * E_pad <= 64) and split d evenly into NKS slices.
+int route_tile_tokens(const moe_config& c) {
+    if (c.dtype != MOE_DTYPE_BF16) return RT_TOK;
+    const int e_pad = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
+    int best = -1, smallest = -1;
+    for (int tt = 16; tt <= RT_TOK; tt *= 2) {
+        const int nks = RT_TOK / tt;
+        if (nks * e_pad > 64 || (c.d / RT_BK) % nks != 0) continue;
+        if (smallest < 0) smallest = tt;
+        if ((c.T + tt - 1) / tt >= 2 * num_sms()) best = tt;
+    }
+    return best > 0 ? best : smallest;
+}
+
 size_t route_ws_bytes(const moe_config& c) {
-    const size_t nblk = (size_t)(c.T + RT_TOK - 1) / RT_TOK;
+    const int tt = route_tile_tokens(c);
+    const size_t nblk = (size_t)(c.T + tt - 1) / tt;
     const int e_pad = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
     size_t b = 0;
     b += align_up(nblk * c.E * 4);          // counts
@@ -348,11 +386,40 @@ size_t route_ws_bytes(const moe_config& c) {
     return b;
 }
 
+namespace {
+int finalize_route(const moe_config& c, const RouteOut& o, int nblk, int32_t* counts,
+                   float* stats, cudaStream_t st) {
+    route_finalize_kernel<<<1, 64, 0, st>>>(nblk, c.T, c.E, c.k, c.aux_coef, o.part_counts,
+                                            o.part_psum, o.part_ent, o.part_bad, counts, stats,
+                                            device_status_ptr());
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+template <int NT, int TT>
+int launch_route_bf16(const __nv_bfloat16* x, const __nv_bfloat16* WrT, const RouteOut& o,
+                      int nblk, cudaStream_t st) {
+    constexpr int E_PAD = NT * 8, NKS = RT_TOK / TT;
+    const size_t smem = (size_t)RT_STAGES * (RT_TOK + NKS * E_PAD) * RT_LDS * 2 +
+                        (size_t)TT * (E_PAD + 1) * 4 + (size_t)TT * 8 * 4 + (size_t)TT * 4 * 2;
+    static bool attr_set = false;  // the size is fixed per instantiation
+    if (!attr_set) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(route_bf16_kernel<NT, TT>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        attr_set = true;
+    }
+    route_bf16_kernel<NT, TT><<<nblk, 256, smem, st>>>(x, WrT, o);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+}  // namespace
+
 int launch_route(const moe_config& c, const void* x, const void* Wr, const float* bias,
                  const float* noise, float* logits, int32_t* topk, float* gate, int32_t* counts,
                  float* stats, void* ws, cudaStream_t st)
 {
-    const int nblk = (c.T + RT_TOK - 1) / RT_TOK;
+    const int tt = route_tile_tokens(c);
+    const int nblk = (c.T + tt - 1) / tt;
     const int e_pad = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
     uint8_t* w = static_cast<uint8_t*>(ws);
     RouteOut o;
@@ -363,46 +430,38 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
     o.part_ent = reinterpret_cast<float*>(w); w += align_up((size_t)nblk * 4);
     o.part_bad = reinterpret_cast<int32_t*>(w); w += align_up((size_t)nblk * 4);
 
-    const size_t tail = (RT_TOK * 8) * 4 + RT_TOK * 4 * 2;  // sSel, sEnt, sBad
     if (c.dtype == MOE_DTYPE_BF16) {
         __nv_bfloat16* WrT = reinterpret_cast<__nv_bfloat16*>(w);
         transpose_router_kernel<<<64, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(Wr), WrT,
                                                     c.d, c.E, e_pad);
         MOE_LAUNCH_CHECK();
-        const size_t smem = (size_t)RT_STAGES * (RT_TOK + e_pad) * RT_LDS * 2 +
-                            (size_t)RT_TOK * (e_pad + 1) * 4 + tail;
         const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-#define MOE_ROUTE_CASE(NT)                                                                   \
-    case NT: {                                                                               \
-        MOE_CUDA_TRY(cudaFuncSetAttribute(route_bf16_kernel<NT>,                             \
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,       \
-                                          (int)smem));                                       \
-        route_bf16_kernel<NT><<<nblk, 256, smem, st>>>(xb, WrT, o);                          \
-        MOE_LAUNCH_CHECK();                                                                  \
-        break;                                                                               \
-    }
-        switch (e_pad / 8) {
-            MOE_ROUTE_CASE(1)
-            MOE_ROUTE_CASE(2)
-            MOE_ROUTE_CASE(4)
-            MOE_ROUTE_CASE(8)
+        const int key = (e_pad / 8) * 1000 + tt;
+        int r = MOE_OK;
+        switch (key) {
+            case 1016: r = launch_route_bf16<1, 16>(xb, WrT, o, nblk, st); break;
+            case 1032: r = launch_route_bf16<1, 32>(xb, WrT, o, nblk, st); break;
+            case 1064: r = launch_route_bf16<1, 64>(xb, WrT, o, nblk, st); break;
+            case 1128: r = launch_route_bf16<1, 128>(xb, WrT, o, nblk, st); break;
+            case 2032: r = launch_route_bf16<2, 32>(xb, WrT, o, nblk, st); break;
+            case 2064: r = launch_route_bf16<2, 64>(xb, WrT, o, nblk, st); break;
+            case 2128: r = launch_route_bf16<2, 128>(xb, WrT, o, nblk, st); break;
+            case 4064: r = launch_route_bf16<4, 64>(xb, WrT, o, nblk, st); break;
+            case 4128: r = launch_route_bf16<4, 128>(xb, WrT, o, nblk, st); break;
+            case 8128: r = launch_route_bf16<8, 128>(xb, WrT, o, nblk, st); break;
             default: return MOE_ERR_UNSUPPORTED;
         }
-#undef MOE_ROUTE_CASE
-    } else {
-        const size_t smem = (size_t)RT_TOK * 33 * 4 + (size_t)32 * c.E * 4 +
-                            (size_t)RT_TOK * (c.E + 1) * 4 + tail;
-        MOE_CUDA_TRY(cudaFuncSetAttribute(route_f32_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        route_f32_kernel<<<nblk, 256, smem, st>>>(static_cast<const float*>(x),
-                                                  static_cast<const float*>(Wr), o);
-        MOE_LAUNCH_CHECK();
+        return r != MOE_OK ? r : finalize_route(c, o, nblk, counts, stats, st);
     }
-    route_finalize_kernel<<<1, 64, 0, st>>>(nblk, c.T, c.E, c.k, c.aux_coef, o.part_counts,
-                                            o.part_psum, o.part_ent, o.part_bad, counts, stats,
-                                            device_status_ptr());
+    const size_t tail = (RT_TOK * 8) * 4 + RT_TOK * 4 * 2;  // sSel, sEnt, sBad
+    const size_t smem = (size_t)RT_TOK * 33 * 4 + (size_t)32 * c.E * 4 +
+                        (size_t)RT_TOK * (c.E + 1) * 4 + tail;
+    MOE_CUDA_TRY(cudaFuncSetAttribute(route_f32_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    route_f32_kernel<<<nblk, 256, smem, st>>>(static_cast<const float*>(x),
+                                              static_cast<const float*>(Wr), o);
     MOE_LAUNCH_CHECK();
-    return MOE_OK;
+    return finalize_route(c, o, nblk, counts, stats, st);
 }
 
 }  // namespace moe
