@@ -6,8 +6,9 @@ One step = the whole hot path on one batch of synthetic tokens: router,
 permutation, grouped expert FFN, combine (forward) and the full backward
 (combine-bwd, grouped FFN backward, router backward), all through the C ABI,
 replayed as one CUDA graph (the ABI does no host sync and no allocation, so
-the step is capturable).  An eager pass with events between the C-ABI calls
-gives the per-stage times and the grouped-GEMM roofline.
+the step is capturable).  Per-stage times (and the grouped-GEMM roofline) come
+from each C-ABI call captured as its own graph and replayed between events,
+in step order; `eager_ms_per_step` is the same step launched call by call.
 Inputs and weights are resident in HBM before the timed region; L2 is
 flushed (512 MB write) before every timed step, outside its event pair.
 Under torchrun each rank runs an independent replica on its own GPU (the
@@ -339,15 +340,50 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         fwd_ms = float(np.mean([a.elapsed_time(c) for a, c in fwd_evs]))
 
-        # per-stage breakdown (eager launches, events between C-ABI calls)
-        stage_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
+        # per-stage breakdown: each C-ABI call captured as its own CUDA graph and
+        # replayed between events (device time, no host launch overhead)
+        stage_fns = [
+            lambda: moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts,
+                                  L.stats, L.ws, st),
+            lambda: moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept,
+                                    L.offsets, L.stats, L.ws, st),
+            lambda: moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
+                                        L.y_perm, L.ws, st),
+            lambda: moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st),
+            lambda: moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token,
+                                             L.offsets, bw["dy"], bw["dgate"], st),
+            lambda: moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved,
+                                                 L.act, bw["dy"], bw["dh"], bw["dxp"], g["dW_up"],
+                                                 g["dW_gate"], g["dW_down"], L.ws, st),
+            lambda: moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of,
+                                            bw["dgate"], bw["dxp"], L.stats, g["dx"], g["dW_r"],
+                                            g["dbias"] if b is not None else None, bw["dlogits"],
+                                            L.ws, st),
+        ]
+        stage_graphs = []
+        for fn in stage_fns:
+            sg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(sg, stream=st):
+                fn()
+            stage_graphs.append(sg)
+        torch.cuda.synchronize(dev)
+        per = np.zeros((args.steps, len(stage_graphs)))
+        for i in range(args.steps):
+            evs = [(ev(), ev()) for _ in stage_graphs]
+            flush.zero_()
+            for j, sg in enumerate(stage_graphs):   # in step order, so inputs are fresh
+                evs[j][0].record(st)
+                sg.replay()
+                evs[j][1].record(st)
+            torch.cuda.synchronize(dev)
+            per[i] = [a.elapsed_time(c) for a, c in evs]
+        stage_ms = per.mean(0)
+        eager_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
         for i in range(args.steps):
             flush.zero_()
-            step(stage_evs[i])
+            step(eager_evs[i])
         torch.cuda.synchronize(dev)
-        per = np.array([[s_[j].elapsed_time(s_[j + 1]) for j in range(7)] for s_ in stage_evs])
-        stage_ms = per.mean(0)
-        eager_ms = float(per.sum(1).mean())
+        eager_ms = float(np.mean([e_[0].elapsed_time(e_[7]) for e_ in eager_evs]))
 
         # end to end through the public API: pinned host inputs in, results out
         x_h = x.cpu().pin_memory()

@@ -130,6 +130,16 @@ def permute(cfg, topk_idx):
     return dict(kept=kept, offsets=offsets, perm_token=perm[:offsets[-1]].copy(), slot_of=slot)
 
 
+def stats(cfg, probs, counts, kept, nonfinite=0):
+    """Step 9 statistics (layout ST_*) from routed probabilities and counts."""
+    out = np.empty(8 + cfg.E)
+    lib().oracle_stats(ctypes.byref(cfg.c()), _p(_d(probs)),
+                       _p(np.ascontiguousarray(counts, np.int32)),
+                       _p(np.ascontiguousarray(kept, np.int32)), ctypes.c_int(int(nonfinite)),
+                       _p(out))
+    return out
+
+
 def expert_apply(cfg, e, x_row, Wup, Wgate, Wdown):
     y = np.empty(cfg.d, np.float64)
     lib().oracle_expert_apply(ctypes.byref(cfg.c()), int(e), _p(_d(x_row)), _p(_d(Wup)),
@@ -166,8 +176,9 @@ def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in
 
 
 def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgate=None,
-             with_bias=False, per_slot=False):
-    """Step 10: gradients of <dout, out> + aux loss (written, not accumulated)."""
+             with_bias=False, per_slot=False, pbar=None, T_aux=0):
+    """Step 10: gradients of <dout, out> + aux loss (written, not accumulated).
+    For a sample of a larger batch pass that batch's ``pbar`` and ``T_aux``."""
     x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
     logits, gate, dout = _d(logits), _d(gate), _d(dout)
     topk_idx = np.ascontiguousarray(topk_idx, np.int32)
@@ -181,5 +192,6 @@ def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgat
     lib().oracle_backward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(Wup), _p(Wgate), _p(Wdown),
                           _p(logits), _p(topk_idx), _p(gate), _p(slot_of), _p(dout),
                           *[_p(g[n]) for n in ("dx", "dWr", "db", "dWup", "dWgate", "dWdown",
-                                               "dgate", "dlogits", "dh_slot", "dxp_slot")])
+                                               "dgate", "dlogits", "dh_slot", "dxp_slot")],
+                          _p(_d(pbar)), ctypes.c_int(int(T_aux)))
     return g

@@ -337,14 +337,18 @@ void oracle_forward(const oracle_cfg* c, const double* x, const double* Wr, cons
  * dx[T,d], dWr[d,E], db[E] (may be NULL), dWup/dWgate[E,d,f], dWdown[E,f,d],
  * dgate[T,k] and dlogits[T,E] (both may be NULL).  Optional per-slot views of
  * the expert path (NULL = not wanted): dh_slot[T,k,nh,f] holds dh (SiLU) or
- * dg then du (SwiGLU); dxp_slot[T,k,d] holds the slot's dx contribution.      */
+ * dg then du (SwiGLU); dxp_slot[T,k,d] holds the slot's dx contribution.
+ * pbar_in (E) and T_aux: when the T tokens given are a sample of a larger batch,
+ * the aux-loss term uses that batch's mean probabilities and token count (NULL /
+ * 0: computed from the tokens given).                                          */
 void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
                      const double* Wup, const double* Wgate, const double* Wdown,
                      const double* logits, const int* topk, const double* gate,
                      const int* slot_of, const double* dout,
                      double* dx, double* dWr, double* db, double* dWup, double* dWgate,
                      double* dWdown, double* dgate_out, double* dlogits_out,
-                     double* dh_slot_out, double* dxp_slot_out)
+                     double* dh_slot_out, double* dxp_slot_out,
+                     const double* pbar_in, int T_aux)
 {
     const int T = c->T, d = c->d, f = c->f, E = c->E, k = c->k;
     const size_t df = (size_t)d * f;
@@ -441,8 +445,11 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
         for (int e = 0; e < E; ++e) { probs[(size_t)t * E + e] = exp(l[e] - m) / z; pbar[e] += probs[(size_t)t * E + e]; }
     }
     for (int e = 0; e < E; ++e) pbar[e] /= (double)T;
+    if (pbar_in)
+        for (int e = 0; e < E; ++e) pbar[e] = pbar_in[e];
+    const double Tn = T_aux > 0 ? (double)T_aux : (double)T;
     double* cvec = (double*)malloc(sizeof(double) * (size_t)E); /* dL_aux / dp[t,e] */
-    for (int e = 0; e < E; ++e) cvec[e] = c->aux_coef * 2.0 * (pbar[e] - 1.0 / E) / (double)T;
+    for (int e = 0; e < E; ++e) cvec[e] = c->aux_coef * 2.0 * (pbar[e] - 1.0 / E) / Tn;
 
     for (int t = 0; t < T; ++t) {
         const double* p = probs + (size_t)t * E;

@@ -257,3 +257,25 @@ def test_backward_gate_gradient_is_dot_with_expert_output(oracle_lib):
             else:
                 y = oracle.expert_apply(cfg, r["topk_idx"][t, j], x[t], Wup, None, Wd)
                 assert g["dgate"][t, j] == pytest.approx(float(dout[t] @ y), rel=1e-12)
+
+
+def test_backward_on_a_token_sample_matches_the_full_batch_rows(oracle_lib):
+    """Per-token gradients of a sampled sub-batch, with the full batch's pbar and T
+    for the aux term, equal those rows of the full-batch backward."""
+    rng = np.random.default_rng(21)
+    T, d, f, E, k = 40, 6, 10, 4, 2
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, swiglu=True, bias=True, noise=True)
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=0.8, swiglu=True,
+                              aux_coef=0.2)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, Wgate=Wg, bias=b, noise=nz)
+    dout = rng.standard_normal((T, d))
+    full = oracle.backward(cfg, x, Wr, Wup, Wd, r["logits"], r["topk_idx"], r["gate"],
+                           r["slot_of"], dout, Wgate=Wg)
+    idx = np.array([0, 3, 17, 39])
+    sub = oracle.OracleConfig(T=len(idx), d=d, f=f, E=E, k=k, capacity_factor=0.8, swiglu=True,
+                              aux_coef=0.2)
+    part = oracle.backward(sub, x[idx], Wr, Wup, Wd, r["logits"][idx], r["topk_idx"][idx],
+                           r["gate"][idx], r["slot_of"][idx], dout[idx], Wgate=Wg,
+                           pbar=r["stats"][oracle.ST_PBAR:], T_aux=T)
+    for key in ("dx", "dlogits", "dgate"):
+        np.testing.assert_allclose(part[key], full[key][idx], rtol=1e-12, atol=1e-14)

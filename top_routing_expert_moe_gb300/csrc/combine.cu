@@ -27,14 +27,17 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// out[t] = sum_j gate[t,j] * y_perm[slot_of[t,j]] (kept slots, j ascending)
+__host__ __device__ constexpr size_t align_up_dev(size_t b) { return (b + 255) / 256 * 256; }
+
+// out[t] = sum_j gate[t,j] * y_perm[slot_of[t,j]] (kept slots, j ascending).
+// One warp per token; each lane keeps 4 vectors of 16 bytes per slot in flight.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_of,
                                                       const float* __restrict__ gate, int Tn,
                                                       int d, int k, T* __restrict__ out)
 {
-    constexpr int V = 16 / sizeof(T);
+    constexpr int V = 16 / sizeof(T), U = 4;
     const int nv = d / V;
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
@@ -46,19 +49,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_pe
             slot[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
             g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
         }
-        for (int v = lane; v < nv; v += 32) {
-            float acc[V];
+        for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+            float acc[U][V];
 #pragma unroll
-            for (int q = 0; q < V; ++q) acc[q] = 0.f;
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[u][q] = 0.f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (slot[j] < 0) continue;
-                float y[V];
-                load16_f<T>(y_perm + (size_t)slot[j] * d + v * V, y);
+                const T* row = y_perm + (size_t)slot[j] * d;
+                uint4 raw[U];
 #pragma unroll
-                for (int q = 0; q < V; ++q) acc[q] = fmaf(g[j], y[q], acc[q]);
+                for (int u = 0; u < U; ++u)
+                    raw[u] = (v0 + 32 * u < nv) ? __ldg(reinterpret_cast<const uint4*>(row) + v0 + 32 * u)
+                                                : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float y[V];
+                    load16_f<T>(reinterpret_cast<const T*>(&raw[u]), y);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g[j], y[q], acc[u][q]);
+                }
             }
-            store16_f<T>(out + (size_t)t * d + v * V, acc);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (v0 + 32 * u < nv) store16_f<T>(out + (size_t)t * d + (v0 + 32 * u) * V, acc[u]);
         }
     }
 }
@@ -125,9 +141,10 @@ __global__ void transpose_wr_f32_kernel(const T* __restrict__ Wr, float* __restr
     }
 }
 
-// One warp per token: dlogits (gate Jacobian + aux term), then
-// dx[t] = sum_kept dx_perm[slot] + dlogits[t] . W_r^T.
-template <typename T>
+// One warp per token: dlogits (gate Jacobian + aux term); with WITH_DX also
+// dx[t] = sum_kept dx_perm[slot] + dlogits[t] . W_r^T (the fp32 path; the bf16
+// path forms dx in router_dx_bf16_kernel on the tensor cores).
+template <typename T, bool WITH_DX>
 __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ topk,
     const float* __restrict__ gate, const int32_t* __restrict__ slot_of,
@@ -187,6 +204,7 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
         }
         if (lane < E) { dlogits[(size_t)t * E + lane] = dl0; s_dl[wib][lane] = dl0; }
         if (lane + 32 < E) { dlogits[(size_t)t * E + lane + 32] = dl1; s_dl[wib][lane + 32] = dl1; }
+        if (!WITH_DX) continue;
         __syncwarp();
         int slot[8];
 #pragma unroll
@@ -221,6 +239,252 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     }
 }
 
+// dx for the bf16 path: dx[t] = sum_kept dx_perm[slot] + dlogits[t] . W_r^T.
+// The router term is a [T, E] x [E, d] contraction with K = E (<= 64): it runs
+// on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulate)
+// with the CTA's 128 columns of W_r staged once in shared memory, so W_r is
+// not re-read per token.  CTA = 8 warps sharing one 128-column chunk; a warp
+// takes 16-token tiles: 16 MMA n-tiles write the router term to its smem
+// tile, then half-warps add the kept dx_perm rows (16-byte vectors) and store.
+constexpr int RDX_CW = 128;  // columns per CTA
+
+template <int KS>  // KS = ceil(E / 16) k-steps
+__global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
+    const float* __restrict__ dlogits, const __nv_bfloat16* __restrict__ Wr,
+    const int32_t* __restrict__ slot_of, const __nv_bfloat16* __restrict__ dx_perm, int Tn, int d,
+    int E, int k, __nv_bfloat16* __restrict__ dx)
+{
+    constexpr int E16 = KS * 16, LDW = E16 + 2, LDO = RDX_CW + 4;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __nv_bfloat16* sW = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [128][LDW]
+    float* sOut = reinterpret_cast<float*>(smem_raw + align_up_dev(RDX_CW * LDW * 2)); // [8][16][LDO]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const int hl = lane & 15, hw = lane >> 4;
+    const int c0 = blockIdx.x * RDX_CW;
+    const int col = c0 + hl * 8;
+    for (int i = tid; i < RDX_CW * E16; i += 256) {
+        const int cc = i / E16, e = i % E16;
+        sW[cc * LDW + e] = (e < E && c0 + cc < d) ? Wr[(size_t)(c0 + cc) * E + e]
+                                                  : __float2bfloat16_rn(0.f);
+    }
+    __syncthreads();
+    float* so = sOut + warp * 16 * LDO;
+    const int ntiles = (Tn + 15) / 16;
+    for (int wt = blockIdx.y * 8 + warp; wt < ntiles; wt += gridDim.y * 8) {
+        const int t0 = wt * 16;
+        // round trip 1: this tile's dlogits (A fragments) and the half-warp's
+        // first two slot indices for its 8 tokens, all independent loads
+        auto dl_pair = [&](int row, int e) -> uint32_t {
+            const int t = t0 + row;
+            const float lo = (t < Tn && e < E) ? __ldg(dlogits + (size_t)t * E + e) : 0.f;
+            const float hi = (t < Tn && e + 1 < E) ? __ldg(dlogits + (size_t)t * E + e + 1) : 0.f;
+            __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
+            return *reinterpret_cast<uint32_t*>(&bb);
+        };
+        uint32_t a[KS][4];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            a[ks][0] = dl_pair(g, ks * 16 + 2 * tq);
+            a[ks][1] = dl_pair(g + 8, ks * 16 + 2 * tq);
+            a[ks][2] = dl_pair(g, ks * 16 + 2 * tq + 8);
+            a[ks][3] = dl_pair(g + 8, ks * 16 + 2 * tq + 8);
+        }
+        int sl[2][8];
+        auto load_slots = [&](int j0) {
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int t = t0 + hw + 2 * i;
+                    sl[jj][i] = (t < Tn && j0 + jj < k) ? __ldg(slot_of + (size_t)t * k + j0 + jj) : -1;
+                }
+        };
+        load_slots(0);
+        // router term of the 16 tokens x 128 columns on the tensor cores
+#pragma unroll 4
+        for (int nt = 0; nt < RDX_CW / 8; ++nt) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            const __nv_bfloat16* wrow = sW + (nt * 8 + g) * LDW;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(wrow + ks * 16 + 2 * tq);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(wrow + ks * 16 + 2 * tq + 8);
+                asm volatile(
+                    "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                    "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                    : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                    : "r"(a[ks][0]), "r"(a[ks][1]), "r"(a[ks][2]), "r"(a[ks][3]), "r"(b0), "r"(b1));
+            }
+            so[g * LDO + nt * 8 + 2 * tq] = c[0];
+            so[g * LDO + nt * 8 + 2 * tq + 1] = c[1];
+            so[(g + 8) * LDO + nt * 8 + 2 * tq] = c[2];
+            so[(g + 8) * LDO + nt * 8 + 2 * tq + 1] = c[3];
+        }
+        __syncwarp();
+        // round trip 2 (per pair of slots): 16 row loads in flight per lane;
+        // a half-warp covers the chunk's 128 columns for 8 tokens
+        if (col < d) {
+            float acc[8][8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = hw + 2 * i;
+                const float4 s0 = *reinterpret_cast<const float4*>(so + r * LDO + hl * 8);
+                const float4 s1 = *reinterpret_cast<const float4*>(so + r * LDO + hl * 8 + 4);
+                acc[i][0] = s0.x; acc[i][1] = s0.y; acc[i][2] = s0.z; acc[i][3] = s0.w;
+                acc[i][4] = s1.x; acc[i][5] = s1.y; acc[i][6] = s1.z; acc[i][7] = s1.w;
+            }
+            for (int j0 = 0; j0 < k; j0 += 2) {
+                if (j0 > 0) load_slots(j0);
+                uint4 y[2][8];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        y[jj][i] = sl[jj][i] >= 0
+                                       ? __ldg(reinterpret_cast<const uint4*>(dx_perm + (size_t)sl[jj][i] * d + col))
+                                       : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t w4[4] = {y[jj][i].x, y[jj][i].y, y[jj][i].z, y[jj][i].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            acc[i][2 * q] += __uint_as_float(w4[q] << 16);
+                            acc[i][2 * q + 1] += __uint_as_float(w4[q] & 0xFFFF0000u);
+                        }
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = t0 + hw + 2 * i;
+                if (t < Tn) store16_f<__nv_bfloat16>(dx + (size_t)t * d + col, acc[i]);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// dW_r on the tensor cores (bf16 path): part[s][i][e] = sum over the token chunk s
+// of x[t,i] dlogits[t,e], as the [E16 x 16 tokens] x [16 tokens x 8 cols] MMAs
+// dl^T x.  CTA = 4 warps on a 128-column chunk (32 columns each); 16-token x
+// tiles stream through a 4-stage cp.async ring; dlogits are staged transposed
+// (tokens contiguous) so the A fragments are plain 32-bit loads; B fragments come
+// from ldmatrix.trans of the row-major x tile.  Column-chunk-0 CTAs also sum
+// dlogits over the chunk for dbias.
+constexpr int DWM_STAGES = 4, DWM_LDX = 128 + 8;
+
+template <int MT>  // MT = ceil(E / 16) expert m-tiles
+__global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __restrict__ x,
+                                                      const float* __restrict__ dlogits, int Tn,
+                                                      int d, int E, int chunk,
+                                                      float* __restrict__ part,
+                                                      float* __restrict__ part_db)
+{
+    constexpr int E16 = MT * 16, LDT = 16 + 8;  // dlT row: 16 tokens (+pad)
+    __shared__ __align__(16) __nv_bfloat16 sX[DWM_STAGES][16][DWM_LDX];
+    __shared__ __align__(16) __nv_bfloat16 sD[DWM_STAGES][E16][LDT];
+    __shared__ float sDb[128];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const int c0 = blockIdx.x * 128;
+    const int tbeg = blockIdx.y * chunk, tend = min(Tn, tbeg + chunk);
+    const int nblk16 = (tend - tbeg + 15) / 16;
+    float db = 0.f;  // this thread's dbias share (expert tid % E16), column chunk 0 only
+    auto load = [&](int b, int st) {
+        const int t0 = tbeg + b * 16;
+        // x tile: 16 rows x 128 columns = 256 vectors of 16 bytes, two per thread
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int v = tid + r * 128;
+            const int row = v >> 4, cv = v & 15;
+            const int t = t0 + row, cc = c0 + cv * 8;
+            const bool ok = t < tend && cc < d;
+            const __nv_bfloat16* src = ok ? x + (size_t)t * d + cc : x;
+            const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&sX[st][row][cv * 8]);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                         "r"(ok ? 16 : 0));
+        }
+        // dlogits tile transposed to [e][t] in bf16
+        for (int i = tid; i < 16 * E16; i += 128) {
+            const int row = i / E16, e = i % E16;
+            const int t = t0 + row;
+            const float v = (t < tend && e < E) ? __ldg(dlogits + (size_t)t * E + e) : 0.f;
+            sD[st][e][row] = __float2bfloat16_rn(v);
+            if (blockIdx.x == 0) db += v;
+        }
+    };
+    float acc[MT][4][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
+#pragma unroll
+    for (int s = 0; s < DWM_STAGES - 1; ++s) {
+        if (s < nblk16) load(s, s);
+        asm volatile("cp.async.commit_group;\n" ::);
+    }
+    for (int b = 0; b < nblk16; ++b) {
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(DWM_STAGES - 2));
+        __syncthreads();
+        const int st = b % DWM_STAGES;
+        uint32_t af[MT][4];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            af[m][0] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g][2 * tq]);
+            af[m][1] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g + 8][2 * tq]);
+            af[m][2] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g][2 * tq + 8]);
+            af[m][3] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g + 8][2 * tq + 8]);
+        }
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            // B (k = token, n = column) from the row-major [token][col] tile
+            const int ncol = warp * 32 + n * 8;
+            const uint32_t addr = (uint32_t)__cvta_generic_to_shared(&sX[st][lane & 15][ncol]);
+            uint32_t b0, b1;
+            asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];\n"
+                         : "=r"(b0), "=r"(b1) : "r"(addr));
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                asm volatile(
+                    "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                    "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                    : "+f"(acc[m][n][0]), "+f"(acc[m][n][1]), "+f"(acc[m][n][2]), "+f"(acc[m][n][3])
+                    : "r"(af[m][0]), "r"(af[m][1]), "r"(af[m][2]), "r"(af[m][3]), "r"(b0), "r"(b1));
+        }
+        const int nxt = b + DWM_STAGES - 1;
+        if (nxt < nblk16) load(nxt, nxt % DWM_STAGES);
+        asm volatile("cp.async.commit_group;\n" ::);
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::);
+    // C fragment: rows = experts (g, g+8 of m-tile m), cols = 2tq, 2tq+1 of n-tile n
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int colb = c0 + warp * 32 + n * 8 + 2 * tq;
+            const int e_lo = m * 16 + g, e_hi = e_lo + 8;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int cc = colb + h;
+                if (cc >= d) continue;
+                float* dst = part + ((size_t)blockIdx.y * d + cc) * E;
+                if (e_lo < E) dst[e_lo] = acc[m][n][h];
+                if (e_hi < E) dst[e_hi] = acc[m][n][2 + h];
+            }
+        }
+    if (blockIdx.x == 0) {
+        sDb[tid] = db;
+        __syncthreads();
+        if (tid < E) {
+            float a = 0.f;
+            for (int i = tid; i < 128; i += E16) a += sDb[i];
+            part_db[(size_t)blockIdx.y * E + tid] = a;
+        }
+    }
+}
+
 // Partial dW_r over a token chunk: part[s][i][e] = sum_{t in chunk s} x[t,i] dlogits[t,e].
 // CTA = 32 column vectors (16 bytes each) x 8 token lanes; each thread keeps
 // V x EB accumulators (V columns of one vector, EB experts of this CTA's expert
@@ -235,10 +499,12 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(const T* __restrict__ 
 {
     constexpr int V = 16 / sizeof(T);
     extern __shared__ __align__(16) float red[];          // [8][32][V*EB]
+    // grid: x = expert group (fastest, so the groups of one x tile run together and
+    // the later ones read it from L2), y = column block, z = token chunk
     const int tid = threadIdx.x, tl = tid >> 5, cv = tid & 31;
-    const int col0 = (blockIdx.x * 32 + cv) * V;
-    const int e0 = blockIdx.z * EB;
-    const int s = blockIdx.y;
+    const int col0 = (blockIdx.y * 32 + cv) * V;
+    const int e0 = blockIdx.x * EB;
+    const int s = blockIdx.z;
     const int tbeg = s * chunk, tend = min(Tn, tbeg + chunk);
     const bool colok = col0 < d;
     float acc[V][EB];
@@ -246,13 +512,7 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(const T* __restrict__ 
     for (int v = 0; v < V; ++v)
 #pragma unroll
         for (int e = 0; e < EB; ++e) acc[v][e] = 0.f;
-    for (int t = tbeg + tl; t < tend; t += 8) {
-        float xv[V];
-        if (colok) load16_f<T>(x + (size_t)t * d + col0, xv);
-        else {
-#pragma unroll
-            for (int v = 0; v < V; ++v) xv[v] = 0.f;
-        }
+    auto consume = [&](const float* xv, int t) {
         float dl[EB];
 #pragma unroll
         for (int e = 0; e < EB; ++e) dl[e] = (e0 + e < E) ? __ldg(dlogits + (size_t)t * E + e0 + e) : 0.f;
@@ -260,6 +520,25 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(const T* __restrict__ 
         for (int v = 0; v < V; ++v)
 #pragma unroll
             for (int e = 0; e < EB; ++e) acc[v][e] = fmaf(xv[v], dl[e], acc[v][e]);
+    };
+    int t = tbeg + tl;
+    if (colok) {
+        for (; t + 24 < tend; t += 32) {   // four rows of this lane in flight
+            float xa[V], xb[V], xc[V], xd[V];
+            load16_f<T>(x + (size_t)t * d + col0, xa);
+            load16_f<T>(x + (size_t)(t + 8) * d + col0, xb);
+            load16_f<T>(x + (size_t)(t + 16) * d + col0, xc);
+            load16_f<T>(x + (size_t)(t + 24) * d + col0, xd);
+            consume(xa, t);
+            consume(xb, t + 8);
+            consume(xc, t + 16);
+            consume(xd, t + 24);
+        }
+        for (; t < tend; t += 8) {
+            float xa[V];
+            load16_f<T>(x + (size_t)t * d + col0, xa);
+            consume(xa, t);
+        }
     }
     float* mine = red + ((size_t)tl * 32 + cv) * (V * EB);
 #pragma unroll
@@ -273,10 +552,10 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(const T* __restrict__ 
         float a = 0.f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) a += red[((size_t)q * 32 + c) * (V * EB) + r];
-        const int col = (blockIdx.x * 32 + c) * V + v;
+        const int col = (blockIdx.y * 32 + c) * V + v;
         if (col < d && e0 + e < E) part[((size_t)s * d + col) * E + e0 + e] = a;
     }
-    if (blockIdx.x == 0 && blockIdx.z == 0 && tid < E) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid < E) {
         float a = 0.f;
         for (int t = tbeg; t < tend; ++t) a += dlogits[(size_t)t * E + tid];
         part_db[(size_t)s * E + tid] = a;
@@ -304,17 +583,29 @@ __global__ void dwr_reduce_kernel(const float* __restrict__ part, const float* _
 
 constexpr int DWR_EB = 8;  // experts per CTA of dwr_partial_kernel
 
-dim3 dwr_grid_xz(const moe_config& c) {
+// grid of dwr_partial_kernel without the token-chunk dimension (z)
+dim3 dwr_grid_xy(const moe_config& c) {
     const int V = c.dtype == MOE_DTYPE_BF16 ? 8 : 4;
-    return dim3((c.d + 32 * V - 1) / (32 * V), 1, (c.E + DWR_EB - 1) / DWR_EB);
+    return dim3((c.E + DWR_EB - 1) / DWR_EB, (c.d + 32 * V - 1) / (32 * V), 1);
 }
 
-// token chunks: enough CTAs for about four per SM
+// token chunks of the dW_r partial kernels: enough CTAs to fill the GPU, at most
+// 32 chunks so the final fixed-order reduction stays short
 int dwr_nsplit(const moe_config& c) {
-    const dim3 g = dwr_grid_xz(c);
-    const int per = (int)(g.x * g.z);
+    if (c.dtype == MOE_DTYPE_BF16) {
+        const int per = (c.d + 127) / 128;
+        const int ns = (8 * num_sms() + per - 1) / per;
+        return std::max(1, std::min(std::min(ns, 32), (c.T + 15) / 16));
+    }
+    const dim3 g = dwr_grid_xy(c);
+    const int per = (int)(g.x * g.y);
     int ns = std::max(1, (4 * num_sms() + per - 1) / per);
     return std::min(ns, std::max(1, (c.T + 63) / 64));
+}
+
+int dwr_chunk(const moe_config& c, int ns) {
+    const int ch = (c.T + ns - 1) / ns;
+    return c.dtype == MOE_DTYPE_BF16 ? (ch + 15) / 16 * 16 : ch;
 }
 
 int row_grid(int64_t rows) {
@@ -359,6 +650,44 @@ int launch_combine_backward(const moe_config& c, const void* dout, const void* y
     return MOE_OK;
 }
 
+#define MOE_TRY_R(x)                   \
+    do {                               \
+        int _r = (x);                  \
+        if (_r != MOE_OK) return _r;   \
+    } while (0)
+
+namespace {
+template <int KS>
+int launch_router_dx_ks(const moe_config& c, const float* dl, const __nv_bfloat16* Wr,
+                        const int32_t* slot_of, const __nv_bfloat16* dxp, __nv_bfloat16* dx,
+                        cudaStream_t st) {
+    constexpr int LDW = KS * 16 + 2;
+    const size_t smem = align_up_dev((size_t)RDX_CW * LDW * 2) + (size_t)8 * 16 * (RDX_CW + 4) * 4;
+    static bool attr = false;
+    if (!attr) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(router_dx_bf16_kernel<KS>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        attr = true;
+    }
+    const int gx = (c.d + RDX_CW - 1) / RDX_CW;
+    const int tiles = (c.T + 15) / 16;
+    // one wave: at most the resident CTA slots (2 per SM), no partial second wave
+    const int gy = std::max(1, std::min((tiles + 7) / 8, (2 * num_sms()) / gx));
+    router_dx_bf16_kernel<KS><<<dim3(gx, gy), 256, smem, st>>>(dl, Wr, slot_of, dxp, c.T, c.d, c.E,
+                                                               c.k, dx);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+}  // namespace
+
+int launch_router_dx_bf16(const moe_config& c, const float* dl, const __nv_bfloat16* Wr,
+                          const int32_t* slot_of, const __nv_bfloat16* dxp, __nv_bfloat16* dx,
+                          cudaStream_t st) {
+    if (c.E <= 16) return launch_router_dx_ks<1>(c, dl, Wr, slot_of, dxp, dx, st);
+    if (c.E <= 32) return launch_router_dx_ks<2>(c, dl, Wr, slot_of, dxp, dx, st);
+    return launch_router_dx_ks<4>(c, dl, Wr, slot_of, dxp, dx, st);
+}
+
 size_t router_bwd_ws_bytes(const moe_config& c) {
     const int ns = dwr_nsplit(c);
     return align_up((size_t)c.E * c.d * 4) + align_up((size_t)ns * c.d * c.E * 4) +
@@ -377,10 +706,10 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
     float* part = reinterpret_cast<float*>(w); w += align_up((size_t)ns * c.d * c.E * 4);
     float* part_db = reinterpret_cast<float*>(w); w += align_up((size_t)ns * c.E * 4);
     if (!dlogits) dlogits = reinterpret_cast<float*>(w);
-    const int chunk = (c.T + ns - 1) / ns;
+    const int chunk = dwr_chunk(c, ns);
     const int grid = row_grid(c.T);
-    dim3 pgrid = dwr_grid_xz(c);
-    pgrid.y = ns;
+    dim3 pgrid = dwr_grid_xy(c);
+    pgrid.z = ns;
     // reduction buffer: 8 token lanes x 32 vectors x (V * EB) floats, V = 16 / sizeof(T)
     const size_t dwr_smem = (size_t)8 * 32 * (c.dtype == MOE_DTYPE_BF16 ? 8 : 4) * DWR_EB * sizeof(float);
     if (c.dtype == MOE_DTYPE_BF16) {
@@ -400,14 +729,22 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
     }
     if (c.dtype == MOE_DTYPE_BF16) {
         using T = __nv_bfloat16;
-        transpose_wr_f32_kernel<T><<<64, 256, 0, st>>>(static_cast<const T*>(Wr), WrT, c.d, c.E);
+        router_bwd_token_kernel<T, false><<<grid, 256, 0, st>>>(
+            logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), nullptr,
+            c.T, c.d, c.E, c.k, c.normalize_gates, c.aux_coef, dlogits, static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();
-        router_bwd_token_kernel<T><<<grid, 256, 0, st>>>(
-            logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), WrT, c.T,
-            c.d, c.E, c.k, c.normalize_gates, c.aux_coef, dlogits, static_cast<T*>(dx));
-        MOE_LAUNCH_CHECK();
-        dwr_partial_kernel<T, DWR_EB><<<pgrid, 256, dwr_smem, st>>>(static_cast<const T*>(x), dlogits,
-                                                                   c.T, c.d, c.E, chunk, part, part_db);
+        MOE_TRY_R(launch_router_dx_bf16(c, dlogits, static_cast<const T*>(Wr), slot_of,
+                                        static_cast<const T*>(dx_perm), static_cast<T*>(dx), st));
+        const dim3 mgrid((c.d + 127) / 128, ns);
+        if (c.E <= 16)
+            dwr_mma_kernel<1><<<mgrid, 128, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
+                                                     chunk, part, part_db);
+        else if (c.E <= 32)
+            dwr_mma_kernel<2><<<mgrid, 128, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
+                                                     chunk, part, part_db);
+        else
+            dwr_mma_kernel<4><<<mgrid, 128, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
+                                                     chunk, part, part_db);
         MOE_LAUNCH_CHECK();
         dwr_reduce_kernel<T><<<std::min(1024, (c.d * c.E + 255) / 256), 256, 0, st>>>(
             part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);
@@ -416,7 +753,7 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
         using T = float;
         transpose_wr_f32_kernel<T><<<64, 256, 0, st>>>(static_cast<const T*>(Wr), WrT, c.d, c.E);
         MOE_LAUNCH_CHECK();
-        router_bwd_token_kernel<T><<<grid, 256, 0, st>>>(
+        router_bwd_token_kernel<T, true><<<grid, 256, 0, st>>>(
             logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), WrT, c.T,
             c.d, c.E, c.k, c.normalize_gates, c.aux_coef, dlogits, static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();

@@ -52,7 +52,7 @@ constexpr int BM = 128, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + 256 * BK * 2;  // 48 KB
 constexpr int GUARD_BYTES = 16 * 1024;        // slack after the ring
-constexpr int CTRL_BYTES = 1024;
+constexpr int CTRL_BYTES = 2048;   // barriers, TMEM slot, offsets[65], prefix[3*64+1]
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + GUARD_BYTES + CTRL_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
@@ -64,17 +64,18 @@ constexpr unsigned long long DRAIN_NS = 500000000ull;   // 0.5 s
 enum Epi { EPI_STORE = 0, EPI_SILU_FWD = 1, EPI_SWIGLU_FWD = 2, EPI_SILU_BWD = 3, EPI_SWIGLU_BWD = 4 };
 enum Sched { SCHED_ROWS = 0, SCHED_KSEG = 1 };
 
-struct TcParams {
+// One GEMM problem of a launch.  A launch runs up to MAX_PROBLEMS independent
+// problems over the same expert segments, their tiles in one schedule (the
+// backward's dgrad2 || dW_down, then dW_up || dW_gate || dgrad1).
+struct TcProblem {
     CUtensorMap tmA0, tmB0, tmA1, tmB1;
-    const int32_t* offsets;
     __nv_bfloat16* out0;
     __nv_bfloat16* out1;
     __nv_bfloat16* out2;
     const __nv_bfloat16* in0;
     const __nv_bfloat16* in1;
-    int* status;
     long long out_estride;  // SCHED_KSEG: elements between experts' outputs
-    int sched, E;
+    int sched;
     int n_blocks;           // N / bn
     int m_blocks;           // SCHED_KSEG: M / 128
     int k_blocks;           // SCHED_ROWS: K / 64 (per operand pair)
@@ -84,6 +85,14 @@ struct TcParams {
     int dual;               // two accumulators (B0 -> cols 0..127, B1 -> 128..255)
     int epi;
     int ldo;
+};
+constexpr int MAX_PROBLEMS = 3;
+
+struct TcParams {
+    TcProblem prob[MAX_PROBLEMS];
+    const int32_t* offsets;
+    int* status;
+    int nprob, E;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -232,28 +241,39 @@ __device__ __forceinline__ float dsilu_fast(float z) {
 
 // ---------------------------------------------------------------- schedule
 struct Tile {
-    int e, m0, n0, krow0, nk;
+    int p, e, m0, n0, krow0, nk;
 };
 
-// prefix[e] = first tile index of expert e; prefix[E] = total tiles
-__device__ __forceinline__ void decode_tile(const TcParams& p, const int* offs, const int* prefix,
+__device__ __forceinline__ int seg_m_blocks(const TcProblem& q, const int* offs, int e) {
+    return q.sched == SCHED_ROWS ? (offs[e + 1] - offs[e]) / BM : q.m_blocks;
+}
+
+// prefix[p*E + e] = first tile of (problem p, expert e); prefix[nprob*E] = total.
+// Binary search for the (problem, expert) slot holding tile tix.
+__device__ __forceinline__ void decode_tile(const TcParams& P, const int* offs, const int* prefix,
                                             int tix, Tile& t) {
-    int e = 0;
-    while (e + 1 < p.E && prefix[e + 1] <= tix) ++e;
-    const int local = tix - prefix[e];
-    const int mb_e = p.sched == SCHED_ROWS ? (offs[e + 1] - offs[e]) / BM : p.m_blocks;
-    const int gsz = RASTER_GM * p.n_blocks;
+    int lo = 0, hi = P.nprob * P.E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tix) lo = mid; else hi = mid - 1;
+    }
+    const int pi = lo / P.E, e = lo % P.E;
+    const TcProblem& q = P.prob[pi];
+    const int local = tix - prefix[lo];
+    const int mb_e = seg_m_blocks(q, offs, e);
+    const int gsz = RASTER_GM * q.n_blocks;
     const int grp = local / gsz;
     const int first = grp * RASTER_GM;
     const int gm = min(RASTER_GM, mb_e - first);
     const int r = local - grp * gsz;
     const int mb = first + r % gm, nb = r / gm;
+    t.p = pi;
     t.e = e;
-    t.n0 = nb * p.bn;
-    if (p.sched == SCHED_ROWS) {
+    t.n0 = nb * q.bn;
+    if (q.sched == SCHED_ROWS) {
         t.m0 = offs[e] + mb * BM;
         t.krow0 = 0;
-        t.nk = p.k_blocks * p.kconcat;
+        t.nk = q.k_blocks * q.kconcat;
     } else {
         t.m0 = mb * BM;
         t.krow0 = offs[e];
@@ -262,7 +282,7 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, const int* offs, 
 }
 
 // ---------------------------------------------------------------- kernel
-__global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams p)
+__global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams P)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -275,7 +295,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* offs = reinterpret_cast<int*>(tmem_slot + 2);  // [E+1] segment offsets
-    int* prefix = offs + 66;                            // [E+1] first tile of each expert
+    int* prefix = offs + 66;                            // [nprob*E+1] first tile of (problem, expert)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -292,7 +312,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < p.E + 1) offs[tid] = p.offsets[tid];
+    if (tid < P.E + 1) offs[tid] = P.offsets[tid];
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS));
@@ -303,53 +323,71 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     tc_fence_after();
     if (tid == 0) {
         int acc = 0;
-        for (int e = 0; e < p.E; ++e) {
-            prefix[e] = acc;
-            const int mb = p.sched == SCHED_ROWS ? (offs[e + 1] - offs[e]) / BM : p.m_blocks;
-            acc += mb * p.n_blocks;
-        }
-        prefix[p.E] = acc;
+        for (int pi = 0; pi < P.nprob; ++pi)
+            for (int e = 0; e < P.E; ++e) {
+                prefix[pi * P.E + e] = acc;
+                acc += seg_m_blocks(P.prob[pi], offs, e) * P.prob[pi].n_blocks;
+            }
+        prefix[P.nprob * P.E] = acc;
     }
     __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = prefix[p.E];
+    const int total = prefix[P.nprob * P.E];
     const uint32_t smem0 = smem_u32(base);
-    const uint32_t b_bytes = p.dual ? 2u * 128u * BK * 2u : (uint32_t)p.bn * BK * 2u;
-    const uint32_t stage_tx = (uint32_t)A_BYTES + b_bytes;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
+        for (int pi = 0; pi < P.nprob; ++pi) {   // the descriptors this launch uses
+            const TcProblem& q = P.prob[pi];
+            const CUtensorMap* m[4] = {&q.tmA0, &q.tmB0, &q.tmA1, &q.tmB1};
+            const int used = q.kconcat == 2 ? 4 : q.dual ? 2 : 2;
+            for (int i = 0; i < used; ++i)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m[i])) : "memory");
+            if (q.dual && q.kconcat != 2)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmB1)) : "memory");
+        }
         int it = 0;
         bool ok = true;
         for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x) {
             Tile t;
-            decode_tile(p, offs, prefix, tix, t);
+            decode_tile(P, offs, prefix, tix, t);
+            // per-tile copies of the problem's fields (registers, not re-read after each
+            // "memory"-clobbering wait)
+            const TcProblem& q = P.prob[t.p];
+            const int q_kseg = q.sched == SCHED_KSEG, q_kb = q.k_blocks, q_dual = q.dual;
+            const int q_bmn = q.b_mn, q_nb64 = q.bn / 64;
+            const CUtensorMap* tA0 = &q.tmA0;
+            const CUtensorMap* tA1 = &q.tmA1;
+            const CUtensorMap* tB0 = &q.tmB0;
+            const CUtensorMap* tB1 = &q.tmB1;
+            const uint32_t b_bytes = q_dual ? 2u * 128u * BK * 2u : (uint32_t)q.bn * BK * 2u;
+            const uint32_t stage_tx = (uint32_t)A_BYTES + b_bytes;
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status)) { ok = false; break; }
                 const uint32_t bar = smem_u32(&full[s]);
                 const uint32_t sA = smem0 + s * STAGE_BYTES, sB = sA + A_BYTES;
                 mbar_expect_tx(bar, stage_tx);
-                if (p.sched == SCHED_KSEG) {
+                if (q_kseg) {
                     const int kr = t.krow0 + kb * BK;
-                    tma_load3(&p.tmA0, sA, bar, t.m0, kr, 0);
-                    tma_load3(&p.tmA0, sA + 8192, bar, t.m0 + 64, kr, 0);
-                    for (int c = 0; c < p.bn / 64; ++c) tma_load3(&p.tmB0, sB + c * 8192, bar, t.n0 + 64 * c, kr, 0);
+                    tma_load3(tA0, sA, bar, t.m0, kr, 0);
+                    tma_load3(tA0, sA + 8192, bar, t.m0 + 64, kr, 0);
+                    for (int c = 0; c < q_nb64; ++c) tma_load3(tB0, sB + c * 8192, bar, t.n0 + 64 * c, kr, 0);
                 } else {
-                    const int phase = kb >= p.k_blocks ? 1 : 0;
-                    const int k0 = (kb - phase * p.k_blocks) * BK;
-                    tma_load3(phase ? &p.tmA1 : &p.tmA0, sA, bar, k0, t.m0, 0);
-                    if (p.dual) {
-                        tma_load3(&p.tmB0, sB, bar, t.n0, k0, t.e);
-                        tma_load3(&p.tmB0, sB + 8192, bar, t.n0 + 64, k0, t.e);
-                        tma_load3(&p.tmB1, sB + 16384, bar, t.n0, k0, t.e);
-                        tma_load3(&p.tmB1, sB + 24576, bar, t.n0 + 64, k0, t.e);
-                    } else if (p.b_mn) {
-                        for (int c = 0; c < p.bn / 64; ++c)
-                            tma_load3(&p.tmB0, sB + c * 8192, bar, t.n0 + 64 * c, k0, t.e);
+                    const int phase = kb >= q_kb ? 1 : 0;
+                    const int k0 = (kb - phase * q_kb) * BK;
+                    tma_load3(phase ? tA1 : tA0, sA, bar, k0, t.m0, 0);
+                    if (q_dual) {
+                        tma_load3(tB0, sB, bar, t.n0, k0, t.e);
+                        tma_load3(tB0, sB + 8192, bar, t.n0 + 64, k0, t.e);
+                        tma_load3(tB1, sB + 16384, bar, t.n0, k0, t.e);
+                        tma_load3(tB1, sB + 24576, bar, t.n0 + 64, k0, t.e);
+                    } else if (q_bmn) {
+                        for (int c = 0; c < q_nb64; ++c)
+                            tma_load3(tB0, sB + c * 8192, bar, t.n0 + 64 * c, k0, t.e);
                     } else {
-                        tma_load3(phase ? &p.tmB1 : &p.tmB0, sB, bar, k0, t.n0, t.e);
+                        tma_load3(phase ? tB1 : tB0, sB, bar, k0, t.n0, t.e);
                     }
                 }
             }
@@ -359,33 +397,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             mbar_drain(smem_u32(&full[i % STAGES]), (uint32_t)(i / STAGES) & 1u);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        const int nmma = p.dual ? 128 : p.bn;
-        const uint32_t idesc = idesc_bf16(BM, nmma, p.a_mn, p.b_mn);
         int it = 0, tcount = 0;
         bool ok = true;
         for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x, ++tcount) {
             Tile t;
-            decode_tile(p, offs, prefix, tix, t);
+            decode_tile(P, offs, prefix, tix, t);
+            const TcProblem& q = P.prob[t.p];
+            const int q_dual = q.dual, q_amn = q.a_mn, q_bmn = q.b_mn;
+            const uint32_t idesc = idesc_bf16(BM, q_dual ? 128 : q.bn, q_amn, q_bmn);
             const int acc = tcount & 1;
             const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-            if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, P.status)) { ok = false; break; }
             tc_fence_after();
             const uint32_t dt = tmem_base + (uint32_t)(acc * 256);
             uint32_t accum = 0;
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, P.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sA = smem0 + s * STAGE_BYTES, sB = sA + A_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BK / 16; ++ks) {
-                    const uint64_t ad = p.a_mn ? sdesc(sA + ks * 2048, 8192, 1024) : sdesc(sA + ks * 32, 16, 1024);
-                    if (p.dual) {
+                    const uint64_t ad = q_amn ? sdesc(sA + ks * 2048, 8192, 1024) : sdesc(sA + ks * 32, 16, 1024);
+                    if (q_dual) {
                         mma_bf16(dt, ad, sdesc(sB + ks * 2048, 8192, 1024), idesc, accum);
                         mma_bf16(dt + 128, ad, sdesc(sB + 16384 + ks * 2048, 8192, 1024), idesc, accum);
                     } else {
-                        const uint64_t bd = p.b_mn ? sdesc(sB + ks * 2048, 8192, 1024) : sdesc(sB + ks * 32, 16, 1024);
+                        const uint64_t bd = q_bmn ? sdesc(sB + ks * 2048, 8192, 1024) : sdesc(sB + ks * 32, 16, 1024);
                         mma_bf16(dt, ad, bd, idesc, accum);
                     }
                     accum = 1;
@@ -399,67 +438,68 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         mbar_drain(smem_u32(drain), 0);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
-        const int q = warp & 3;                   // TMEM lane quarter this warp may access
+        const int qd = warp & 3;                  // TMEM lane quarter this warp may access
         const int half = (warp - 2) / 4;          // which half of the tile's columns
-        const int row_in_tile = q * 32 + lane;
-        const int width = p.dual ? 128 : p.bn;
-        const int c_lo = half * (width / 64), c_hi = c_lo + width / 64;  // 32-column chunks
+        const int row_in_tile = qd * 32 + lane;
         int tcount = 0;
         for (int tix = blockIdx.x; tix < total; tix += gridDim.x, ++tcount) {
             Tile t;
-            decode_tile(p, offs, prefix, tix, t);
+            decode_tile(P, offs, prefix, tix, t);
+            const TcProblem& q = P.prob[t.p];
+            const int width = q.dual ? 128 : q.bn;
+            const int c_lo = half * (width / 64), c_hi = c_lo + width / 64;  // 32-column chunks
             const int acc = tcount & 1;
             const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, p.status)) break;
+            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, P.status)) break;
             tc_fence_after();
             const long long row = (long long)t.m0 + row_in_tile;
-            const long long obase = (p.sched == SCHED_KSEG ? (long long)t.e * p.out_estride : 0) +
-                                    row * p.ldo + t.n0;
-            const uint32_t taddr = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(q * 32) << 16);
+            const long long obase = (q.sched == SCHED_KSEG ? (long long)t.e * q.out_estride : 0) +
+                                    row * q.ldo + t.n0;
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(qd * 32) << 16);
             for (int c = c_lo; c < c_hi; ++c) {
                 float v[32];
                 if (t.nk == 0) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                    store32_bf16(p.out0 + obase + c * 32, v);
+                    store32_bf16(q.out0 + obase + c * 32, v);
                     continue;
                 }
                 tmem_ld32(taddr + c * 32, v);
-                if (p.epi == EPI_SWIGLU_FWD) {
+                if (q.epi == EPI_SWIGLU_FWD) {
                     float u[32];
                     tmem_ld32(taddr + 128 + c * 32, u);
                     tmem_wait_ld();
-                    store32_bf16(p.out0 + obase + c * 32, v);
-                    store32_bf16(p.out1 + obase + c * 32, u);
+                    store32_bf16(q.out0 + obase + c * 32, v);
+                    store32_bf16(q.out1 + obase + c * 32, u);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = silu_fast(v[i]) * u[i];
-                    store32_bf16(p.out2 + obase + c * 32, v);
+                    store32_bf16(q.out2 + obase + c * 32, v);
                     continue;
                 }
                 tmem_wait_ld();
-                if (p.epi == EPI_STORE) {
-                    store32_bf16(p.out0 + obase + c * 32, v);
-                } else if (p.epi == EPI_SILU_FWD) {
-                    store32_bf16(p.out0 + obase + c * 32, v);
+                if (q.epi == EPI_STORE) {
+                    store32_bf16(q.out0 + obase + c * 32, v);
+                } else if (q.epi == EPI_SILU_FWD) {
+                    store32_bf16(q.out0 + obase + c * 32, v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = silu_fast(v[i]);
-                    store32_bf16(p.out1 + obase + c * 32, v);
-                } else if (p.epi == EPI_SILU_BWD) {
+                    store32_bf16(q.out1 + obase + c * 32, v);
+                } else if (q.epi == EPI_SILU_BWD) {
                     float h[32];
-                    load32_bf16(p.in0 + obase + c * 32, h);
+                    load32_bf16(q.in0 + obase + c * 32, h);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= dsilu_fast(h[i]);
-                    store32_bf16(p.out0 + obase + c * 32, v);
+                    store32_bf16(q.out0 + obase + c * 32, v);
                 } else {  // EPI_SWIGLU_BWD: v = dact
                     float g[32], u[32], o[32];
-                    load32_bf16(p.in0 + obase + c * 32, g);
-                    load32_bf16(p.in1 + obase + c * 32, u);
+                    load32_bf16(q.in0 + obase + c * 32, g);
+                    load32_bf16(q.in1 + obase + c * 32, u);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = v[i] * u[i] * dsilu_fast(g[i]);
-                    store32_bf16(p.out0 + obase + c * 32, o);
+                    store32_bf16(q.out0 + obase + c * 32, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = v[i] * silu_fast(g[i]);
-                    store32_bf16(p.out1 + obase + c * 32, o);
+                    store32_bf16(q.out1 + obase + c * 32, o);
                 }
             }
             tc_fence_before();
@@ -523,7 +563,21 @@ int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool 
 
 int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
 
-int launch_tc(TcParams& p, int64_t max_tiles, cudaStream_t st) {
+#define MOE_TRY(x)                \
+    do {                          \
+        int _r = (x);             \
+        if (_r != MOE_OK) return _r; \
+    } while (0)
+
+// Upper bound of a problem's tile count (grid sizing only; the kernel counts
+// the real tiles from the device offsets).
+int64_t max_tiles(const moe_config& c, const TcProblem& q) {
+    if (q.sched == SCHED_ROWS) return (rows_cap_of(c) / BM) * q.n_blocks;
+    return (int64_t)c.E * q.m_blocks * q.n_blocks;
+}
+
+int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* probs, int nprob,
+              cudaStream_t st) {
     static bool attr_done[64] = {};
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
@@ -532,27 +586,57 @@ int launch_tc(TcParams& p, int64_t max_tiles, cudaStream_t st) {
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
         attr_done[dev] = true;
     }
-    p.status = device_status_ptr();
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, num_sms()));
-    tc_grouped_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(p);
+    TcParams P;
+    memset(&P, 0, sizeof(P));
+    int64_t tiles = 0;
+    for (int i = 0; i < nprob; ++i) {
+        P.prob[i] = probs[i];
+        tiles += max_tiles(c, probs[i]);
+    }
+    P.nprob = nprob;
+    P.E = c.E;
+    P.offsets = offsets;
+    P.status = device_status_ptr();
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms()));
+    tc_grouped_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(P);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
-TcParams base_params(const moe_config& c, const int32_t* offsets) {
-    TcParams p;
-    memset(&p, 0, sizeof(p));
-    p.offsets = offsets;
-    p.E = c.E;
-    p.kconcat = 1;
-    return p;
+TcProblem new_problem() {
+    TcProblem q;
+    memset(&q, 0, sizeof(q));
+    q.kconcat = 1;
+    return q;
 }
 
-#define MOE_TRY(x)                \
-    do {                          \
-        int _r = (x);             \
-        if (_r != MOE_OK) return _r; \
-    } while (0)
+// Row-segmented problem: C[rows, N] = A[rows, K] (K-major) x B_e (expert weights)
+int rows_problem(TcProblem& q, const moe_config& c, const void* A, int K, int N) {
+    q.sched = SCHED_ROWS;
+    q.k_blocks = K / BK;
+    q.bn = pick_bn(N);
+    q.n_blocks = N / q.bn;
+    q.ldo = N;
+    return act_map(&q.tmA0, A, rows_cap_of(c), K, false);
+}
+
+// Weight-gradient problem: out_e[M, N] = A_e^T B_e over expert e's rows (both MN-major)
+int wgrad_problem(TcProblem& q, const moe_config& c, const void* A, int M, const void* B, int N,
+                  void* out) {
+    const int64_t rc = rows_cap_of(c);
+    q.sched = SCHED_KSEG;
+    q.a_mn = 1;
+    q.b_mn = 1;
+    q.bn = pick_bn(N);
+    q.m_blocks = M / BM;
+    q.n_blocks = N / q.bn;
+    q.epi = EPI_STORE;
+    q.out0 = static_cast<__nv_bfloat16*>(out);
+    q.ldo = N;
+    q.out_estride = (long long)M * N;
+    MOE_TRY(act_map(&q.tmA0, A, rc, M, true));
+    return act_map(&q.tmB0, B, rc, N, true);
+}
 
 }  // namespace
 
@@ -565,49 +649,38 @@ int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offse
     using bf = __nv_bfloat16;
     const int64_t rc = rows_cap_of(c);
     const int d = c.d, f = c.f, E = c.E;
-    const bool sw = c.ffn == MOE_FFN_SWIGLU;
     // GEMM1 (+ activation)
     {
-        TcParams p = base_params(c, offsets);
-        p.sched = SCHED_ROWS;
-        p.k_blocks = d / BK;
-        MOE_TRY(act_map(&p.tmA0, x_perm, rc, d, false));
-        if (sw) {
-            p.dual = 1;
-            p.bn = 128;
-            p.b_mn = 1;
-            MOE_TRY(weight_map(&p.tmB0, W_gate, E, d, f, true, 0));
-            MOE_TRY(weight_map(&p.tmB1, W_up, E, d, f, true, 0));
-            p.epi = EPI_SWIGLU_FWD;
-            p.out0 = static_cast<bf*>(h_saved);
-            p.out1 = static_cast<bf*>(h_saved) + rc * f;
-            p.out2 = static_cast<bf*>(act);
+        TcProblem q = new_problem();
+        MOE_TRY(rows_problem(q, c, x_perm, d, f));
+        q.b_mn = 1;
+        if (c.ffn == MOE_FFN_SWIGLU) {
+            q.dual = 1;
+            q.bn = 128;
+            q.n_blocks = f / 128;
+            MOE_TRY(weight_map(&q.tmB0, W_gate, E, d, f, true, 0));
+            MOE_TRY(weight_map(&q.tmB1, W_up, E, d, f, true, 0));
+            q.epi = EPI_SWIGLU_FWD;
+            q.out0 = static_cast<bf*>(h_saved);
+            q.out1 = static_cast<bf*>(h_saved) + rc * f;
+            q.out2 = static_cast<bf*>(act);
         } else {
-            p.bn = pick_bn(f);
-            p.b_mn = 1;
-            MOE_TRY(weight_map(&p.tmB0, W_up, E, d, f, true, 0));
-            p.epi = EPI_SILU_FWD;
-            p.out0 = static_cast<bf*>(h_saved);
-            p.out1 = static_cast<bf*>(act);
+            MOE_TRY(weight_map(&q.tmB0, W_up, E, d, f, true, 0));
+            q.epi = EPI_SILU_FWD;
+            q.out0 = static_cast<bf*>(h_saved);
+            q.out1 = static_cast<bf*>(act);
         }
-        p.n_blocks = f / p.bn;
-        p.ldo = f;
-        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
+        MOE_TRY(launch_tc(c, offsets, &q, 1, st));
     }
     // GEMM2
     {
-        TcParams p = base_params(c, offsets);
-        p.sched = SCHED_ROWS;
-        p.k_blocks = f / BK;
-        p.bn = pick_bn(d);
-        p.b_mn = 1;
-        MOE_TRY(act_map(&p.tmA0, act, rc, f, false));
-        MOE_TRY(weight_map(&p.tmB0, W_down, E, f, d, true, 0));
-        p.n_blocks = d / p.bn;
-        p.epi = EPI_STORE;
-        p.out0 = static_cast<bf*>(y_perm);
-        p.ldo = d;
-        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
+        TcProblem q = new_problem();
+        MOE_TRY(rows_problem(q, c, act, f, d));
+        q.b_mn = 1;
+        MOE_TRY(weight_map(&q.tmB0, W_down, E, f, d, true, 0));
+        q.epi = EPI_STORE;
+        q.out0 = static_cast<bf*>(y_perm);
+        MOE_TRY(launch_tc(c, offsets, &q, 1, st));
     }
     return MOE_OK;
 }
@@ -621,75 +694,49 @@ int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offs
     const int64_t rc = rows_cap_of(c);
     const int d = c.d, f = c.f, E = c.E;
     const bool sw = c.ffn == MOE_FFN_SWIGLU;
-    bf* dh0 = static_cast<bf*>(dh);                       // dh (SiLU) or dg (SwiGLU)
+    bf* dh0 = static_cast<bf*>(dh);                          // dh (SiLU) or dg (SwiGLU)
     bf* dh1 = sw ? static_cast<bf*>(dh) + rc * f : nullptr;  // du (SwiGLU)
     const bf* h0 = static_cast<const bf*>(h_saved);
     const bf* h1 = sw ? h0 + rc * f : nullptr;
-    // dact = dy W_down^T, activation derivative fused
-    {
-        TcParams p = base_params(c, offsets);
-        p.sched = SCHED_ROWS;
-        p.k_blocks = d / BK;
-        p.bn = pick_bn(f);
-        MOE_TRY(act_map(&p.tmA0, dy_perm, rc, d, false));
-        MOE_TRY(weight_map(&p.tmB0, W_down, E, f, d, false, p.bn));
-        p.n_blocks = f / p.bn;
-        p.ldo = f;
-        p.in0 = h0;
-        p.out0 = dh0;
-        if (sw) {
-            p.epi = EPI_SWIGLU_BWD;
-            p.in1 = h1;
-            p.out1 = dh1;
-        } else {
-            p.epi = EPI_SILU_BWD;
-        }
-        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
-    }
-    // weight gradients: reductions over each expert's rows
-    auto wgrad = [&](const void* A, int M, const void* B, int N, void* out) -> int {
-        TcParams p = base_params(c, offsets);
-        p.sched = SCHED_KSEG;
-        p.a_mn = 1;
-        p.b_mn = 1;
-        p.bn = pick_bn(N);
-        p.m_blocks = M / BM;
-        p.n_blocks = N / p.bn;
-        MOE_TRY(act_map(&p.tmA0, A, rc, M, true));
-        MOE_TRY(act_map(&p.tmB0, B, rc, N, true));
-        p.epi = EPI_STORE;
-        p.out0 = static_cast<bf*>(out);
-        p.ldo = N;
-        p.out_estride = (long long)M * N;
-        return launch_tc(p, (int64_t)E * p.m_blocks * p.n_blocks, st);
-    };
-    MOE_TRY(wgrad(act, f, dy_perm, d, dW_down));
+    TcProblem q[MAX_PROBLEMS];
+    // launch 1: dact = dy W_down^T with the activation derivative fused  ||  dW_down = act^T dy
+    q[0] = new_problem();
+    MOE_TRY(rows_problem(q[0], c, dy_perm, d, f));
+    MOE_TRY(weight_map(&q[0].tmB0, W_down, E, f, d, false, q[0].bn));
+    q[0].in0 = h0;
+    q[0].out0 = dh0;
     if (sw) {
-        MOE_TRY(wgrad(x_perm, d, dh1, f, dW_up));
-        MOE_TRY(wgrad(x_perm, d, dh0, f, dW_gate));
+        q[0].epi = EPI_SWIGLU_BWD;
+        q[0].in1 = h1;
+        q[0].out1 = dh1;
     } else {
-        MOE_TRY(wgrad(x_perm, d, dh0, f, dW_up));
+        q[0].epi = EPI_SILU_BWD;
     }
-    // dx_perm = dh W_up^T (+ dg W_gate^T)
-    {
-        TcParams p = base_params(c, offsets);
-        p.sched = SCHED_ROWS;
-        p.k_blocks = f / BK;
-        p.bn = pick_bn(d);
-        MOE_TRY(act_map(&p.tmA0, sw ? dh1 : dh0, rc, f, false));
-        MOE_TRY(weight_map(&p.tmB0, W_up, E, d, f, false, p.bn));
-        if (sw) {
-            p.kconcat = 2;
-            MOE_TRY(act_map(&p.tmA1, dh0, rc, f, false));
-            MOE_TRY(weight_map(&p.tmB1, W_gate, E, d, f, false, p.bn));
-        }
-        p.n_blocks = d / p.bn;
-        p.epi = EPI_STORE;
-        p.out0 = static_cast<bf*>(dx_perm);
-        p.ldo = d;
-        MOE_TRY(launch_tc(p, (rc / BM) * p.n_blocks, st));
+    q[1] = new_problem();
+    MOE_TRY(wgrad_problem(q[1], c, act, f, dy_perm, d, dW_down));
+    MOE_TRY(launch_tc(c, offsets, q, 2, st));
+    // launch 2: dW_up = x^T dh (du)  ||  [dW_gate = x^T dg]  ||  dx_perm = dh W_up^T (+ dg W_gate^T)
+    int n = 0;
+    q[n] = new_problem();
+    MOE_TRY(wgrad_problem(q[n], c, x_perm, d, sw ? dh1 : dh0, f, dW_up));
+    ++n;
+    if (sw) {
+        q[n] = new_problem();
+        MOE_TRY(wgrad_problem(q[n], c, x_perm, d, dh0, f, dW_gate));
+        ++n;
     }
-    return MOE_OK;
+    q[n] = new_problem();
+    MOE_TRY(rows_problem(q[n], c, sw ? dh1 : dh0, f, d));
+    MOE_TRY(weight_map(&q[n].tmB0, W_up, E, d, f, false, q[n].bn));
+    if (sw) {
+        q[n].kconcat = 2;
+        MOE_TRY(act_map(&q[n].tmA1, dh0, rc, f, false));
+        MOE_TRY(weight_map(&q[n].tmB1, W_gate, E, d, f, false, q[n].bn));
+    }
+    q[n].epi = EPI_STORE;
+    q[n].out0 = static_cast<bf*>(dx_perm);
+    ++n;
+    return launch_tc(c, offsets, q, n, st);
 }
 
 }  // namespace moe

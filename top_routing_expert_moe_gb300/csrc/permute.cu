@@ -40,21 +40,34 @@ __global__ void __launch_bounds__(PT_TOK) tile_hist_kernel(const int32_t* __rest
     if (threadIdx.x < E) tile_counts[(size_t)blockIdx.x * E + threadIdx.x] = h[threadIdx.x];
 }
 
-__global__ void __launch_bounds__(256) scan_layout_kernel(
+// One CTA (1024 threads).  A warp per expert scans that expert's tile counts
+// 32 tiles at a time (exclusive prefix = the tile's first rank); thread 0 then
+// applies the capacity and lays out the padded segments.
+__global__ void __launch_bounds__(1024) scan_layout_kernel(
     const int32_t* __restrict__ tile_counts, int ntiles, int E, int C, int pad_m,
     int32_t* __restrict__ tile_base, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm_token, float* __restrict__ stats)
 {
     __shared__ int s_total[64], s_kept[64], s_off[65];
-    const int tid = threadIdx.x;
-    if (tid < E) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int e = warp; e < E; e += 32) {
         int run = 0;
-        for (int b = 0; b < ntiles; ++b) {
-            tile_base[(size_t)b * E + tid] = run;
-            run += tile_counts[(size_t)b * E + tid];
+        for (int b0 = 0; b0 < ntiles; b0 += 32) {
+            const int b = b0 + lane;
+            const int v = b < ntiles ? tile_counts[(size_t)b * E + e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (b < ntiles) tile_base[(size_t)b * E + e] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
         }
-        s_total[tid] = run;
-        s_kept[tid] = min(run, C);
+        if (lane == 0) {
+            s_total[e] = run;
+            s_kept[e] = min(run, C);
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -176,7 +189,7 @@ int launch_permute(const moe_config& c, const void* x, const int32_t* topk, void
     tile_hist_kernel<<<ntiles, PT_TOK, 0, st>>>(topk, c.T, c.E, c.k, tile_counts,
                                                 device_status_ptr());
     MOE_LAUNCH_CHECK();
-    scan_layout_kernel<<<1, 256, 0, st>>>(tile_counts, ntiles, c.E, C, c.pad_m, tile_base, kept,
+    scan_layout_kernel<<<1, 1024, 0, st>>>(tile_counts, ntiles, c.E, C, c.pad_m, tile_base, kept,
                                           offsets, perm_token, stats);
     MOE_LAUNCH_CHECK();
     assign_kernel<<<ntiles, PT_TOK, 0, st>>>(topk, c.T, c.E, c.k, C, tile_base, offsets, slot_of,

@@ -301,35 +301,52 @@ __global__ void __launch_bounds__(256) route_f32_kernel(const float* __restrict_
     finish_tile(sLog, ldl, sSel, sEnt, sBad, t0, ntok, o);
 }
 
-// Sum the per-CTA partials in block order; derive the statistics.
-__global__ void route_finalize_kernel(int nblk, int T, int E, int k, float aux_coef,
-                                      const int32_t* __restrict__ part_counts,
-                                      const float* __restrict__ part_psum,
-                                      const float* __restrict__ part_ent,
-                                      const int32_t* __restrict__ part_bad,
-                                      int32_t* __restrict__ counts, float* __restrict__ stats,
-                                      int* status)
+// Sum the per-CTA partials (a warp per expert, lane-strided, then a fixed
+// shuffle tree: deterministic); derive the statistics.  1024 threads.
+__global__ void __launch_bounds__(1024) route_finalize_kernel(
+    int nblk, int T, int E, int k, float aux_coef, const int32_t* __restrict__ part_counts,
+    const float* __restrict__ part_psum, const float* __restrict__ part_ent,
+    const int32_t* __restrict__ part_bad, int32_t* __restrict__ counts, float* __restrict__ stats,
+    int* status)
 {
     __shared__ float s_pbar[64];
     __shared__ int s_cnt[64];
-    const int e = threadIdx.x;
-    if (e < E) {
+    __shared__ float s_h[32];
+    __shared__ int s_b[32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int e = warp; e < E; e += 32) {
         int c = 0;
         float ps = 0.f;
-        for (int b = 0; b < nblk; ++b) {
+        for (int b = lane; b < nblk; b += 32) {
             c += part_counts[(size_t)b * E + e];
             ps += part_psum[(size_t)b * E + e];
         }
-        counts[e] = c;
-        s_cnt[e] = c;
-        s_pbar[e] = ps / (float)T;
-        if (stats) stats[MOE_STAT_PBAR + e] = ps / (float)T;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            c += __shfl_xor_sync(0xffffffffu, c, o);
+            ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        }
+        if (lane == 0) {
+            counts[e] = c;
+            s_cnt[e] = c;
+            s_pbar[e] = ps / (float)T;
+            if (stats) stats[MOE_STAT_PBAR + e] = ps / (float)T;
+        }
     }
+    float h = 0.f;
+    int bad = 0;
+    for (int b = tid; b < nblk; b += blockDim.x) { h += part_ent[b]; bad += part_bad[b]; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        h += __shfl_xor_sync(0xffffffffu, h, o);
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) { s_h[warp] = h; s_b[warp] = bad; }
     __syncthreads();
-    if (e == 0) {
-        float h = 0.f;
-        int bad = 0;
-        for (int b = 0; b < nblk; ++b) { h += part_ent[b]; bad += part_bad[b]; }
+    if (tid == 0) {
+        h = 0.f;
+        bad = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) { h += s_h[w]; bad += s_b[w]; }
         float aux = 0.f, sw = 0.f, cmean = 0.f, cmax = 0.f;
         for (int q = 0; q < E; ++q) {
             float dq = s_pbar[q] - 1.0f / (float)E;
@@ -389,7 +406,7 @@ size_t route_ws_bytes(const moe_config& c) {
 namespace {
 int finalize_route(const moe_config& c, const RouteOut& o, int nblk, int32_t* counts,
                    float* stats, cudaStream_t st) {
-    route_finalize_kernel<<<1, 64, 0, st>>>(nblk, c.T, c.E, c.k, c.aux_coef, o.part_counts,
+    route_finalize_kernel<<<1, 1024, 0, st>>>(nblk, c.T, c.E, c.k, c.aux_coef, o.part_counts,
                                             o.part_psum, o.part_ent, o.part_bad, counts, stats,
                                             device_status_ptr());
     MOE_LAUNCH_CHECK();
