@@ -26,7 +26,7 @@ _LIB = os.path.join(_BUILD, "liboracle.so")
 # statistics layout (see moe_oracle.c, OST_*)
 ST_AUX_LOSS, ST_AUX_SWITCH, ST_ENTROPY, ST_NONFINITE = 0, 1, 2, 3
 ST_DROPPED, ST_MAX_OVER_MEAN_KEPT, ST_COUNT_CV, ST_MAX_OVER_MEAN_COUNT = 4, 5, 6, 7
-ST_PBAR = 8
+ST_TOKENS, ST_PBAR = 8, 9
 
 
 def build(force: bool = False) -> str:
@@ -45,7 +45,8 @@ class _Cfg(ctypes.Structure):
                 ("E", ctypes.c_int), ("k", ctypes.c_int),
                 ("capacity_factor", ctypes.c_double), ("swiglu", ctypes.c_int),
                 ("normalize_gates", ctypes.c_int), ("aux_coef", ctypes.c_double),
-                ("pad_m", ctypes.c_int)]
+                ("pad_m", ctypes.c_int), ("temperature", ctypes.c_double),
+                ("straight_through", ctypes.c_int)]
 
 
 @dataclass
@@ -60,11 +61,13 @@ class OracleConfig:
     normalize_gates: bool = True
     aux_coef: float = 0.0
     pad_m: int = 1
+    temperature: float = 1.0       # softmax temperature tau; pass the fp32 value the GPU sees
+    straight_through: bool = False  # Gumbel top-k: select on logits + noise, gates 1
 
     def c(self) -> _Cfg:
         return _Cfg(self.T, self.d, self.f, self.E, self.k, float(self.capacity_factor),
                     int(self.swiglu), int(self.normalize_gates), float(self.aux_coef),
-                    int(self.pad_m))
+                    int(self.pad_m), float(self.temperature), int(self.straight_through))
 
 
 _lib = None
@@ -110,13 +113,21 @@ def router_logits(cfg, x, Wr, bias=None, noise=None):
     return out
 
 
-def route(cfg, logits):
+def _mask(mask):
+    return None if mask is None else np.ascontiguousarray(mask, np.uint8)
+
+
+def route(cfg, logits, noise=None, mask=None):
+    """Steps 2-4 on given logits.  ``noise`` is the selection noise of the
+    straight-through mode; ``mask`` (uint8 [T], 0 = padding) may be None."""
     logits = _d(logits)
+    noise, mask = _d(noise), _mask(mask)
     probs = np.empty((cfg.T, cfg.E), np.float64)
     topk = np.empty((cfg.T, cfg.k), np.int32)
     gate = np.empty((cfg.T, cfg.k), np.float64)
     counts = np.empty(cfg.E, np.int32)
-    nf = lib().oracle_route(ctypes.byref(cfg.c()), _p(logits), _p(probs), _p(topk), _p(gate), _p(counts))
+    nf = lib().oracle_route(ctypes.byref(cfg.c()), _p(logits), _p(noise), _p(mask), _p(probs),
+                            _p(topk), _p(gate), _p(counts))
     return dict(probs=probs, topk_idx=topk, gate=gate, counts=counts, nonfinite=nf)
 
 
@@ -130,10 +141,11 @@ def permute(cfg, topk_idx):
     return dict(kept=kept, offsets=offsets, perm_token=perm[:offsets[-1]].copy(), slot_of=slot)
 
 
-def stats(cfg, probs, counts, kept, nonfinite=0):
+def stats(cfg, probs, topk_idx, counts, kept, nonfinite=0):
     """Step 9 statistics (layout ST_*) from routed probabilities and counts."""
-    out = np.empty(8 + cfg.E)
+    out = np.empty(9 + cfg.E)
     lib().oracle_stats(ctypes.byref(cfg.c()), _p(_d(probs)),
+                       _p(np.ascontiguousarray(topk_idx, np.int32)),
                        _p(np.ascontiguousarray(counts, np.int32)),
                        _p(np.ascontiguousarray(kept, np.int32)), ctypes.c_int(int(nonfinite)),
                        _p(out))
@@ -158,16 +170,16 @@ def expert_forward(cfg, e, x_row, Wup, Wdown, Wgate=None):
     return dict(h=h, u=u, act=act, y=y)
 
 
-def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in=None):
+def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in=None, mask=None):
     """Steps 1-9. ``logits_in`` (e.g. the GPU's fp32 logits) replaces step 1."""
     x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
-    bias, noise, logits_in = _d(bias), _d(noise), _d(logits_in)
+    bias, noise, logits_in, mask = _d(bias), _d(noise), _d(logits_in), _mask(mask)
     T, E, k, d = cfg.T, cfg.E, cfg.k, cfg.d
     r = dict(logits=np.empty((T, E)), probs=np.empty((T, E)), topk_idx=np.empty((T, k), np.int32),
              gate=np.empty((T, k)), counts=np.empty(E, np.int32), kept=np.empty(E, np.int32),
              offsets=np.empty(E + 1, np.int32), perm_token=np.empty(rows_bound(cfg), np.int32),
-             slot_of=np.empty((T, k), np.int32), out=np.empty((T, d)), stats=np.empty(8 + E))
-    lib().oracle_forward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(bias), _p(noise), _p(Wup),
+             slot_of=np.empty((T, k), np.int32), out=np.empty((T, d)), stats=np.empty(9 + E))
+    lib().oracle_forward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(bias), _p(noise), _p(mask), _p(Wup),
                          _p(Wgate), _p(Wdown), _p(logits_in),
                          *[_p(r[n]) for n in ("logits", "probs", "topk_idx", "gate", "counts", "kept",
                                                "offsets", "perm_token", "slot_of", "out", "stats")])

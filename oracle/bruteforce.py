@@ -37,8 +37,10 @@ def topk_by_sort(logits, k):
 
 
 def forward(x, Wr, Wup, Wdown, k, capacity_factor=0.0, Wgate=None, bias=None, noise=None,
-            normalize_gates=True, logits=None):
-    """Returns (out, topk_idx, gate, kept_mask[T,k])."""
+            normalize_gates=True, logits=None, temperature=1.0, straight_through=False,
+            mask=None):
+    """Returns (out, topk_idx, gate, kept_mask[T,k]).  Masked tokens (mask 0)
+    are routed nowhere: topk -1, gates 0."""
     x = np.asarray(x, np.float64)
     T, d = x.shape
     E = Wr.shape[1]
@@ -46,31 +48,41 @@ def forward(x, Wr, Wup, Wdown, k, capacity_factor=0.0, Wgate=None, bias=None, no
         logits = x @ np.asarray(Wr, np.float64)
         if bias is not None:
             logits = logits + np.asarray(bias, np.float64)[None, :]
-        if noise is not None:
+        if noise is not None and not straight_through:
             logits = logits + np.asarray(noise, np.float64)
     logits = np.asarray(logits, np.float64)
-    probs = np.exp(logits - logits.max(axis=1, keepdims=True))
+    z = logits / temperature
+    probs = np.exp(z - z.max(axis=1, keepdims=True))
     probs /= probs.sum(axis=1, keepdims=True)
-    topk = topk_by_sort(logits, k)
-    sel_logits = np.take_along_axis(logits, topk, axis=1)
-    if normalize_gates:
-        w = np.exp(sel_logits - sel_logits[:, :1])
+    key = logits
+    if straight_through and noise is not None:
+        key = (logits.astype(np.float32) + np.asarray(noise, np.float32)).astype(np.float64)
+    topk = topk_by_sort(key, k)
+    sel = np.take_along_axis(z, topk, axis=1)
+    if straight_through:
+        gate = np.ones((T, k))
+    elif normalize_gates:
+        w = np.exp(sel - sel.max(axis=1, keepdims=True))
         gate = w / w.sum(axis=1, keepdims=True)
     else:
         gate = np.take_along_axis(probs, topk, axis=1)
+    if mask is not None:
+        pad = np.asarray(mask) == 0
+        topk[pad] = -1
+        gate[pad] = 0.0
 
     # routing matrix [T, E] of slot indices (-1 = not selected), then capacity
     C = capacity(T, k, E, capacity_factor)
     kept = np.zeros((T, k), bool)
     for e in range(E):
-        tok, slot = np.nonzero(topk == e)          # row-major => ascending token order
+        tok, slot = np.nonzero(topk == e)          # row-major => ascending token order (masked: -1)
         keep = np.arange(len(tok)) < C
         kept[tok[keep], slot[keep]] = True
 
     out = np.zeros((T, d))
     for e in range(E):
-        mask = (topk == e) & kept                    # [T, k]
-        tok, slot = np.nonzero(mask)
+        sel_e = (topk == e) & kept                   # [T, k]
+        tok, slot = np.nonzero(sel_e)
         if len(tok) == 0:
             continue
         xe = x[tok]

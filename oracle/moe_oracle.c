@@ -41,9 +41,14 @@ typedef struct {
     int normalize_gates;    /* 1: softmax over the k selected logits; 0: raw probabilities */
     double aux_coef;        /* lambda of the variance-form aux loss */
     int pad_m;              /* segment padding of the expert-contiguous layout (>= 1) */
+    double temperature;     /* softmax temperature tau (<= 0 means 1) */
+    int straight_through;   /* 1: select on logits + noise, gates 1, gradient through
+                               softmax(logits / tau) (Gumbel top-k, straight-through) */
 } oracle_cfg;
 
-/* Layout of the statistics vector written by oracle_stats (length 8 + E). */
+static double tau_of(const oracle_cfg* c) { return c->temperature > 0.0 ? c->temperature : 1.0; }
+
+/* Layout of the statistics vector written by oracle_stats (length 9 + E). */
 enum {
     OST_AUX_LOSS = 0,   /* lambda * sum_i (pbar_i - 1/E)^2                         */
     OST_AUX_SWITCH = 1, /* E * sum_i f_i pbar_i, f_i = counts_i / (T k)             */
@@ -53,7 +58,8 @@ enum {
     OST_MAX_OVER_MEAN_KEPT = 5, /* max_e kept_e / mean_e kept_e                   */
     OST_COUNT_CV = 6,   /* std/mean of counts over experts                         */
     OST_MAX_OVER_MEAN_COUNT = 7,
-    OST_PBAR = 8        /* pbar[0..E)                                              */
+    OST_TOKENS = 8,     /* tokens that take part in routing (not masked)           */
+    OST_PBAR = 9        /* pbar[0..E), mean over those tokens                      */
 };
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
@@ -89,51 +95,70 @@ static int ranks_above(double la, int a, double lb, int b)
 }
 
 /* ---- Steps 2-4: softmax, top-k, gates  [LLaMA4-MoE] §2.4; [Twinkle] §3.1 ----
- * probs  [T,E] softmax of the logits (max subtracted)
+ * probs  [T,E] softmax of logits / tau (max subtracted)   [Twinkle] §3.1, [ZeRO3-MoE] §3.2
  * topk   [T,k] experts in rank order; gate [T,k]; counts [E] selections.
- * Returns the number of tokens that had a non-finite logit.                   */
-int oracle_route(const oracle_cfg* c, const double* logits, double* probs,
-                 int* topk, double* gate, int* counts)
+ * noise_sel (straight-through mode only, may be NULL): selection key =
+ *   logits + noise, summed in fp32 (the precision the kernel decides in);
+ *   gates are 1 ([Twinkle] §3.1, Gumbel top-k with straight-through).
+ * mask (may be NULL): tokens with mask 0 are padding and take no part in
+ *   routing ([LLaMA4-MoE] §4.1): topk -1, gates 0, probs 0.
+ * Returns the number of routed tokens that had a non-finite logit.            */
+int oracle_route(const oracle_cfg* c, const double* logits, const double* noise_sel,
+                 const unsigned char* mask, double* probs, int* topk, double* gate, int* counts)
 {
     const int T = c->T, E = c->E, k = c->k;
+    const double tau = tau_of(c);
+    double* key = (double*)malloc(sizeof(double) * (size_t)E);
     int nonfinite = 0;
     for (int e = 0; e < E; ++e) counts[e] = 0;
     for (int t = 0; t < T; ++t) {
         const double* l = logits + (size_t)t * E;
+        int* sel = topk + (size_t)t * k;
+        double* g = gate + (size_t)t * k;
+        if (mask && !mask[t]) {
+            for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = 0.0;
+            for (int j = 0; j < k; ++j) { sel[j] = -1; g[j] = 0.0; }
+            continue;
+        }
         double m = -INFINITY;
         int bad = 0;
         for (int e = 0; e < E; ++e) {
             if (!isfinite(l[e])) bad = 1;
             if (l[e] > m) m = l[e];
+            key[e] = l[e];
+            if (c->straight_through && noise_sel)
+                key[e] = (double)((float)l[e] + (float)noise_sel[(size_t)t * E + e]);
         }
         nonfinite += bad;
         double z = 0.0;
-        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
-        for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = exp(l[e] - m) / z;
+        for (int e = 0; e < E; ++e) z += exp((l[e] - m) / tau);
+        for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = exp((l[e] - m) / tau) / z;
 
         /* selection: k passes, each taking the best expert not yet taken */
-        int* sel = topk + (size_t)t * k;
         for (int j = 0; j < k; ++j) {
             int best = -1;
             for (int e = 0; e < E; ++e) {
                 int taken = 0;
                 for (int q = 0; q < j; ++q) taken |= (sel[q] == e);
                 if (taken) continue;
-                if (best < 0 || ranks_above(l[e], e, l[best], best)) best = e;
+                if (best < 0 || ranks_above(key[e], e, key[best], best)) best = e;
             }
             sel[j] = best;
             counts[best] += 1;
         }
-        /* gates: softmax restricted to the selected logits, or raw probs */
-        double* g = gate + (size_t)t * k;
-        if (c->normalize_gates) {
+        /* gates: 1 (straight-through), softmax over the selected, or raw probs */
+        if (c->straight_through) {
+            for (int j = 0; j < k; ++j) g[j] = 1.0;
+        } else if (c->normalize_gates) {
             double ms = l[sel[0]], zs = 0.0;
-            for (int j = 0; j < k; ++j) zs += exp(l[sel[j]] - ms);
-            for (int j = 0; j < k; ++j) g[j] = exp(l[sel[j]] - ms) / zs;
+            for (int j = 0; j < k; ++j) ms = l[sel[j]] > ms ? l[sel[j]] : ms;
+            for (int j = 0; j < k; ++j) zs += exp((l[sel[j]] - ms) / tau);
+            for (int j = 0; j < k; ++j) g[j] = exp((l[sel[j]] - ms) / tau) / zs;
         } else {
             for (int j = 0; j < k; ++j) g[j] = probs[(size_t)t * E + sel[j]];
         }
     }
+    free(key);
     return nonfinite;
 }
 
@@ -163,6 +188,7 @@ void oracle_permute(const oracle_cfg* c, const int* topk, int* kept, int* offset
     for (int t = 0; t < T; ++t)
         for (int j = 0; j < k; ++j) {
             int e = topk[(size_t)t * k + j];
+            if (e < 0) { rank[(size_t)t * k + j] = -1; continue; }   /* masked token */
             if (taken[e] < C) { rank[(size_t)t * k + j] = taken[e]; taken[e]++; }
             else rank[(size_t)t * k + j] = -1;
         }
@@ -177,7 +203,7 @@ void oracle_permute(const oracle_cfg* c, const int* topk, int* kept, int* offset
         for (int j = 0; j < k; ++j) {
             int e = topk[(size_t)t * k + j];
             int q = rank[(size_t)t * k + j];
-            if (q < 0) { slot_of[(size_t)t * k + j] = -1; continue; }
+            if (e < 0 || q < 0) { slot_of[(size_t)t * k + j] = -1; continue; }
             slot_of[(size_t)t * k + j] = offsets[e] + q;
             perm_token[offsets[e] + q] = t;
         }
@@ -270,15 +296,19 @@ void oracle_combine(const oracle_cfg* c, const double* x, const int* topk,
 }
 
 /* ---- Step 9: aux statistics  [ZeRO3-MoE] §3.2; [LLaMA4-MoE] §3.2, §3.3 ----
- * stats has 8 + E entries (layout OST_*).                                     */
-void oracle_stats(const oracle_cfg* c, const double* probs, const int* counts,
+ * Means run over the routed tokens (those with topk[t][0] >= 0).
+ * stats has 9 + E entries (layout OST_*).                                     */
+void oracle_stats(const oracle_cfg* c, const double* probs, const int* topk, const int* counts,
                   const int* kept, int nonfinite, double* stats)
 {
     const int T = c->T, E = c->E, k = c->k;
     double* pbar = stats + OST_PBAR;
     for (int e = 0; e < E; ++e) pbar[e] = 0.0;
     double ent = 0.0;
+    int real = 0;
     for (int t = 0; t < T; ++t) {
+        if (topk[(size_t)t * k] < 0) continue;
+        ++real;
         double h = 0.0;
         for (int e = 0; e < E; ++e) {
             double p = probs[(size_t)t * E + e];
@@ -287,16 +317,18 @@ void oracle_stats(const oracle_cfg* c, const double* probs, const int* counts,
         }
         ent += h;
     }
+    const double Tr = real > 0 ? (double)real : 1.0;
     double aux = 0.0, sw = 0.0;
     for (int e = 0; e < E; ++e) {
-        pbar[e] /= (double)T;
+        pbar[e] /= Tr;
         aux += (pbar[e] - 1.0 / E) * (pbar[e] - 1.0 / E);
-        sw += ((double)counts[e] / ((double)T * k)) * pbar[e];
+        sw += ((double)counts[e] / (Tr * k)) * pbar[e];
     }
     stats[OST_AUX_LOSS] = c->aux_coef * aux;
     stats[OST_AUX_SWITCH] = (double)E * sw;
-    stats[OST_ENTROPY] = ent / (double)T;
+    stats[OST_ENTROPY] = ent / Tr;
     stats[OST_NONFINITE] = (double)nonfinite;
+    stats[OST_TOKENS] = (double)real;
     long dropped = 0, kmax = 0, ksum = 0, cmax = 0, csum = 0;
     for (int e = 0; e < E; ++e) {
         dropped += counts[e] - kept[e];
@@ -314,20 +346,23 @@ void oracle_stats(const oracle_cfg* c, const double* probs, const int* counts,
 }
 
 /* ---- Whole forward: steps 1-9.  If logits_in is given, step 1 is skipped and
- * those logits are routed instead (the "conditioned" oracle).                 */
+ * those logits are routed instead (the "conditioned" oracle).  Gate noise is
+ * added to the logits, except in straight-through mode, where it only enters
+ * the selection key.  mask may be NULL.                                       */
 void oracle_forward(const oracle_cfg* c, const double* x, const double* Wr, const double* bias,
-                    const double* noise, const double* Wup, const double* Wgate,
-                    const double* Wdown, const double* logits_in,
+                    const double* noise, const unsigned char* mask, const double* Wup,
+                    const double* Wgate, const double* Wdown, const double* logits_in,
                     double* logits, double* probs, int* topk, double* gate, int* counts,
                     int* kept, int* offsets, int* perm_token, int* slot_of,
                     double* out, double* stats)
 {
     if (logits_in) memcpy(logits, logits_in, sizeof(double) * (size_t)c->T * c->E);
-    else oracle_router_logits(c, x, Wr, bias, noise, logits);
-    int nf = oracle_route(c, logits, probs, topk, gate, counts);
+    else oracle_router_logits(c, x, Wr, bias, c->straight_through ? NULL : noise, logits);
+    int nf = oracle_route(c, logits, c->straight_through ? noise : NULL, mask, probs, topk, gate,
+                          counts);
     oracle_permute(c, topk, kept, offsets, perm_token, slot_of);
     oracle_combine(c, x, topk, gate, slot_of, Wup, Wgate, Wdown, out);
-    oracle_stats(c, probs, counts, kept, nf, stats);
+    oracle_stats(c, probs, topk, counts, kept, nf, stats);
 }
 
 /* ---- Step 10: backward of L = <dout, out> + aux loss ----
@@ -371,7 +406,7 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
         const double* Wd = Wdown + e * df;
         for (int t = 0; t < T; ++t)
             for (int j = 0; j < k; ++j) {
-                if (topk[(size_t)t * k + j] != e || slot_of[(size_t)t * k + j] < 0) continue;
+                if (topk[(size_t)t * k + j] != e || slot_of[(size_t)t * k + j] < 0) continue;  /* not e, dropped or masked */
                 const double* xt = x + (size_t)t * d;
                 const double* go = dout + (size_t)t * d;
                 expert_ffn(c, xt, Wu, Wg, Wd, h, u, a, y);
@@ -433,21 +468,27 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
         free(h);
     }
 
-    /* router: dL/dlogits from the gates and from the aux loss */
+    /* router: dL/dlogits from the gates and from the aux loss.  p = softmax(l/tau)
+     * over the routed tokens; every derivative through it carries 1/tau.      */
+    const double tau = tau_of(c);
     double* probs = (double*)malloc(sizeof(double) * (size_t)T * E);
     double* pbar = (double*)calloc((size_t)E, sizeof(double));
     double* dl = (double*)malloc(sizeof(double) * (size_t)T * E);
+    int real = 0;
     for (int t = 0; t < T; ++t) {
         const double* l = logits + (size_t)t * E;
         double m = -INFINITY, z = 0.0;
         for (int e = 0; e < E; ++e) if (l[e] > m) m = l[e];
-        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
-        for (int e = 0; e < E; ++e) { probs[(size_t)t * E + e] = exp(l[e] - m) / z; pbar[e] += probs[(size_t)t * E + e]; }
+        for (int e = 0; e < E; ++e) z += exp((l[e] - m) / tau);
+        for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = exp((l[e] - m) / tau) / z;
+        if (topk[(size_t)t * k] < 0) continue;              /* masked token */
+        ++real;
+        for (int e = 0; e < E; ++e) pbar[e] += probs[(size_t)t * E + e];
     }
-    for (int e = 0; e < E; ++e) pbar[e] /= (double)T;
+    for (int e = 0; e < E; ++e) pbar[e] /= real > 0 ? (double)real : 1.0;
     if (pbar_in)
         for (int e = 0; e < E; ++e) pbar[e] = pbar_in[e];
-    const double Tn = T_aux > 0 ? (double)T_aux : (double)T;
+    const double Tn = T_aux > 0 ? (double)T_aux : (real > 0 ? (double)real : 1.0);
     double* cvec = (double*)malloc(sizeof(double) * (size_t)E); /* dL_aux / dp[t,e] */
     for (int e = 0; e < E; ++e) cvec[e] = c->aux_coef * 2.0 * (pbar[e] - 1.0 / E) / Tn;
 
@@ -458,22 +499,24 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
         const int* sel = topk + (size_t)t * k;
         double* dlt = dl + (size_t)t * E;
         for (int e = 0; e < E; ++e) dlt[e] = 0.0;
-        if (c->normalize_gates) {
-            /* gate_j = exp(l_j) / sum_sel exp: d gate_j / d l_i = gate_j (delta_ji - gate_i) */
+        if (sel[0] < 0) continue;                            /* masked token: no gradient */
+        if (c->normalize_gates && !c->straight_through) {
+            /* gate_j = exp(l_j/tau) / sum_sel: d gate_j / d l_i = gate_j (delta_ji - gate_i) / tau */
             double s = 0.0;
             for (int j = 0; j < k; ++j) s += g[j] * dg[j];
-            for (int j = 0; j < k; ++j) dlt[sel[j]] += g[j] * (dg[j] - s);
+            for (int j = 0; j < k; ++j) dlt[sel[j]] += g[j] * (dg[j] - s) / tau;
         } else {
-            /* gate_j = p_{e_j}: d p_a / d l_b = p_a (delta_ab - p_b) */
+            /* raw probabilities (gate_j = p_{e_j}), and the straight-through estimator
+             * (forward gates 1, backward through p_{e_j}): d p_a / d l_b = p_a (delta_ab - p_b) / tau */
             double s = 0.0;
             for (int j = 0; j < k; ++j) s += dg[j] * p[sel[j]];
-            for (int j = 0; j < k; ++j) dlt[sel[j]] += dg[j] * p[sel[j]];
-            for (int e = 0; e < E; ++e) dlt[e] -= p[e] * s;
+            for (int j = 0; j < k; ++j) dlt[sel[j]] += dg[j] * p[sel[j]] / tau;
+            for (int e = 0; e < E; ++e) dlt[e] -= p[e] * s / tau;
         }
         /* aux: dL/dp[t,e] = cvec[e], through the full softmax */
         double s = 0.0;
         for (int e = 0; e < E; ++e) s += p[e] * cvec[e];
-        for (int e = 0; e < E; ++e) dlt[e] += p[e] * (cvec[e] - s);
+        for (int e = 0; e < E; ++e) dlt[e] += p[e] * (cvec[e] - s) / tau;
     }
 
     /* dx = sum over kept slots of the expert dx, plus the router term */

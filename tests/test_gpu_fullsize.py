@@ -48,7 +48,7 @@ def fullsize_check(w, inp, n_tok, n_entries=48, seed=0):
     slot = L.slot_of.cpu().numpy()
     assert (slot == po["slot_of"]).all()
     rep["gate_rel"] = parity.rel_fro(parity.np64(L.gate), ro["gate"])
-    st = oracle.stats(ocfg, ro["probs"], ro["counts"], po["kept"], ro["nonfinite"])
+    st = oracle.stats(ocfg, ro["probs"], ro["topk_idx"], ro["counts"], po["kept"], ro["nonfinite"])
     gst = parity.np64(L.stats)
     rep["pbar_rel"] = parity.rel_fro(gst[moe.STAT_PBAR:], st[oracle.ST_PBAR:])
     assert gst[moe.STAT_DROPPED] == st[oracle.ST_DROPPED]

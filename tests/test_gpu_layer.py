@@ -143,3 +143,16 @@ def test_nonfinite_logits_are_flagged():
     assert r["status"] == moe.ERR_NONFINITE
     assert r["layer"].stats[moe.STAT_NONFINITE].item() == 1.0
     assert moe.last_device_status() == 0   # reading clears it
+
+
+@pytest.mark.parametrize("E,k,dtype", [(2, 1, "bf16"), (8, 1, "bf16"), (16, 4, "bf16"),
+                                       (32, 2, "bf16"), (64, 2, "bf16"), (64, 8, "bf16"),
+                                       (12, 3, "fp32"), (64, 5, "fp32")])
+def test_expert_count_and_top_k_sweep(E, k, dtype):
+    """Top-k / expert-count sweep (top-1 routing, wide k, up to 64 experts)."""
+    base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
+    w = _w(base, T=640, E=E, k=k, d=256 if dtype == "bf16" else 64,
+           f=256 if dtype == "bf16" else 96, capacity_factor=1.1)
+    rep, _ = parity.full_check(w, _edge_inputs(w, seed=E * 10 + k),
+                               pad_m=128 if dtype == "bf16" else 8)
+    _report(f"sweep E{E} k{k} {dtype}", rep)

@@ -279,3 +279,132 @@ def test_backward_on_a_token_sample_matches_the_full_batch_rows(oracle_lib):
                            pbar=r["stats"][oracle.ST_PBAR:], T_aux=T)
     for key in ("dx", "dlogits", "dgate"):
         np.testing.assert_allclose(part[key], full[key][idx], rtol=1e-12, atol=1e-14)
+
+
+# --------------------------------------------------------------------------- router variants
+@pytest.mark.parametrize("tau,st,masked,norm", [(0.6, False, False, True), (1.7, False, True, False),
+                                                (0.7, True, False, True), (0.7, True, True, True)])
+def test_router_variants_match_bruteforce(oracle_lib, tau, st, masked, norm):
+    """Temperature, straight-through (Gumbel) top-k and padding masks agree with
+    the brute-force restatement ([Twinkle] §3.1; [LLaMA4-MoE] §4.1)."""
+    rng = np.random.default_rng(int(tau * 10) + 2 * st + 4 * masked)
+    T, d, f, E, k = 41, 10, 14, 6, 2
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, bias=True, noise=True)
+    nz = -np.log(-np.log(rng.uniform(1e-9, 1.0, (T, E)))) if st else nz   # Gumbel draws
+    mask = (rng.uniform(size=T) > 0.3).astype(np.uint8) if masked else None
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=0.8, normalize_gates=norm,
+                              temperature=tau, straight_through=st, aux_coef=0.1, pad_m=4)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, bias=b, noise=nz, mask=mask)
+    out, topk, gate, kept = bruteforce.forward(x, Wr, Wup, Wd, k, 0.8, bias=b, noise=nz,
+                                               normalize_gates=norm, temperature=tau,
+                                               straight_through=st, mask=mask)
+    assert (r["topk_idx"] == topk).all()
+    np.testing.assert_allclose(r["gate"], gate, rtol=1e-13, atol=0)
+    assert ((r["slot_of"] >= 0) == kept).all()
+    np.testing.assert_allclose(r["out"], out, rtol=1e-12, atol=1e-13)
+    if masked:
+        assert r["stats"][oracle.ST_TOKENS] == mask.sum()
+        assert (r["topk_idx"][mask == 0] == -1).all() and (r["out"][mask == 0] == 0).all()
+    if st:
+        assert (r["gate"][r["topk_idx"] >= 0] == 1.0).all()
+
+
+def test_temperature_backward_matches_finite_differences(oracle_lib):
+    rng = np.random.default_rng(77)
+    T, d, f, E, k = 8, 6, 12, 4, 2
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, bias=True, noise=True)
+    dout = rng.standard_normal((T, d))
+    for norm in (True, False):
+        cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, normalize_gates=norm, aux_coef=0.3,
+                                  temperature=0.7)
+        L0, r0 = _loss(cfg, x, Wr, Wup, Wd, None, b, nz, dout)
+        g = oracle.backward(cfg, x, Wr, Wup, Wd, r0["logits"], r0["topk_idx"], r0["gate"],
+                            r0["slot_of"], dout, with_bias=True)
+        h = 1e-6
+        for name, arr, grad in (("Wr", Wr, g["dWr"]), ("b", b, g["db"]), ("x", x, g["dx"])):
+            for ix in [np.unravel_index(i, arr.shape) for i in range(0, arr.size, max(1, arr.size // 12))]:
+                vals = []
+                for s in (+h, -h):
+                    a2 = arr.copy()
+                    a2[ix] += s
+                    kw = dict(x=x, Wr=Wr, b=b)
+                    kw[name] = a2
+                    L, r = _loss(cfg, kw["x"], kw["Wr"], Wup, Wd, None, kw["b"], nz, dout)
+                    assert (r["topk_idx"] == r0["topk_idx"]).all()
+                    vals.append(L)
+                assert grad[ix] == pytest.approx((vals[0] - vals[1]) / (2 * h), rel=2e-5, abs=2e-7)
+
+
+def test_straight_through_gradient_is_the_surrogate_derivative(oracle_lib):
+    """Straight-through Gumbel top-k ([Twinkle] §3.1): forward gates are 1; the
+    router gradient is that of the surrogate sum_j dgate_j p_{e_j}(logits/tau)
+    plus the aux loss, at fixed selection.  The expert-weight gradients are exact."""
+    rng = np.random.default_rng(88)
+    T, d, f, E, k, tau = 9, 6, 10, 5, 2, 0.7
+    x, Wr, Wup, Wg, Wd, b, _ = _rand_case(rng, T, d, f, E, k, bias=True)
+    gum = -np.log(-np.log(rng.uniform(1e-9, 1.0, (T, E))))
+    dout = rng.standard_normal((T, d))
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, aux_coef=0.2, temperature=tau,
+                              straight_through=True)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, bias=b, noise=gum)
+    g = oracle.backward(cfg, x, Wr, Wup, Wd, r["logits"], r["topk_idx"], r["gate"], r["slot_of"],
+                        dout, with_bias=True)
+    topk, dg = r["topk_idx"], g["dgate"]
+
+    def surrogate(logits):
+        z = logits / tau
+        p = np.exp(z - z.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        pbar = p.mean(0)
+        return float((dg * np.take_along_axis(p, topk, 1)).sum() + 0.2 * ((pbar - 1 / E) ** 2).sum())
+
+    h = 1e-6
+    for t in range(T):
+        for e in range(E):
+            lp, lm = r["logits"].copy(), r["logits"].copy()
+            lp[t, e] += h
+            lm[t, e] -= h
+            fd = (surrogate(lp) - surrogate(lm)) / (2 * h)
+            assert g["dlogits"][t, e] == pytest.approx(fd, rel=1e-6, abs=1e-9)
+    # expert weights: exact derivative of <dout, out> (gates are constants 1)
+    L0, _ = _loss(cfg, x, Wr, Wup, Wd, None, b, gum, dout)
+    for ix in [(0, 1, 2), (1, 0, 3), (3, 5, 1)]:
+        for arr_name in ("Wup", "Wd"):
+            arr = Wup if arr_name == "Wup" else Wd
+            grad = g["dWup"] if arr_name == "Wup" else g["dWdown"]
+            vals = []
+            for s in (+h, -h):
+                a2 = arr.copy()
+                a2[ix] += s
+                L, _ = _loss(cfg, x, Wr, a2 if arr_name == "Wup" else Wup,
+                             a2 if arr_name == "Wd" else Wd, None, b, gum, dout)
+                vals.append(L)
+            assert grad[ix] == pytest.approx((vals[0] - vals[1]) / (2 * h), rel=2e-5, abs=2e-7)
+
+
+def test_masked_batch_equals_the_batch_without_padding(oracle_lib):
+    """Padding tokens take no part in routing ([LLaMA4-MoE] §4.1): outputs,
+    statistics and gradients equal those of the real tokens alone."""
+    rng = np.random.default_rng(99)
+    T, d, f, E, k = 30, 8, 12, 4, 2
+    x, Wr, Wup, Wg, Wd, b, _ = _rand_case(rng, T, d, f, E, k, swiglu=True, bias=True)
+    mask = (rng.uniform(size=T) > 0.35).astype(np.uint8)
+    real = np.nonzero(mask)[0]
+    dout = rng.standard_normal((T, d))
+    full = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, swiglu=True, aux_coef=0.3, temperature=0.9)
+    sub = oracle.OracleConfig(T=len(real), d=d, f=f, E=E, k=k, swiglu=True, aux_coef=0.3,
+                              temperature=0.9)
+    rf = oracle.forward(full, x, Wr, Wup, Wd, Wgate=Wg, bias=b, mask=mask)
+    rs = oracle.forward(sub, x[real], Wr, Wup, Wd, Wgate=Wg, bias=b)
+    np.testing.assert_allclose(rf["out"][real], rs["out"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(rf["stats"][oracle.ST_PBAR:], rs["stats"][oracle.ST_PBAR:], rtol=1e-13)
+    for i in (oracle.ST_AUX_LOSS, oracle.ST_AUX_SWITCH, oracle.ST_ENTROPY, oracle.ST_TOKENS):
+        assert rf["stats"][i] == pytest.approx(rs["stats"][i], rel=1e-13)
+    gf = oracle.backward(full, x, Wr, Wup, Wd, rf["logits"], rf["topk_idx"], rf["gate"],
+                         rf["slot_of"], dout, Wgate=Wg, with_bias=True)
+    gs = oracle.backward(sub, x[real], Wr, Wup, Wd, rs["logits"], rs["topk_idx"], rs["gate"],
+                         rs["slot_of"], dout[real], Wgate=Wg, with_bias=True)
+    np.testing.assert_allclose(gf["dx"][real], gs["dx"], rtol=1e-12, atol=1e-14)
+    assert (gf["dx"][mask == 0] == 0).all()
+    for key in ("dWr", "db", "dWup", "dWgate", "dWdown"):
+        np.testing.assert_allclose(gf[key], gs[key], rtol=1e-12, atol=1e-14)
