@@ -255,7 +255,7 @@ def run_ours(args, w):
     # one step through the C ABI; optional events around each call (all on `st`)
     def forward(evs=None):
         rec(evs, 0)
-        moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
+        moe.moe_route(cfg, x, Wr, b, nz, None, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
         rec(evs, 1)
         moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept, L.offsets,
                         L.stats, L.ws, st)
@@ -343,7 +343,7 @@ def run_ours(args, w):
         # per-stage breakdown: each C-ABI call captured as its own CUDA graph and
         # replayed between events (device time, no host launch overhead)
         stage_fns = [
-            lambda: moe.moe_route(cfg, x, Wr, b, nz, L.logits, L.topk_idx, L.gate, L.counts,
+            lambda: moe.moe_route(cfg, x, Wr, b, nz, None, L.logits, L.topk_idx, L.gate, L.counts,
                                   L.stats, L.ws, st),
             lambda: moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept,
                                     L.offsets, L.stats, L.ws, st),

@@ -90,9 +90,18 @@ typedef struct {
     float aux_coef;          /* lambda of L_aux = lambda * sum_e (pbar_e - 1/E)^2 */
     int32_t pad_m;           /* rows of each expert segment are padded to a
                                 multiple of pad_m; bf16 needs a multiple of 128  */
+    float temperature;       /* softmax temperature tau: p = softmax(logits / tau)
+                                ([Twinkle] §3.1, [ZeRO3-MoE] §3.2); 0 means 1     */
+    int32_t straight_through;/* 1: Gumbel top-k with a straight-through estimator
+                                ([Twinkle] §3.1): experts are selected on
+                                logits + noise (noise = the caller's Gumbel draws),
+                                `logits` stays noise-free, gates are 1 in the
+                                forward, and the backward flows through
+                                softmax(logits / tau) at the selected experts     */
 } moe_config;
 
-/* ---- statistics vector written by moe_route / moe_permute (fp32, 8 + E) ---- */
+/* ---- statistics vector written by moe_route / moe_permute (fp32, 9 + E) ----
+ * Means run over the routed tokens (tokens not masked out).                  */
 #define MOE_STAT_AUX_LOSS 0      /* lambda * sum_e (pbar_e - 1/E)^2   [ZeRO3-MoE] §3.2 */
 #define MOE_STAT_AUX_SWITCH 1    /* E * sum_e f_e pbar_e, f = counts/(T k) [LLaMA4-MoE] §3.2 */
 #define MOE_STAT_ENTROPY 2       /* mean over tokens of -sum_e p log p  [LLaMA4-MoE] §3.3 */
@@ -101,8 +110,9 @@ typedef struct {
 #define MOE_STAT_MAX_OVER_MEAN_KEPT 5  /* max_e kept_e / mean_e kept_e (moe_permute) */
 #define MOE_STAT_COUNT_CV 6      /* std/mean of counts over experts                  */
 #define MOE_STAT_MAX_OVER_MEAN_COUNT 7
-#define MOE_STAT_PBAR 8          /* pbar[0..E): mean softmax probability per expert  */
-#define MOE_STATS_LEN(E) (8 + (E))
+#define MOE_STAT_TOKENS 8        /* routed tokens (not masked out)                   */
+#define MOE_STAT_PBAR 9          /* pbar[0..E): mean softmax probability per expert  */
+#define MOE_STATS_LEN(E) (9 + (E))
 
 /* Validate a configuration.  MOE_OK, MOE_ERR_INVALID_ARG (impossible shape)
  * or MOE_ERR_UNSUPPORTED (bf16 needs d % 128 == 0, f % 128 == 0 and
@@ -122,17 +132,22 @@ MOE_API int moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* ---- forward ---- */
 
-/* Router: logits = x W_r (+ bias) (+ noise) in fp32 accumulation; softmax;
- * top-k (largest logits; ties to the lowest expert id; NaN ranks lowest),
- * slot j = rank j; gates; per-expert selection counts; statistics.
+/* Router: logits = x W_r (+ bias) (+ noise) in fp32 accumulation; softmax of
+ * logits / tau; top-k (largest logits; ties to the lowest expert id; NaN ranks
+ * lowest), slot j = rank j; gates; per-expert selection counts; statistics.
  *   x[T,d] act dtype; W_r[d,E] act dtype; bias[E] fp32 or NULL;
- *   noise[T,E] fp32 or NULL (gate noise drawn by the caller, [LLaMA4-MoE] §3.2);
+ *   noise[T,E] fp32 or NULL: gate noise drawn by the caller ([LLaMA4-MoE] §3.2),
+ *     added to the logits; in straight-through mode the Gumbel draws that
+ *     perturb only the selection;
+ *   token_mask[T] uint8 or NULL: 0 marks a padding token, which takes no part
+ *     in routing ([LLaMA4-MoE] §4.1): topk -1, gates 0, no counts, no output,
+ *     no gradient, and it is left out of every statistic;
  *   out: logits[T,E] fp32, topk_idx[T,k] int32, gate[T,k] fp32,
- *        counts[E] int32, stats[8+E] fp32 (entries 4 and 5 by moe_permute).
+ *        counts[E] int32, stats[9+E] fp32 (entries 4 and 5 by moe_permute).
  * [LLaMA4-MoE] §2.4; [Twinkle] §3.1; [ZeRO3-MoE] §5.3.                         */
 MOE_API int moe_route(const moe_config* cfg, const void* x, const void* W_r, const float* bias,
-              const float* noise, float* logits, int32_t* topk_idx, float* gate,
-              int32_t* counts, float* stats, void* ws, moe_stream_t stream);
+              const float* noise, const uint8_t* token_mask, float* logits, int32_t* topk_idx,
+              float* gate, int32_t* counts, float* stats, void* ws, moe_stream_t stream);
 
 /* Router for callers that cannot allocate device memory (no counterpart in the
  * pages: it exists for embedding).  Some hosts own all device memory through
@@ -152,9 +167,9 @@ MOE_API int moe_route(const moe_config* cfg, const void* x, const void* W_r, con
  *     whose kernels overlap on the GPU race on it.                            */
 #define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
 MOE_API int moe_route_noalloc(const moe_config* cfg, const void* x, const void* W_r,
-                              const float* bias, const float* noise, float* logits,
-                              int32_t* topk_idx, float* gate, int32_t* counts, float* stats,
-                              moe_stream_t stream);
+                              const float* bias, const float* noise, const uint8_t* token_mask,
+                              float* logits, int32_t* topk_idx, float* gate, int32_t* counts,
+                              float* stats, moe_stream_t stream);
 
 /* Capacity + permutation: rank each assignment (t, j) among its expert's
  * assignments in ascending token order; keep it iff rank < C; lay experts out
@@ -210,8 +225,10 @@ MOE_API int moe_grouped_ffn_backward(const moe_config* cfg, const void* x_perm, 
                              void* ws, moe_stream_t stream);
 
 /* Router backward.  dlogits[t] = gate softmax Jacobian applied to dgate
- * (selected logits only) + aux term lambda*2(pbar-1/E)/T through the full
- * softmax; dx[t] = sum over kept slots of dx_perm[slot] + dlogits[t] W_r^T;
+ * (selected logits only; raw and straight-through gates through the full
+ * softmax) + aux term lambda*2(pbar-1/E)/T_routed through the full softmax,
+ * all divided by tau; masked tokens get none; dx[t] = sum over kept slots of
+ * dx_perm[slot] + dlogits[t] W_r^T;
  * dW_r = x^T dlogits; dbias = sum_t dlogits (if non-NULL).
  *   stats: the moe_route statistics of the same forward (pbar is used).
  *   dlogits[T,E] fp32 output (may be NULL: then ws is used).

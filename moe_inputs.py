@@ -23,7 +23,7 @@ ZIPF_BIAS_FILE = os.path.join(_HERE, "tests", "golden", "skewed16_zipf_bias.json
 
 # fixed stream ids (one per tensor)
 _TENSOR_IDS = {"x": 1, "W_r": 2, "bias": 3, "W_up": 4, "W_gate": 5, "W_down": 6,
-               "noise": 7, "dout": 8}
+               "noise": 7, "dout": 8, "gumbel": 9, "mask": 10}
 
 
 @dataclass(frozen=True)
@@ -146,3 +146,26 @@ def make_inputs(w: Workload, seed: int = 0, parts=("x", "W_r", "bias", "W_up", "
     if "dout" in parts:
         out["dout"] = normal(seed, "dout", (w.T, w.d), 1.0, dt)
     return out
+
+
+def gumbel(seed: int, T: int, E: int) -> np.ndarray:
+    """fp32 [T, E] standard Gumbel draws, -ln(-ln U) with U uniform on (0, 1):
+    the selection noise of Gumbel top-k routing."""
+    rng = np.random.Generator(np.random.PCG64([seed, _TENSOR_IDS["gumbel"]]))
+    u = rng.random((T, E))
+    u = np.clip(u, np.finfo(np.float64).tiny, 1.0 - 2.0 ** -53)
+    return (-np.log(-np.log(u))).astype(np.float32)
+
+
+def padding_mask(seed: int, T: int, seq_len: int = 128) -> np.ndarray:
+    """uint8 [T] token mask of a right-padded batch (1 = real token, 0 = padding):
+    the tokens form sequences of ``seq_len``; each keeps a uniformly drawn real
+    length in [seq_len / 2, seq_len], the last sequence is all padding and the
+    tokens past the last full sequence are padding too."""
+    rng = np.random.Generator(np.random.PCG64([seed, _TENSOR_IDS["mask"]]))
+    m = np.zeros(T, np.uint8)
+    nseq = T // seq_len
+    for s in range(max(nseq - 1, 0)):
+        n = int(rng.integers(seq_len // 2, seq_len + 1))
+        m[s * seq_len: s * seq_len + n] = 1
+    return m

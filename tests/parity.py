@@ -42,29 +42,37 @@ def np64(t) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def gpu_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True) -> moe.MoEConfig:
+def gpu_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True, temperature=1.0,
+            straight_through=False) -> moe.MoEConfig:
     return moe.MoEConfig(T=w.T, d=w.d, f=w.f, E=w.E, k=w.k,
                          capacity_factor=w.capacity_factor,
                          ffn=moe.SWIGLU if w.swiglu else moe.SILU,
                          dtype=moe.BF16 if w.dtype == "bf16" else moe.F32,
-                         normalize_gates=1 if normalize else 0, aux_coef=w.aux_coef, pad_m=pad_m)
+                         normalize_gates=1 if normalize else 0, aux_coef=w.aux_coef, pad_m=pad_m,
+                         temperature=temperature, straight_through=int(straight_through))
 
 
-def oracle_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True) -> oracle.OracleConfig:
+def oracle_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True, temperature=1.0,
+               straight_through=False) -> oracle.OracleConfig:
     return oracle.OracleConfig(T=w.T, d=w.d, f=w.f, E=w.E, k=w.k,
                                capacity_factor=float(np.float32(w.capacity_factor)),
                                swiglu=w.swiglu, normalize_gates=normalize,
-                               aux_coef=float(np.float32(w.aux_coef)), pad_m=pad_m)
+                               aux_coef=float(np.float32(w.aux_coef)), pad_m=pad_m,
+                               temperature=float(np.float32(temperature)),
+                               straight_through=bool(straight_through))
 
 
 def f64_inputs(w, inp):
-    return {k: moe_inputs.as_f64(v, w.dtype if k not in ("bias", "noise") else "fp32")
+    return {k: (v if k == "mask" else
+                moe_inputs.as_f64(v, w.dtype if k not in ("bias", "noise") else "fp32"))
             for k, v in inp.items()}
 
 
-def run_gpu(w, inp, pad_m=128, normalize=True, backward=True):
-    """Forward (and the backward sub-steps with their intermediates) on the GPU."""
-    cfg = gpu_cfg(w, pad_m, normalize)
+def run_gpu(w, inp, pad_m=128, normalize=True, backward=True, temperature=1.0,
+            straight_through=False):
+    """Forward (and the backward sub-steps with their intermediates) on the GPU.
+    ``inp["mask"]`` (uint8 [T], 0 = padding token) is optional."""
+    cfg = gpu_cfg(w, pad_m, normalize, temperature, straight_through)
     dt = w.dtype
     x = to_torch(inp["x"], dt)
     Wr = to_torch(inp["W_r"], dt)
@@ -73,8 +81,9 @@ def run_gpu(w, inp, pad_m=128, normalize=True, backward=True):
     Wd = to_torch(inp["W_down"], dt)
     b = to_torch(inp.get("bias"), "fp32")
     nz = to_torch(inp.get("noise"), "fp32")
+    mk = to_torch(inp.get("mask"), "u8")
     L = moe.MoELayer(cfg)
-    L.forward(x, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz)
+    L.forward(x, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, token_mask=mk)
     res = dict(cfg=cfg, layer=L)
     if backward:
         dout = to_torch(inp["dout"], dt)
@@ -102,12 +111,15 @@ def check_routing(w, ocfg, r, inp64, report):
     """Route/permute parity.  Returns the conditioned oracle forward."""
     L = r["layer"]
     logits = np64(L.logits)
-    # logits vs fp64 oracle
-    ol = oracle.router_logits(ocfg, inp64["x"], inp64["W_r"], inp64.get("bias"), inp64.get("noise"))
+    noise, mask = inp64.get("noise"), inp64.get("mask")
+    st_mode = ocfg.straight_through
+    # logits vs fp64 oracle (straight-through: the noise enters only the selection)
+    ol = oracle.router_logits(ocfg, inp64["x"], inp64["W_r"], inp64.get("bias"),
+                              None if st_mode else noise)
     report["logits_rel"] = rel_fro(logits, ol)
     # conditioned oracle: route the GPU's fp32 logits
     o = oracle.forward(ocfg, inp64["x"], inp64["W_r"], inp64["W_up"], inp64["W_down"],
-                       Wgate=inp64.get("W_gate"), logits_in=logits)
+                       Wgate=inp64.get("W_gate"), noise=noise, logits_in=logits, mask=mask)
     topk = L.topk_idx.cpu().numpy()
     assert (topk == o["topk_idx"]).all(), "top-k differs from the oracle on the same logits"
     assert (L.counts.cpu().numpy() == o["counts"]).all(), "counts differ"
@@ -124,13 +136,15 @@ def check_routing(w, ocfg, r, inp64, report):
         assert abs(st[i] - o["stats"][i]) <= 1e-4 * max(1.0, abs(o["stats"][i])), (i, st[i], o["stats"][i])
     assert abs(st[moe.STAT_AUX_LOSS] - o["stats"][oracle.ST_AUX_LOSS]) <= \
         1e-3 * abs(o["stats"][oracle.ST_AUX_LOSS]) + 1e-9
-    for i in (moe.STAT_NONFINITE, moe.STAT_DROPPED):
+    for i in (moe.STAT_NONFINITE, moe.STAT_DROPPED, moe.STAT_TOKENS):
         assert st[i] == o["stats"][i], (i, st[i], o["stats"][i])
     for i in (moe.STAT_MAX_OVER_MEAN_KEPT, moe.STAT_COUNT_CV, moe.STAT_MAX_OVER_MEAN_COUNT):
         assert abs(st[i] - o["stats"][i]) <= 1e-5 * max(1.0, abs(o["stats"][i])), (i, st[i], o["stats"][i])
     # independent routing (oracle's own fp64 logits)
-    oi = oracle.route(ocfg, ol)
-    srt = -np.sort(-ol, axis=1)
+    oi = oracle.route(ocfg, ol, noise if st_mode else None, mask)
+    key = (ol.astype(np.float32) + noise.astype(np.float32)).astype(np.float64) \
+        if st_mode and noise is not None else ol
+    srt = -np.sort(-key, axis=1)
     gap = srt[:, ocfg.k - 1] - srt[:, ocfg.k] if ocfg.k < ocfg.E else np.full(ocfg.T, np.inf)
     near = gap < NEAR_TIE
     same = (np.sort(oi["topk_idx"], 1) == np.sort(topk, 1)).all(1)
@@ -165,12 +179,15 @@ def check_forward(w, ocfg, r, o, inp64, report, sample_rows=None):
         want_h.append(ef["h"]); want_a.append(ef["act"]); want_y.append(ef["y"])
         if ocfg.swiglu:
             want_u.append(ef["u"])
+    report["out_rel"] = rel_fro(np64(L.out), o["out"])
+    if len(idx) == 0:        # nothing routed (e.g. every token is padding)
+        assert (np64(L.out) == 0).all(), "out is not zero with no routed token"
+        return
     report["h_rel"] = rel_fro(H[0][idx], np.array(want_h))
     if ocfg.swiglu:
         report["u_rel"] = rel_fro(H[1][idx], np.array(want_u))
     report["act_rel"] = rel_fro(A[idx], np.array(want_a))
     report["y_rel"] = rel_fro(Y[idx], np.array(want_y))
-    report["out_rel"] = rel_fro(np64(L.out), o["out"])
     for key in ("h_rel", "u_rel", "act_rel", "y_rel", "out_rel"):
         if key in report:
             assert report[key] <= tol, (key, report[key], tol)
@@ -214,11 +231,13 @@ def check_backward(w, ocfg, r, o, inp64, report, with_bias):
             assert v <= tol, (key, v, tol)
 
 
-def full_check(w, inp, pad_m=128, normalize=True, backward=True, sample_rows=None):
+def full_check(w, inp, pad_m=128, normalize=True, backward=True, sample_rows=None,
+               temperature=1.0, straight_through=False):
     report = {}
-    r = run_gpu(w, inp, pad_m=pad_m, normalize=normalize, backward=backward)
+    r = run_gpu(w, inp, pad_m=pad_m, normalize=normalize, backward=backward,
+                temperature=temperature, straight_through=straight_through)
     assert r["status"] == 0, f"device status {r['status']}"
-    ocfg = oracle_cfg(w, pad_m, normalize)
+    ocfg = oracle_cfg(w, pad_m, normalize, temperature, straight_through)
     inp64 = f64_inputs(w, inp)
     o = check_routing(w, ocfg, r, inp64, report)
     check_forward(w, ocfg, r, o, inp64, report, sample_rows=sample_rows)

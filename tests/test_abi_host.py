@@ -49,15 +49,17 @@ def test_binding_signatures_match_header():
 
 
 def test_struct_layout_matches_header():
-    # 11 four-byte fields, no padding
-    assert ctypes.sizeof(moe.MoEConfig) == 44
+    # 13 four-byte fields, no padding
+    assert ctypes.sizeof(moe.MoEConfig) == 52
 
 
 def test_config_validation():
     ok = moe.MoEConfig(T=2048, d=1024, f=2048, E=4, k=2, capacity_factor=1.2)
     assert moe.check_config(ok) == moe.OK
     bad = [dict(T=0), dict(k=5), dict(E=0), dict(pad_m=0), dict(dtype=7), dict(ffn=3),
-           dict(normalize_gates=2), dict(capacity_factor=float("nan"))]
+           dict(normalize_gates=2), dict(capacity_factor=float("nan")),
+           dict(temperature=float("nan")), dict(temperature=-1.0), dict(temperature=float("inf")),
+           dict(straight_through=2)]
     for b in bad:
         kw = dict(T=64, d=256, f=256, E=4, k=2)
         kw.update(b)
@@ -91,13 +93,13 @@ def test_rows_capacity_and_workspace():
 def test_null_and_misaligned_pointers_are_rejected_before_launch():
     lib = moe.load_library()
     c = moe.MoEConfig(T=64, d=256, f=256, E=4, k=2)
-    args = [ctypes.byref(c)] + [None] * 10 + [None]
+    args = [ctypes.byref(c)] + [None] * 11 + [None]
     assert lib.moe_route(*args) == moe.ERR_INVALID_ARG
     p = ctypes.c_void_p(0x1000 + 8)  # misaligned
-    args = [ctypes.byref(c)] + [p] * 10 + [None]
+    args = [ctypes.byref(c)] + [p] * 11 + [None]
     assert lib.moe_route(*args) == moe.ERR_INVALID_ARG
     assert lib.moe_combine(ctypes.byref(c), None, None, None, None, None) == moe.ERR_INVALID_ARG
-    assert lib.moe_route(None, *([None] * 11)) == moe.ERR_INVALID_ARG
+    assert lib.moe_route(None, *([None] * 12)) == moe.ERR_INVALID_ARG
 
 
 def test_error_strings():

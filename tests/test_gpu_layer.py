@@ -6,6 +6,7 @@ import pytest
 import torch
 
 import moe_inputs
+import top_routing_expert_moe_gb300 as moe
 from tests import parity
 
 pytestmark = pytest.mark.gpu
@@ -156,3 +157,71 @@ def test_expert_count_and_top_k_sweep(E, k, dtype):
     rep, _ = parity.full_check(w, _edge_inputs(w, seed=E * 10 + k),
                                pad_m=128 if dtype == "bf16" else 8)
     _report(f"sweep E{E} k{k} {dtype}", rep)
+
+
+# ------------------------------------------------------------------ router variants
+@pytest.mark.parametrize("tau,normalize,dtype", [(0.5, True, "bf16"), (2.0, False, "bf16"),
+                                                 (0.7, True, "fp32"), (3.0, False, "fp32")])
+def test_softmax_temperature(tau, normalize, dtype):
+    base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
+    w = _w(base, T=777, d=256 if dtype == "bf16" else 64, f=256 if dtype == "bf16" else 96,
+           E=8, k=2, capacity_factor=1.25)
+    rep, _ = parity.full_check(w, _edge_inputs(w, seed=11), pad_m=128 if dtype == "bf16" else 4,
+                               normalize=normalize, temperature=tau)
+    _report(f"temperature {tau} norm{int(normalize)} {dtype}", rep)
+
+
+@pytest.mark.parametrize("dtype,E,k,tau", [("bf16", 8, 2, 1.0), ("bf16", 16, 4, 0.5),
+                                           ("fp32", 6, 1, 2.0)])
+def test_straight_through_gumbel_topk(dtype, E, k, tau):
+    """Selection on logits + Gumbel draws, gates 1, gradient through softmax(l / tau)."""
+    base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
+    w = _w(base, T=640, d=256 if dtype == "bf16" else 64, f=256 if dtype == "bf16" else 96,
+           E=E, k=k, capacity_factor=1.3)
+    inp = _edge_inputs(w, seed=21)
+    inp["noise"] = moe_inputs.gumbel(21, w.T, w.E)
+    rep, r = parity.full_check(w, inp, pad_m=128 if dtype == "bf16" else 8,
+                               temperature=tau, straight_through=True)
+    assert (r["layer"].gate == 1).all()
+    # the draws change the selection relative to the noise-free logits
+    plain = np.argsort(-parity.np64(r["layer"].logits), axis=1, kind="stable")[:, :k]
+    assert (np.sort(plain, 1) != np.sort(r["layer"].topk_idx.cpu().numpy(), 1)).any(1).mean() > 0.2
+    _report(f"straight-through E{E} k{k} tau{tau} {dtype}", rep)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_padding_tokens_take_no_part(dtype):
+    base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
+    w = _w(base, T=1100, d=256 if dtype == "bf16" else 64, f=256 if dtype == "bf16" else 96,
+           E=8, k=2, capacity_factor=1.1)
+    inp = _edge_inputs(w, seed=31)
+    inp["mask"] = moe_inputs.padding_mask(31, w.T)
+    rep, r = parity.full_check(w, inp, pad_m=128 if dtype == "bf16" else 4)
+    L = r["layer"]
+    pad = inp["mask"] == 0
+    assert pad.sum() > 128
+    assert (L.topk_idx.cpu().numpy()[pad] == -1).all()
+    assert (L.out.float().cpu().numpy()[pad] == 0).all()
+    assert (r["grads"]["dx"].float().cpu().numpy()[pad] == 0).all()
+    assert L.stats[moe.STAT_TOKENS].item() == int((~pad).sum())
+    _report(f"padding mask {dtype}", rep)
+
+
+def test_padding_mask_with_noise_temperature_and_raw_gates():
+    w = _w("llama4_bf16").with_tokens(1024)
+    inp = moe_inputs.make_inputs(w, 4)
+    inp["mask"] = moe_inputs.padding_mask(4, w.T, seq_len=256)
+    rep, _ = parity.full_check(w, inp, sample_rows=256, normalize=False, temperature=1.5)
+    _report("llama4 mask+noise+tau", rep)
+
+
+def test_every_token_padding():
+    w = _w("small_bf16", T=300, d=256, f=256)
+    inp = _edge_inputs(w, seed=41)
+    inp["mask"] = np.zeros(w.T, np.uint8)
+    rep, r = parity.full_check(w, inp)
+    L = r["layer"]
+    assert int(L.offsets[-1].item()) == 0 and int(L.counts.sum().item()) == 0
+    for name in ("dx", "dW_up", "dW_down", "dW_r"):
+        assert (r["grads"][name].float() == 0).all(), name
+    _report("all padding", rep)

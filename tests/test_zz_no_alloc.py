@@ -35,14 +35,14 @@ def _route_both(w, seed):
                     topk=torch.empty(w.T, w.k, dtype=torch.int32, device=dev),
                     gate=torch.empty(w.T, w.k, dtype=torch.float32, device=dev),
                     counts=torch.empty(w.E, dtype=torch.int32, device=dev),
-                    stats=torch.empty(8 + w.E, dtype=torch.float32, device=dev))
+                    stats=torch.empty(9 + w.E, dtype=torch.float32, device=dev))
 
     ref = outputs()
     ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=dev)
-    moe.moe_route(cfg, x, Wr, b, nz, ref["logits"], ref["topk"], ref["gate"], ref["counts"],
+    moe.moe_route(cfg, x, Wr, b, nz, None, ref["logits"], ref["topk"], ref["gate"], ref["counts"],
                   ref["stats"], ws)
     got = outputs()
-    moe.moe_route_noalloc(cfg, x, Wr, b, nz, got["logits"], got["topk"], got["gate"],
+    moe.moe_route_noalloc(cfg, x, Wr, b, nz, None, got["logits"], got["topk"], got["gate"],
                           got["counts"], got["stats"])
     torch.cuda.synchronize()
     return ref, got
@@ -79,5 +79,5 @@ def test_route_noalloc_rejects_configs_beyond_its_scratch():
     gate = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
     counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
     with pytest.raises(moe.MoEError) as ei:
-        moe.moe_route_noalloc(cfg, x, Wr, None, None, logits, topk, gate, counts, None)
+        moe.moe_route_noalloc(cfg, x, Wr, None, None, None, logits, topk, gate, counts, None)
     assert ei.value.code == moe.ERR_SCRATCH_LIMIT

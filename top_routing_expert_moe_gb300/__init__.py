@@ -26,7 +26,7 @@ F32, BF16 = 0, 1
 SILU, SWIGLU = 0, 1
 STAT_AUX_LOSS, STAT_AUX_SWITCH, STAT_ENTROPY, STAT_NONFINITE = 0, 1, 2, 3
 STAT_DROPPED, STAT_MAX_OVER_MEAN_KEPT, STAT_COUNT_CV, STAT_MAX_OVER_MEAN_COUNT = 4, 5, 6, 7
-STAT_PBAR = 8
+STAT_TOKENS, STAT_PBAR = 8, 9
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE, ERR_DEVICE_BOUNDS = \
     0, -1, -2, -3, -4, -5, -6
@@ -40,12 +40,14 @@ class MoEConfig(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("ffn", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("normalize_gates", ctypes.c_int32),
-                ("aux_coef", ctypes.c_float), ("pad_m", ctypes.c_int32)]
+                ("aux_coef", ctypes.c_float), ("pad_m", ctypes.c_int32),
+                ("temperature", ctypes.c_float), ("straight_through", ctypes.c_int32)]
 
     def __init__(self, T, d, f, E, k, capacity_factor=0.0, ffn=SILU, dtype=BF16,
-                 normalize_gates=1, aux_coef=0.0, pad_m=128):
+                 normalize_gates=1, aux_coef=0.0, pad_m=128, temperature=1.0,
+                 straight_through=0):
         super().__init__(T, d, f, E, k, capacity_factor, ffn, dtype, normalize_gates, aux_coef,
-                         pad_m)
+                         pad_m, temperature, int(straight_through))
 
     @property
     def torch_dtype(self):
@@ -71,8 +73,8 @@ _SIGS = {
     "moe_capacity": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_rows_capacity": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_workspace_size": [ctypes.c_void_p, ctypes.c_void_p],
-    "moe_route": [ctypes.c_void_p] * 12,
-    "moe_route_noalloc": [ctypes.c_void_p] * 11,
+    "moe_route": [ctypes.c_void_p] * 13,
+    "moe_route_noalloc": [ctypes.c_void_p] * 12,
     "moe_permute": [ctypes.c_void_p] * 11,
     "moe_grouped_ffn": [ctypes.c_void_p] * 11,
     "moe_combine": [ctypes.c_void_p] * 6,
@@ -169,18 +171,19 @@ def last_device_status(stream=None) -> int:
 
 
 # ----------------------------------------------------------------- entry points
-def moe_route(cfg, x, W_r, bias, noise, logits, topk_idx, gate, counts, stats, ws, stream=None):
-    _call("moe_route", ctypes.byref(cfg), _p(x), _p(W_r), _p(bias), _p(noise), _p(logits),
-          _p(topk_idx), _p(gate), _p(counts), _p(stats), _p(ws), _s(stream))
+def moe_route(cfg, x, W_r, bias, noise, token_mask, logits, topk_idx, gate, counts, stats, ws,
+              stream=None):
+    _call("moe_route", ctypes.byref(cfg), _p(x), _p(W_r), _p(bias), _p(noise), _p(token_mask),
+          _p(logits), _p(topk_idx), _p(gate), _p(counts), _p(stats), _p(ws), _s(stream))
 
 
-def moe_route_noalloc(cfg, x, W_r, bias, noise, logits, topk_idx, gate, counts, stats,
+def moe_route_noalloc(cfg, x, W_r, bias, noise, token_mask, logits, topk_idx, gate, counts, stats,
                       stream=None):
     """moe_route without a workspace, for callers that cannot allocate device
     memory: scratch comes from the library's static device array (shared by all
     calls; overlapping calls race)."""
     _call("moe_route_noalloc", ctypes.byref(cfg), _p(x), _p(W_r), _p(bias), _p(noise),
-          _p(logits), _p(topk_idx), _p(gate), _p(counts), _p(stats), _s(stream))
+          _p(token_mask), _p(logits), _p(topk_idx), _p(gate), _p(counts), _p(stats), _s(stream))
 
 
 def moe_permute(cfg, x, topk_idx, x_perm, perm_token, slot_of, kept, offsets, stats, ws,
@@ -248,7 +251,7 @@ class MoELayer:
         self.topk_idx = e(T, k, dtype=torch.int32)
         self.gate = e(T, k, dtype=torch.float32)
         self.counts = e(E, dtype=torch.int32)
-        self.stats = e(8 + E, dtype=torch.float32)
+        self.stats = e(9 + E, dtype=torch.float32)
         self.x_perm = e(R, d)
         self.perm_token = e(R, dtype=torch.int32)
         self.slot_of = e(T, k, dtype=torch.int32)
@@ -262,10 +265,11 @@ class MoELayer:
         self._grads = None
         self._inputs = None
 
-    def forward(self, x, W_r, W_up, W_down, W_gate=None, bias=None, noise=None, stream=None):
+    def forward(self, x, W_r, W_up, W_down, W_gate=None, bias=None, noise=None, token_mask=None,
+                stream=None):
         c = self.cfg
-        moe_route(c, x, W_r, bias, noise, self.logits, self.topk_idx, self.gate, self.counts,
-                  self.stats, self.ws, stream)
+        moe_route(c, x, W_r, bias, noise, token_mask, self.logits, self.topk_idx, self.gate,
+                  self.counts, self.stats, self.ws, stream)
         moe_permute(c, x, self.topk_idx, self.x_perm, self.perm_token, self.slot_of, self.kept,
                     self.offsets, self.stats, self.ws, stream)
         moe_grouped_ffn(c, self.x_perm, self.offsets, W_up, W_gate, W_down, self.h_saved,

@@ -150,7 +150,8 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     const float* __restrict__ gate, const int32_t* __restrict__ slot_of,
     const float* __restrict__ dgate, const float* __restrict__ stats,
     const T* __restrict__ dx_perm, const float* __restrict__ WrT, int Tn, int d, int E, int k,
-    int normalize, float aux_coef, float* __restrict__ dlogits, T* __restrict__ dx)
+    int normalize, int st, float inv_tau, float aux_coef, float* __restrict__ dlogits,
+    T* __restrict__ dx)
 {
     constexpr int V = 16 / sizeof(T);
     __shared__ float s_dl[8][64];
@@ -159,8 +160,9 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     const int warps = gridDim.x * (blockDim.x >> 5);
     for (int t = blockIdx.x * (blockDim.x >> 5) + wib; t < Tn; t += warps) {
         // lanes hold experts e = lane and lane + 32
-        float l0 = lane < E ? logits[(size_t)t * E + lane] : -INFINITY;
-        float l1 = lane + 32 < E ? logits[(size_t)t * E + lane + 32] : -INFINITY;
+        // p = softmax(l / tau); every derivative through it carries 1 / tau
+        float l0 = lane < E ? logits[(size_t)t * E + lane] * inv_tau : -INFINITY;
+        float l1 = lane + 32 < E ? logits[(size_t)t * E + lane + 32] * inv_tau : -INFINITY;
         const float m = warp_max(fmaxf(l0, l1));
         float p0 = lane < E ? expf(l0 - m) : 0.f;
         float p1 = lane + 32 < E ? expf(l1 - m) : 0.f;
@@ -168,7 +170,9 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
         p0 /= z;
         p1 /= z;
         float dl0 = 0.f, dl1 = 0.f;
-        if (normalize) {
+        const bool routed = topk[(size_t)t * k] >= 0;   // padding tokens: no gradient
+        if (!routed) {
+        } else if (normalize && !st) {
             float s = 0.f;
             for (int j = 0; j < k; ++j) {
                 float dg = slot_of[(size_t)t * k + j] >= 0 ? dgate[(size_t)t * k + j] : 0.f;
@@ -182,6 +186,8 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
                 if (e == lane + 32) dl1 += v;
             }
         } else {
+            // raw probabilities, and the straight-through estimator (gates 1 forward,
+            // gradient through p of the selected experts)
             float s = 0.f;
             for (int j = 0; j < k; ++j) {
                 float dg = slot_of[(size_t)t * k + j] >= 0 ? dgate[(size_t)t * k + j] : 0.f;
@@ -194,14 +200,17 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
             dl0 -= p0 * s;
             dl1 -= p1 * s;
         }
-        if (aux_coef != 0.f) {
-            const float invE = 1.0f / (float)E, sc = aux_coef * 2.0f / (float)Tn;
+        if (routed && aux_coef != 0.f) {
+            const float invE = 1.0f / (float)E;
+            const float sc = aux_coef * 2.0f / fmaxf(stats[MOE_STAT_TOKENS], 1.0f);
             const float c0 = lane < E ? sc * (stats[MOE_STAT_PBAR + lane] - invE) : 0.f;
             const float c1 = lane + 32 < E ? sc * (stats[MOE_STAT_PBAR + lane + 32] - invE) : 0.f;
             const float s2 = warp_sum(p0 * c0 + p1 * c1);
             dl0 += p0 * (c0 - s2);
             dl1 += p1 * (c1 - s2);
         }
+        dl0 *= inv_tau;
+        dl1 *= inv_tau;
         if (lane < E) { dlogits[(size_t)t * E + lane] = dl0; s_dl[wib][lane] = dl0; }
         if (lane + 32 < E) { dlogits[(size_t)t * E + lane + 32] = dl1; s_dl[wib][lane + 32] = dl1; }
         if (!WITH_DX) continue;
@@ -708,6 +717,7 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
     if (!dlogits) dlogits = reinterpret_cast<float*>(w);
     const int chunk = dwr_chunk(c, ns);
     const int grid = row_grid(c.T);
+    const float inv_tau = c.temperature > 0.f ? 1.0f / c.temperature : 1.0f;
     dim3 pgrid = dwr_grid_xy(c);
     pgrid.z = ns;
     // reduction buffer: 8 token lanes x 32 vectors x (V * EB) floats, V = 16 / sizeof(T)
@@ -731,7 +741,8 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
         using T = __nv_bfloat16;
         router_bwd_token_kernel<T, false><<<grid, 256, 0, st>>>(
             logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), nullptr,
-            c.T, c.d, c.E, c.k, c.normalize_gates, c.aux_coef, dlogits, static_cast<T*>(dx));
+            c.T, c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau, c.aux_coef, dlogits,
+            static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();
         MOE_TRY_R(launch_router_dx_bf16(c, dlogits, static_cast<const T*>(Wr), slot_of,
                                         static_cast<const T*>(dx_perm), static_cast<T*>(dx), st));
@@ -755,7 +766,8 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
         MOE_LAUNCH_CHECK();
         router_bwd_token_kernel<T, true><<<grid, 256, 0, st>>>(
             logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), WrT, c.T,
-            c.d, c.E, c.k, c.normalize_gates, c.aux_coef, dlogits, static_cast<T*>(dx));
+            c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau, c.aux_coef, dlogits,
+            static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();
         dwr_partial_kernel<T, DWR_EB><<<pgrid, 256, dwr_smem, st>>>(static_cast<const T*>(x), dlogits,
                                                                    c.T, c.d, c.E, chunk, part, part_db);

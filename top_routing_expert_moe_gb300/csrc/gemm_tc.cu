@@ -43,6 +43,7 @@
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace moe {
 
@@ -58,8 +59,6 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
 constexpr int RASTER_GM = 16;
-constexpr unsigned long long WAIT_NS = 4000000000ull;   // 4 s
-constexpr unsigned long long DRAIN_NS = 500000000ull;   // 0.5 s
 
 enum Epi { EPI_STORE = 0, EPI_SILU_FWD = 1, EPI_SWIGLU_FWD = 2, EPI_SILU_BWD = 3, EPI_SWIGLU_BWD = 4 };
 enum Sched { SCHED_ROWS = 0, SCHED_KSEG = 1 };
@@ -95,69 +94,7 @@ struct TcParams {
     int nprob, E;
 };
 
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ unsigned long long gtimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n.reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-// Bounded wait.  Returns false when the wait gave up (timeout or another
-// role's abort); the first to time out records the status and raises abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-    if (mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = gtimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 15) == 0) {
-            if (*abort_flag) return false;
-            if (gtimer() - t0 > WAIT_NS) {
-                set_status(status, MOE_ERR_TIMEOUT);
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-// Bounded wait used while draining (ignores the abort flag).
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = gtimer();
-    while (!mbar_try(bar, parity))
-        if (gtimer() - t0 > DRAIN_NS) break;
-}
-
-__device__ __forceinline__ void tma_load3(const CUtensorMap* map, uint32_t dst, uint32_t bar, int c0,
-                                          int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
+// mbarrier / TMA / timer helpers: tma.cuh
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -535,9 +472,12 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D bf16 map: dims {d0 (contiguous), d1, d2}, byte strides {s1, s2}, box {b0, b1, 1}
-int make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-             uint64_t s2, uint32_t b0, uint32_t b1) {
+}  // namespace
+
+// 3-D bf16 map with 128-byte swizzle: dims {d0 (contiguous), d1, d2}, byte strides
+// {s1, s2}, box {b0, b1, 1}
+int encode_bf16_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return MOE_ERR_CUDA;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -548,6 +488,13 @@ int make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+namespace {
+
+int make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+             uint64_t s2, uint32_t b0, uint32_t b1) {
+    return encode_bf16_map(m, ptr, d0, d1, d2, s1, s2, b0, b1);
 }
 
 // activations [rows_cap, cols]: K-major box {64, 128} or MN-major box {64, 64}

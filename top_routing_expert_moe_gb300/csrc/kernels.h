@@ -16,8 +16,8 @@ int64_t rows_cap_of(const moe_config& c);  // worst-case permuted rows
 // route.cu
 size_t route_ws_bytes(const moe_config& c);
 int launch_route(const moe_config& c, const void* x, const void* Wr, const float* bias,
-                 const float* noise, float* logits, int32_t* topk, float* gate, int32_t* counts,
-                 float* stats, void* ws, cudaStream_t st);
+                 const float* noise, const uint8_t* mask, float* logits, int32_t* topk,
+                 float* gate, int32_t* counts, float* stats, void* ws, cudaStream_t st);
 
 // permute.cu
 size_t permute_ws_bytes(const moe_config& c);

@@ -106,6 +106,8 @@ int moe_check_config(const moe_config* c) {
     if (c->normalize_gates != 0 && c->normalize_gates != 1) return MOE_ERR_INVALID_ARG;
     if (std::isnan(c->capacity_factor) || std::isinf(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (!std::isfinite(c->aux_coef)) return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(c->temperature) || c->temperature < 0.0f) return MOE_ERR_INVALID_ARG;
+    if (c->straight_through != 0 && c->straight_through != 1) return MOE_ERR_INVALID_ARG;
     if (c->E > 64 || c->k > 8) return MOE_ERR_UNSUPPORTED;
     if (c->d % 8 != 0 || c->f % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (c->dtype == MOE_DTYPE_BF16 && (c->d % 128 != 0 || c->f % 128 != 0 || c->pad_m % 128 != 0))
@@ -147,15 +149,16 @@ int moe_workspace_size(const moe_config* c, size_t* bytes) {
 }
 
 int moe_route(const moe_config* c, const void* x, const void* W_r, const float* bias,
-              const float* noise, float* logits, int32_t* topk_idx, float* gate, int32_t* counts,
-              float* stats, void* ws, moe_stream_t stream) {
+              const float* noise, const uint8_t* token_mask, float* logits, int32_t* topk_idx,
+              float* gate, int32_t* counts, float* stats, void* ws, moe_stream_t stream) {
     int r = moe_check_config(c);
     if (r) return r;
-    if (!ok_ptr(x) || !ok_ptr(W_r) || !ok_opt(bias) || !ok_opt(noise) || !ok_ptr(logits) ||
-        !ok_ptr(topk_idx) || !ok_ptr(gate) || !ok_ptr(counts) || !ok_opt(stats) || !ok_ptr(ws))
+    if (!ok_ptr(x) || !ok_ptr(W_r) || !ok_opt(bias) || !ok_opt(noise) || !ok_opt(token_mask) ||
+        !ok_ptr(logits) || !ok_ptr(topk_idx) || !ok_ptr(gate) || !ok_ptr(counts) ||
+        !ok_opt(stats) || !ok_ptr(ws))
         return MOE_ERR_INVALID_ARG;
-    return launch_route(*c, x, W_r, bias, noise, logits, topk_idx, gate, counts, stats, ws,
-                        (cudaStream_t)stream);
+    return launch_route(*c, x, W_r, bias, noise, token_mask, logits, topk_idx, gate, counts,
+                        stats, ws, (cudaStream_t)stream);
 }
 
 int moe_permute(const moe_config* c, const void* x, const int32_t* topk_idx, void* x_perm,

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(PT_TOK) tile_hist_kernel(const int32_t* __rest
         for (int j = 0; j < k; ++j) {
             int e = topk[(size_t)t * k + j];
             if (e >= 0 && e < E) atomicAdd(&h[e], 1);  // integer count: order-free
-            else set_status(status, MOE_ERR_DEVICE_BOUNDS);
+            else if (e != -1) set_status(status, MOE_ERR_DEVICE_BOUNDS);  // -1: masked token
         }
     __syncthreads();
     if (threadIdx.x < E) tile_counts[(size_t)blockIdx.x * E + threadIdx.x] = h[threadIdx.x];

@@ -14,6 +14,7 @@
 // reduced in a fixed order by a one-CTA finalize kernel (deterministic).
 #include "common.cuh"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace moe {
 
@@ -26,8 +27,11 @@ constexpr int RT_STAGES = 4;
 
 struct RouteOut {
     int T, d, E, k, normalize;
+    int st;                // straight-through: noise enters the selection key only, gates 1
+    float inv_tau;         // 1 / softmax temperature
     const float* bias;
     const float* noise;
+    const uint8_t* mask;   // 0 = padding token (or NULL)
     float* logits;
     int32_t* topk;
     float* gate;
@@ -35,7 +39,12 @@ struct RouteOut {
     float* part_psum;      // [nblk][E]
     float* part_ent;       // [nblk]
     int32_t* part_bad;     // [nblk]
+    int32_t* part_real;    // [nblk] routed (unmasked) tokens
 };
+
+// barrier among the 256 threads (warps 0-7) that compute the router; a
+// producer warp, when present, does not take part
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // a ranks above b: larger logit; a NaN ranks below any number; then lower id
 __device__ __forceinline__ bool ranks_above(float la, int a, float lb, int b) {
@@ -45,81 +54,142 @@ __device__ __forceinline__ bool ranks_above(float la, int a, float lb, int b) {
     return a < b;
 }
 
-// Finish a tile of raw router sums held in sLog[tok][ldl]: one thread per
-// token, then fixed-order column sums for the per-CTA statistics.
-// sSel needs RT_TOK * k ints, sEnt/sBad RT_TOK entries.
-__device__ void finish_tile(float* sLog, int ldl, int* sSel, float* sEnt, int* sBad,
-                            int t0, int ntok, const RouteOut& o)
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Finish a tile of raw router sums held in sLog[tok][ldl], by nthr threads
+// (index i) sharing named barrier bar_id.  G = nthr / TT consecutive lanes
+// (a power of two, at most 32) work on one token: each lane takes experts
+// e = sub, sub + G, ..., and the lanes combine the row's max, sums, entropy
+// and each top-k pick with butterfly shuffles (exact, fixed order).  Then
+// fixed-order column sums give the tile's partial statistics (index pidx).
+template <int G>
+__device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, int* sBad, int t0,
+                                int ntok, int TT, int pidx, const RouteOut& o, int i, int nthr,
+                                int bar_id)
 {
     const int E = o.E, k = o.k;
-    const int i = threadIdx.x;
-    if (i < ntok) {
-        const int t = t0 + i;
-        float* l = sLog + i * ldl;
+    const int sub = i % G, per_pass = nthr / G;
+    const unsigned mask = 0xffffffffu;
+    const float itau = o.inv_tau;
+    for (int tok = i / G; tok < TT; tok += per_pass) {      // uniform trip count per G-group
+        const bool valid = tok < ntok;
+        const int t = t0 + tok;
+        const bool routed = valid && !(o.mask && o.mask[t] == 0);
+        float* l = sLog + tok * ldl;
         bool bad = false;
         float m = -INFINITY;
-        for (int e = 0; e < E; ++e) {
+        uint64_t taken = 0;                                  // my experts already selected
+        for (int e = sub; e < E; e += G) {
             float v = l[e];
             if (o.bias) v += o.bias[e];
-            if (o.noise) v += o.noise[(size_t)t * E + e];
+            if (o.noise && valid && !o.st) v += o.noise[(size_t)t * E + e];  // gate noise
             l[e] = v;
-            o.logits[(size_t)t * E + e] = v;
+            if (valid) o.logits[(size_t)t * E + e] = v;
             bad |= !isfinite(v);
-            m = fmaxf(m, v);  // fmaxf ignores NaN
+            m = fmaxf(m, v);
         }
-        // top-k: k passes of "best not yet taken"
-        int* sel = sSel + i * k;
-        for (int j = 0; j < k; ++j) {
-            int best = -1;
-            float bl = 0.f;
-            for (int e = 0; e < E; ++e) {
-                bool taken = false;
-                for (int q = 0; q < j; ++q) taken |= (sel[q] == e);
-                if (taken) continue;
-                if (best < 0 || ranks_above(l[e], e, bl, best)) { best = e; bl = l[e]; }
-            }
-            sel[j] = best;
-            o.topk[(size_t)t * k + j] = best;
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) {
+            m = fmaxf(m, __shfl_xor_sync(mask, m, off));
+            bad |= __shfl_xor_sync(mask, (int)bad, off) != 0;
         }
-        // softmax (fp32)
         float z = 0.f;
-        for (int e = 0; e < E; ++e) z += expf(l[e] - m);
+        for (int e = sub; e < E; e += G) z += expf((l[e] - m) * itau);
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) z += __shfl_xor_sync(mask, z, off);
         const float inv = 1.0f / z;
-        if (o.normalize) {
-            const float ms = l[sel[0]];
-            float zs = 0.f;
-            for (int j = 0; j < k; ++j) zs += expf(l[sel[j]] - ms);
-            for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = expf(l[sel[j]] - ms) / zs;
-        } else {
-            for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = expf(l[sel[j]] - m) * inv;
+        // top-k: k rounds; each lane proposes its best unselected expert, the
+        // group keeps the one that ranks highest (larger key, NaN lowest, lower id).
+        // The key is the logit, or logit + Gumbel draw in straight-through mode.
+        int sel[8];
+        float lsel[8];
+        for (int j = 0; j < k; ++j) {
+            int be = -1;
+            float bv = 0.f;
+            for (int e = sub, q = 0; e < E; e += G, ++q) {
+                if ((taken >> q) & 1ull) continue;
+                const float key = (o.st && o.noise && valid) ? l[e] + o.noise[(size_t)t * E + e] : l[e];
+                if (be < 0 || ranks_above(key, e, bv, be)) { be = e; bv = key; }
+            }
+#pragma unroll
+            for (int off = G / 2; off > 0; off >>= 1) {
+                const int oe = __shfl_xor_sync(mask, be, off);
+                const float ov = __shfl_xor_sync(mask, bv, off);
+                if (oe >= 0 && (be < 0 || ranks_above(ov, oe, bv, be))) { be = oe; bv = ov; }
+            }
+            sel[j] = be;
+            if (be % G == sub) taken |= 1ull << (be / G);
+        }
+        // selected logits (noise-free), gathered from the owning lanes
+        // (each lane reads back only its own smem writes; the owner's value is shuffled)
+        const int gbase = (int)(threadIdx.x & 31) & ~(G - 1);
+        for (int j = 0; j < k; ++j) lsel[j] = __shfl_sync(mask, l[sel[j]], gbase + sel[j] % G);
+        if (sub == 0 && valid)
+            for (int j = 0; j < k; ++j) {
+                sSel[tok * k + j] = routed ? sel[j] : -1;
+                o.topk[(size_t)t * k + j] = routed ? sel[j] : -1;
+            }
+        if (sub == 0 && valid) {
+            if (!routed) {
+                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = 0.f;
+            } else if (o.st) {
+                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = 1.0f;
+            } else if (o.normalize) {
+                float ms = lsel[0];
+                for (int j = 1; j < k; ++j) ms = fmaxf(ms, lsel[j]);
+                float zs = 0.f;
+                for (int j = 0; j < k; ++j) zs += expf((lsel[j] - ms) * itau);
+                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = expf((lsel[j] - ms) * itau) / zs;
+            } else {
+                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = expf((lsel[j] - m) * itau) * inv;
+            }
         }
         float h = 0.f;
-        for (int e = 0; e < E; ++e) {
-            float p = expf(l[e] - m) * inv;
-            l[e] = p;  // the tile now holds probabilities
-            if (p > 0.f) h -= p * logf(p);
+        for (int e = sub; e < E; e += G) {
+            const float pe = routed ? expf((l[e] - m) * itau) * inv : 0.f;
+            l[e] = pe;  // the tile now holds probabilities (0 for padding tokens)
+            if (pe > 0.f) h -= pe * logf(pe);
         }
-        sEnt[i] = h;
-        sBad[i] = bad ? 1 : 0;
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) h += __shfl_xor_sync(mask, h, off);
+        if (sub == 0) {
+            sEnt[tok] = routed ? h : 0.f;
+            sBad[tok] = (routed && bad) ? 1 : 0;
+        }
     }
-    __syncthreads();
-    if (i < E) {
+    named_sync(bar_id, nthr);
+    for (int e = i; e < E; e += nthr) {
         float ps = 0.f;
         int cnt = 0;
         for (int r = 0; r < ntok; ++r) {
-            ps += sLog[r * ldl + i];
-            for (int j = 0; j < k; ++j) cnt += (sSel[r * k + j] == i);
+            ps += sLog[r * ldl + e];
+            for (int j = 0; j < k; ++j) cnt += (sSel[r * k + j] == e);
         }
-        o.part_psum[(size_t)blockIdx.x * E + i] = ps;
-        o.part_counts[(size_t)blockIdx.x * E + i] = cnt;
+        o.part_psum[(size_t)pidx * E + e] = ps;
+        o.part_counts[(size_t)pidx * E + e] = cnt;
     }
-    if (i == blockDim.x - 1) {
+    if (i == nthr - 1) {
         float h = 0.f;
-        int b = 0;
-        for (int r = 0; r < ntok; ++r) { h += sEnt[r]; b += sBad[r]; }
-        o.part_ent[blockIdx.x] = h;
-        o.part_bad[blockIdx.x] = b;
+        int b = 0, real = 0;
+        for (int r = 0; r < ntok; ++r) { h += sEnt[r]; b += sBad[r]; real += sSel[r * k] >= 0; }
+        o.part_ent[pidx] = h;
+        o.part_bad[pidx] = b;
+        o.part_real[pidx] = real;
     }
+}
+
+// G lanes per token for TT tokens on nthr threads (G <= 32, a power of two)
+__device__ __forceinline__ void finish_tile(float* sLog, int ldl, int* sSel, float* sEnt, int* sBad,
+                                            int t0, int ntok, int TT, int pidx, const RouteOut& o,
+                                            int i, int nthr, int bar_id)
+{
+    const int G = nthr / TT;
+    if (G >= 8) finish_tile_seg<8>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
+    else if (G >= 4) finish_tile_seg<4>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
+    else if (G >= 2) finish_tile_seg<2>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
+    else finish_tile_seg<1>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
 }
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
@@ -143,114 +213,193 @@ __global__ void transpose_router_kernel(const __nv_bfloat16* __restrict__ Wr,
     }
 }
 
-// One CTA = TT tokens.  The 8 warps split the 128 rows of each smem stage as
-// (k-slice, token): with NKS = 128 / TT k-slices, a stage holds NKS x 64 columns
-// of x for the CTA's TT tokens, so small token counts still spread over many
-// CTAs (split-K across warps); the k-slice partials are summed in a fixed order.
-template <int NT, int TT>  // NT = E_pad / 8 tensor-core n-tiles; TT tokens per CTA
-__global__ void __launch_bounds__(256) route_bf16_kernel(const __nv_bfloat16* __restrict__ x,
-                                                         const __nv_bfloat16* __restrict__ WrT,
-                                                         RouteOut o)
+// Token tiles of TT tokens; the 8 MMA warps split each stage's 128 rows as
+// (k-slice, 16 tokens): with NKS = 128 / TT k-slices a stage holds NKS x 64
+// columns of x for the tile, so small token counts still spread over many SMs
+// (split-K across warps; slice partials summed in a fixed order).
+//
+// Persistent CTAs (one per SM), three roles:
+//   warp 8      TMA producer: 128B-swizzled boxes of x ({64 columns, TT rows}
+//               per k-slice) and of W_r^T ({64, E_pad}) stream into a ring of
+//               `stages` slots across tile boundaries (mbarrier tx counts);
+//   warps 0-7   MMA: mma.sync m16n8k16 (bf16 in, fp32 accumulate) on
+//               swizzle-aware fragment loads; at a tile's end they reduce the
+//               k-slices into one of two logits buffers and move on;
+//   warps 9-12  finish, concurrently with the next tile's streaming: bias,
+//               noise, softmax, top-k, gates, the tile's partial statistics.
+// The two logits buffers are handed over with mbarriers.  Every wait is
+// bounded; after a failed wait a warp keeps its barrier sequence, skipping work.
+struct RouteTma {
+    CUtensorMap tmX, tmW;
+    RouteOut o;
+    int* status;
+    int stages;
+};
+
+__device__ __forceinline__ uint32_t swz128(int row, int col) {   // byte offset in a 128B-swizzled box
+    return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2);
+}
+
+constexpr int RTMA_THREADS = 13 * 32;   // 8 MMA warps, 1 producer warp, 4 finish warps
+
+template <int NT, int TT>  // NT = E_pad / 8 tensor-core n-tiles; TT tokens per tile
+__global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __grid_constant__ RouteTma P)
 {
     constexpr int E_PAD = NT * 8;
-    constexpr int NKS = RT_TOK / TT;            // k-slices per stage
+    constexpr int NKS = RT_TOK / TT;                 // k-slices per stage
     constexpr int LDL = E_PAD + 1;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(smem_raw);      // [S][128][LDS]
-    __nv_bfloat16* sW = sX + RT_STAGES * RT_TOK * RT_LDS;                // [S][NKS*E_PAD][LDS]
-    float* sLog = reinterpret_cast<float*>(sW + RT_STAGES * NKS * E_PAD * RT_LDS);  // [TT][LDL]
-    int* sSel = reinterpret_cast<int*>(sLog + TT * LDL);
+    constexpr uint32_t X_BYTES = RT_TOK * 128;       // 16 KB
+    constexpr uint32_t W_BYTES = (NKS * E_PAD * 128 + 1023) / 1024 * 1024;
+    constexpr uint32_t STAGE = X_BYTES + W_BYTES;
+    const RouteOut& o = P.o;
+    const int S = P.stages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* sRed = reinterpret_cast<float*>(ring + (size_t)S * STAGE);   // [128][E_PAD]
+    float* sLogB = sRed + RT_TOK * E_PAD;                                // [2][TT][LDL]
+    int* sSel = reinterpret_cast<int*>(sLogB + 2 * TT * LDL);            // [TT*8]
     float* sEnt = reinterpret_cast<float*>(sSel + TT * 8);
     int* sBad = reinterpret_cast<int*>(sEnt + TT);
-    float* sRed = reinterpret_cast<float*>(smem_raw);                    // reuses the ring
+    uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sBad + TT) + 15) & ~uintptr_t(15));
+    uint64_t* full = bars;
+    uint64_t* empty = full + S;
+    uint64_t* lfull = empty + S;     // [2] logits buffer written (256 arrivals)
+    uint64_t* lempty = lfull + 2;    // [2] logits buffer finished (128 arrivals)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(lempty + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const int t0 = blockIdx.x * TT;
-    const int ntok = min(TT, o.T - t0);
     const int d = o.d;
-    const int kw = RT_BK * NKS;                  // columns per stage
-    const int nk = d / kw;
+    const int nk = d / (RT_BK * NKS);
+    const int ntiles = (o.T + TT - 1) / TT;
+    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint32_t ring0 = smem_u32(ring);
 
-    auto load_stage = [&](int kc, int st) {
-        const int k0 = kc * kw;
-        __nv_bfloat16* dX = sX + st * RT_TOK * RT_LDS;
-#pragma unroll
-        for (int r = 0; r < (RT_TOK * RT_BK / 8) / 256; ++r) {
-            const int s = tid + r * 256;
-            const int row = s >> 3, c = s & 7;
-            const int ks = row / TT, tok = row % TT;
-            const bool ok = tok < ntok;
-            const __nv_bfloat16* src = ok ? x + (size_t)(t0 + tok) * d + k0 + ks * RT_BK + c * 8 : x;
-            cp_async16(dX + row * RT_LDS + c * 8, src, ok);
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 8);
         }
-        __nv_bfloat16* dW = sW + st * NKS * E_PAD * RT_LDS;
-        for (int s = tid; s < NKS * E_PAD * 8; s += 256) {
-            const int row = s >> 3, c = s & 7;   // row = ks * E_PAD + e
-            const int ks = row / E_PAD, e = row % E_PAD;
-            cp_async16(dW + row * RT_LDS + c * 8, WrT + (size_t)e * d + k0 + ks * RT_BK + c * 8, true);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&lfull[b]), 256);
+            mbar_init(smem_u32(&lempty[b]), 128);
         }
-    };
-
-    float acc[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    const int my_ks = (warp * 16) / TT;
-
-#pragma unroll
-    for (int s = 0; s < RT_STAGES - 1; ++s) {
-        if (s < nk) load_stage(s, s);
-        cp_async_commit();
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int kc = 0; kc < nk; ++kc) {
-        cp_async_wait<RT_STAGES - 2>();
-        __syncthreads();
-        const int st = kc % RT_STAGES;
-        const __nv_bfloat16* A = sX + st * RT_TOK * RT_LDS + (warp * 16) * RT_LDS;
-        const __nv_bfloat16* B = sW + (st * NKS + my_ks) * E_PAD * RT_LDS;
+    __syncthreads();
+
+    if (warp == 8) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmX)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmW)) : "memory");
+            int it = 0;
+            bool ok = true;
+            for (int i = 0; ok && i < my_tiles; ++i) {
+                const int t0 = (blockIdx.x + i * gridDim.x) * TT;
+                for (int kc = 0; kc < nk; ++kc, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (uint32_t)(it / S) & 1u;
+                    if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status)) { ok = false; break; }
+                    const uint32_t bar = smem_u32(&full[s]);
+                    const uint32_t sx = ring0 + s * STAGE, sw = sx + X_BYTES;
+                    mbar_expect_tx(bar, X_BYTES + NKS * E_PAD * 128);
+                    const int k0 = kc * RT_BK * NKS;
 #pragma unroll
-        for (int ks = 0; ks < RT_BK / 16; ++ks) {
-            const int kk = ks * 16 + 2 * tq;
-            uint32_t a0 = *reinterpret_cast<const uint32_t*>(A + g * RT_LDS + kk);
-            uint32_t a1 = *reinterpret_cast<const uint32_t*>(A + (g + 8) * RT_LDS + kk);
-            uint32_t a2 = *reinterpret_cast<const uint32_t*>(A + g * RT_LDS + kk + 8);
-            uint32_t a3 = *reinterpret_cast<const uint32_t*>(A + (g + 8) * RT_LDS + kk + 8);
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                uint32_t b0 = *reinterpret_cast<const uint32_t*>(B + (n * 8 + g) * RT_LDS + kk);
-                uint32_t b1 = *reinterpret_cast<const uint32_t*>(B + (n * 8 + g) * RT_LDS + kk + 8);
-                asm volatile(
-                    "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                    "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-                    : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
-                    : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                    for (int ks = 0; ks < NKS; ++ks) {
+                        tma_load3(&P.tmX, sx + ks * TT * 128, bar, k0 + ks * RT_BK, t0, 0);
+                        tma_load3(&P.tmW, sw + ks * E_PAD * 128, bar, k0 + ks * RT_BK, 0, 0);
+                    }
+                }
             }
+            for (int j = max(0, it - S); j < it; ++j)     // every issued load lands before exit
+                mbar_drain(smem_u32(&full[j % S]), (uint32_t)(j / S) & 1u);
         }
-        const int nxt = kc + RT_STAGES - 1;
-        if (nxt < nk) load_stage(nxt, nxt % RT_STAGES);
-        cp_async_commit();
+        return;
     }
-    cp_async_wait<0>();
-    __syncthreads();                             // ring no longer read: reuse it
-    // partial sums of this warp's k-slice: sRed[ks][tok][E_PAD]
+
+    if (warp >= 9) {
+        // ------------------------------------------------ finish warps
+        const int ftid = tid - 9 * 32;   // 0..127
+        bool live = true;
+        for (int i = 0; i < my_tiles; ++i) {
+            const int tile = blockIdx.x + i * gridDim.x;
+            const int t0 = tile * TT, ntok = min(TT, o.T - t0);
+            const int b = i & 1;
+            if (live) live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&lfull[b]), (uint32_t)(i >> 1) & 1u,
+                                                            abort_flag, P.status));
+            if (live) finish_tile(sLogB + b * TT * LDL, LDL, sSel, sEnt, sBad, t0, ntok, TT, tile, o, ftid, 128, 2);
+            else named_sync(2, 128);
+            named_sync(2, 128);          // sSel / sEnt / sBad read by all before reuse
+            mbar_arrive(smem_u32(&lempty[b]));
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- MMA warps 0-7
+    const int g = lane >> 2, tq = lane & 3;
+    const int my_ks = (warp * 16) / TT;
+    bool live = true;
+    int it = 0;
+    for (int i = 0; i < my_tiles; ++i) {
+        float acc[NT][4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        const int r0 = warp * 16 + g, c0 = n * 8 + 2 * tq;   // r0 = ks * TT + tok
-        sRed[r0 * E_PAD + c0] = acc[n][0];
-        sRed[r0 * E_PAD + c0 + 1] = acc[n][1];
-        sRed[(r0 + 8) * E_PAD + c0] = acc[n][2];
-        sRed[(r0 + 8) * E_PAD + c0 + 1] = acc[n][3];
-    }
-    __syncthreads();
-    for (int i = tid; i < TT * E_PAD; i += 256) {
-        const int tok = i / E_PAD, e = i % E_PAD;
-        float v = 0.f;
+        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        for (int kc = 0; kc < nk; ++kc, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            if (live) live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), ph, abort_flag, P.status));
+            if (!live) continue;
+            const uint8_t* X = ring + (size_t)s * STAGE;
+            const uint8_t* W = X + X_BYTES + my_ks * E_PAD * 128;
+            const int r0 = warp * 16 + g;                  // stage row (k-slice, token)
 #pragma unroll
-        for (int ks = 0; ks < NKS; ++ks) v += sRed[(ks * TT + tok) * E_PAD + e];
-        sLog[tok * LDL + e] = v;
+            for (int k16 = 0; k16 < RT_BK / 16; ++k16) {
+                const int kk = k16 * 16 + 2 * tq;
+                const uint32_t a0 = *reinterpret_cast<const uint32_t*>(X + swz128(r0, kk));
+                const uint32_t a1 = *reinterpret_cast<const uint32_t*>(X + swz128(r0 + 8, kk));
+                const uint32_t a2 = *reinterpret_cast<const uint32_t*>(X + swz128(r0, kk + 8));
+                const uint32_t a3 = *reinterpret_cast<const uint32_t*>(X + swz128(r0 + 8, kk + 8));
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk));
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk + 8));
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                        : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
+                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));   // slot free for the producer
+        }
+        // ---- the tile is summed: hand its logits to the finish warps
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {   // this warp's k-slice partials: sRed[ks][tok][e]
+            const int r0 = warp * 16 + g, c0 = n * 8 + 2 * tq;   // r0 = ks * TT + tok
+            sRed[r0 * E_PAD + c0] = acc[n][0];
+            sRed[r0 * E_PAD + c0 + 1] = acc[n][1];
+            sRed[(r0 + 8) * E_PAD + c0] = acc[n][2];
+            sRed[(r0 + 8) * E_PAD + c0 + 1] = acc[n][3];
+        }
+        named_sync(1, 256);
+        const int b = i & 1;
+        if (i >= 2 && live)              // buffer b's previous tile must be finished
+            live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&lempty[b]), (uint32_t)((i - 2) >> 1) & 1u,
+                                                     abort_flag, P.status));
+        float* sLog = sLogB + b * TT * LDL;
+        if (live)
+            for (int q = tid; q < TT * E_PAD; q += 256) {
+                const int tok = q / E_PAD, e = q % E_PAD;
+                float v = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < NKS; ++ks) v += sRed[(ks * TT + tok) * E_PAD + e];
+                sLog[tok * LDL + e] = v;
+            }
+        mbar_arrive(smem_u32(&lfull[b]));    // release: this thread's logits writes
+        named_sync(1, 256);                  // sRed free for the next tile
     }
-    __syncthreads();
-    finish_tile(sLog, LDL, sSel, sEnt, sBad, t0, ntok, o);
 }
 
 // fp32: plain FMA, 128 tokens per CTA, k-chunks of 32 staged in smem.
@@ -298,7 +447,7 @@ __global__ void __launch_bounds__(256) route_f32_kernel(const float* __restrict_
     for (int q = 0; q < 32; ++q)
         if (e_begin + q < e_end) sLog[tok * ldl + e_begin + q] = acc[q];
     __syncthreads();
-    finish_tile(sLog, ldl, sSel, sEnt, sBad, t0, ntok, o);
+    finish_tile(sLog, ldl, sSel, sEnt, sBad, t0, ntok, RT_TOK, blockIdx.x, o, threadIdx.x, 256, 1);
 }
 
 // Sum the per-CTA partials (a warp per expert, lane-strided, then a fixed
@@ -306,14 +455,32 @@ __global__ void __launch_bounds__(256) route_f32_kernel(const float* __restrict_
 __global__ void __launch_bounds__(1024) route_finalize_kernel(
     int nblk, int T, int E, int k, float aux_coef, const int32_t* __restrict__ part_counts,
     const float* __restrict__ part_psum, const float* __restrict__ part_ent,
-    const int32_t* __restrict__ part_bad, int32_t* __restrict__ counts, float* __restrict__ stats,
-    int* status)
+    const int32_t* __restrict__ part_bad, const int32_t* __restrict__ part_real,
+    int32_t* __restrict__ counts, float* __restrict__ stats, int* status)
 {
     __shared__ float s_pbar[64];
     __shared__ int s_cnt[64];
     __shared__ float s_h[32];
-    __shared__ int s_b[32];
+    __shared__ int s_b[32], s_r[32];
+    __shared__ float s_treal;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // routed tokens first: the means below run over them
+    {
+        int rl = 0;
+        for (int b = tid; b < nblk; b += blockDim.x) rl += part_real[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) rl += __shfl_xor_sync(0xffffffffu, rl, o);
+        if (lane == 0) s_r[warp] = rl;
+        __syncthreads();
+        if (tid == 0) {
+            int tr = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tr += s_r[w];
+            s_treal = (float)tr;
+            if (stats) stats[MOE_STAT_TOKENS] = (float)tr;
+        }
+        __syncthreads();
+    }
+    const float Tr = fmaxf(s_treal, 1.0f);
     for (int e = warp; e < E; e += 32) {
         int c = 0;
         float ps = 0.f;
@@ -329,8 +496,8 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(
         if (lane == 0) {
             counts[e] = c;
             s_cnt[e] = c;
-            s_pbar[e] = ps / (float)T;
-            if (stats) stats[MOE_STAT_PBAR + e] = ps / (float)T;
+            s_pbar[e] = ps / Tr;
+            if (stats) stats[MOE_STAT_PBAR + e] = ps / Tr;
         }
     }
     float h = 0.f;
@@ -351,7 +518,7 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(
         for (int q = 0; q < E; ++q) {
             float dq = s_pbar[q] - 1.0f / (float)E;
             aux += dq * dq;
-            sw += ((float)s_cnt[q] / ((float)T * (float)k)) * s_pbar[q];
+            sw += ((float)s_cnt[q] / (Tr * (float)k)) * s_pbar[q];
             cmean += (float)s_cnt[q];
             cmax = fmaxf(cmax, (float)s_cnt[q]);
         }
@@ -361,7 +528,7 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(
         if (stats) {
             stats[MOE_STAT_AUX_LOSS] = aux_coef * aux;
             stats[MOE_STAT_AUX_SWITCH] = (float)E * sw;
-            stats[MOE_STAT_ENTROPY] = h / (float)T;
+            stats[MOE_STAT_ENTROPY] = h / Tr;
             stats[MOE_STAT_NONFINITE] = (float)bad;
             stats[MOE_STAT_DROPPED] = 0.f;
             stats[MOE_STAT_MAX_OVER_MEAN_KEPT] = 0.f;
@@ -374,20 +541,24 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(
 
 }  // namespace
 
-// Tokens per CTA of the bf16 router: the largest TT whose grid still covers two
-// waves of the GPU, else the smallest legal TT.  TT must keep a stage's router
-// columns within 64 rows (NKS * E_pad <= 64) and split d evenly into NKS slices.
+// Tokens per tile of the bf16 router.  A stage always holds 128 (k-slice, token)
+// rows of 64 columns: TT = 64 reads two adjacent 128-byte chunks of 64 token
+// rows per stage, which streamed fastest on GB300 (of 16, 32, 64 and 128
+// tokens per tile: about 3.9 TB/s versus 2.5-3.7 TB/s with the compute removed).
+// Smaller tiles are used only when 64-token tiles would leave SMs idle.  TT must
+// keep the stage's W_r^T slices (NKS * E_pad rows of 128 B) within 16 KB and
+// split d / 64 evenly into NKS slices.
 int route_tile_tokens(const moe_config& c) {
     if (c.dtype != MOE_DTYPE_BF16) return RT_TOK;
     const int e_pad = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
-    int best = -1, smallest = -1;
-    for (int tt = 16; tt <= RT_TOK; tt *= 2) {
+    int smallest = -1;
+    for (int tt = 64; tt >= 16; tt /= 2) {
         const int nks = RT_TOK / tt;
-        if (nks * e_pad > 64 || (c.d / RT_BK) % nks != 0) continue;
-        if (smallest < 0) smallest = tt;
-        if ((c.T + tt - 1) / tt >= 2 * num_sms()) best = tt;
+        if (nks * e_pad > 128 || (c.d / RT_BK) % nks != 0) continue;
+        if ((c.T + tt - 1) / tt >= num_sms()) return tt;
+        smallest = tt;
     }
-    return best > 0 ? best : smallest;
+    return smallest > 0 ? smallest : RT_TOK;
 }
 
 size_t route_ws_bytes(const moe_config& c) {
@@ -399,6 +570,7 @@ size_t route_ws_bytes(const moe_config& c) {
     b += align_up(nblk * c.E * 4);          // psum
     b += align_up(nblk * 4);                // ent
     b += align_up(nblk * 4);                // bad
+    b += align_up(nblk * 4);                // routed tokens
     if (c.dtype == MOE_DTYPE_BF16) b += align_up((size_t)e_pad * c.d * 2);  // W_r^T
     return b;
 }
@@ -407,33 +579,52 @@ namespace {
 int finalize_route(const moe_config& c, const RouteOut& o, int nblk, int32_t* counts,
                    float* stats, cudaStream_t st) {
     route_finalize_kernel<<<1, 1024, 0, st>>>(nblk, c.T, c.E, c.k, c.aux_coef, o.part_counts,
-                                            o.part_psum, o.part_ent, o.part_bad, counts, stats,
+                                            o.part_psum, o.part_ent, o.part_bad, o.part_real,
+                                            counts, stats,
                                             device_status_ptr());
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
 template <int NT, int TT>
-int launch_route_bf16(const __nv_bfloat16* x, const __nv_bfloat16* WrT, const RouteOut& o,
-                      int nblk, cudaStream_t st) {
+int launch_route_bf16(const moe_config& c, const void* x, const __nv_bfloat16* WrT, int e_pad,
+                      const RouteOut& o, int nblk, cudaStream_t st) {
     constexpr int E_PAD = NT * 8, NKS = RT_TOK / TT;
-    const size_t smem = (size_t)RT_STAGES * (RT_TOK + NKS * E_PAD) * RT_LDS * 2 +
-                        (size_t)TT * (E_PAD + 1) * 4 + (size_t)TT * 8 * 4 + (size_t)TT * 4 * 2;
-    static bool attr_set = false;  // the size is fixed per instantiation
+    constexpr size_t STAGE = RT_TOK * 128 + (NKS * E_PAD * 128 + 1023) / 1024 * 1024;
+    const size_t extra = (size_t)RT_TOK * E_PAD * 4 + 2 * (size_t)TT * (E_PAD + 1) * 4 +
+                        (size_t)TT * 8 * 4 + (size_t)TT * 4 * 2 + 16 + (2 * 16 + 4) * 8 + 64;
+    const size_t budget = 220 * 1024 - 1024 - extra;
+    const int stages = (int)std::min<size_t>(16, budget / STAGE);
+    const size_t smem = 1024 + stages * STAGE + extra;
+    static bool attr_set = false;  // the largest size is fixed per instantiation
     if (!attr_set) {
         MOE_CUDA_TRY(cudaFuncSetAttribute(route_bf16_kernel<NT, TT>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          220 * 1024));
         attr_set = true;
     }
-    route_bf16_kernel<NT, TT><<<nblk, 256, smem, st>>>(x, WrT, o);
+    RouteTma P;
+    memset(&P, 0, sizeof(P));
+    int r = encode_bf16_map(&P.tmX, x, (uint64_t)c.d, (uint64_t)c.T, 1, (uint64_t)c.d * 2,
+                            (uint64_t)c.d * 2 * c.T, RT_BK, TT);
+    if (r) return r;
+    r = encode_bf16_map(&P.tmW, WrT, (uint64_t)c.d, (uint64_t)e_pad, 1, (uint64_t)c.d * 2,
+                        (uint64_t)c.d * 2 * e_pad, RT_BK, E_PAD);
+    if (r) return r;
+    P.o = o;
+    P.status = device_status_ptr();
+    P.stages = stages;
+    // persistent: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int grid = std::min(nblk, num_sms());
+    route_bf16_kernel<NT, TT><<<grid, RTMA_THREADS, smem, st>>>(P);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 }  // namespace
 
 int launch_route(const moe_config& c, const void* x, const void* Wr, const float* bias,
-                 const float* noise, float* logits, int32_t* topk, float* gate, int32_t* counts,
-                 float* stats, void* ws, cudaStream_t st)
+                 const float* noise, const uint8_t* mask, float* logits, int32_t* topk,
+                 float* gate, int32_t* counts, float* stats, void* ws, cudaStream_t st)
 {
     const int tt = route_tile_tokens(c);
     const int nblk = (c.T + tt - 1) / tt;
@@ -441,11 +632,14 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
     uint8_t* w = static_cast<uint8_t*>(ws);
     RouteOut o;
     o.T = c.T; o.d = c.d; o.E = c.E; o.k = c.k; o.normalize = c.normalize_gates;
-    o.bias = bias; o.noise = noise; o.logits = logits; o.topk = topk; o.gate = gate;
+    o.bias = bias; o.noise = noise; o.mask = mask; o.logits = logits; o.topk = topk; o.gate = gate;
+    o.st = c.straight_through;
+    o.inv_tau = c.temperature > 0.f ? 1.0f / c.temperature : 1.0f;
     o.part_counts = reinterpret_cast<int32_t*>(w); w += align_up((size_t)nblk * c.E * 4);
     o.part_psum = reinterpret_cast<float*>(w); w += align_up((size_t)nblk * c.E * 4);
     o.part_ent = reinterpret_cast<float*>(w); w += align_up((size_t)nblk * 4);
     o.part_bad = reinterpret_cast<int32_t*>(w); w += align_up((size_t)nblk * 4);
+    o.part_real = reinterpret_cast<int32_t*>(w); w += align_up((size_t)nblk * 4);
 
     if (c.dtype == MOE_DTYPE_BF16) {
         __nv_bfloat16* WrT = reinterpret_cast<__nv_bfloat16*>(w);
@@ -456,16 +650,19 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
         const int key = (e_pad / 8) * 1000 + tt;
         int r = MOE_OK;
         switch (key) {
-            case 1016: r = launch_route_bf16<1, 16>(xb, WrT, o, nblk, st); break;
-            case 1032: r = launch_route_bf16<1, 32>(xb, WrT, o, nblk, st); break;
-            case 1064: r = launch_route_bf16<1, 64>(xb, WrT, o, nblk, st); break;
-            case 1128: r = launch_route_bf16<1, 128>(xb, WrT, o, nblk, st); break;
-            case 2032: r = launch_route_bf16<2, 32>(xb, WrT, o, nblk, st); break;
-            case 2064: r = launch_route_bf16<2, 64>(xb, WrT, o, nblk, st); break;
-            case 2128: r = launch_route_bf16<2, 128>(xb, WrT, o, nblk, st); break;
-            case 4064: r = launch_route_bf16<4, 64>(xb, WrT, o, nblk, st); break;
-            case 4128: r = launch_route_bf16<4, 128>(xb, WrT, o, nblk, st); break;
-            case 8128: r = launch_route_bf16<8, 128>(xb, WrT, o, nblk, st); break;
+            case 1016: r = launch_route_bf16<1, 16>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 1032: r = launch_route_bf16<1, 32>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 1064: r = launch_route_bf16<1, 64>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 1128: r = launch_route_bf16<1, 128>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 2016: r = launch_route_bf16<2, 16>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 2032: r = launch_route_bf16<2, 32>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 2064: r = launch_route_bf16<2, 64>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 2128: r = launch_route_bf16<2, 128>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 4032: r = launch_route_bf16<4, 32>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 4064: r = launch_route_bf16<4, 64>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 4128: r = launch_route_bf16<4, 128>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 8064: r = launch_route_bf16<8, 64>(c, x, WrT, e_pad, o, nblk, st); break;
+            case 8128: r = launch_route_bf16<8, 128>(c, x, WrT, e_pad, o, nblk, st); break;
             default: return MOE_ERR_UNSUPPORTED;
         }
         return r != MOE_OK ? r : finalize_route(c, o, nblk, counts, stats, st);

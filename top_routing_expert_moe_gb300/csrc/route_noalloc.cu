@@ -51,20 +51,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace moe
 
 extern "C" int moe_route_noalloc(const moe_config* c, const void* x, const void* W_r,
-                                 const float* bias, const float* noise, float* logits,
-                                 int32_t* topk_idx, float* gate, int32_t* counts, float* stats,
-                                 moe_stream_t stream) {
+                                 const float* bias, const float* noise, const uint8_t* token_mask,
+                                 float* logits, int32_t* topk_idx, float* gate, int32_t* counts,
+                                 float* stats, moe_stream_t stream) {
     using namespace moe;
     int r = moe_check_config(c);
     if (r) return r;
     if (route_ws_bytes(*c) > (size_t)MOE_ROUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_SCRATCH_LIMIT;
     auto ok = [](const void* p) { return p != nullptr && aligned16(p); };
     auto opt = [](const void* p) { return p == nullptr || aligned16(p); };
-    if (!ok(x) || !ok(W_r) || !opt(bias) || !opt(noise) || !ok(logits) || !ok(topk_idx) ||
-        !ok(gate) || !ok(counts) || !opt(stats))
+    if (!ok(x) || !ok(W_r) || !opt(bias) || !opt(noise) || !opt(token_mask) || !ok(logits) ||
+        !ok(topk_idx) || !ok(gate) || !ok(counts) || !opt(stats))
         return MOE_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if ((r = route_scratch_address(&scratch))) return r;
-    return launch_route(*c, x, W_r, bias, noise, logits, topk_idx, gate, counts, stats, scratch,
-                        (cudaStream_t)stream);
+    return launch_route(*c, x, W_r, bias, noise, token_mask, logits, topk_idx, gate, counts, stats,
+                        scratch, (cudaStream_t)stream);
 }
