@@ -46,7 +46,7 @@ class _Cfg(ctypes.Structure):
                 ("capacity_factor", ctypes.c_double), ("swiglu", ctypes.c_int),
                 ("normalize_gates", ctypes.c_int), ("aux_coef", ctypes.c_double),
                 ("pad_m", ctypes.c_int), ("temperature", ctypes.c_double),
-                ("straight_through", ctypes.c_int)]
+                ("straight_through", ctypes.c_int), ("f_shared", ctypes.c_int)]
 
 
 @dataclass
@@ -63,11 +63,13 @@ class OracleConfig:
     pad_m: int = 1
     temperature: float = 1.0       # softmax temperature tau; pass the fp32 value the GPU sees
     straight_through: bool = False  # Gumbel top-k: select on logits + noise, gates 1
+    f_shared: int = 0              # hidden width of the shared experts' FFN (0: none)
 
     def c(self) -> _Cfg:
         return _Cfg(self.T, self.d, self.f, self.E, self.k, float(self.capacity_factor),
                     int(self.swiglu), int(self.normalize_gates), float(self.aux_coef),
-                    int(self.pad_m), float(self.temperature), int(self.straight_through))
+                    int(self.pad_m), float(self.temperature), int(self.straight_through),
+                    int(self.f_shared))
 
 
 _lib = None
@@ -82,7 +84,7 @@ def lib():
         _lib.oracle_route.restype = ctypes.c_int
         for name in ("oracle_router_logits", "oracle_permute", "oracle_combine", "oracle_stats",
                      "oracle_forward", "oracle_backward", "oracle_expert_apply",
-                     "oracle_expert_forward"):
+                     "oracle_expert_forward", "oracle_shared_forward", "oracle_shared_add"):
             getattr(_lib, name).restype = None
     return _lib
 
@@ -170,8 +172,31 @@ def expert_forward(cfg, e, x_row, Wup, Wdown, Wgate=None):
     return dict(h=h, u=u, act=act, y=y)
 
 
-def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in=None, mask=None):
-    """Steps 1-9. ``logits_in`` (e.g. the GPU's fp32 logits) replaces step 1."""
+def shared_forward(cfg, x_row, Wup_s, Wdown_s, Wgate_s=None):
+    """The shared experts' FFN on one token: dict(h, u, act, y) (width f_shared)."""
+    fs, d = cfg.f_shared, cfg.d
+    h, act, y = np.empty(fs), np.empty(fs), np.empty(d)
+    u = np.empty(fs) if cfg.swiglu else None
+    lib().oracle_shared_forward(ctypes.byref(cfg.c()), _p(_d(x_row)), _p(_d(Wup_s)),
+                                _p(_d(Wgate_s) if cfg.swiglu else None), _p(_d(Wdown_s)), _p(h),
+                                _p(u), _p(act), _p(y))
+    return dict(h=h, u=u, act=act, y=y)
+
+
+def _shared_args(cfg, Wup_s, Wgate_s, Wdown_s):
+    if cfg.f_shared <= 0:
+        return None, None, None
+    if Wup_s is None or Wdown_s is None or (cfg.swiglu and Wgate_s is None):
+        raise ValueError("f_shared > 0 needs the shared experts' weights")
+    return _d(Wup_s), _d(Wgate_s) if cfg.swiglu else None, _d(Wdown_s)
+
+
+def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in=None, mask=None,
+            Wup_s=None, Wdown_s=None, Wgate_s=None):
+    """Steps 1-9. ``logits_in`` (e.g. the GPU's fp32 logits) replaces step 1.
+    With ``cfg.f_shared > 0`` the shared experts' FFN (weights ``*_s``) joins
+    every token's output with weight 1."""
+    Wus, Wgs, Wds = _shared_args(cfg, Wup_s, Wgate_s, Wdown_s)
     x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
     bias, noise, logits_in, mask = _d(bias), _d(noise), _d(logits_in), _mask(mask)
     T, E, k, d = cfg.T, cfg.E, cfg.k, cfg.d
@@ -182,15 +207,19 @@ def forward(cfg, x, Wr, Wup, Wdown, Wgate=None, bias=None, noise=None, logits_in
     lib().oracle_forward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(bias), _p(noise), _p(mask), _p(Wup),
                          _p(Wgate), _p(Wdown), _p(logits_in),
                          *[_p(r[n]) for n in ("logits", "probs", "topk_idx", "gate", "counts", "kept",
-                                               "offsets", "perm_token", "slot_of", "out", "stats")])
+                                               "offsets", "perm_token", "slot_of", "out", "stats")],
+                         _p(Wus), _p(Wgs), _p(Wds))
     r["perm_token"] = r["perm_token"][: r["offsets"][-1]].copy()
     return r
 
 
 def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgate=None,
-             with_bias=False, per_slot=False, pbar=None, T_aux=0):
+             with_bias=False, per_slot=False, pbar=None, T_aux=0, Wup_s=None, Wdown_s=None,
+             Wgate_s=None):
     """Step 10: gradients of <dout, out> + aux loss (written, not accumulated).
-    For a sample of a larger batch pass that batch's ``pbar`` and ``T_aux``."""
+    For a sample of a larger batch pass that batch's ``pbar`` and ``T_aux``.
+    With shared experts the result also holds dWup_s, dWgate_s, dWdown_s."""
+    Wus, Wgs, Wds = _shared_args(cfg, Wup_s, Wgate_s, Wdown_s)
     x, Wr, Wup, Wdown, Wgate = _d(x), _d(Wr), _d(Wup), _d(Wdown), _d(Wgate)
     logits, gate, dout = _d(logits), _d(gate), _d(dout)
     topk_idx = np.ascontiguousarray(topk_idx, np.int32)
@@ -201,9 +230,15 @@ def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgat
              dWdown=np.empty((E, f, d)), dgate=np.empty((T, k)), dlogits=np.empty((T, E)),
              dh_slot=np.empty((T, k, 2 if cfg.swiglu else 1, f)) if per_slot else None,
              dxp_slot=np.empty((T, k, d)) if per_slot else None)
+    fs = cfg.f_shared
+    if fs > 0:
+        g.update(dWup_s=np.empty((d, fs)), dWgate_s=np.empty((d, fs)) if cfg.swiglu else None,
+                 dWdown_s=np.empty((fs, d)))
     lib().oracle_backward(ctypes.byref(cfg.c()), _p(x), _p(Wr), _p(Wup), _p(Wgate), _p(Wdown),
                           _p(logits), _p(topk_idx), _p(gate), _p(slot_of), _p(dout),
                           *[_p(g[n]) for n in ("dx", "dWr", "db", "dWup", "dWgate", "dWdown",
                                                "dgate", "dlogits", "dh_slot", "dxp_slot")],
-                          _p(_d(pbar)), ctypes.c_int(int(T_aux)))
+                          _p(_d(pbar)), ctypes.c_int(int(T_aux)),
+                          _p(Wus), _p(Wgs), _p(Wds),
+                          *[_p(g.get(n)) for n in ("dWup_s", "dWgate_s", "dWdown_s")])
     return g

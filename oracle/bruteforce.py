@@ -38,9 +38,10 @@ def topk_by_sort(logits, k):
 
 def forward(x, Wr, Wup, Wdown, k, capacity_factor=0.0, Wgate=None, bias=None, noise=None,
             normalize_gates=True, logits=None, temperature=1.0, straight_through=False,
-            mask=None):
+            mask=None, shared=None):
     """Returns (out, topk_idx, gate, kept_mask[T,k]).  Masked tokens (mask 0)
-    are routed nowhere: topk -1, gates 0."""
+    are routed nowhere: topk -1, gates 0.  ``shared`` = (Wup_s, Wdown_s, Wgate_s
+    or None): a dense FFN that every token also passes through, weight 1."""
     x = np.asarray(x, np.float64)
     T, d = x.shape
     E = Wr.shape[1]
@@ -92,4 +93,8 @@ def forward(x, Wr, Wup, Wdown, k, capacity_factor=0.0, Wgate=None, bias=None, no
             a = _silu(xe @ np.asarray(Wgate[e], np.float64)) * (xe @ np.asarray(Wup[e], np.float64))
         ye = a @ np.asarray(Wdown[e], np.float64)
         np.add.at(out, tok, gate[tok, slot][:, None] * ye)
+    if shared is not None:
+        Wus, Wds, Wgs = (None if a is None else np.asarray(a, np.float64) for a in shared)
+        a = _silu(x @ Wus) if Wgs is None else _silu(x @ Wgs) * (x @ Wus)
+        out = out + a @ Wds
     return out, topk, gate, kept

@@ -44,6 +44,7 @@ typedef struct {
     double temperature;     /* softmax temperature tau (<= 0 means 1) */
     int straight_through;   /* 1: select on logits + noise, gates 1, gradient through
                                softmax(logits / tau) (Gumbel top-k, straight-through) */
+    int f_shared;           /* hidden width of the shared experts' FFN (0: none) */
 } oracle_cfg;
 
 static double tau_of(const oracle_cfg* c) { return c->temperature > 0.0 ? c->temperature : 1.0; }
@@ -216,11 +217,11 @@ void oracle_permute(const oracle_cfg* c, const int* topk, int* kept, int* offset
  * SwiGLU   : g = Wg^T x, u = Wu^T x, a = silu(g) * u, y = Wd^T a
  * Wu, Wg point at expert e's [d,f] block, Wd at its [f,d] block.
  * h_out receives h (SiLU) or g (SwiGLU); u_out receives u (SwiGLU only).    */
-static void expert_ffn(const oracle_cfg* c, const double* x, const double* Wu,
+static void expert_ffn(const oracle_cfg* c, int f, const double* x, const double* Wu,
                        const double* Wg, const double* Wd, double* h_out,
                        double* u_out, double* a_out, double* y)
 {
-    const int d = c->d, f = c->f;
+    const int d = c->d;
     for (int j = 0; j < f; ++j) { h_out[j] = 0.0; if (c->swiglu) u_out[j] = 0.0; }
     for (int i = 0; i < d; ++i) {
         const double xi = x[i];
@@ -250,7 +251,8 @@ void oracle_expert_forward(const oracle_cfg* c, int e, const double* x, const do
     const size_t df = (size_t)c->d * c->f;
     double* tmp = NULL;
     if (c->swiglu && !u) u = tmp = (double*)malloc(sizeof(double) * (size_t)c->f);
-    expert_ffn(c, x, Wup + e * df, c->swiglu ? Wgate + e * df : NULL, Wdown + e * df, h, u, act, y);
+    expert_ffn(c, c->f, x, Wup + e * df, c->swiglu ? Wgate + e * df : NULL, Wdown + e * df, h, u,
+               act, y);
     free(tmp);
 }
 
@@ -260,7 +262,7 @@ void oracle_expert_apply(const oracle_cfg* c, int e, const double* x, const doub
 {
     const size_t df = (size_t)c->d * c->f;
     double* h = (double*)malloc(sizeof(double) * 3 * (size_t)c->f);
-    expert_ffn(c, x, Wup + e * df, c->swiglu ? Wgate + e * df : NULL, Wdown + e * df,
+    expert_ffn(c, c->f, x, Wup + e * df, c->swiglu ? Wgate + e * df : NULL, Wdown + e * df,
                h, h + c->f, h + 2 * (size_t)c->f, y);
     free(h);
 }
@@ -285,11 +287,47 @@ void oracle_combine(const oracle_cfg* c, const double* x, const int* topk,
             for (int j = 0; j < k; ++j) {
                 if (slot_of[(size_t)t * k + j] < 0) continue;
                 int e = topk[(size_t)t * k + j];
-                expert_ffn(c, x + (size_t)t * d, Wup + e * df, c->swiglu ? Wgate + e * df : NULL,
+                expert_ffn(c, f, x + (size_t)t * d, Wup + e * df, c->swiglu ? Wgate + e * df : NULL,
                            Wdown + e * df, h, h + f, h + 2 * (size_t)f, y);
                 const double g = gate[(size_t)t * k + j];
                 for (int i = 0; i < d; ++i) o[i] += g * y[i];
             }
+        }
+        free(h);
+    }
+}
+
+/* ---- Shared experts  [LLaMA4-MoE] §5.2 ----
+ * A fixed set of experts joins every token's computation.  They form one
+ * dense FFN of hidden width f_shared (several shared experts of width f_e are
+ * the same FFN with their weight blocks side by side, f_shared = n f_e), of
+ * the routed experts' kind (SiLU-MLP or SwiGLU), added with weight 1:
+ *   out[t] += FFN_shared(x_t)   for every token, masked or not.
+ * Wup_s, Wgate_s [d, f_shared], Wdown_s [f_shared, d].                        */
+void oracle_shared_forward(const oracle_cfg* c, const double* x, const double* Wup_s,
+                           const double* Wgate_s, const double* Wdown_s, double* h, double* u,
+                           double* act, double* y)
+{
+    double* tmp = NULL;
+    if (c->swiglu && !u) u = tmp = (double*)malloc(sizeof(double) * (size_t)c->f_shared);
+    expert_ffn(c, c->f_shared, x, Wup_s, c->swiglu ? Wgate_s : NULL, Wdown_s, h, u, act, y);
+    free(tmp);
+}
+
+void oracle_shared_add(const oracle_cfg* c, const double* x, const double* Wup_s,
+                       const double* Wgate_s, const double* Wdown_s, double* out)
+{
+    const int T = c->T, d = c->d, fs = c->f_shared;
+#pragma omp parallel
+    {
+        double* h = (double*)malloc(sizeof(double) * (3 * (size_t)fs + d));
+        double* y = h + 3 * (size_t)fs;
+#pragma omp for schedule(dynamic, 4)
+        for (int t = 0; t < T; ++t) {
+            expert_ffn(c, fs, x + (size_t)t * d, Wup_s, c->swiglu ? Wgate_s : NULL, Wdown_s, h,
+                       h + fs, h + 2 * (size_t)fs, y);
+            double* o = out + (size_t)t * d;
+            for (int i = 0; i < d; ++i) o[i] += y[i];
         }
         free(h);
     }
@@ -354,7 +392,8 @@ void oracle_forward(const oracle_cfg* c, const double* x, const double* Wr, cons
                     const double* Wgate, const double* Wdown, const double* logits_in,
                     double* logits, double* probs, int* topk, double* gate, int* counts,
                     int* kept, int* offsets, int* perm_token, int* slot_of,
-                    double* out, double* stats)
+                    double* out, double* stats,
+                    const double* Wup_s, const double* Wgate_s, const double* Wdown_s)
 {
     if (logits_in) memcpy(logits, logits_in, sizeof(double) * (size_t)c->T * c->E);
     else oracle_router_logits(c, x, Wr, bias, c->straight_through ? NULL : noise, logits);
@@ -362,7 +401,68 @@ void oracle_forward(const oracle_cfg* c, const double* x, const double* Wr, cons
                           counts);
     oracle_permute(c, topk, kept, offsets, perm_token, slot_of);
     oracle_combine(c, x, topk, gate, slot_of, Wup, Wgate, Wdown, out);
+    if (c->f_shared > 0) oracle_shared_add(c, x, Wup_s, Wgate_s, Wdown_s, out);
     oracle_stats(c, probs, topk, counts, kept, nf, stats);
+}
+
+/* Backward of one FFN application y = FFN(x_t) of width f, given its forward
+ * intermediates h (SwiGLU: g), u (SwiGLU) and a, and dy = dL/dy:
+ *   da = Wd dy; dWd += a dy^T;
+ *   SiLU:   dh = da * silu'(h);                    dWu += x dh^T;  dx = Wu dh
+ *   SwiGLU: du = da * silu(g), dg = da * u * silu'(g);
+ *           dWu += x du^T, dWg += x dg^T;           dx = Wu du + Wg dg
+ * dx is written; dh_out (nh*f: dh, or dg then du) is written when not NULL.
+ * scratch holds 3f doubles.                                                   */
+static void ffn_token_backward(const oracle_cfg* c, int f, const double* xt, const double* h,
+                               const double* u, const double* a, const double* Wu,
+                               const double* Wg, const double* Wd, const double* dy,
+                               double* dWu, double* dWg, double* dWd, double* dx,
+                               double* dh_out, double* scratch)
+{
+    const int d = c->d;
+    double *da = scratch, *dh = scratch + f, *du = scratch + 2 * (size_t)f;
+    /* y = Wd^T a */
+    for (int q = 0; q < f; ++q) {
+        const double* wd = Wd + (size_t)q * d;
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += wd[i] * dy[i];
+        da[q] = acc;
+        double* gw = dWd + (size_t)q * d;
+        for (int i = 0; i < d; ++i) gw[i] += a[q] * dy[i];
+    }
+    /* activation */
+    for (int q = 0; q < f; ++q) {
+        if (c->swiglu) {
+            du[q] = da[q] * silu(h[q]);          /* d/du (silu(g) u) */
+            dh[q] = da[q] * u[q] * dsilu(h[q]);  /* d/dg             */
+        } else {
+            dh[q] = da[q] * dsilu(h[q]);
+        }
+    }
+    if (dh_out)
+        for (int q = 0; q < f; ++q) {
+            dh_out[q] = dh[q];
+            if (c->swiglu) dh_out[f + q] = du[q];
+        }
+    /* h = Wu^T x (SiLU) ; g = Wg^T x, u = Wu^T x (SwiGLU) */
+    for (int i = 0; i < d; ++i) {
+        const double xi = xt[i];
+        double acc = 0.0;
+        double* gu = dWu + (size_t)i * f;
+        const double* wu = Wu + (size_t)i * f;
+        if (c->swiglu) {
+            double* gg = dWg + (size_t)i * f;
+            const double* wg = Wg + (size_t)i * f;
+            for (int q = 0; q < f; ++q) {
+                gu[q] += xi * du[q];
+                gg[q] += xi * dh[q];
+                acc += wu[q] * du[q] + wg[q] * dh[q];
+            }
+        } else {
+            for (int q = 0; q < f; ++q) { gu[q] += xi * dh[q]; acc += wu[q] * dh[q]; }
+        }
+        dx[i] = acc;
+    }
 }
 
 /* ---- Step 10: backward of L = <dout, out> + aux loss ----
@@ -383,7 +483,9 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
                      double* dx, double* dWr, double* db, double* dWup, double* dWgate,
                      double* dWdown, double* dgate_out, double* dlogits_out,
                      double* dh_slot_out, double* dxp_slot_out,
-                     const double* pbar_in, int T_aux)
+                     const double* pbar_in, int T_aux,
+                     const double* Wup_s, const double* Wgate_s, const double* Wdown_s,
+                     double* dWup_s, double* dWgate_s, double* dWdown_s)
 {
     const int T = c->T, d = c->d, f = c->f, E = c->E, k = c->k;
     const size_t df = (size_t)d * f;
@@ -398,8 +500,7 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
 #pragma omp parallel for schedule(dynamic, 1)
     for (int e = 0; e < E; ++e) {
         double* h = (double*)malloc(sizeof(double) * (6 * (size_t)f + 2 * (size_t)d));
-        double *u = h + f, *a = h + 2 * (size_t)f, *da = h + 3 * (size_t)f;
-        double *dh = h + 4 * (size_t)f, *du = h + 5 * (size_t)f;
+        double *u = h + f, *a = h + 2 * (size_t)f, *tmp = h + 3 * (size_t)f;
         double *y = h + 6 * (size_t)f, *dy = y + d;
         const double* Wu = Wup + e * df;
         const double* Wg = c->swiglu ? Wgate + e * df : NULL;
@@ -409,62 +510,44 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
                 if (topk[(size_t)t * k + j] != e || slot_of[(size_t)t * k + j] < 0) continue;  /* not e, dropped or masked */
                 const double* xt = x + (size_t)t * d;
                 const double* go = dout + (size_t)t * d;
-                expert_ffn(c, xt, Wu, Wg, Wd, h, u, a, y);
+                expert_ffn(c, f, xt, Wu, Wg, Wd, h, u, a, y);
                 /* out += gate * y  =>  dgate = <dout, y>, dy = gate * dout */
                 double s = 0.0;
                 for (int i = 0; i < d; ++i) s += go[i] * y[i];
                 dgate[(size_t)t * k + j] = s;
                 const double gt = gate[(size_t)t * k + j];
                 for (int i = 0; i < d; ++i) dy[i] = gt * go[i];
-                /* y = Wd^T a */
-                for (int q = 0; q < f; ++q) {
-                    const double* wd = Wd + (size_t)q * d;
-                    double acc = 0.0;
-                    for (int i = 0; i < d; ++i) acc += wd[i] * dy[i];
-                    da[q] = acc;
-                    double* gw = dWdown + e * df + (size_t)q * d;
-                    for (int i = 0; i < d; ++i) gw[i] += a[q] * dy[i];
-                }
-                /* activation */
-                for (int q = 0; q < f; ++q) {
-                    if (c->swiglu) {
-                        du[q] = da[q] * silu(h[q]);          /* d/du (silu(g) u) */
-                        dh[q] = da[q] * u[q] * dsilu(h[q]);  /* d/dg             */
-                    } else {
-                        dh[q] = da[q] * dsilu(h[q]);
-                    }
-                }
-                if (dh_slot_out) {
-                    const int nh = c->swiglu ? 2 : 1;
-                    double* o = dh_slot_out + ((size_t)t * k + j) * nh * f;
-                    for (int q = 0; q < f; ++q) {
-                        o[q] = dh[q];
-                        if (c->swiglu) o[f + q] = du[q];
-                    }
-                }
-                /* h = Wu^T x (SiLU) ; g = Wg^T x, u = Wu^T x (SwiGLU) */
-                double* dxr = dxp + ((size_t)t * k + j) * d;
-                for (int i = 0; i < d; ++i) {
-                    const double xi = xt[i];
-                    double acc = 0.0;
-                    if (c->swiglu) {
-                        double* gu = dWup + e * df + (size_t)i * f;
-                        double* gg = dWgate + e * df + (size_t)i * f;
-                        const double* wu = Wu + (size_t)i * f;
-                        const double* wg = Wg + (size_t)i * f;
-                        for (int q = 0; q < f; ++q) {
-                            gu[q] += xi * du[q];
-                            gg[q] += xi * dh[q];
-                            acc += wu[q] * du[q] + wg[q] * dh[q];
-                        }
-                    } else {
-                        double* gu = dWup + e * df + (size_t)i * f;
-                        const double* wu = Wu + (size_t)i * f;
-                        for (int q = 0; q < f; ++q) { gu[q] += xi * dh[q]; acc += wu[q] * dh[q]; }
-                    }
-                    dxr[i] = acc;
-                }
+                ffn_token_backward(c, f, xt, h, u, a, Wu, Wg, Wd, dy, dWup + e * df,
+                                   c->swiglu ? dWgate + e * df : NULL, dWdown + e * df,
+                                   dxp + ((size_t)t * k + j) * d,
+                                   dh_slot_out ? dh_slot_out + ((size_t)t * k + j) * (c->swiglu ? 2 : 1) * f
+                                               : NULL,
+                                   tmp);
             }
+        free(h);
+    }
+
+    /* shared experts ([LLaMA4-MoE] §5.2): out[t] += FFN_shared(x_t) on every
+     * token, weight 1, so dy = dout[t]; their input gradient joins dx below.  */
+    double* dxs = NULL;
+    if (c->f_shared > 0) {
+        const int fs = c->f_shared;
+        const size_t dfs = (size_t)d * fs;
+        memset(dWup_s, 0, sizeof(double) * dfs);
+        memset(dWdown_s, 0, sizeof(double) * dfs);
+        if (c->swiglu) memset(dWgate_s, 0, sizeof(double) * dfs);
+        dxs = (double*)calloc((size_t)T * d, sizeof(double));
+        /* the weight gradients sum over all tokens: run tokens in order, one thread */
+        double* h = (double*)malloc(sizeof(double) * (6 * (size_t)fs + (size_t)d));
+        double *u = h + fs, *a = h + 2 * (size_t)fs, *tmp = h + 3 * (size_t)fs;
+        double* y = h + 6 * (size_t)fs;
+        for (int t = 0; t < T; ++t) {
+            const double* xt = x + (size_t)t * d;
+            expert_ffn(c, fs, xt, Wup_s, c->swiglu ? Wgate_s : NULL, Wdown_s, h, u, a, y);
+            ffn_token_backward(c, fs, xt, h, u, a, Wup_s, c->swiglu ? Wgate_s : NULL, Wdown_s,
+                               dout + (size_t)t * d, dWup_s, c->swiglu ? dWgate_s : NULL,
+                               dWdown_s, dxs + (size_t)t * d, NULL, tmp);
+        }
         free(h);
     }
 
@@ -519,7 +602,8 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
         for (int e = 0; e < E; ++e) dlt[e] += p[e] * (cvec[e] - s) / tau;
     }
 
-    /* dx = sum over kept slots of the expert dx, plus the router term */
+    /* dx = sum over kept slots of the expert dx, plus the router term, plus the
+     * shared experts' term */
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t) {
         double* o = dx + (size_t)t * d;
@@ -534,6 +618,8 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
             for (int e = 0; e < E; ++e) acc += dl[(size_t)t * E + e] * Wr[(size_t)i * E + e];
             o[i] += acc;
         }
+        if (dxs)
+            for (int i = 0; i < d; ++i) o[i] += dxs[(size_t)t * d + i];
     }
     /* dW_r = x^T dlogits ; db = sum_t dlogits */
 #pragma omp parallel for schedule(static)
@@ -552,5 +638,5 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
     if (dgate_out) memcpy(dgate_out, dgate, sizeof(double) * (size_t)T * k);
     if (dxp_slot_out) memcpy(dxp_slot_out, dxp, sizeof(double) * (size_t)T * k * d);
     if (dlogits_out) memcpy(dlogits_out, dl, sizeof(double) * (size_t)T * E);
-    free(dgate); free(dxp); free(probs); free(pbar); free(dl); free(cvec);
+    free(dgate); free(dxp); free(probs); free(pbar); free(dl); free(cvec); free(dxs);
 }

@@ -408,3 +408,110 @@ def test_masked_batch_equals_the_batch_without_padding(oracle_lib):
     assert (gf["dx"][mask == 0] == 0).all()
     for key in ("dWr", "db", "dWup", "dWgate", "dWdown"):
         np.testing.assert_allclose(gf[key], gs[key], rtol=1e-12, atol=1e-14)
+
+
+# --------------------------------------------------------------------------- shared experts
+def _shared_case(rng, d, fs, swiglu):
+    return (rng.standard_normal((d, fs)) * 0.3, rng.standard_normal((fs, d)) * 0.3,
+            rng.standard_normal((d, fs)) * 0.3 if swiglu else None)
+
+
+@pytest.mark.parametrize("swiglu,cf,masked", [(False, 0.0, False), (True, 0.75, False),
+                                              (False, 0.6, True)])
+def test_shared_experts_match_bruteforce(oracle_lib, swiglu, cf, masked):
+    rng = np.random.default_rng(500 + int(swiglu) + 2 * int(masked))
+    T, d, f, E, k, fs = 40, 12, 10, 5, 2, 24
+    x, Wr, Wup, Wg, Wd, b, _ = _rand_case(rng, T, d, f, E, k, swiglu, bias=True)
+    Wus, Wds, Wgs = _shared_case(rng, d, fs, swiglu)
+    mask = (rng.random(T) > 0.3).astype(np.uint8) if masked else None
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=cf, swiglu=swiglu,
+                              f_shared=fs)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, Wgate=Wg, bias=b, mask=mask, Wup_s=Wus, Wdown_s=Wds,
+                       Wgate_s=Wgs)
+    out, topk, _, _ = bruteforce.forward(x, Wr, Wup, Wd, k, cf, Wgate=Wg, bias=b, mask=mask,
+                                         shared=(Wus, Wds, Wgs))
+    assert (r["topk_idx"] == topk).all()
+    np.testing.assert_allclose(r["out"], out, rtol=1e-11, atol=1e-11)
+    if masked:   # padding tokens skip the routed experts, not the shared ones
+        pad = mask == 0
+        sh = bruteforce.forward(x, Wr, Wup, Wd, k, cf, Wgate=Wg, bias=b,
+                                mask=np.zeros(T, np.uint8), shared=(Wus, Wds, Wgs))[0]
+        np.testing.assert_allclose(r["out"][pad], sh[pad], rtol=1e-11, atol=1e-11)
+
+
+def test_shared_expert_equal_to_the_routed_one_doubles_a_plain_ffn(oracle_lib):
+    """E = k = 1 routes every token to expert 0 with gate 1; a shared FFN with
+    the same weights adds the same FFN once more: out = 2 W_d^T silu(W_u^T x)."""
+    rng = np.random.default_rng(7)
+    T, d, f = 9, 7, 11
+    x = rng.standard_normal((T, d))
+    Wup = rng.standard_normal((1, d, f))
+    Wd = rng.standard_normal((1, f, d))
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=1, k=1, f_shared=f)
+    r = oracle.forward(cfg, x, rng.standard_normal((d, 1)), Wup, Wd, Wup_s=Wup[0], Wdown_s=Wd[0])
+    h = x @ Wup[0]
+    np.testing.assert_allclose(r["out"], 2 * (h / (1 + np.exp(-h))) @ Wd[0], rtol=1e-12,
+                               atol=1e-12)
+
+
+def test_shared_experts_side_by_side_are_one_wide_ffn(oracle_lib):
+    """Two shared experts of width f, run as straight-through experts that every
+    token selects (E = k = 2, gates 1), equal one shared FFN of width 2f whose
+    weight blocks are the two experts' side by side."""
+    rng = np.random.default_rng(8)
+    T, d, f = 10, 6, 9
+    x = rng.standard_normal((T, d))
+    Wup = rng.standard_normal((2, d, f)) * 0.5
+    Wg = rng.standard_normal((2, d, f)) * 0.5
+    Wd = rng.standard_normal((2, f, d)) * 0.5
+    Wr = rng.standard_normal((d, 2))
+    two = oracle.forward(oracle.OracleConfig(T=T, d=d, f=f, E=2, k=2, swiglu=True,
+                                             straight_through=True), x, Wr, Wup, Wd, Wgate=Wg)
+    assert (two["gate"] == 1.0).all()
+    # a layer whose routed experts are all zero, plus the wide shared FFN
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=2, k=1, swiglu=True, f_shared=2 * f)
+    z = np.zeros_like(Wup)
+    wide = oracle.forward(cfg, x, Wr, z, z, Wgate=z, Wup_s=np.concatenate([Wup[0], Wup[1]], 1),
+                          Wgate_s=np.concatenate([Wg[0], Wg[1]], 1),
+                          Wdown_s=np.concatenate([Wd[0], Wd[1]], 0))
+    np.testing.assert_allclose(wide["out"], two["out"], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("swiglu,cf", [(False, 0.75), (True, 0.0)])
+def test_shared_expert_backward_matches_finite_differences(oracle_lib, swiglu, cf):
+    rng = np.random.default_rng(600 + int(swiglu))
+    T, d, f, E, k, fs = 8, 8, 16, 4, 2, 12
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, swiglu, bias=True, noise=True)
+    Wus, Wds, Wgs = _shared_case(rng, d, fs, swiglu)
+    dout = rng.standard_normal((T, d))
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=cf, swiglu=swiglu,
+                              aux_coef=0.3, f_shared=fs)
+
+    def loss(kw):
+        r = oracle.forward(cfg, kw["x"], Wr, Wup, Wd, Wgate=Wg, bias=b, noise=nz,
+                           Wup_s=kw["Wus"], Wdown_s=kw["Wds"], Wgate_s=kw["Wgs"])
+        return float((dout * r["out"]).sum() + r["stats"][oracle.ST_AUX_LOSS]), r
+
+    base = dict(x=x, Wus=Wus, Wds=Wds, Wgs=Wgs)
+    L0, r0 = loss(base)
+    g = oracle.backward(cfg, x, Wr, Wup, Wd, r0["logits"], r0["topk_idx"], r0["gate"],
+                        r0["slot_of"], dout, Wgate=Wg, Wup_s=Wus, Wdown_s=Wds, Wgate_s=Wgs)
+    params = {"x": g["dx"], "Wus": g["dWup_s"], "Wds": g["dWdown_s"]}
+    if swiglu:
+        params["Wgs"] = g["dWgate_s"]
+    h, checked = 1e-6, 0
+    for name, grad in params.items():
+        arr = base[name]
+        for i in rng.choice(arr.size, size=min(arr.size, 40), replace=False):
+            ix = np.unravel_index(i, arr.shape)
+            vals = []
+            for s in (+h, -h):
+                kw = dict(base)
+                kw[name] = arr.copy()
+                kw[name][ix] += s
+                L, r = loss(kw)
+                assert (r["slot_of"] == r0["slot_of"]).all(), "routing moved under +-h"
+                vals.append(L)
+            assert grad[ix] == pytest.approx((vals[0] - vals[1]) / (2 * h), rel=2e-5, abs=2e-7)
+            checked += 1
+    assert checked >= 120
