@@ -38,7 +38,7 @@ import numpy as np  # noqa: E402
 
 import moe_inputs  # noqa: E402
 
-METRIC = "MoE layer tokens/sec fwd+bwd on 1 GB300 (grouped-GEMM % of bf16 peak in roofline)"
+METRIC = "MoE layer tokens/sec fwd and fwd+bwd on 1 GB300; grouped-GEMM % of bf16 peak"
 DEFAULT_WORKLOAD = "small_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "tc_grouped_gemm_small_bf16.md")
@@ -65,12 +65,13 @@ def algorithmic_work(w, A_kept: int):
     s = 2 if w.dtype == "bf16" else 4
     T, d, f, E, k = w.T, w.d, w.f, w.E, w.k
     A = T * k
-    fwd = (6 if w.swiglu else 4) * A_kept * d * f
+    # routed experts on the kept assignments, plus the shared experts on every token
+    fwd = (6 if w.swiglu else 4) * (A_kept * d * f + T * d * w.f_shared)
     return dict(
         gemm_fwd_flop=fwd, gemm_bwd_flop=2 * fwd,
         route_bytes=T * d * s + d * E * s + T * (4 * E + 8 * k),
         permute_bytes=2 * A_kept * d * s + 8 * A,
-        combine_bytes=A_kept * d * s + T * d * s + 8 * A)
+        combine_bytes=A_kept * d * s + T * d * s + 8 * A + (T * d * s if w.f_shared else 0))
 
 
 def gemm_traffic_from_profile():
@@ -151,13 +152,15 @@ def oracle_step(w, T_s: int, seed: int = 0):
            for k, v in inp.items()}
     cfg = oracle.OracleConfig(T=T_s, d=w.d, f=w.f, E=w.E, k=w.k,
                               capacity_factor=float(np.float32(w.capacity_factor)),
-                              swiglu=w.swiglu, aux_coef=w.aux_coef, pad_m=128)
+                              swiglu=w.swiglu, aux_coef=w.aux_coef, pad_m=128,
+                              f_shared=w.f_shared)
+    sh = dict(Wup_s=f64.get("W_up_s"), Wdown_s=f64.get("W_down_s"), Wgate_s=f64.get("W_gate_s"))
     t0 = time.perf_counter()
     o = oracle.forward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], Wgate=f64["W_gate"],
-                       bias=f64["bias"], noise=f64["noise"])
+                       bias=f64["bias"], noise=f64["noise"], **sh)
     oracle.backward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], o["logits"],
                     o["topk_idx"], o["gate"], o["slot_of"], f64["dout"], Wgate=f64["W_gate"],
-                    with_bias=f64["bias"] is not None)
+                    with_bias=f64["bias"] is not None, **sh)
     return time.perf_counter() - t0
 
 
@@ -203,7 +206,8 @@ def workload_config(w, l2):
     return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E,
             "top_k": w.k, "capacity_factor": w.capacity_factor,
             "ffn": "swiglu" if w.swiglu else "silu", "gate_noise_std": w.noise_std,
-            "zipf_router_bias": w.zipf_bias, "aux_coef": w.aux_coef, "l2": l2,
+            "zipf_router_bias": w.zipf_bias, "aux_coef": w.aux_coef, "f_shared": w.f_shared,
+            "l2": l2,
             "parallelism": "replicas (one independent layer per GPU)"}
 
 
@@ -235,6 +239,20 @@ def run_ours(args, w):
     dout = to_torch(inp["dout"], dt, dev)
     L = moe.MoELayer(cfg, device=dev)
     g = L.grads()
+    shared_w = None
+    sh_f = sh_b = None
+    if w.f_shared > 0:             # the shared experts' FFN (same launches as the routed one)
+        shared_w = (to_torch(inp["W_up_s"], dt, dev), to_torch(inp["W_down_s"], dt, dev),
+                    to_torch(inp.get("W_gate_s"), dt, dev))
+        Ts = L.shared_rows
+        sh_f = moe.shared_block(x=x, W_up=shared_w[0], W_down=shared_w[1], W_gate=shared_w[2],
+                                h=L.h_shared, act=L.act_shared, y=L.y_shared)
+        sh_b = moe.shared_block(
+            x=x, W_up=shared_w[0], W_down=shared_w[1], W_gate=shared_w[2], h=L.h_shared,
+            act=L.act_shared, y=L.y_shared, dout=dout,
+            dh=torch.empty(cfg.nh, Ts, w.f_shared, dtype=cfg.torch_dtype, device=dev),
+            dx=torch.empty(Ts, w.d, dtype=cfg.torch_dtype, device=dev),
+            dW_up=g["dW_up_s"], dW_gate=g["dW_gate_s"], dW_down=g["dW_down_s"])
     st = torch.cuda.Stream(dev)           # a side stream: graphs cannot capture the default one
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
     R = L.rows_cap
@@ -261,9 +279,9 @@ def run_ours(args, w):
                         L.stats, L.ws, st)
         rec(evs, 2)
         moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, L.y_perm,
-                            L.ws, st)
+                            L.ws, st, shared=sh_f)
         rec(evs, 3)
-        moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st)
+        moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st, shared=sh_f)
         rec(evs, 4)
 
     def backward(evs=None):
@@ -272,11 +290,12 @@ def run_ours(args, w):
         rec(evs, 5)
         moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
                                      bw["dy"], bw["dh"], bw["dxp"], g["dW_up"], g["dW_gate"],
-                                     g["dW_down"], L.ws, st)
+                                     g["dW_down"], L.ws, st, shared=sh_b)
         rec(evs, 6)
         moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of, bw["dgate"],
                                 bw["dxp"], L.stats, g["dx"], g["dW_r"],
-                                g["dbias"] if b is not None else None, bw["dlogits"], L.ws, st)
+                                g["dbias"] if b is not None else None, bw["dlogits"], L.ws, st,
+                                shared=sh_b)
         rec(evs, 7)
 
     def step(evs=None):
@@ -348,17 +367,17 @@ def run_ours(args, w):
             lambda: moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept,
                                     L.offsets, L.stats, L.ws, st),
             lambda: moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
-                                        L.y_perm, L.ws, st),
-            lambda: moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st),
+                                        L.y_perm, L.ws, st, shared=sh_f),
+            lambda: moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st, shared=sh_f),
             lambda: moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token,
                                              L.offsets, bw["dy"], bw["dgate"], st),
             lambda: moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved,
                                                  L.act, bw["dy"], bw["dh"], bw["dxp"], g["dW_up"],
-                                                 g["dW_gate"], g["dW_down"], L.ws, st),
+                                                 g["dW_gate"], g["dW_down"], L.ws, st, shared=sh_b),
             lambda: moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of,
                                             bw["dgate"], bw["dxp"], L.stats, g["dx"], g["dW_r"],
                                             g["dbias"] if b is not None else None, bw["dlogits"],
-                                            L.ws, st),
+                                            L.ws, st, shared=sh_b),
         ]
         stage_graphs = []
         for fn in stage_fns:
@@ -400,7 +419,7 @@ def run_ours(args, w):
             e0.record(st)
             x_d.copy_(x_h, non_blocking=True)
             dout_d.copy_(dout_h, non_blocking=True)
-            L.forward(x_d, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, stream=st)
+            L.forward(x_d, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, stream=st, shared=shared_w)
             gg = L.backward(dout_d, stream=st)
             out_h.copy_(L.out, non_blocking=True)
             dx_h.copy_(gg["dx"], non_blocking=True)
@@ -420,7 +439,7 @@ def run_ours(args, w):
         peaks, src = load_peaks()
         gemm_ms = float(stage_ms[2] + stage_ms[5])
         gemm_flop = work["gemm_fwd_flop"] + work["gemm_bwd_flop"]
-        launches_gemm = 7 if w.swiglu else 6
+        launches_gemm = 4   # GEMM1, GEMM2, {dgrad2 || dW_down}, {dW_up [|| dW_gate] || dgrad1}
         achieved = gemm_flop / (gemm_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         traffic = gemm_traffic_from_profile()
@@ -486,8 +505,13 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="CPU seconds of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--f-shared", type=int, default=0,
+                    help="add shared experts: a dense FFN of this hidden width on every token")
     args = ap.parse_args(argv)
     w = moe_inputs.get(args.workload)
+    if args.f_shared:
+        from dataclasses import replace
+        w = replace(w, f_shared=args.f_shared, name=f"{w.name}+shared{args.f_shared}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -16,6 +16,8 @@
  *                §3.2 (variance aux loss), §5.3 (gating computed in fp32).
  *   [Twinkle]    "Twinkle adapts DeepSeek-V4 training" notes, §3.1
  *                (scores = W_router x, softmax, top-k with k = 2).
+ *   Shared experts (experts every token passes through, [LLaMA4-MoE] §5.2)
+ *   are optional: moe_config.f_shared > 0 and a moe_shared_ffn block.
  *
  * Conventions (all entry points):
  *   - Every pointer argument is a DEVICE pointer unless stated, owned by the
@@ -98,7 +100,36 @@ typedef struct {
                                 `logits` stays noise-free, gates are 1 in the
                                 forward, and the backward flows through
                                 softmax(logits / tau) at the selected experts     */
+    int32_t f_shared;        /* hidden width of the shared experts' FFN, 0 = none
+                                ([LLaMA4-MoE] §5.2).  n shared experts of width
+                                f_e are one FFN of width n f_e (weight blocks
+                                side by side); bf16 needs a multiple of 128      */
 } moe_config;
+
+/* Shared experts ([LLaMA4-MoE] §5.2: a fixed set of experts joins every
+ * token's computation).  They are one dense FFN of width f_shared, of the
+ * routed experts' kind (cfg->ffn), added to every token's output with weight
+ * 1 -- padding tokens included, since the token mask concerns expert
+ * selection only.  Ts = moe_shared_rows(cfg) rows (T rounded up to 128 for
+ * bf16; rows >= T of h, act and y are zeros).  Entry points that take a
+ * `const moe_shared_ffn*` require it iff cfg->f_shared > 0 (NULL otherwise);
+ * each reads or writes only the fields listed for it.                        */
+typedef struct {
+    const void* x;        /* [T, d] layer input                (ffn, ffn_backward)   */
+    const void* W_up;     /* [d, f_shared]                     (ffn, ffn_backward)   */
+    const void* W_gate;   /* [d, f_shared], SwiGLU only, else NULL                   */
+    const void* W_down;   /* [f_shared, d]                     (ffn, ffn_backward)   */
+    void* h;              /* [nh, Ts, f_shared] h, or g then u (ffn writes)          */
+    void* act;            /* [Ts, f_shared]                    (ffn writes)          */
+    void* y;              /* [Ts, d] shared output (ffn writes, moe_combine reads)   */
+    const void* dout;     /* [T, d] gradient of the layer output (ffn_backward reads)*/
+    void* dh;             /* [nh, Ts, f_shared] intermediate   (ffn_backward writes) */
+    void* dx;             /* [Ts, d] the shared FFN's input gradient (ffn_backward
+                             writes; moe_router_backward adds it into dx)           */
+    void* dW_up;          /* [d, f_shared] weight gradients    (ffn_backward writes) */
+    void* dW_gate;        /* [d, f_shared], SwiGLU only                              */
+    void* dW_down;        /* [f_shared, d]                                           */
+} moe_shared_ffn;
 
 /* ---- statistics vector written by moe_route / moe_permute (fp32, 9 + E) ----
  * Means run over the routed tokens (tokens not masked out).                  */
@@ -125,6 +156,10 @@ MOE_API int moe_capacity(const moe_config* cfg, int32_t* capacity);
 /* Worst-case row count of the permuted buffers (x_perm, act, y_perm, ...):
  * min(T*k, E*C) + E*(pad_m - 1).  Each buffer holds rows_cap rows.            */
 MOE_API int moe_rows_capacity(const moe_config* cfg, int64_t* rows_cap);
+
+/* Rows Ts of the shared experts' buffers (h, act, y, dh, dx of moe_shared_ffn):
+ * T rounded up to a multiple of 128 for bf16, T for fp32; 0 if f_shared = 0. */
+MOE_API int moe_shared_rows(const moe_config* cfg, int64_t* rows);
 
 /* Bytes of scratch `ws` that every entry point below may use (the maximum
  * over all of them, including moe_backward's intermediate gradients).        */
@@ -190,16 +225,21 @@ MOE_API int moe_permute(const moe_config* cfg, const void* x, const int32_t* top
  *   SwiGLU: g = x_perm W_gate[e]; u = x_perm W_up[e]; act = silu(g)*u; y = act W_down[e]
  *   h_saved[nh,rows_cap,f] (nh = 1: h; nh = 2: g then u), act[rows_cap,f],
  *   y_perm[rows_cap,d]; all act dtype; W_gate may be NULL for SiLU.
- * [LLaMA4-MoE] §2.4 (each expert a two-layer FFN).                            */
+ *   shared: the shared experts' FFN on all T tokens, run in the same GEMM
+ *   launches as the routed experts (reads x, W_*; writes h, act, y).
+ * [LLaMA4-MoE] §2.4 (each expert a two-layer FFN), §5.2 (shared experts).    */
 MOE_API int moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                     const void* W_up, const void* W_gate, const void* W_down,
-                    void* h_saved, void* act, void* y_perm, void* ws, moe_stream_t stream);
+                    void* h_saved, void* act, void* y_perm, const moe_shared_ffn* shared,
+                    void* ws, moe_stream_t stream);
 
-/* Combine: out[t] = sum over kept slots j (ascending) of gate[t,j] * y_perm[slot_of[t,j]],
- * fp32 accumulation; a token whose slots were all dropped gets zeros.
+/* Combine: out[t] = sum over kept slots j (ascending) of gate[t,j] * y_perm[slot_of[t,j]]
+ * (+ shared->y[t] with weight 1), fp32 accumulation; a token whose slots were
+ * all dropped gets only the shared output (zeros without shared experts).
  * [LLaMA4-MoE] §2.4 (weighted by the post-softmax routing score).             */
 MOE_API int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_of,
-                const float* gate, void* out, moe_stream_t stream);
+                const float* gate, const moe_shared_ffn* shared, void* out,
+                moe_stream_t stream);
 
 /* ---- backward of  L = <dout, out> + L_aux  ---- */
 
@@ -217,18 +257,20 @@ MOE_API int moe_combine_backward(const moe_config* cfg, const void* dout, const 
  * dx_perm = dh W_up[e]^T (+ dg W_gate[e]^T).
  *   dh[nh,rows_cap,f] act dtype is an output buffer of intermediate gradients
  *   (nh as h_saved: dh, or dg then du); dx_perm[rows_cap,d];
- *   dW_up/dW_gate[E,d,f], dW_down[E,f,d] act dtype.                           */
+ *   dW_up/dW_gate[E,d,f], dW_down[E,f,d] act dtype.
+ *   shared: the same for the shared FFN with dy = dout (weight 1), in the same
+ *   launches (reads x, W_*, h, act, dout; writes dh, dx, dW_*).               */
 MOE_API int moe_grouped_ffn_backward(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                              const void* W_up, const void* W_gate, const void* W_down,
                              const void* h_saved, const void* act, const void* dy_perm,
                              void* dh, void* dx_perm, void* dW_up, void* dW_gate, void* dW_down,
-                             void* ws, moe_stream_t stream);
+                             const moe_shared_ffn* shared, void* ws, moe_stream_t stream);
 
 /* Router backward.  dlogits[t] = gate softmax Jacobian applied to dgate
  * (selected logits only; raw and straight-through gates through the full
  * softmax) + aux term lambda*2(pbar-1/E)/T_routed through the full softmax,
  * all divided by tau; masked tokens get none; dx[t] = sum over kept slots of
- * dx_perm[slot] + dlogits[t] W_r^T;
+ * dx_perm[slot] + dlogits[t] W_r^T (+ shared->dx[t]);
  * dW_r = x^T dlogits; dbias = sum_t dlogits (if non-NULL).
  *   stats: the moe_route statistics of the same forward (pbar is used).
  *   dlogits[T,E] fp32 output (may be NULL: then ws is used).
@@ -236,18 +278,21 @@ MOE_API int moe_grouped_ffn_backward(const moe_config* cfg, const void* x_perm, 
 MOE_API int moe_router_backward(const moe_config* cfg, const void* x, const void* W_r,
                         const float* logits, const int32_t* topk_idx, const float* gate,
                         const int32_t* slot_of, const float* dgate, const void* dx_perm,
-                        const float* stats, void* dx, void* dW_r, float* dbias, float* dlogits,
-                        void* ws, moe_stream_t stream);
+                        const moe_shared_ffn* shared, const float* stats, void* dx, void* dW_r,
+                        float* dbias, float* dlogits, void* ws, moe_stream_t stream);
 
 /* Whole backward: moe_combine_backward -> moe_grouped_ffn_backward ->
- * moe_router_backward, intermediates in ws.  Saved forward tensors as above. */
+ * moe_router_backward, intermediates in ws.  Saved forward tensors as above;
+ * with shared experts, shared->dout is taken to be `dout` and shared->dh /
+ * shared->dx may be NULL (the workspace then holds them).                    */
 MOE_API int moe_backward(const moe_config* cfg, const void* x, const void* W_r, const void* W_up,
                  const void* W_gate, const void* W_down, const float* logits,
                  const int32_t* topk_idx, const float* gate, const int32_t* slot_of,
                  const int32_t* perm_token, const int32_t* offsets, const void* x_perm,
                  const void* h_saved, const void* act, const void* y_perm, const float* stats,
                  const void* dout, void* dx, void* dW_r, float* dbias, void* dW_up,
-                 void* dW_gate, void* dW_down, void* ws, moe_stream_t stream);
+                 void* dW_gate, void* dW_down, const moe_shared_ffn* shared, void* ws,
+                 moe_stream_t stream);
 
 /* ---- status and bookkeeping ---- */
 

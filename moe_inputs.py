@@ -23,7 +23,8 @@ ZIPF_BIAS_FILE = os.path.join(_HERE, "tests", "golden", "skewed16_zipf_bias.json
 
 # fixed stream ids (one per tensor)
 _TENSOR_IDS = {"x": 1, "W_r": 2, "bias": 3, "W_up": 4, "W_gate": 5, "W_down": 6,
-               "noise": 7, "dout": 8, "gumbel": 9, "mask": 10}
+               "noise": 7, "dout": 8, "gumbel": 9, "mask": 10, "W_up_s": 11, "W_gate_s": 12,
+               "W_down_s": 13}
 
 
 @dataclass(frozen=True)
@@ -42,6 +43,7 @@ class Workload:
     aux_coef: float = 0.01
     w_std: float = 0.02
     backward: bool = True
+    f_shared: int = 0           # hidden width of the shared experts' FFN (0: none)
 
     def with_tokens(self, T: int) -> "Workload":
         return replace(self, T=T, name=f"{self.name.split('@')[0]}@T{T}")
@@ -118,10 +120,12 @@ def stored_zipf_alpha() -> float:
 
 
 def make_inputs(w: Workload, seed: int = 0, parts=("x", "W_r", "bias", "W_up", "W_gate",
-                                                    "W_down", "noise", "dout"),
+                                                    "W_down", "noise", "dout", "shared"),
                 zipf_alpha: float | None = None) -> dict:
     """Seeded inputs of workload ``w``.  Router bias and noise are fp32; the rest
-    follow ``w.dtype``.  Absent optional tensors are None."""
+    follow ``w.dtype``.  Absent optional tensors are None.  With ``w.f_shared``
+    the shared experts' weights W_up_s, W_gate_s (SwiGLU) [d, f_shared] and
+    W_down_s [f_shared, d] are drawn too."""
     dt = w.dtype
     out = {}
     if "x" in parts:
@@ -145,6 +149,11 @@ def make_inputs(w: Workload, seed: int = 0, parts=("x", "W_r", "bias", "W_up", "
                         if w.noise_std > 0 else None)
     if "dout" in parts:
         out["dout"] = normal(seed, "dout", (w.T, w.d), 1.0, dt)
+    if "shared" in parts and w.f_shared > 0:
+        fs = w.f_shared
+        out["W_up_s"] = normal(seed, "W_up_s", (w.d, fs), w.w_std, dt)
+        out["W_gate_s"] = normal(seed, "W_gate_s", (w.d, fs), w.w_std, dt) if w.swiglu else None
+        out["W_down_s"] = normal(seed, "W_down_s", (fs, w.d), w.w_std, dt)
     return out
 
 

@@ -49,7 +49,8 @@ def gpu_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True, temperature=1.0,
                          ffn=moe.SWIGLU if w.swiglu else moe.SILU,
                          dtype=moe.BF16 if w.dtype == "bf16" else moe.F32,
                          normalize_gates=1 if normalize else 0, aux_coef=w.aux_coef, pad_m=pad_m,
-                         temperature=temperature, straight_through=int(straight_through))
+                         temperature=temperature, straight_through=int(straight_through),
+                         f_shared=w.f_shared)
 
 
 def oracle_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True, temperature=1.0,
@@ -59,7 +60,7 @@ def oracle_cfg(w: moe_inputs.Workload, pad_m=128, normalize=True, temperature=1.
                                swiglu=w.swiglu, normalize_gates=normalize,
                                aux_coef=float(np.float32(w.aux_coef)), pad_m=pad_m,
                                temperature=float(np.float32(temperature)),
-                               straight_through=bool(straight_through))
+                               straight_through=bool(straight_through), f_shared=w.f_shared)
 
 
 def f64_inputs(w, inp):
@@ -82,8 +83,12 @@ def run_gpu(w, inp, pad_m=128, normalize=True, backward=True, temperature=1.0,
     b = to_torch(inp.get("bias"), "fp32")
     nz = to_torch(inp.get("noise"), "fp32")
     mk = to_torch(inp.get("mask"), "u8")
+    shared = None
+    if w.f_shared > 0:
+        shared = (to_torch(inp["W_up_s"], dt), to_torch(inp["W_down_s"], dt),
+                  to_torch(inp.get("W_gate_s"), dt))
     L = moe.MoELayer(cfg)
-    L.forward(x, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, token_mask=mk)
+    L.forward(x, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, token_mask=mk, shared=shared)
     res = dict(cfg=cfg, layer=L)
     if backward:
         dout = to_torch(inp["dout"], dt)
@@ -94,13 +99,20 @@ def run_gpu(w, inp, pad_m=128, normalize=True, backward=True, temperature=1.0,
         dxp = torch.empty(R, w.d, dtype=tdt, device=dev)
         dlogits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
         g = L.grads()
+        sh = None
+        if w.f_shared > 0:
+            Ts = L.shared_rows
+            res["dh_shared"] = torch.empty(cfg.nh, Ts, w.f_shared, dtype=tdt, device=dev)
+            res["dx_shared"] = torch.empty(Ts, w.d, dtype=tdt, device=dev)
+            sh = L.shared_block(dout=dout, dh=res["dh_shared"], dx=res["dx_shared"])
         moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token, L.offsets,
                                  dy, dgate)
         moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, dy,
-                                     dh, dxp, g["dW_up"], g["dW_gate"], g["dW_down"], L.ws)
+                                     dh, dxp, g["dW_up"], g["dW_gate"], g["dW_down"], L.ws,
+                                     shared=sh)
         moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of, dgate, dxp,
                                 L.stats, g["dx"], g["dW_r"], g["dbias"] if b is not None else None,
-                                dlogits, L.ws)
+                                dlogits, L.ws, shared=sh)
         res.update(dy=dy, dgate=dgate, dh=dh, dxp=dxp, dlogits=dlogits, grads=g, dout=dout)
     torch.cuda.synchronize()
     res["status"] = moe.last_device_status()
@@ -119,7 +131,9 @@ def check_routing(w, ocfg, r, inp64, report):
     report["logits_rel"] = rel_fro(logits, ol)
     # conditioned oracle: route the GPU's fp32 logits
     o = oracle.forward(ocfg, inp64["x"], inp64["W_r"], inp64["W_up"], inp64["W_down"],
-                       Wgate=inp64.get("W_gate"), noise=noise, logits_in=logits, mask=mask)
+                       Wgate=inp64.get("W_gate"), noise=noise, logits_in=logits, mask=mask,
+                       Wup_s=inp64.get("W_up_s"), Wdown_s=inp64.get("W_down_s"),
+                       Wgate_s=inp64.get("W_gate_s"))
     topk = L.topk_idx.cpu().numpy()
     assert (topk == o["topk_idx"]).all(), "top-k differs from the oracle on the same logits"
     assert (L.counts.cpu().numpy() == o["counts"]).all(), "counts differ"
@@ -180,8 +194,12 @@ def check_forward(w, ocfg, r, o, inp64, report, sample_rows=None):
         if ocfg.swiglu:
             want_u.append(ef["u"])
     report["out_rel"] = rel_fro(np64(L.out), o["out"])
+    if ocfg.f_shared > 0:
+        check_shared_forward(w, ocfg, L, inp64, report, sample_rows)
     if len(idx) == 0:        # nothing routed (e.g. every token is padding)
-        assert (np64(L.out) == 0).all(), "out is not zero with no routed token"
+        if ocfg.f_shared == 0:
+            assert (np64(L.out) == 0).all(), "out is not zero with no routed token"
+        assert report["out_rel"] <= tol, ("out_rel", report["out_rel"], tol)
         return
     report["h_rel"] = rel_fro(H[0][idx], np.array(want_h))
     if ocfg.swiglu:
@@ -193,13 +211,37 @@ def check_forward(w, ocfg, r, o, inp64, report, sample_rows=None):
             assert report[key] <= tol, (key, report[key], tol)
 
 
+def check_shared_forward(w, ocfg, L, inp64, report, sample_rows=None):
+    """Shared experts' h / act / y rows (sampled) against the oracle's FFN; the
+    rows past T are zero."""
+    T = ocfg.T
+    toks = np.arange(T)
+    if sample_rows is not None and T > sample_rows:
+        toks = np.sort(np.random.default_rng(1).choice(T, sample_rows, replace=False))
+    want = [oracle.shared_forward(ocfg, inp64["x"][t], inp64["W_up_s"], inp64["W_down_s"],
+                                  inp64.get("W_gate_s")) for t in toks]
+    H, A, Y = np64(L.h_shared), np64(L.act_shared), np64(L.y_shared)
+    report["h_shared_rel"] = rel_fro(H[0][toks], np.array([q["h"] for q in want]))
+    if ocfg.swiglu:
+        report["u_shared_rel"] = rel_fro(H[1][toks], np.array([q["u"] for q in want]))
+    report["act_shared_rel"] = rel_fro(A[toks], np.array([q["act"] for q in want]))
+    report["y_shared_rel"] = rel_fro(Y[toks], np.array([q["y"] for q in want]))
+    assert (Y[T:] == 0).all() and (A[T:] == 0).all(), "shared rows past T are not zero"
+    tol = TOL[w.dtype]
+    for key in ("h_shared_rel", "u_shared_rel", "act_shared_rel", "y_shared_rel"):
+        if key in report:
+            assert report[key] <= tol, (key, report[key], tol)
+
+
 def check_backward(w, ocfg, r, o, inp64, report, with_bias):
     L = r["layer"]
     tol = TOL[w.dtype]
     logits = np64(L.logits)
     ob = oracle.backward(ocfg, inp64["x"], inp64["W_r"], inp64["W_up"], inp64["W_down"], logits,
                          o["topk_idx"], o["gate"], o["slot_of"], inp64["dout"],
-                         Wgate=inp64.get("W_gate"), with_bias=with_bias, per_slot=True)
+                         Wgate=inp64.get("W_gate"), with_bias=with_bias, per_slot=True,
+                         Wup_s=inp64.get("W_up_s"), Wdown_s=inp64.get("W_down_s"),
+                         Wgate_s=inp64.get("W_gate_s"))
     g = r["grads"]
     slot = o["slot_of"]
     kept = slot >= 0
@@ -226,6 +268,11 @@ def check_backward(w, ocfg, r, o, inp64, report, with_bias):
         report["dWgate_rel"] = rel_fro(np64(g["dW_gate"]), ob["dWgate"])
     if with_bias:
         report["db_rel"] = rel_fro(np64(g["dbias"]), ob["db"])
+    if ocfg.f_shared > 0:
+        report["dWup_s_rel"] = rel_fro(np64(g["dW_up_s"]), ob["dWup_s"])
+        report["dWdown_s_rel"] = rel_fro(np64(g["dW_down_s"]), ob["dWdown_s"])
+        if ocfg.swiglu:
+            report["dWgate_s_rel"] = rel_fro(np64(g["dW_gate_s"]), ob["dWgate_s"])
     for key, v in list(report.items()):
         if key.startswith("d") and key.endswith("_rel"):
             assert v <= tol, (key, v, tol)

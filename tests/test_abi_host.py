@@ -49,8 +49,9 @@ def test_binding_signatures_match_header():
 
 
 def test_struct_layout_matches_header():
-    # 13 four-byte fields, no padding
-    assert ctypes.sizeof(moe.MoEConfig) == 52
+    # 14 four-byte fields, no padding
+    assert ctypes.sizeof(moe.MoEConfig) == 56
+    assert ctypes.sizeof(moe.MoESharedFFN) == 13 * 8
 
 
 def test_config_validation():
@@ -59,12 +60,13 @@ def test_config_validation():
     bad = [dict(T=0), dict(k=5), dict(E=0), dict(pad_m=0), dict(dtype=7), dict(ffn=3),
            dict(normalize_gates=2), dict(capacity_factor=float("nan")),
            dict(temperature=float("nan")), dict(temperature=-1.0), dict(temperature=float("inf")),
-           dict(straight_through=2)]
+           dict(straight_through=2), dict(f_shared=-128)]
     for b in bad:
         kw = dict(T=64, d=256, f=256, E=4, k=2)
         kw.update(b)
         assert moe.check_config(moe.MoEConfig(**kw)) == moe.ERR_INVALID_ARG, b
-    unsup = [dict(E=65, k=2), dict(k=9, E=16), dict(d=200), dict(f=136), dict(pad_m=64)]
+    unsup = [dict(E=65, k=2), dict(k=9, E=16), dict(d=200), dict(f=136), dict(pad_m=64),
+             dict(f_shared=200)]
     for b in unsup:
         kw = dict(T=64, d=256, f=256, E=4, k=2)
         kw.update(b)
@@ -98,7 +100,7 @@ def test_null_and_misaligned_pointers_are_rejected_before_launch():
     p = ctypes.c_void_p(0x1000 + 8)  # misaligned
     args = [ctypes.byref(c)] + [p] * 11 + [None]
     assert lib.moe_route(*args) == moe.ERR_INVALID_ARG
-    assert lib.moe_combine(ctypes.byref(c), None, None, None, None, None) == moe.ERR_INVALID_ARG
+    assert lib.moe_combine(ctypes.byref(c), None, None, None, None, None, None) == moe.ERR_INVALID_ARG
     assert lib.moe_route(None, *([None] * 12)) == moe.ERR_INVALID_ARG
 
 
@@ -106,3 +108,24 @@ def test_error_strings():
     for code in range(-7, 1):
         assert moe.error_string(code)
     assert moe.error_string(-99) == "unknown status"
+
+
+def test_shared_rows_and_block_presence_checks():
+    c = moe.MoEConfig(T=333, d=256, f=256, E=4, k=2, f_shared=384)
+    assert moe.shared_rows(c) == 384                      # T rounded up to 128 (bf16)
+    assert moe.shared_rows(moe.MoEConfig(T=333, d=256, f=256, E=4, k=2)) == 0
+    assert moe.shared_rows(moe.MoEConfig(T=97, d=64, f=96, E=4, k=2, dtype=moe.F32,
+                                         pad_m=1, f_shared=40)) == 97
+    # the workspace covers the shared FFN's backward intermediates
+    assert moe.workspace_size(c) > moe.workspace_size(moe.MoEConfig(T=333, d=256, f=256, E=4, k=2))
+    lib = moe.load_library()
+    p = ctypes.c_void_p(0x10000)                          # aligned, never dereferenced
+    # f_shared > 0 needs the block; f_shared = 0 forbids it (checked before any launch)
+    assert lib.moe_combine(ctypes.byref(c), p, p, p, None, p, None) == moe.ERR_INVALID_ARG
+    c0 = moe.MoEConfig(T=333, d=256, f=256, E=4, k=2)
+    blk = moe.MoESharedFFN()
+    assert lib.moe_combine(ctypes.byref(c0), p, p, p, ctypes.byref(blk), p, None) == \
+        moe.ERR_INVALID_ARG
+    # a block missing the field moe_combine reads
+    assert lib.moe_combine(ctypes.byref(c), p, p, p, ctypes.byref(blk), p, None) == \
+        moe.ERR_INVALID_ARG

@@ -225,3 +225,39 @@ def test_every_token_padding():
     for name in ("dx", "dW_up", "dW_down", "dW_r"):
         assert (r["grads"][name].float() == 0).all(), name
     _report("all padding", rep)
+
+
+# ------------------------------------------------------------------ shared experts
+@pytest.mark.parametrize("dtype,swiglu,T,fs", [("bf16", False, 333, 384), ("bf16", True, 256, 256),
+                                               ("fp32", False, 150, 96), ("fp32", True, 97, 40)])
+def test_shared_experts(dtype, swiglu, T, fs):
+    """Routed experts plus a shared FFN on every token (weight 1), in the same
+    GEMM launches; ragged T leaves zero rows past T in the shared buffers."""
+    base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
+    w = _w(base, T=T, d=256 if dtype == "bf16" else 64, f=256 if dtype == "bf16" else 96,
+           E=6, k=2, capacity_factor=1.0, swiglu=swiglu, f_shared=fs)
+    rep, _ = parity.full_check(w, _edge_inputs(w, seed=51), pad_m=128 if dtype == "bf16" else 4)
+    assert "y_shared_rel" in rep and "dWup_s_rel" in rep
+    _report(f"shared {dtype} swiglu{int(swiglu)} T{T} fs{fs}", rep)
+
+
+def test_shared_experts_with_padding_and_llama4_shape():
+    w = _w("llama4_bf16", f_shared=1024).with_tokens(512)
+    inp = moe_inputs.make_inputs(w, 6)
+    inp["mask"] = moe_inputs.padding_mask(6, w.T)
+    rep, _ = parity.full_check(w, inp, sample_rows=128)
+    _report("llama4 + shared + mask", rep)
+
+
+def test_shared_experts_composite_backward_matches_substeps():
+    w = _w("small_bf16", T=384, d=256, f=256, f_shared=512)
+    inp = moe_inputs.make_inputs(w, 7)
+    r = parity.run_gpu(w, inp)
+    L = r["layer"]
+    sub = {k: v.clone() for k, v in r["grads"].items() if v is not None}
+    g = L.backward(r["dout"])
+    torch.cuda.synchronize()
+    for k, v in sub.items():
+        if k == "dbias":
+            continue
+        assert torch.equal(v, g[k]), k

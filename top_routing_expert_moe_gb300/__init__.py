@@ -41,13 +41,14 @@ class MoEConfig(ctypes.Structure):
                 ("capacity_factor", ctypes.c_float), ("ffn", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("normalize_gates", ctypes.c_int32),
                 ("aux_coef", ctypes.c_float), ("pad_m", ctypes.c_int32),
-                ("temperature", ctypes.c_float), ("straight_through", ctypes.c_int32)]
+                ("temperature", ctypes.c_float), ("straight_through", ctypes.c_int32),
+                ("f_shared", ctypes.c_int32)]
 
     def __init__(self, T, d, f, E, k, capacity_factor=0.0, ffn=SILU, dtype=BF16,
                  normalize_gates=1, aux_coef=0.0, pad_m=128, temperature=1.0,
-                 straight_through=0):
+                 straight_through=0, f_shared=0):
         super().__init__(T, d, f, E, k, capacity_factor, ffn, dtype, normalize_gates, aux_coef,
-                         pad_m, temperature, int(straight_through))
+                         pad_m, temperature, int(straight_through), int(f_shared))
 
     @property
     def torch_dtype(self):
@@ -61,6 +62,34 @@ class MoEConfig(ctypes.Structure):
         return ("MoEConfig(" + ", ".join(f"{n}={getattr(self, n)!r}" for n, _ in self._fields_) + ")")
 
 
+_SHARED_FIELDS = ("x", "W_up", "W_gate", "W_down", "h", "act", "y", "dout", "dh", "dx",
+                  "dW_up", "dW_gate", "dW_down")
+
+
+class MoESharedFFN(ctypes.Structure):
+    """Mirror of ``moe_shared_ffn`` (include/moe.h): device pointers of the
+    shared experts' FFN (weights, saved activations, gradients)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in _SHARED_FIELDS]
+
+
+def shared_block(**tensors) -> MoESharedFFN:
+    """A ``moe_shared_ffn`` from torch tensors given by field name (others NULL).
+    The block holds references to the tensors, so their memory stays allocated
+    for as long as the block (or a CUDA graph captured with it) is in use."""
+    unknown = set(tensors) - set(_SHARED_FIELDS)
+    if unknown:
+        raise ValueError(f"unknown shared-expert fields {sorted(unknown)}")
+    b = MoESharedFFN()
+    for n, t in tensors.items():
+        setattr(b, n, None if t is None else _p(t).value)
+    b._tensors = dict(tensors)
+    return b
+
+
+def _sh(shared):
+    return None if shared is None else ctypes.byref(shared)
+
+
 class MoEError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
@@ -72,16 +101,17 @@ _SIGS = {
     "moe_check_config": [ctypes.c_void_p],
     "moe_capacity": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_rows_capacity": [ctypes.c_void_p, ctypes.c_void_p],
+    "moe_shared_rows": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_workspace_size": [ctypes.c_void_p, ctypes.c_void_p],
     "moe_route": [ctypes.c_void_p] * 13,
     "moe_route_noalloc": [ctypes.c_void_p] * 12,
     "moe_permute": [ctypes.c_void_p] * 11,
-    "moe_grouped_ffn": [ctypes.c_void_p] * 11,
-    "moe_combine": [ctypes.c_void_p] * 6,
+    "moe_grouped_ffn": [ctypes.c_void_p] * 12,
+    "moe_combine": [ctypes.c_void_p] * 7,
     "moe_combine_backward": [ctypes.c_void_p] * 10,
-    "moe_grouped_ffn_backward": [ctypes.c_void_p] * 16,
-    "moe_router_backward": [ctypes.c_void_p] * 16,
-    "moe_backward": [ctypes.c_void_p] * 26,
+    "moe_grouped_ffn_backward": [ctypes.c_void_p] * 17,
+    "moe_router_backward": [ctypes.c_void_p] * 17,
+    "moe_backward": [ctypes.c_void_p] * 27,
     "moe_last_device_status": [ctypes.c_void_p, ctypes.c_void_p],
 }
 
@@ -154,6 +184,12 @@ def rows_capacity(cfg: MoEConfig) -> int:
     return v.value
 
 
+def shared_rows(cfg: MoEConfig) -> int:
+    v = ctypes.c_int64()
+    _call("moe_shared_rows", ctypes.byref(cfg), ctypes.byref(v))
+    return v.value
+
+
 def workspace_size(cfg: MoEConfig) -> int:
     v = ctypes.c_size_t()
     _call("moe_workspace_size", ctypes.byref(cfg), ctypes.byref(v))
@@ -193,14 +229,14 @@ def moe_permute(cfg, x, topk_idx, x_perm, perm_token, slot_of, kept, offsets, st
 
 
 def moe_grouped_ffn(cfg, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, y_perm, ws,
-                    stream=None):
+                    stream=None, shared=None):
     _call("moe_grouped_ffn", ctypes.byref(cfg), _p(x_perm), _p(offsets), _p(W_up), _p(W_gate),
-          _p(W_down), _p(h_saved), _p(act), _p(y_perm), _p(ws), _s(stream))
+          _p(W_down), _p(h_saved), _p(act), _p(y_perm), _sh(shared), _p(ws), _s(stream))
 
 
-def moe_combine(cfg, y_perm, slot_of, gate, out, stream=None):
-    _call("moe_combine", ctypes.byref(cfg), _p(y_perm), _p(slot_of), _p(gate), _p(out),
-          _s(stream))
+def moe_combine(cfg, y_perm, slot_of, gate, out, stream=None, shared=None):
+    _call("moe_combine", ctypes.byref(cfg), _p(y_perm), _p(slot_of), _p(gate), _sh(shared),
+          _p(out), _s(stream))
 
 
 def moe_combine_backward(cfg, dout, y_perm, gate, slot_of, perm_token, offsets, dy_perm, dgate,
@@ -210,32 +246,35 @@ def moe_combine_backward(cfg, dout, y_perm, gate, slot_of, perm_token, offsets, 
 
 
 def moe_grouped_ffn_backward(cfg, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, dy_perm,
-                             dh, dx_perm, dW_up, dW_gate, dW_down, ws, stream=None):
+                             dh, dx_perm, dW_up, dW_gate, dW_down, ws, stream=None, shared=None):
     _call("moe_grouped_ffn_backward", ctypes.byref(cfg), _p(x_perm), _p(offsets), _p(W_up),
           _p(W_gate), _p(W_down), _p(h_saved), _p(act), _p(dy_perm), _p(dh), _p(dx_perm),
-          _p(dW_up), _p(dW_gate), _p(dW_down), _p(ws), _s(stream))
+          _p(dW_up), _p(dW_gate), _p(dW_down), _sh(shared), _p(ws), _s(stream))
 
 
 def moe_router_backward(cfg, x, W_r, logits, topk_idx, gate, slot_of, dgate, dx_perm, stats, dx,
-                        dW_r, dbias, dlogits, ws, stream=None):
+                        dW_r, dbias, dlogits, ws, stream=None, shared=None):
     _call("moe_router_backward", ctypes.byref(cfg), _p(x), _p(W_r), _p(logits), _p(topk_idx),
-          _p(gate), _p(slot_of), _p(dgate), _p(dx_perm), _p(stats), _p(dx), _p(dW_r), _p(dbias),
-          _p(dlogits), _p(ws), _s(stream))
+          _p(gate), _p(slot_of), _p(dgate), _p(dx_perm), _sh(shared), _p(stats), _p(dx),
+          _p(dW_r), _p(dbias), _p(dlogits), _p(ws), _s(stream))
 
 
 def moe_backward(cfg, x, W_r, W_up, W_gate, W_down, logits, topk_idx, gate, slot_of, perm_token,
                  offsets, x_perm, h_saved, act, y_perm, stats, dout, dx, dW_r, dbias, dW_up,
-                 dW_gate, dW_down, ws, stream=None):
+                 dW_gate, dW_down, ws, stream=None, shared=None):
     _call("moe_backward", ctypes.byref(cfg), _p(x), _p(W_r), _p(W_up), _p(W_gate), _p(W_down),
           _p(logits), _p(topk_idx), _p(gate), _p(slot_of), _p(perm_token), _p(offsets),
           _p(x_perm), _p(h_saved), _p(act), _p(y_perm), _p(stats), _p(dout), _p(dx), _p(dW_r),
-          _p(dbias), _p(dW_up), _p(dW_gate), _p(dW_down), _p(ws), _s(stream))
+          _p(dbias), _p(dW_up), _p(dW_gate), _p(dW_down), _sh(shared), _p(ws), _s(stream))
 
 
 # ----------------------------------------------------------------- convenience layer
 class MoELayer:
     """Owns the routing cache, permuted buffers and workspace of one layer
-    configuration (all torch-allocated once) and chains the entry points."""
+    configuration (all torch-allocated once) and chains the entry points.
+    With cfg.f_shared > 0, forward() takes the shared experts' weights
+    (``shared=(W_up_s, W_down_s, W_gate_s or None)``) and backward() also
+    returns their gradients (dW_up_s, dW_gate_s, dW_down_s)."""
 
     def __init__(self, cfg: MoEConfig, device="cuda"):
         rc = check_config(cfg)
@@ -262,19 +301,40 @@ class MoELayer:
         self.y_perm = e(R, d)
         self.out = e(T, d)
         self.ws = e(max(workspace_size(cfg), 256), dtype=torch.uint8)
+        self.shared_rows = Ts = shared_rows(cfg)
+        if cfg.f_shared > 0:
+            fs = cfg.f_shared
+            self.h_shared = e(cfg.nh, Ts, fs)
+            self.act_shared = e(Ts, fs)
+            self.y_shared = e(Ts, d)
         self._grads = None
         self._inputs = None
+        self._shared_w = None
+
+    def _shared_fwd(self, x):
+        if self.cfg.f_shared <= 0:
+            return None
+        Wu, Wd, Wg = self._shared_w
+        return shared_block(x=x, W_up=Wu, W_gate=Wg, W_down=Wd, h=self.h_shared,
+                            act=self.act_shared, y=self.y_shared)
 
     def forward(self, x, W_r, W_up, W_down, W_gate=None, bias=None, noise=None, token_mask=None,
-                stream=None):
+                stream=None, shared=None):
         c = self.cfg
+        if (c.f_shared > 0) != (shared is not None):
+            raise ValueError("shared-expert weights are required iff cfg.f_shared > 0")
+        if shared is not None:
+            Wu_s, Wd_s = shared[0], shared[1]
+            Wg_s = shared[2] if len(shared) > 2 else None
+            self._shared_w = (Wu_s, Wd_s, Wg_s)
+        sh = self._shared_fwd(x)
         moe_route(c, x, W_r, bias, noise, token_mask, self.logits, self.topk_idx, self.gate,
                   self.counts, self.stats, self.ws, stream)
         moe_permute(c, x, self.topk_idx, self.x_perm, self.perm_token, self.slot_of, self.kept,
                     self.offsets, self.stats, self.ws, stream)
         moe_grouped_ffn(c, self.x_perm, self.offsets, W_up, W_gate, W_down, self.h_saved,
-                        self.act, self.y_perm, self.ws, stream)
-        moe_combine(c, self.y_perm, self.slot_of, self.gate, self.out, stream)
+                        self.act, self.y_perm, self.ws, stream, shared=sh)
+        moe_combine(c, self.y_perm, self.slot_of, self.gate, self.out, stream, shared=sh)
         self._inputs = (x, W_r, W_up, W_gate, W_down, bias)
         return self.out
 
@@ -290,7 +350,26 @@ class MoELayer:
                 dW_gate=(torch.empty(c.E, c.d, c.f, dtype=dt, device=dev)
                          if c.ffn == SWIGLU else None),
                 dW_down=torch.empty(c.E, c.f, c.d, dtype=dt, device=dev))
+            if c.f_shared > 0:
+                fs = c.f_shared
+                self._grads.update(
+                    dW_up_s=torch.empty(c.d, fs, dtype=dt, device=dev),
+                    dW_gate_s=(torch.empty(c.d, fs, dtype=dt, device=dev)
+                               if c.ffn == SWIGLU else None),
+                    dW_down_s=torch.empty(fs, c.d, dtype=dt, device=dev))
         return self._grads
+
+    def shared_block(self, dout=None, dh=None, dx=None):
+        """The layer's moe_shared_ffn block (forward buffers, weights, gradient
+        outputs; dout / dh / dx as given), or None without shared experts."""
+        if self.cfg.f_shared <= 0:
+            return None
+        x = self._inputs[0]
+        Wu, Wd, Wg = self._shared_w
+        g = self.grads()
+        return shared_block(x=x, W_up=Wu, W_gate=Wg, W_down=Wd, h=self.h_shared,
+                            act=self.act_shared, y=self.y_shared, dout=dout, dh=dh, dx=dx,
+                            dW_up=g["dW_up_s"], dW_gate=g["dW_gate_s"], dW_down=g["dW_down_s"])
 
     def backward(self, dout, stream=None):
         if self._inputs is None:
@@ -301,5 +380,5 @@ class MoELayer:
                      self.slot_of, self.perm_token, self.offsets, self.x_perm, self.h_saved,
                      self.act, self.y_perm, self.stats, dout, g["dx"], g["dW_r"],
                      g["dbias"] if bias is not None else None, g["dW_up"], g["dW_gate"],
-                     g["dW_down"], self.ws, stream)
+                     g["dW_down"], self.ws, stream, shared=self.shared_block())
         return g

@@ -29,12 +29,14 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __host__ __device__ constexpr size_t align_up_dev(size_t b) { return (b + 255) / 256 * 256; }
 
-// out[t] = sum_j gate[t,j] * y_perm[slot_of[t,j]] (kept slots, j ascending).
+// out[t] = sum_j gate[t,j] * y_perm[slot_of[t,j]] (kept slots, j ascending),
+// plus y_shared[t] (the shared experts, weight 1) when given.
 // One warp per token; each lane keeps 4 vectors of 16 bytes per slot in flight.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_of,
-                                                      const float* __restrict__ gate, int Tn,
+                                                      const float* __restrict__ gate,
+                                                      const T* __restrict__ y_shared, int Tn,
                                                       int d, int k, T* __restrict__ out)
 {
     constexpr int V = 16 / sizeof(T), U = 4;
@@ -55,6 +57,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_pe
             for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int q = 0; q < V; ++q) acc[u][q] = 0.f;
+            if (y_shared) {
+                const T* row = y_shared + (size_t)t * d;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (v0 + 32 * u < nv) load16_f<T>(row + (v0 + 32 * u) * V, acc[u]);
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (slot[j] < 0) continue;
@@ -149,9 +157,9 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ topk,
     const float* __restrict__ gate, const int32_t* __restrict__ slot_of,
     const float* __restrict__ dgate, const float* __restrict__ stats,
-    const T* __restrict__ dx_perm, const float* __restrict__ WrT, int Tn, int d, int E, int k,
-    int normalize, int st, float inv_tau, float aux_coef, float* __restrict__ dlogits,
-    T* __restrict__ dx)
+    const T* __restrict__ dx_perm, const T* __restrict__ dx_shared, const float* __restrict__ WrT,
+    int Tn, int d, int E, int k, int normalize, int st, float inv_tau, float aux_coef,
+    float* __restrict__ dlogits, T* __restrict__ dx)
 {
     constexpr int V = 16 / sizeof(T);
     __shared__ float s_dl[8][64];
@@ -222,6 +230,7 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
             float acc[V];
 #pragma unroll
             for (int q = 0; q < V; ++q) acc[q] = 0.f;
+            if (dx_shared) load16_f<T>(dx_shared + (size_t)t * d + v * V, acc);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (slot[j] < 0) continue;
@@ -260,8 +269,9 @@ constexpr int RDX_CW = 128;  // columns per CTA
 template <int KS>  // KS = ceil(E / 16) k-steps
 __global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
     const float* __restrict__ dlogits, const __nv_bfloat16* __restrict__ Wr,
-    const int32_t* __restrict__ slot_of, const __nv_bfloat16* __restrict__ dx_perm, int Tn, int d,
-    int E, int k, __nv_bfloat16* __restrict__ dx)
+    const int32_t* __restrict__ slot_of, const __nv_bfloat16* __restrict__ dx_perm,
+    const __nv_bfloat16* __restrict__ dx_shared, int Tn, int d, int E, int k,
+    __nv_bfloat16* __restrict__ dx)
 {
     constexpr int E16 = KS * 16, LDW = E16 + 2, LDO = RDX_CW + 4;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -364,6 +374,24 @@ __global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
                             acc[i][2 * q + 1] += __uint_as_float(w4[q] & 0xFFFF0000u);
                         }
                     }
+            }
+            if (dx_shared) {   // the shared experts' input gradient
+                uint4 y[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int t = t0 + hw + 2 * i;
+                    y[i] = t < Tn ? __ldg(reinterpret_cast<const uint4*>(dx_shared + (size_t)t * d + col))
+                                  : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t w4[4] = {y[i].x, y[i].y, y[i].z, y[i].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[i][2 * q] += __uint_as_float(w4[q] << 16);
+                        acc[i][2 * q + 1] += __uint_as_float(w4[q] & 0xFFFF0000u);
+                    }
+                }
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -624,16 +652,18 @@ int row_grid(int64_t rows) {
 }  // namespace
 
 int launch_combine(const moe_config& c, const void* y_perm, const int32_t* slot_of,
-                   const float* gate, void* out, cudaStream_t st)
+                   const float* gate, const void* y_shared, void* out, cudaStream_t st)
 {
     const int grid = row_grid(c.T);
     if (c.dtype == MOE_DTYPE_BF16)
         combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(y_perm), slot_of, gate, c.T, c.d, c.k,
+            static_cast<const __nv_bfloat16*>(y_perm), slot_of, gate,
+            static_cast<const __nv_bfloat16*>(y_shared), c.T, c.d, c.k,
             static_cast<__nv_bfloat16*>(out));
     else
         combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(y_perm), slot_of,
-                                                    gate, c.T, c.d, c.k, static_cast<float*>(out));
+                                                    gate, static_cast<const float*>(y_shared),
+                                                    c.T, c.d, c.k, static_cast<float*>(out));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
@@ -668,8 +698,8 @@ int launch_combine_backward(const moe_config& c, const void* dout, const void* y
 namespace {
 template <int KS>
 int launch_router_dx_ks(const moe_config& c, const float* dl, const __nv_bfloat16* Wr,
-                        const int32_t* slot_of, const __nv_bfloat16* dxp, __nv_bfloat16* dx,
-                        cudaStream_t st) {
+                        const int32_t* slot_of, const __nv_bfloat16* dxp,
+                        const __nv_bfloat16* dxs, __nv_bfloat16* dx, cudaStream_t st) {
     constexpr int LDW = KS * 16 + 2;
     const size_t smem = align_up_dev((size_t)RDX_CW * LDW * 2) + (size_t)8 * 16 * (RDX_CW + 4) * 4;
     static bool attr = false;
@@ -682,19 +712,19 @@ int launch_router_dx_ks(const moe_config& c, const float* dl, const __nv_bfloat1
     const int tiles = (c.T + 15) / 16;
     // one wave: at most the resident CTA slots (2 per SM), no partial second wave
     const int gy = std::max(1, std::min((tiles + 7) / 8, (2 * num_sms()) / gx));
-    router_dx_bf16_kernel<KS><<<dim3(gx, gy), 256, smem, st>>>(dl, Wr, slot_of, dxp, c.T, c.d, c.E,
-                                                               c.k, dx);
+    router_dx_bf16_kernel<KS><<<dim3(gx, gy), 256, smem, st>>>(dl, Wr, slot_of, dxp, dxs, c.T,
+                                                               c.d, c.E, c.k, dx);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 }  // namespace
 
 int launch_router_dx_bf16(const moe_config& c, const float* dl, const __nv_bfloat16* Wr,
-                          const int32_t* slot_of, const __nv_bfloat16* dxp, __nv_bfloat16* dx,
-                          cudaStream_t st) {
-    if (c.E <= 16) return launch_router_dx_ks<1>(c, dl, Wr, slot_of, dxp, dx, st);
-    if (c.E <= 32) return launch_router_dx_ks<2>(c, dl, Wr, slot_of, dxp, dx, st);
-    return launch_router_dx_ks<4>(c, dl, Wr, slot_of, dxp, dx, st);
+                          const int32_t* slot_of, const __nv_bfloat16* dxp,
+                          const __nv_bfloat16* dxs, __nv_bfloat16* dx, cudaStream_t st) {
+    if (c.E <= 16) return launch_router_dx_ks<1>(c, dl, Wr, slot_of, dxp, dxs, dx, st);
+    if (c.E <= 32) return launch_router_dx_ks<2>(c, dl, Wr, slot_of, dxp, dxs, dx, st);
+    return launch_router_dx_ks<4>(c, dl, Wr, slot_of, dxp, dxs, dx, st);
 }
 
 size_t router_bwd_ws_bytes(const moe_config& c) {
@@ -706,8 +736,8 @@ size_t router_bwd_ws_bytes(const moe_config& c) {
 int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
                            const float* logits, const int32_t* topk, const float* gate,
                            const int32_t* slot_of, const float* dgate, const void* dx_perm,
-                           const float* stats, void* dx, void* dWr, float* dbias, float* dlogits,
-                           void* ws, cudaStream_t st)
+                           const void* dx_shared, const float* stats, void* dx, void* dWr,
+                           float* dbias, float* dlogits, void* ws, cudaStream_t st)
 {
     const int ns = dwr_nsplit(c);
     uint8_t* w = static_cast<uint8_t*>(ws);
@@ -741,11 +771,12 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
         using T = __nv_bfloat16;
         router_bwd_token_kernel<T, false><<<grid, 256, 0, st>>>(
             logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), nullptr,
-            c.T, c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau, c.aux_coef, dlogits,
-            static_cast<T*>(dx));
+            nullptr, c.T, c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau,
+            c.aux_coef, dlogits, static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();
         MOE_TRY_R(launch_router_dx_bf16(c, dlogits, static_cast<const T*>(Wr), slot_of,
-                                        static_cast<const T*>(dx_perm), static_cast<T*>(dx), st));
+                                        static_cast<const T*>(dx_perm),
+                                        static_cast<const T*>(dx_shared), static_cast<T*>(dx), st));
         const dim3 mgrid((c.d + 127) / 128, ns);
         if (c.E <= 16)
             dwr_mma_kernel<1><<<mgrid, 128, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
@@ -765,9 +796,9 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
         transpose_wr_f32_kernel<T><<<64, 256, 0, st>>>(static_cast<const T*>(Wr), WrT, c.d, c.E);
         MOE_LAUNCH_CHECK();
         router_bwd_token_kernel<T, true><<<grid, 256, 0, st>>>(
-            logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), WrT, c.T,
-            c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau, c.aux_coef, dlogits,
-            static_cast<T*>(dx));
+            logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm),
+            static_cast<const T*>(dx_shared), WrT, c.T, c.d, c.E, c.k, c.normalize_gates,
+            c.straight_through, inv_tau, c.aux_coef, dlogits, static_cast<T*>(dx));
         MOE_LAUNCH_CHECK();
         dwr_partial_kernel<T, DWR_EB><<<pgrid, 256, dwr_smem, st>>>(static_cast<const T*>(x), dlogits,
                                                                    c.T, c.d, c.E, chunk, part, part_db);

@@ -19,6 +19,7 @@ namespace {
 // C[m,n] (+)= sum_k A(m,k) B(n,k) over expert segments.
 //   SEG_ROWS: rows m in [offsets[e], offsets[e+1]); B advanced by e*b_se.
 //   SEG_K   : k in [offsets[e], offsets[e+1]) (weight gradient); C advanced by e*c_se.
+// Without offsets there is one segment [0, fixed) (the shared experts' FFN).
 enum SegMode { SEG_ROWS = 0, SEG_K = 1 };
 
 struct SimtGemm {
@@ -28,6 +29,7 @@ struct SimtGemm {
     int M, N, K;      // extents of the non-segmented dimensions
     int mode;
     const int32_t* offsets;
+    int fixed;
     int accumulate;
 };
 
@@ -45,16 +47,18 @@ __global__ void __launch_bounds__(256) simt_seg_gemm_kernel(SimtGemm g)
     const T* A = static_cast<const T*>(g.A);
     const T* B = static_cast<const T*>(g.B);
     T* C = static_cast<T*>(g.C);
+    const int s_lo = g.offsets ? g.offsets[e] : 0;
+    const int s_hi = g.offsets ? g.offsets[e + 1] : g.fixed;
     if (g.mode == SEG_ROWS) {
-        m_lo = g.offsets[e] + blockIdx.y * SG_BM;
-        m_hi = g.offsets[e + 1];
+        m_lo = s_lo + blockIdx.y * SG_BM;
+        m_hi = s_hi;
         if (m_lo >= m_hi) return;
         k_lo = 0; k_hi = g.K;
         B += (long long)e * g.b_se;
     } else {
         m_lo = blockIdx.y * SG_BM;
         m_hi = g.M;
-        k_lo = g.offsets[e]; k_hi = g.offsets[e + 1];
+        k_lo = s_lo; k_hi = s_hi;
         C += (long long)e * g.c_se;
     }
     const int n0 = blockIdx.x * SG_BN;
@@ -96,12 +100,13 @@ __global__ void __launch_bounds__(256) simt_seg_gemm_kernel(SimtGemm g)
     }
 }
 
-// act = silu(h)  or  silu(g) * u, on rows [0, offsets[E])
+// act = silu(h)  or  silu(g) * u, on rows [0, offsets[E]) (or [0, rows) without offsets)
 template <typename T>
 __global__ void act_fwd_kernel(const T* __restrict__ h0, const T* __restrict__ h1, T* __restrict__ act,
-                               const int32_t* __restrict__ offsets, int E, int f, int swiglu)
+                               const int32_t* __restrict__ offsets, int E, int rows, int f,
+                               int swiglu)
 {
-    const long long n = (long long)offsets[E] * f;
+    const long long n = (long long)(offsets ? offsets[E] : rows) * f;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         float z = to_f<T>(h0[i]);
@@ -115,9 +120,10 @@ __global__ void act_fwd_kernel(const T* __restrict__ h0, const T* __restrict__ h
 // SwiGLU: dg = dact * u * silu'(g), du = dact * silu(g)   (dact held in dh1)
 template <typename T>
 __global__ void act_bwd_kernel(const T* __restrict__ h0, const T* __restrict__ h1, T* dh0, T* dh1,
-                               const int32_t* __restrict__ offsets, int E, int f, int swiglu)
+                               const int32_t* __restrict__ offsets, int E, int rows, int f,
+                               int swiglu)
 {
-    const long long n = (long long)offsets[E] * f;
+    const long long n = (long long)(offsets ? offsets[E] : rows) * f;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         const float z = to_f<T>(h0[i]);
@@ -145,9 +151,10 @@ int simt_gemm(const SimtGemm& g, int E, int max_seg_rows, cudaStream_t st)
 
 SimtGemm rows_gemm(const void* A, long long lda, const void* B, long long b_sn, long long b_sk,
                    long long b_se, void* C, long long ldc, int N, int K, const int32_t* off,
-                   int accumulate)
+                   int accumulate, int fixed = 0)
 {
     SimtGemm g{};
+    g.fixed = fixed;
     g.A = A; g.a_sm = lda; g.a_sk = 1;
     g.B = B; g.b_sn = b_sn; g.b_sk = b_sk; g.b_se = b_se;
     g.C = C; g.c_sm = ldc; g.c_sn = 1; g.c_se = 0;
@@ -157,9 +164,10 @@ SimtGemm rows_gemm(const void* A, long long lda, const void* B, long long b_sn, 
 
 // dW[e][m][n] = sum_{rows r of e} A[r][m] B[r][n]
 SimtGemm wgrad_gemm(const void* A, long long lda, const void* B, long long ldb, void* C, int M,
-                    int N, const int32_t* off)
+                    int N, const int32_t* off, int fixed = 0)
 {
     SimtGemm g{};
+    g.fixed = fixed;
     g.A = A; g.a_sm = 1; g.a_sk = lda;
     g.B = B; g.b_sn = 1; g.b_sk = ldb; g.b_se = 0;
     g.C = C; g.c_sm = N; g.c_sn = 1; g.c_se = (long long)M * N;
@@ -171,10 +179,10 @@ int max_seg_rows(const moe_config& c) {
     return std::min(c.T, capacity_of(c)) + c.pad_m - 1;
 }
 
-int ew_grid(const moe_config& c) {
-    const long long n = rows_cap_of(c) * (long long)c.f;
+int ew_grid(long long n) {
     return (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, num_sms() * 8LL));
 }
+int ew_grid(const moe_config& c) { return ew_grid(rows_cap_of(c) * (long long)c.f); }
 
 int ffn_forward_f32(const moe_config& c, const float* xp, const int32_t* off, const float* Wu,
                     const float* Wg, const float* Wd, float* h, float* act, float* y,
@@ -192,7 +200,7 @@ int ffn_forward_f32(const moe_config& c, const float* xp, const int32_t* off, co
     } else {
         if ((r = simt_gemm<float>(rows_gemm(xp, d, Wu, 1, f, (long long)d * f, h0, f, f, d, off, 0), E, msr, st))) return r;
     }
-    act_fwd_kernel<float><<<ew_grid(c), 256, 0, st>>>(h0, h1, act, off, E, f, sw);
+    act_fwd_kernel<float><<<ew_grid(c), 256, 0, st>>>(h0, h1, act, off, E, 0, f, sw);
     MOE_LAUNCH_CHECK();
     return simt_gemm<float>(rows_gemm(act, f, Wd, 1, d, (long long)f * d, y, d, d, f, off, 0), E, msr, st);
 }
@@ -213,7 +221,7 @@ int ffn_backward_f32(const moe_config& c, const float* xp, const int32_t* off, c
     int r;
     // dact = dy W_down^T   (B(n=j,k=i) = W_down[j][i])
     if ((r = simt_gemm<float>(rows_gemm(dy, d, Wd, d, 1, (long long)f * d, dact, f, f, d, off, 0), E, msr, st))) return r;
-    act_bwd_kernel<float><<<ew_grid(c), 256, 0, st>>>(h0, h1, dh0, dh1, off, E, f, sw);
+    act_bwd_kernel<float><<<ew_grid(c), 256, 0, st>>>(h0, h1, dh0, dh1, off, E, 0, f, sw);
     MOE_LAUNCH_CHECK();
     // weight gradients
     if ((r = simt_gemm<float>(wgrad_gemm(act, f, dy, d, dWd, f, d, off), E, 0, st))) return r;
@@ -231,6 +239,53 @@ int ffn_backward_f32(const moe_config& c, const float* xp, const int32_t* off, c
     return simt_gemm<float>(rows_gemm(dh0, f, Wu, f, 1, (long long)d * f, dxp, d, d, f, off, 0), E, msr, st);
 }
 
+// The shared experts' FFN in fp32: the same GEMMs over one segment of T rows.
+int shared_forward_f32(const moe_config& c, const moe_shared_ffn& s, cudaStream_t st)
+{
+    const int d = c.d, f = c.f_shared, T = c.T;
+    const bool sw = c.ffn == MOE_FFN_SWIGLU;
+    const float* x = static_cast<const float*>(s.x);
+    float* h0 = static_cast<float*>(s.h);
+    float* h1 = sw ? h0 + (long long)T * f : nullptr;
+    float* act = static_cast<float*>(s.act);
+    int r;
+    if (sw) {
+        if ((r = simt_gemm<float>(rows_gemm(x, d, s.W_gate, 1, f, 0, h0, f, f, d, nullptr, 0, T), 1, T, st))) return r;
+        if ((r = simt_gemm<float>(rows_gemm(x, d, s.W_up, 1, f, 0, h1, f, f, d, nullptr, 0, T), 1, T, st))) return r;
+    } else {
+        if ((r = simt_gemm<float>(rows_gemm(x, d, s.W_up, 1, f, 0, h0, f, f, d, nullptr, 0, T), 1, T, st))) return r;
+    }
+    act_fwd_kernel<float><<<ew_grid((long long)T * f), 256, 0, st>>>(h0, h1, act, nullptr, 0, T, f, sw);
+    MOE_LAUNCH_CHECK();
+    return simt_gemm<float>(rows_gemm(act, f, s.W_down, 1, d, 0, s.y, d, d, f, nullptr, 0, T), 1, T, st);
+}
+
+int shared_backward_f32(const moe_config& c, const moe_shared_ffn& s, cudaStream_t st)
+{
+    const int d = c.d, f = c.f_shared, T = c.T;
+    const bool sw = c.ffn == MOE_FFN_SWIGLU;
+    const float* x = static_cast<const float*>(s.x);
+    const float* dy = static_cast<const float*>(s.dout);
+    const float* h0 = static_cast<const float*>(s.h);
+    const float* h1 = sw ? h0 + (long long)T * f : nullptr;
+    float* dh0 = static_cast<float*>(s.dh);
+    float* dh1 = sw ? dh0 + (long long)T * f : nullptr;
+    float* dact = sw ? dh1 : dh0;
+    int r;
+    if ((r = simt_gemm<float>(rows_gemm(dy, d, s.W_down, d, 1, 0, dact, f, f, d, nullptr, 0, T), 1, T, st))) return r;
+    act_bwd_kernel<float><<<ew_grid((long long)T * f), 256, 0, st>>>(h0, h1, dh0, dh1, nullptr, 0, T, f, sw);
+    MOE_LAUNCH_CHECK();
+    if ((r = simt_gemm<float>(wgrad_gemm(s.act, f, dy, d, s.dW_down, f, d, nullptr, T), 1, 0, st))) return r;
+    if (sw) {
+        if ((r = simt_gemm<float>(wgrad_gemm(x, d, dh1, f, s.dW_up, d, f, nullptr, T), 1, 0, st))) return r;
+        if ((r = simt_gemm<float>(wgrad_gemm(x, d, dh0, f, s.dW_gate, d, f, nullptr, T), 1, 0, st))) return r;
+        if ((r = simt_gemm<float>(rows_gemm(dh1, f, s.W_up, f, 1, 0, s.dx, d, d, f, nullptr, 0, T), 1, T, st))) return r;
+        return simt_gemm<float>(rows_gemm(dh0, f, s.W_gate, f, 1, 0, s.dx, d, d, f, nullptr, 1, T), 1, T, st);
+    }
+    if ((r = simt_gemm<float>(wgrad_gemm(x, d, dh0, f, s.dW_up, d, f, nullptr, T), 1, 0, st))) return r;
+    return simt_gemm<float>(rows_gemm(dh0, f, s.W_up, f, 1, 0, s.dx, d, d, f, nullptr, 0, T), 1, T, st);
+}
+
 }  // namespace
 
 size_t ffn_ws_bytes(const moe_config& c) {
@@ -239,32 +294,38 @@ size_t ffn_ws_bytes(const moe_config& c) {
 
 int launch_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                        const void* W_up, const void* W_gate, const void* W_down, void* h_saved,
-                       void* act, void* y_perm, void* ws, cudaStream_t st)
+                       void* act, void* y_perm, const moe_shared_ffn* shared, void* ws,
+                       cudaStream_t st)
 {
     if (c.dtype == MOE_DTYPE_BF16)
-        return tc_ffn_forward(c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, y_perm, ws, st);
-    return ffn_forward_f32(c, static_cast<const float*>(x_perm), offsets,
-                           static_cast<const float*>(W_up), static_cast<const float*>(W_gate),
-                           static_cast<const float*>(W_down), static_cast<float*>(h_saved),
-                           static_cast<float*>(act), static_cast<float*>(y_perm), st);
+        return tc_ffn_forward(c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, y_perm,
+                              shared, ws, st);
+    int r = ffn_forward_f32(c, static_cast<const float*>(x_perm), offsets,
+                            static_cast<const float*>(W_up), static_cast<const float*>(W_gate),
+                            static_cast<const float*>(W_down), static_cast<float*>(h_saved),
+                            static_cast<float*>(act), static_cast<float*>(y_perm), st);
+    if (r || !shared) return r;
+    return shared_forward_f32(c, *shared, st);
 }
 
 int launch_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                         const void* W_up, const void* W_gate, const void* W_down,
                         const void* h_saved, const void* act, const void* dy_perm, void* dh,
-                        void* dx_perm, void* dW_up, void* dW_gate, void* dW_down, void* ws,
-                        cudaStream_t st)
+                        void* dx_perm, void* dW_up, void* dW_gate, void* dW_down,
+                        const moe_shared_ffn* shared, void* ws, cudaStream_t st)
 {
     if (c.dtype == MOE_DTYPE_BF16)
         return tc_ffn_backward(c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, dy_perm,
-                               dh, dx_perm, dW_up, dW_gate, dW_down, ws, st);
-    return ffn_backward_f32(c, static_cast<const float*>(x_perm), offsets,
+                               dh, dx_perm, dW_up, dW_gate, dW_down, shared, ws, st);
+    int r = ffn_backward_f32(c, static_cast<const float*>(x_perm), offsets,
                             static_cast<const float*>(W_up), static_cast<const float*>(W_gate),
                             static_cast<const float*>(W_down), static_cast<const float*>(h_saved),
                             static_cast<const float*>(act), static_cast<const float*>(dy_perm),
                             static_cast<float*>(dh), static_cast<float*>(dx_perm),
                             static_cast<float*>(dW_up), static_cast<float*>(dW_gate),
                             static_cast<float*>(dW_down), st);
+    if (r || !shared) return r;
+    return shared_backward_f32(c, *shared, st);
 }
 
 }  // namespace moe

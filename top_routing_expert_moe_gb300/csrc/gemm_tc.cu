@@ -53,7 +53,7 @@ constexpr int BM = 128, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + 256 * BK * 2;  // 48 KB
 constexpr int GUARD_BYTES = 16 * 1024;        // slack after the ring
-constexpr int CTRL_BYTES = 2048;   // barriers, TMEM slot, offsets[65], prefix[3*64+1]
+constexpr int CTRL_BYTES = 3072;   // barriers, TMEM slot, offsets[65], prefix[6*64+1], slot bases
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + GUARD_BYTES + CTRL_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
@@ -64,8 +64,11 @@ enum Epi { EPI_STORE = 0, EPI_SILU_FWD = 1, EPI_SWIGLU_FWD = 2, EPI_SILU_BWD = 3
 enum Sched { SCHED_ROWS = 0, SCHED_KSEG = 1 };
 
 // One GEMM problem of a launch.  A launch runs up to MAX_PROBLEMS independent
-// problems over the same expert segments, their tiles in one schedule (the
-// backward's dgrad2 || dW_down, then dW_up || dW_gate || dgrad1).
+// problems, their tiles in one schedule (the backward's dgrad2 || dW_down, then
+// dW_up || dW_gate || dgrad1, for the routed experts and the shared FFN).
+// A problem either runs over the routed experts' segments (rows taken from
+// the device offsets) or over one fixed segment of fixed_rows rows with
+// expert index 0 (the shared FFN, which every token passes through).
 struct TcProblem {
     CUtensorMap tmA0, tmB0, tmA1, tmB1;
     __nv_bfloat16* out0;
@@ -84,8 +87,9 @@ struct TcProblem {
     int dual;               // two accumulators (B0 -> cols 0..127, B1 -> 128..255)
     int epi;
     int ldo;
+    int fixed_rows;         // > 0: one segment [0, fixed_rows) (a multiple of BM)
 };
-constexpr int MAX_PROBLEMS = 3;
+constexpr int MAX_PROBLEMS = 6;
 
 struct TcParams {
     TcProblem prob[MAX_PROBLEMS];
@@ -93,6 +97,7 @@ struct TcParams {
     int* status;
     int nprob, E;
 };
+static_assert(sizeof(TcParams) <= 4096, "kernel parameters stay within 4 KB");
 
 // mbarrier / TMA / timer helpers: tma.cuh
 
@@ -182,19 +187,23 @@ struct Tile {
 };
 
 __device__ __forceinline__ int seg_m_blocks(const TcProblem& q, const int* offs, int e) {
-    return q.sched == SCHED_ROWS ? (offs[e + 1] - offs[e]) / BM : q.m_blocks;
+    if (q.sched != SCHED_ROWS) return q.m_blocks;
+    return q.fixed_rows ? q.fixed_rows / BM : (offs[e + 1] - offs[e]) / BM;
 }
 
-// prefix[p*E + e] = first tile of (problem p, expert e); prefix[nprob*E] = total.
-// Binary search for the (problem, expert) slot holding tile tix.
+// Slots: problem p's segments (E of them, or 1 for a fixed-rows problem) are
+// slots sbase[p] .. sbase[p+1]-1.  prefix[s] = first tile of slot s;
+// prefix[sbase[nprob]] = total.  Binary search for the slot holding tile tix.
 __device__ __forceinline__ void decode_tile(const TcParams& P, const int* offs, const int* prefix,
-                                            int tix, Tile& t) {
-    int lo = 0, hi = P.nprob * P.E - 1;
+                                            const int* sbase, int tix, Tile& t) {
+    int lo = 0, hi = sbase[P.nprob] - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (prefix[mid] <= tix) lo = mid; else hi = mid - 1;
     }
-    const int pi = lo / P.E, e = lo % P.E;
+    int pi = 0;
+    while (pi + 1 < P.nprob && sbase[pi + 1] <= lo) ++pi;
+    const int e = lo - sbase[pi];
     const TcProblem& q = P.prob[pi];
     const int local = tix - prefix[lo];
     const int mb_e = seg_m_blocks(q, offs, e);
@@ -208,13 +217,13 @@ __device__ __forceinline__ void decode_tile(const TcParams& P, const int* offs, 
     t.e = e;
     t.n0 = nb * q.bn;
     if (q.sched == SCHED_ROWS) {
-        t.m0 = offs[e] + mb * BM;
+        t.m0 = (q.fixed_rows ? 0 : offs[e]) + mb * BM;
         t.krow0 = 0;
         t.nk = q.k_blocks * q.kconcat;
     } else {
         t.m0 = mb * BM;
-        t.krow0 = offs[e];
-        t.nk = (offs[e + 1] - offs[e]) / BK;
+        t.krow0 = q.fixed_rows ? 0 : offs[e];
+        t.nk = (q.fixed_rows ? q.fixed_rows : offs[e + 1] - offs[e]) / BK;
     }
 }
 
@@ -232,7 +241,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* offs = reinterpret_cast<int*>(tmem_slot + 2);  // [E+1] segment offsets
-    int* prefix = offs + 66;                            // [nprob*E+1] first tile of (problem, expert)
+    int* prefix = offs + 66;                            // [slots+1] first tile of each slot
+    int* sbase = prefix + MAX_PROBLEMS * 64 + 4;        // [nprob+1] first slot of each problem
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < P.E + 1) offs[tid] = P.offsets[tid];
+    if (P.offsets && tid < P.E + 1) offs[tid] = P.offsets[tid];
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS));
@@ -259,17 +269,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-        int acc = 0;
-        for (int pi = 0; pi < P.nprob; ++pi)
-            for (int e = 0; e < P.E; ++e) {
-                prefix[pi * P.E + e] = acc;
+        int acc = 0, sl = 0;
+        for (int pi = 0; pi < P.nprob; ++pi) {
+            sbase[pi] = sl;
+            const int nseg = P.prob[pi].fixed_rows ? 1 : P.E;
+            for (int e = 0; e < nseg; ++e, ++sl) {
+                prefix[sl] = acc;
                 acc += seg_m_blocks(P.prob[pi], offs, e) * P.prob[pi].n_blocks;
             }
-        prefix[P.nprob * P.E] = acc;
+        }
+        sbase[P.nprob] = sl;
+        prefix[sl] = acc;
     }
     __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = prefix[P.nprob * P.E];
+    const int total = prefix[sbase[P.nprob]];
     const uint32_t smem0 = smem_u32(base);
 
     if (warp == 0 && lane == 0) {
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         bool ok = true;
         for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x) {
             Tile t;
-            decode_tile(P, offs, prefix, tix, t);
+            decode_tile(P, offs, prefix, sbase, tix, t);
             // per-tile copies of the problem's fields (registers, not re-read after each
             // "memory"-clobbering wait)
             const TcProblem& q = P.prob[t.p];
@@ -338,7 +352,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         bool ok = true;
         for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x, ++tcount) {
             Tile t;
-            decode_tile(P, offs, prefix, tix, t);
+            decode_tile(P, offs, prefix, sbase, tix, t);
             const TcProblem& q = P.prob[t.p];
             const int q_dual = q.dual, q_amn = q.a_mn, q_bmn = q.b_mn;
             const uint32_t idesc = idesc_bf16(BM, q_dual ? 128 : q.bn, q_amn, q_bmn);
@@ -381,7 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         int tcount = 0;
         for (int tix = blockIdx.x; tix < total; tix += gridDim.x, ++tcount) {
             Tile t;
-            decode_tile(P, offs, prefix, tix, t);
+            decode_tile(P, offs, prefix, sbase, tix, t);
             const TcProblem& q = P.prob[t.p];
             const int width = q.dual ? 128 : q.bn;
             const int c_lo = half * (width / 64), c_hi = c_lo + width / 64;  // 32-column chunks
@@ -519,8 +533,9 @@ int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
 // Upper bound of a problem's tile count (grid sizing only; the kernel counts
 // the real tiles from the device offsets).
 int64_t max_tiles(const moe_config& c, const TcProblem& q) {
-    if (q.sched == SCHED_ROWS) return (rows_cap_of(c) / BM) * q.n_blocks;
-    return (int64_t)c.E * q.m_blocks * q.n_blocks;
+    if (q.sched == SCHED_ROWS)
+        return (q.fixed_rows ? q.fixed_rows / BM : rows_cap_of(c) / BM) * q.n_blocks;
+    return (int64_t)(q.fixed_rows ? 1 : c.E) * q.m_blocks * q.n_blocks;
 }
 
 int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* probs, int nprob,
@@ -533,6 +548,7 @@ int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* prob
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
         attr_done[dev] = true;
     }
+    if (nprob < 1 || nprob > MAX_PROBLEMS) return MOE_ERR_INVALID_ARG;
     TcParams P;
     memset(&P, 0, sizeof(P));
     int64_t tiles = 0;
@@ -557,21 +573,35 @@ TcProblem new_problem() {
     return q;
 }
 
+// One family of expert FFNs sharing a row layout: the routed experts (rows of
+// the expert-contiguous layout, segments from the device offsets, E weight
+// blocks) or the shared FFN (rows = tokens, one fixed segment, one block).
+struct Family {
+    const void* x;            // GEMM1 input rows
+    int64_t x_rows;           // rows of x (the tensor map's extent; TMA zero-fills past it)
+    int64_t rows;             // rows of the h / act / y / dh / dx buffers
+    int fixed;                // 0: segments from offsets; else the one segment's rows
+    int E;                    // weight blocks
+    int f;                    // hidden width
+    const void *Wu, *Wg, *Wd;
+};
+
 // Row-segmented problem: C[rows, N] = A[rows, K] (K-major) x B_e (expert weights)
-int rows_problem(TcProblem& q, const moe_config& c, const void* A, int K, int N) {
+int rows_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, int K, int N) {
     q.sched = SCHED_ROWS;
+    q.fixed_rows = F.fixed;
     q.k_blocks = K / BK;
     q.bn = pick_bn(N);
     q.n_blocks = N / q.bn;
     q.ldo = N;
-    return act_map(&q.tmA0, A, rows_cap_of(c), K, false);
+    return act_map(&q.tmA0, A, a_rows, K, false);
 }
 
-// Weight-gradient problem: out_e[M, N] = A_e^T B_e over expert e's rows (both MN-major)
-int wgrad_problem(TcProblem& q, const moe_config& c, const void* A, int M, const void* B, int N,
-                  void* out) {
-    const int64_t rc = rows_cap_of(c);
+// Weight-gradient problem: out_e[M, N] = A_e^T B_e over the segment's rows (both MN-major)
+int wgrad_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, int M,
+                  const void* B, int64_t b_rows, int N, void* out) {
     q.sched = SCHED_KSEG;
+    q.fixed_rows = F.fixed;
     q.a_mn = 1;
     q.b_mn = 1;
     q.bn = pick_bn(N);
@@ -581,8 +611,97 @@ int wgrad_problem(TcProblem& q, const moe_config& c, const void* A, int M, const
     q.out0 = static_cast<__nv_bfloat16*>(out);
     q.ldo = N;
     q.out_estride = (long long)M * N;
-    MOE_TRY(act_map(&q.tmA0, A, rc, M, true));
-    return act_map(&q.tmB0, B, rc, N, true);
+    MOE_TRY(act_map(&q.tmA0, A, a_rows, M, true));
+    return act_map(&q.tmB0, B, b_rows, N, true);
+}
+
+// GEMM1 with the activation fused: h|g,u = x W_up|W_gate; act = silu(h) | silu(g) u
+int gemm1_problem(TcProblem& q, const moe_config& c, const Family& F, void* h, void* act) {
+    using bf = __nv_bfloat16;
+    const int d = c.d, f = F.f;
+    MOE_TRY(rows_problem(q, F, F.x, F.x_rows, d, f));
+    q.b_mn = 1;
+    if (c.ffn == MOE_FFN_SWIGLU) {
+        q.dual = 1;
+        q.bn = 128;
+        q.n_blocks = f / 128;
+        MOE_TRY(weight_map(&q.tmB0, F.Wg, F.E, d, f, true, 0));
+        MOE_TRY(weight_map(&q.tmB1, F.Wu, F.E, d, f, true, 0));
+        q.epi = EPI_SWIGLU_FWD;
+        q.out0 = static_cast<bf*>(h);
+        q.out1 = static_cast<bf*>(h) + F.rows * f;
+        q.out2 = static_cast<bf*>(act);
+    } else {
+        MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, d, f, true, 0));
+        q.epi = EPI_SILU_FWD;
+        q.out0 = static_cast<bf*>(h);
+        q.out1 = static_cast<bf*>(act);
+    }
+    return MOE_OK;
+}
+
+// GEMM2: y = act W_down
+int gemm2_problem(TcProblem& q, const moe_config& c, const Family& F, const void* act, void* y) {
+    MOE_TRY(rows_problem(q, F, act, F.rows, F.f, c.d));
+    q.b_mn = 1;
+    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, F.f, c.d, true, 0));
+    q.epi = EPI_STORE;
+    q.out0 = static_cast<__nv_bfloat16*>(y);
+    return MOE_OK;
+}
+
+// dgrad2 with the activation derivative fused: dact = dy W_down^T -> dh (SiLU) or dg, du (SwiGLU)
+int dgrad2_problem(TcProblem& q, const moe_config& c, const Family& F, const void* dy,
+                   int64_t dy_rows, const void* h, void* dh) {
+    using bf = __nv_bfloat16;
+    const int f = F.f;
+    MOE_TRY(rows_problem(q, F, dy, dy_rows, c.d, f));
+    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, f, c.d, false, q.bn));
+    q.in0 = static_cast<const bf*>(h);
+    q.out0 = static_cast<bf*>(dh);
+    if (c.ffn == MOE_FFN_SWIGLU) {
+        q.epi = EPI_SWIGLU_BWD;
+        q.in1 = static_cast<const bf*>(h) + F.rows * f;
+        q.out1 = static_cast<bf*>(dh) + F.rows * f;
+    } else {
+        q.epi = EPI_SILU_BWD;
+    }
+    return MOE_OK;
+}
+
+// dgrad1: dx = dh W_up^T  (SwiGLU: du W_up^T + dg W_gate^T, one K loop over both)
+int dgrad1_problem(TcProblem& q, const moe_config& c, const Family& F, const void* dh, void* dx) {
+    using bf = __nv_bfloat16;
+    const bool sw = c.ffn == MOE_FFN_SWIGLU;
+    const bf* dh0 = static_cast<const bf*>(dh);
+    const bf* dh1 = sw ? dh0 + F.rows * F.f : nullptr;
+    MOE_TRY(rows_problem(q, F, sw ? dh1 : dh0, F.rows, F.f, c.d));
+    MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, c.d, F.f, false, q.bn));
+    if (sw) {
+        q.kconcat = 2;
+        MOE_TRY(act_map(&q.tmA1, dh0, F.rows, F.f, false));
+        MOE_TRY(weight_map(&q.tmB1, F.Wg, F.E, c.d, F.f, false, q.bn));
+    }
+    q.epi = EPI_STORE;
+    q.out0 = static_cast<bf*>(dx);
+    return MOE_OK;
+}
+
+// weight gradients: dW_down = act^T dy; dW_up = x^T dh (du); dW_gate = x^T dg
+int wgrads_down(TcProblem& q, const moe_config& c, const Family& F, const void* act,
+                const void* dy, int64_t dy_rows, void* dWd) {
+    return wgrad_problem(q, F, act, F.rows, F.f, dy, dy_rows, c.d, dWd);
+}
+
+Family routed_family(const moe_config& c, const void* x_perm, const void* Wu, const void* Wg,
+                     const void* Wd) {
+    const int64_t rc = rows_cap_of(c);
+    return Family{x_perm, rc, rc, 0, c.E, c.f, Wu, Wg, Wd};
+}
+
+Family shared_family(const moe_config& c, const moe_shared_ffn& s) {
+    const int64_t ts = shared_rows_of(c);
+    return Family{s.x, c.T, ts, (int)ts, 1, c.f_shared, s.W_up, s.W_gate, s.W_down};
 }
 
 }  // namespace
@@ -591,98 +710,69 @@ size_t tc_ws_bytes(const moe_config&) { return 0; }
 
 int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                    const void* W_up, const void* W_gate, const void* W_down, void* h_saved,
-                   void* act, void* y_perm, void*, cudaStream_t st)
+                   void* act, void* y_perm, const moe_shared_ffn* sh, void*, cudaStream_t st)
 {
-    using bf = __nv_bfloat16;
-    const int64_t rc = rows_cap_of(c);
-    const int d = c.d, f = c.f, E = c.E;
-    // GEMM1 (+ activation)
-    {
-        TcProblem q = new_problem();
-        MOE_TRY(rows_problem(q, c, x_perm, d, f));
-        q.b_mn = 1;
-        if (c.ffn == MOE_FFN_SWIGLU) {
-            q.dual = 1;
-            q.bn = 128;
-            q.n_blocks = f / 128;
-            MOE_TRY(weight_map(&q.tmB0, W_gate, E, d, f, true, 0));
-            MOE_TRY(weight_map(&q.tmB1, W_up, E, d, f, true, 0));
-            q.epi = EPI_SWIGLU_FWD;
-            q.out0 = static_cast<bf*>(h_saved);
-            q.out1 = static_cast<bf*>(h_saved) + rc * f;
-            q.out2 = static_cast<bf*>(act);
-        } else {
-            MOE_TRY(weight_map(&q.tmB0, W_up, E, d, f, true, 0));
-            q.epi = EPI_SILU_FWD;
-            q.out0 = static_cast<bf*>(h_saved);
-            q.out1 = static_cast<bf*>(act);
-        }
-        MOE_TRY(launch_tc(c, offsets, &q, 1, st));
+    const Family R = routed_family(c, x_perm, W_up, W_gate, W_down);
+    TcProblem q[2];
+    // GEMM1 (+ activation), routed experts || shared FFN
+    q[0] = new_problem();
+    MOE_TRY(gemm1_problem(q[0], c, R, h_saved, act));
+    if (sh) {
+        q[1] = new_problem();
+        MOE_TRY(gemm1_problem(q[1], c, shared_family(c, *sh), sh->h, sh->act));
     }
+    MOE_TRY(launch_tc(c, offsets, q, sh ? 2 : 1, st));
     // GEMM2
-    {
-        TcProblem q = new_problem();
-        MOE_TRY(rows_problem(q, c, act, f, d));
-        q.b_mn = 1;
-        MOE_TRY(weight_map(&q.tmB0, W_down, E, f, d, true, 0));
-        q.epi = EPI_STORE;
-        q.out0 = static_cast<bf*>(y_perm);
-        MOE_TRY(launch_tc(c, offsets, &q, 1, st));
+    q[0] = new_problem();
+    MOE_TRY(gemm2_problem(q[0], c, R, act, y_perm));
+    if (sh) {
+        q[1] = new_problem();
+        MOE_TRY(gemm2_problem(q[1], c, shared_family(c, *sh), sh->act, sh->y));
     }
-    return MOE_OK;
+    return launch_tc(c, offsets, q, sh ? 2 : 1, st);
 }
 
 int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                     const void* W_up, const void* W_gate, const void* W_down,
                     const void* h_saved, const void* act, const void* dy_perm, void* dh,
-                    void* dx_perm, void* dW_up, void* dW_gate, void* dW_down, void*, cudaStream_t st)
+                    void* dx_perm, void* dW_up, void* dW_gate, void* dW_down,
+                    const moe_shared_ffn* sh, void*, cudaStream_t st)
 {
     using bf = __nv_bfloat16;
-    const int64_t rc = rows_cap_of(c);
-    const int d = c.d, f = c.f, E = c.E;
     const bool sw = c.ffn == MOE_FFN_SWIGLU;
-    bf* dh0 = static_cast<bf*>(dh);                          // dh (SiLU) or dg (SwiGLU)
-    bf* dh1 = sw ? static_cast<bf*>(dh) + rc * f : nullptr;  // du (SwiGLU)
-    const bf* h0 = static_cast<const bf*>(h_saved);
-    const bf* h1 = sw ? h0 + rc * f : nullptr;
+    const Family R = routed_family(c, x_perm, W_up, W_gate, W_down);
     TcProblem q[MAX_PROBLEMS];
-    // launch 1: dact = dy W_down^T with the activation derivative fused  ||  dW_down = act^T dy
-    q[0] = new_problem();
-    MOE_TRY(rows_problem(q[0], c, dy_perm, d, f));
-    MOE_TRY(weight_map(&q[0].tmB0, W_down, E, f, d, false, q[0].bn));
-    q[0].in0 = h0;
-    q[0].out0 = dh0;
-    if (sw) {
-        q[0].epi = EPI_SWIGLU_BWD;
-        q[0].in1 = h1;
-        q[0].out1 = dh1;
-    } else {
-        q[0].epi = EPI_SILU_BWD;
-    }
-    q[1] = new_problem();
-    MOE_TRY(wgrad_problem(q[1], c, act, f, dy_perm, d, dW_down));
-    MOE_TRY(launch_tc(c, offsets, q, 2, st));
-    // launch 2: dW_up = x^T dh (du)  ||  [dW_gate = x^T dg]  ||  dx_perm = dh W_up^T (+ dg W_gate^T)
     int n = 0;
+    // launch 1: dact = dy W_down^T with the activation derivative fused  ||  dW_down = act^T dy
+    // (the shared FFN's dy is the layer's output gradient: it joins with weight 1)
     q[n] = new_problem();
-    MOE_TRY(wgrad_problem(q[n], c, x_perm, d, sw ? dh1 : dh0, f, dW_up));
-    ++n;
-    if (sw) {
+    MOE_TRY(dgrad2_problem(q[n++], c, R, dy_perm, R.rows, h_saved, dh));
+    q[n] = new_problem();
+    MOE_TRY(wgrads_down(q[n++], c, R, act, dy_perm, R.rows, dW_down));
+    if (sh) {
+        const Family S = shared_family(c, *sh);
         q[n] = new_problem();
-        MOE_TRY(wgrad_problem(q[n], c, x_perm, d, dh0, f, dW_gate));
-        ++n;
+        MOE_TRY(dgrad2_problem(q[n++], c, S, sh->dout, c.T, sh->h, sh->dh));
+        q[n] = new_problem();
+        MOE_TRY(wgrads_down(q[n++], c, S, sh->act, sh->dout, c.T, sh->dW_down));
     }
-    q[n] = new_problem();
-    MOE_TRY(rows_problem(q[n], c, sw ? dh1 : dh0, f, d));
-    MOE_TRY(weight_map(&q[n].tmB0, W_up, E, d, f, false, q[n].bn));
-    if (sw) {
-        q[n].kconcat = 2;
-        MOE_TRY(act_map(&q[n].tmA1, dh0, rc, f, false));
-        MOE_TRY(weight_map(&q[n].tmB1, W_gate, E, d, f, false, q[n].bn));
-    }
-    q[n].epi = EPI_STORE;
-    q[n].out0 = static_cast<bf*>(dx_perm);
-    ++n;
+    MOE_TRY(launch_tc(c, offsets, q, n, st));
+    // launch 2: dW_up = x^T dh (du)  ||  [dW_gate = x^T dg]  ||  dx = dh W_up^T (+ dg W_gate^T)
+    n = 0;
+    auto second = [&](const Family& F, const void* dhF, void* dWu, void* dWg, void* dx) -> int {
+        const bf* dh0 = static_cast<const bf*>(dhF);
+        const bf* dh1 = sw ? dh0 + F.rows * F.f : nullptr;
+        q[n] = new_problem();
+        MOE_TRY(wgrad_problem(q[n++], F, F.x, F.x_rows, c.d, sw ? dh1 : dh0, F.rows, F.f, dWu));
+        if (sw) {
+            q[n] = new_problem();
+            MOE_TRY(wgrad_problem(q[n++], F, F.x, F.x_rows, c.d, dh0, F.rows, F.f, dWg));
+        }
+        q[n] = new_problem();
+        return dgrad1_problem(q[n++], c, F, dhF, dx);
+    };
+    MOE_TRY(second(R, dh, dW_up, dW_gate, dx_perm));
+    if (sh) MOE_TRY(second(shared_family(c, *sh), sh->dh, sh->dW_up, sh->dW_gate, sh->dx));
     return launch_tc(c, offsets, q, n, st);
 }
 

@@ -60,6 +60,11 @@ int64_t rows_cap_of(const moe_config& c) {
     return (a < b ? a : b) + (int64_t)c.E * (c.pad_m - 1);
 }
 
+int64_t shared_rows_of(const moe_config& c) {
+    if (c.f_shared <= 0) return 0;
+    return c.dtype == MOE_DTYPE_BF16 ? ((int64_t)c.T + 127) / 128 * 128 : (int64_t)c.T;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -72,12 +77,38 @@ bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
 size_t esize(const moe_config& c) { return c.dtype == MOE_DTYPE_BF16 ? 2 : 4; }
 int nh_of(const moe_config& c) { return c.ffn == MOE_FFN_SWIGLU ? 2 : 1; }
 
+// The shared-experts block: present iff f_shared > 0; the fields each entry
+// point uses must be set and 16-byte aligned.
+enum SharedUse { SH_FWD, SH_COMBINE, SH_BWD, SH_ROUTER_BWD };
+bool shared_ok(const moe_config& c, const moe_shared_ffn* s, SharedUse use) {
+    if (c.f_shared <= 0) return s == nullptr;
+    if (!s) return false;
+    const bool sw = c.ffn == MOE_FFN_SWIGLU;
+    switch (use) {
+        case SH_FWD:
+            return ok_ptr(s->x) && ok_ptr(s->W_up) && ok_ptr(s->W_down) &&
+                   (sw ? ok_ptr(s->W_gate) : ok_opt(s->W_gate)) && ok_ptr(s->h) &&
+                   ok_ptr(s->act) && ok_ptr(s->y);
+        case SH_COMBINE:
+            return ok_ptr(s->y);
+        case SH_BWD:
+            return ok_ptr(s->x) && ok_ptr(s->W_up) && ok_ptr(s->W_down) &&
+                   (sw ? ok_ptr(s->W_gate) : ok_opt(s->W_gate)) && ok_ptr(s->h) &&
+                   ok_ptr(s->act) && ok_ptr(s->dout) && ok_ptr(s->dh) && ok_ptr(s->dx) &&
+                   ok_ptr(s->dW_up) && (sw ? ok_ptr(s->dW_gate) : ok_opt(s->dW_gate)) &&
+                   ok_ptr(s->dW_down);
+        case SH_ROUTER_BWD:
+            return ok_ptr(s->dx);
+    }
+    return false;
+}
+
 // intermediate buffers of moe_backward, carved from the workspace
 struct BwdLayout {
-    size_t dy, dgate, dh, dxp, dlogits, rest, total;
+    size_t dy, dgate, dh, dxp, dlogits, sdh, sdx, rest, total;
 };
 BwdLayout bwd_layout(const moe_config& c) {
-    const size_t rc = (size_t)rows_cap_of(c), es = esize(c);
+    const size_t rc = (size_t)rows_cap_of(c), es = esize(c), ts = (size_t)shared_rows_of(c);
     BwdLayout L;
     size_t o = 0;
     L.dy = o; o += align_up(rc * c.d * es);
@@ -85,6 +116,8 @@ BwdLayout bwd_layout(const moe_config& c) {
     L.dh = o; o += align_up((size_t)nh_of(c) * rc * c.f * es);
     L.dxp = o; o += align_up(rc * c.d * es);
     L.dlogits = o; o += align_up((size_t)c.T * c.E * 4);
+    L.sdh = o; o += align_up((size_t)nh_of(c) * ts * (c.f_shared > 0 ? c.f_shared : 0) * es);
+    L.sdx = o; o += align_up(ts * c.d * es);
     L.rest = o;
     size_t r = ffn_ws_bytes(c);
     size_t rb = router_bwd_ws_bytes(c);
@@ -108,6 +141,9 @@ int moe_check_config(const moe_config* c) {
     if (!std::isfinite(c->aux_coef)) return MOE_ERR_INVALID_ARG;
     if (!std::isfinite(c->temperature) || c->temperature < 0.0f) return MOE_ERR_INVALID_ARG;
     if (c->straight_through != 0 && c->straight_through != 1) return MOE_ERR_INVALID_ARG;
+    if (c->f_shared < 0) return MOE_ERR_INVALID_ARG;
+    if (c->f_shared % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (c->dtype == MOE_DTYPE_BF16 && c->f_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (c->E > 64 || c->k > 8) return MOE_ERR_UNSUPPORTED;
     if (c->d % 8 != 0 || c->f % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (c->dtype == MOE_DTYPE_BF16 && (c->d % 128 != 0 || c->f % 128 != 0 || c->pad_m % 128 != 0))
@@ -132,6 +168,14 @@ int moe_rows_capacity(const moe_config* c, int64_t* rows) {
     if (r) return r;
     if (!rows) return MOE_ERR_INVALID_ARG;
     *rows = rows_cap_of(*c);
+    return MOE_OK;
+}
+
+int moe_shared_rows(const moe_config* c, int64_t* rows) {
+    int r = moe_check_config(c);
+    if (r) return r;
+    if (!rows) return MOE_ERR_INVALID_ARG;
+    *rows = shared_rows_of(*c);
     return MOE_OK;
 }
 
@@ -175,25 +219,29 @@ int moe_permute(const moe_config* c, const void* x, const int32_t* topk_idx, voi
 
 int moe_grouped_ffn(const moe_config* c, const void* x_perm, const int32_t* offsets,
                     const void* W_up, const void* W_gate, const void* W_down, void* h_saved,
-                    void* act, void* y_perm, void* ws, moe_stream_t stream) {
+                    void* act, void* y_perm, const moe_shared_ffn* shared, void* ws,
+                    moe_stream_t stream) {
     int r = moe_check_config(c);
     if (r) return r;
     const bool sw = c->ffn == MOE_FFN_SWIGLU;
     if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(W_up) || !ok_ptr(W_down) ||
         (sw ? !ok_ptr(W_gate) : !ok_opt(W_gate)) || !ok_ptr(h_saved) || !ok_ptr(act) ||
-        !ok_ptr(y_perm) || !ok_opt(ws))
+        !ok_ptr(y_perm) || !ok_opt(ws) || !shared_ok(*c, shared, SH_FWD))
         return MOE_ERR_INVALID_ARG;
     if (ffn_ws_bytes(*c) > 0 && !ws) return MOE_ERR_INVALID_ARG;
-    return launch_ffn_forward(*c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, y_perm, ws,
-                              (cudaStream_t)stream);
+    return launch_ffn_forward(*c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, y_perm,
+                              shared, ws, (cudaStream_t)stream);
 }
 
 int moe_combine(const moe_config* c, const void* y_perm, const int32_t* slot_of, const float* gate,
-                void* out, moe_stream_t stream) {
+                const moe_shared_ffn* shared, void* out, moe_stream_t stream) {
     int r = moe_check_config(c);
     if (r) return r;
-    if (!ok_ptr(y_perm) || !ok_ptr(slot_of) || !ok_ptr(gate) || !ok_ptr(out)) return MOE_ERR_INVALID_ARG;
-    return launch_combine(*c, y_perm, slot_of, gate, out, (cudaStream_t)stream);
+    if (!ok_ptr(y_perm) || !ok_ptr(slot_of) || !ok_ptr(gate) || !ok_ptr(out) ||
+        !shared_ok(*c, shared, SH_COMBINE))
+        return MOE_ERR_INVALID_ARG;
+    return launch_combine(*c, y_perm, slot_of, gate, shared ? shared->y : nullptr, out,
+                          (cudaStream_t)stream);
 }
 
 int moe_combine_backward(const moe_config* c, const void* dout, const void* y_perm,
@@ -211,34 +259,38 @@ int moe_combine_backward(const moe_config* c, const void* dout, const void* y_pe
 int moe_grouped_ffn_backward(const moe_config* c, const void* x_perm, const int32_t* offsets,
                              const void* W_up, const void* W_gate, const void* W_down,
                              const void* h_saved, const void* act, const void* dy_perm, void* dh,
-                             void* dx_perm, void* dW_up, void* dW_gate, void* dW_down, void* ws,
-                             moe_stream_t stream) {
+                             void* dx_perm, void* dW_up, void* dW_gate, void* dW_down,
+                             const moe_shared_ffn* shared, void* ws, moe_stream_t stream) {
     int r = moe_check_config(c);
     if (r) return r;
     const bool sw = c->ffn == MOE_FFN_SWIGLU;
     if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(W_up) || !ok_ptr(W_down) ||
         (sw ? !ok_ptr(W_gate) : !ok_opt(W_gate)) || !ok_ptr(h_saved) || !ok_ptr(act) ||
         !ok_ptr(dy_perm) || !ok_ptr(dh) || !ok_ptr(dx_perm) || !ok_ptr(dW_up) ||
-        (sw ? !ok_ptr(dW_gate) : !ok_opt(dW_gate)) || !ok_ptr(dW_down) || !ok_opt(ws))
+        (sw ? !ok_ptr(dW_gate) : !ok_opt(dW_gate)) || !ok_ptr(dW_down) || !ok_opt(ws) ||
+        !shared_ok(*c, shared, SH_BWD))
         return MOE_ERR_INVALID_ARG;
     if (ffn_ws_bytes(*c) > 0 && !ws) return MOE_ERR_INVALID_ARG;
     return launch_ffn_backward(*c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, dy_perm, dh,
-                               dx_perm, dW_up, dW_gate, dW_down, ws, (cudaStream_t)stream);
+                               dx_perm, dW_up, dW_gate, dW_down, shared, ws, (cudaStream_t)stream);
 }
 
 int moe_router_backward(const moe_config* c, const void* x, const void* W_r, const float* logits,
                         const int32_t* topk_idx, const float* gate, const int32_t* slot_of,
-                        const float* dgate, const void* dx_perm, const float* stats, void* dx,
-                        void* dW_r, float* dbias, float* dlogits, void* ws, moe_stream_t stream) {
+                        const float* dgate, const void* dx_perm, const moe_shared_ffn* shared,
+                        const float* stats, void* dx, void* dW_r, float* dbias, float* dlogits,
+                        void* ws, moe_stream_t stream) {
     int r = moe_check_config(c);
     if (r) return r;
     if (!ok_ptr(x) || !ok_ptr(W_r) || !ok_ptr(logits) || !ok_ptr(topk_idx) || !ok_ptr(gate) ||
         !ok_ptr(slot_of) || !ok_ptr(dgate) || !ok_ptr(dx_perm) || !ok_opt(stats) || !ok_ptr(dx) ||
-        !ok_ptr(dW_r) || !ok_opt(dbias) || !ok_opt(dlogits) || !ok_ptr(ws))
+        !ok_ptr(dW_r) || !ok_opt(dbias) || !ok_opt(dlogits) || !ok_ptr(ws) ||
+        !shared_ok(*c, shared, SH_ROUTER_BWD))
         return MOE_ERR_INVALID_ARG;
     if (c->aux_coef != 0.0f && !stats) return MOE_ERR_INVALID_ARG;
     return launch_router_backward(*c, x, W_r, logits, topk_idx, gate, slot_of, dgate, dx_perm,
-                                  stats, dx, dW_r, dbias, dlogits, ws, (cudaStream_t)stream);
+                                  shared ? shared->dx : nullptr, stats, dx, dW_r, dbias, dlogits,
+                                  ws, (cudaStream_t)stream);
 }
 
 int moe_backward(const moe_config* c, const void* x, const void* W_r, const void* W_up,
@@ -247,10 +299,11 @@ int moe_backward(const moe_config* c, const void* x, const void* W_r, const void
                  const int32_t* perm_token, const int32_t* offsets, const void* x_perm,
                  const void* h_saved, const void* act, const void* y_perm, const float* stats,
                  const void* dout, void* dx, void* dW_r, float* dbias, void* dW_up, void* dW_gate,
-                 void* dW_down, void* ws, moe_stream_t stream) {
+                 void* dW_down, const moe_shared_ffn* shared, void* ws, moe_stream_t stream) {
     int r = moe_check_config(c);
     if (r) return r;
     if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+    if ((c->f_shared > 0) != (shared != nullptr)) return MOE_ERR_INVALID_ARG;
     const BwdLayout L = bwd_layout(*c);
     uint8_t* w = static_cast<uint8_t*>(ws);
     void* dy = w + L.dy;
@@ -259,13 +312,21 @@ int moe_backward(const moe_config* c, const void* x, const void* W_r, const void
     void* dxp = w + L.dxp;
     float* dlogits = reinterpret_cast<float*>(w + L.dlogits);
     void* rest = w + L.rest;
+    moe_shared_ffn sh;
+    if (shared) {                     // the shared FFN's dy is the layer's dout (weight 1)
+        sh = *shared;
+        sh.dout = dout;
+        if (!sh.dh) sh.dh = w + L.sdh;
+        if (!sh.dx) sh.dx = w + L.sdx;
+    }
+    const moe_shared_ffn* shp = shared ? &sh : nullptr;
     if ((r = moe_combine_backward(c, dout, y_perm, gate, slot_of, perm_token, offsets, dy, dgate, stream)))
         return r;
     if ((r = moe_grouped_ffn_backward(c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, dy, dh,
-                                      dxp, dW_up, dW_gate, dW_down, rest, stream)))
+                                      dxp, dW_up, dW_gate, dW_down, shp, rest, stream)))
         return r;
-    return moe_router_backward(c, x, W_r, logits, topk_idx, gate, slot_of, dgate, dxp, stats, dx,
-                               dW_r, dbias, dlogits, rest, stream);
+    return moe_router_backward(c, x, W_r, logits, topk_idx, gate, slot_of, dgate, dxp, shp, stats,
+                               dx, dW_r, dbias, dlogits, rest, stream);
 }
 
 const char* moe_error_string(int code) {

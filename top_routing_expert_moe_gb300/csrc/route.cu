@@ -22,8 +22,6 @@ namespace {
 
 constexpr int RT_TOK = 128;      // tokens per CTA
 constexpr int RT_BK = 64;        // k-chunk (elements)
-constexpr int RT_LDS = RT_BK + 8;  // smem row stride (bf16 elements), conflict-free
-constexpr int RT_STAGES = 4;
 
 struct RouteOut {
     int T, d, E, k, normalize;
@@ -41,10 +39,6 @@ struct RouteOut {
     int32_t* part_bad;     // [nblk]
     int32_t* part_real;    // [nblk] routed (unmasked) tokens
 };
-
-// barrier among the 256 threads (warps 0-7) that compute the router; a
-// producer warp, when present, does not take part
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // a ranks above b: larger logit; a NaN ranks below any number; then lower id
 __device__ __forceinline__ bool ranks_above(float la, int a, float lb, int b) {
@@ -191,15 +185,6 @@ __device__ __forceinline__ void finish_tile(float* sLog, int ldl, int* sSel, flo
     else if (G >= 2) finish_tile_seg<2>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
     else finish_tile_seg<1>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
 }
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
-    uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-    int n = pred ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
 // W_r [d,E] bf16 -> WrT [E_pad, d] bf16 (zero rows for e >= E)
 __global__ void transpose_router_kernel(const __nv_bfloat16* __restrict__ Wr,
@@ -646,7 +631,6 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
         transpose_router_kernel<<<64, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(Wr), WrT,
                                                     c.d, c.E, e_pad);
         MOE_LAUNCH_CHECK();
-        const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
         const int key = (e_pad / 8) * 1000 + tt;
         int r = MOE_OK;
         switch (key) {
