@@ -1,17 +1,23 @@
 // route.cu -- router GEMM + softmax + top-k + gates + per-expert statistics.
 //
 // [LLaMA4-MoE] §2.4: a linear router with softmax scores over the experts,
-// a [B,K] top-K index, outputs weighted by the post-softmax score.
-// [ZeRO3-MoE] §5.3: gating in fp32 even for half-precision models.
+// a [B,K] top-K index, outputs weighted by the post-softmax score; §3.2 gate
+// noise; §4.1 padding tokens kept out of expert selection.  [ZeRO3-MoE] §5.3:
+// gating in fp32 even for half-precision models.  [Twinkle] §3.1: softmax with
+// a temperature, and Gumbel top-k with a straight-through estimator.
 //
-// bf16: one CTA per TT tokens (16..128, chosen so the grid covers the GPU),
-// 8 warps splitting each stage's 128 rows into (k-slice, 16 tokens); the x
-// tile streams through a 4-stage cp.async ring (HBM-bound: x is read once);
-// the router contraction runs on the tensor cores (mma.sync m16n8k16, fp32
-// accumulate) so that the E flops/byte never throttle the HBM stream.  The
-// logits tile lands in shared memory and one thread per token finishes the
-// row: bias, noise, softmax, top-k, gates.  Per-CTA partial statistics are
+// bf16: a persistent CTA per SM walks tiles of TT tokens (16..64, the largest
+// that still gives every SM a tile).  Warp 8 streams x (and the transposed
+// router weights) with TMA into a ring of 128-row stages (mbarrier transaction
+// counts); warps 0-7 split each stage's rows into (k-slice, 16 tokens) and run
+// the router contraction on the tensor cores (mma.sync m16n8k16, fp32
+// accumulate), so the E flops/byte never throttle the HBM stream; warps 9-12
+// take the finished logit tile (double-buffered, so the next tile's loads and
+// MMAs overlap) and finish it with G lanes per token: bias, noise, softmax of
+// logits / tau, top-k, gates, entropy.  Per-tile partial statistics are
 // reduced in a fixed order by a one-CTA finalize kernel (deterministic).
+// fp32: plain FMA over 128-token tiles (k-chunks staged in shared memory),
+// finished by the same per-token code.
 #include "common.cuh"
 #include "kernels.h"
 #include "tma.cuh"
