@@ -14,10 +14,11 @@
 // accumulate), so the E flops/byte never throttle the HBM stream; warps 9-12
 // take the finished logit tile (double-buffered, so the next tile's loads and
 // MMAs overlap) and finish it with G lanes per token: bias, noise, softmax of
-// logits / tau, top-k, gates, entropy.  Per-tile partial statistics are
-// reduced in a fixed order by a one-CTA finalize kernel (deterministic).
+// logits / tau, top-k, gates, entropy.  Each CTA sums its tiles' statistics;
+// the last CTA to finish (an atomic ticket) reduces all CTAs' sums in CTA
+// order (deterministic), so no separate reduction launch follows.
 // fp32: plain FMA over 128-token tiles (k-chunks staged in shared memory),
-// finished by the same per-token code.
+// finished by the same per-token code, then a one-CTA reduction kernel.
 #include "common.cuh"
 #include "kernels.h"
 #include "tma.cuh"
@@ -44,6 +45,9 @@ struct RouteOut {
     float* part_ent;       // [nblk]
     int32_t* part_bad;     // [nblk]
     int32_t* part_real;    // [nblk] routed (unmasked) tokens
+    int* ticket;           // CTAs done (zeroed before the bf16 kernel); the last one reduces
+    int32_t* counts;       // [E] selections per expert (bf16 kernel's last CTA writes)
+    float* stats;          // statistics vector or NULL (idem)
 };
 
 // a ranks above b: larger logit; a NaN ranks below any number; then lower id
@@ -63,11 +67,15 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 // (a power of two, at most 32) work on one token: each lane takes experts
 // e = sub, sub + G, ..., and the lanes combine the row's max, sums, entropy
 // and each top-k pick with butterfly shuffles (exact, fixed order).  Then
-// fixed-order column sums give the tile's partial statistics (index pidx).
+// fixed-order column sums give the tile's partial statistics: written to the
+// partials at index pidx, or, when acc (shared memory, ACC_FLOATS words) is
+// given, added to the running sums of this CTA's tiles.
+constexpr int ACC_FLOATS = 64 + 64 + 4;   // psum[64], counts[64] (int), h, bad (int), real (int)
+
 template <int G>
 __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, int* sBad, int t0,
                                 int ntok, int TT, int pidx, const RouteOut& o, int i, int nthr,
-                                int bar_id)
+                                int bar_id, float* acc)
 {
     const int E = o.E, k = o.k;
     const int sub = i % G, per_pass = nthr / G;
@@ -160,42 +168,178 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
         }
     }
     named_sync(bar_id, nthr);
-    for (int e = i; e < E; e += nthr) {
+    // The tile's per-expert column sums (probabilities, selections): R lanes of
+    // one warp per expert, each over rows r, r + R, ..., then a shuffle tree
+    // (a fixed order: deterministic).  nthr is a multiple of 32.
+    {
+        int R = 32;
+        while (R > 1 && R * E > nthr) R >>= 1;
+        const int e = i / R, r = i % R;
         float ps = 0.f;
         int cnt = 0;
-        for (int r = 0; r < ntok; ++r) {
-            ps += sLog[r * ldl + e];
-            for (int j = 0; j < k; ++j) cnt += (sSel[r * k + j] == e);
+        if (e < E)
+            for (int row = r; row < ntok; row += R) {
+                ps += sLog[row * ldl + e];
+                for (int j = 0; j < k; ++j) cnt += (sSel[row * k + j] == e);
+            }
+        for (int off = R / 2; off > 0; off >>= 1) {
+            ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
         }
-        o.part_psum[(size_t)pidx * E + e] = ps;
-        o.part_counts[(size_t)pidx * E + e] = cnt;
+        if (e < E && r == 0) {
+            if (acc) {
+                acc[e] += ps;
+                reinterpret_cast<int*>(acc + 64)[e] += cnt;
+            } else {
+                o.part_psum[(size_t)pidx * E + e] = ps;
+                o.part_counts[(size_t)pidx * E + e] = cnt;
+            }
+        }
     }
-    if (i == nthr - 1) {
+    // the tile's entropy, non-finite and routed-token counts: the first warp
+    if (i < 32) {
         float h = 0.f;
         int b = 0, real = 0;
-        for (int r = 0; r < ntok; ++r) { h += sEnt[r]; b += sBad[r]; real += sSel[r * k] >= 0; }
-        o.part_ent[pidx] = h;
-        o.part_bad[pidx] = b;
-        o.part_real[pidx] = real;
+        for (int row = i; row < ntok; row += 32) {
+            h += sEnt[row];
+            b += sBad[row];
+            real += sSel[row * k] >= 0;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            h += __shfl_xor_sync(0xffffffffu, h, off);
+            b += __shfl_xor_sync(0xffffffffu, b, off);
+            real += __shfl_xor_sync(0xffffffffu, real, off);
+        }
+        if (i == 0) {
+            if (acc) {
+                acc[128] += h;
+                reinterpret_cast<int*>(acc)[129] += b;
+                reinterpret_cast<int*>(acc)[130] += real;
+            } else {
+                o.part_ent[pidx] = h;
+                o.part_bad[pidx] = b;
+                o.part_real[pidx] = real;
+            }
+        }
     }
 }
 
 // G lanes per token for TT tokens on nthr threads (G <= 32, a power of two)
 __device__ __forceinline__ void finish_tile(float* sLog, int ldl, int* sSel, float* sEnt, int* sBad,
                                             int t0, int ntok, int TT, int pidx, const RouteOut& o,
-                                            int i, int nthr, int bar_id)
+                                            int i, int nthr, int bar_id, float* acc = nullptr)
 {
     const int G = nthr / TT;
-    if (G >= 8) finish_tile_seg<8>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
-    else if (G >= 4) finish_tile_seg<4>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
-    else if (G >= 2) finish_tile_seg<2>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
-    else finish_tile_seg<1>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id);
+    if (G >= 8) finish_tile_seg<8>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
+    else if (G >= 4) finish_tile_seg<4>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
+    else if (G >= 2) finish_tile_seg<2>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
+    else finish_tile_seg<1>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
 }
 
-// W_r [d,E] bf16 -> WrT [E_pad, d] bf16 (zero rows for e >= E)
-__global__ void transpose_router_kernel(const __nv_bfloat16* __restrict__ Wr,
-                                        __nv_bfloat16* __restrict__ WrT, int d, int E, int E_pad)
+// Reduce the per-tile (or per-CTA) partials into counts and the statistics,
+// by nthr threads (index tid, a multiple of 32) sharing named barrier bar_id.
+// All partial loads are issued in one pass (R lanes of a warp per expert, up
+// to 16 independent loads each) so the reduction costs about one memory
+// round trip; every sum runs in a fixed order (deterministic).  Partials are
+// read with L1-bypassing loads: other CTAs wrote them.
+__device__ void finalize_stats(int nblk, int E, int k, float aux_coef,
+                               const int32_t* __restrict__ part_counts,
+                               const float* __restrict__ part_psum,
+                               const float* __restrict__ part_ent,
+                               const int32_t* __restrict__ part_bad,
+                               const int32_t* __restrict__ part_real, int32_t* __restrict__ counts,
+                               float* __restrict__ stats, int* status, int tid, int nthr,
+                               int bar_id)
 {
+    __shared__ float s_psum[64];
+    __shared__ int s_cnt[64];
+    __shared__ float s_h[32];
+    __shared__ int s_b[32], s_r[32];
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    // per-tile scalars: routed tokens, entropy, non-finite tokens
+    int rl = 0, bad = 0;
+    float h = 0.f;
+    for (int b = tid; b < nblk; b += nthr) {
+        rl += __ldcg(part_real + b);
+        h += __ldcg(part_ent + b);
+        bad += __ldcg(part_bad + b);
+    }
+    // per-expert sums: lanes (e, r), r < R, take partials r, r + R, ...
+    int R = 32;
+    while (R > 1 && R * E > nthr) R >>= 1;
+    const int e = tid / R, r = tid % R;
+    float ps = 0.f;
+    int c = 0;
+    if (e < E) {
+        for (int b0 = r; b0 < nblk; b0 += 16 * R) {
+            float pv[16];
+            int cv[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int bb = b0 + u * R;
+                pv[u] = bb < nblk ? __ldcg(part_psum + (size_t)bb * E + e) : 0.f;
+                cv[u] = bb < nblk ? __ldcg(part_counts + (size_t)bb * E + e) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) { ps += pv[u]; c += cv[u]; }
+        }
+    }
+    for (int off = R / 2; off > 0; off >>= 1) {
+        ps += __shfl_xor_sync(0xffffffffu, ps, off);
+        c += __shfl_xor_sync(0xffffffffu, c, off);
+    }
+    if (e < E && r == 0) { s_psum[e] = ps; s_cnt[e] = c; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        rl += __shfl_xor_sync(0xffffffffu, rl, o);
+        h += __shfl_xor_sync(0xffffffffu, h, o);
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) { s_r[warp] = rl; s_h[warp] = h; s_b[warp] = bad; }
+    named_sync(bar_id, nthr);
+    if (tid == 0) {
+        int tr = 0;
+        h = 0.f;
+        bad = 0;
+        for (int w = 0; w < nwarps; ++w) { tr += s_r[w]; h += s_h[w]; bad += s_b[w]; }
+        const float Tr = fmaxf((float)tr, 1.0f);   // means over the routed tokens
+        float aux = 0.f, sw = 0.f, cmean = 0.f, cmax = 0.f;
+        for (int q = 0; q < E; ++q) {
+            const float pbar = s_psum[q] / Tr;
+            counts[q] = s_cnt[q];
+            if (stats) stats[MOE_STAT_PBAR + q] = pbar;
+            const float dq = pbar - 1.0f / (float)E;
+            aux += dq * dq;
+            sw += ((float)s_cnt[q] / (Tr * (float)k)) * pbar;
+            cmean += (float)s_cnt[q];
+            cmax = fmaxf(cmax, (float)s_cnt[q]);
+        }
+        cmean /= (float)E;
+        float var = 0.f;
+        for (int q = 0; q < E; ++q) var += ((float)s_cnt[q] - cmean) * ((float)s_cnt[q] - cmean);
+        if (stats) {
+            stats[MOE_STAT_TOKENS] = (float)tr;
+            stats[MOE_STAT_AUX_LOSS] = aux_coef * aux;
+            stats[MOE_STAT_AUX_SWITCH] = (float)E * sw;
+            stats[MOE_STAT_ENTROPY] = h / Tr;
+            stats[MOE_STAT_NONFINITE] = (float)bad;
+            stats[MOE_STAT_DROPPED] = 0.f;
+            stats[MOE_STAT_MAX_OVER_MEAN_KEPT] = 0.f;
+            stats[MOE_STAT_COUNT_CV] = cmean > 0.f ? sqrtf(var / (float)E) / cmean : 0.f;
+            stats[MOE_STAT_MAX_OVER_MEAN_COUNT] = cmean > 0.f ? cmax / cmean : 0.f;
+        }
+        if (bad) set_status(status, MOE_ERR_NONFINITE);
+    }
+}
+
+// W_r [d,E] bf16 -> WrT [E_pad, d] bf16 (zero rows for e >= E); also zeroes the
+// router kernel's CTA ticket (this kernel runs just before it on the stream)
+__global__ void transpose_router_kernel(const __nv_bfloat16* __restrict__ Wr,
+                                        __nv_bfloat16* __restrict__ WrT, int d, int E, int E_pad,
+                                        int* ticket)
+{
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;
     const size_t n = (size_t)E_pad * d;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n;
          idx += (size_t)gridDim.x * blockDim.x) {
@@ -204,10 +348,12 @@ __global__ void transpose_router_kernel(const __nv_bfloat16* __restrict__ Wr,
     }
 }
 
-// Token tiles of TT tokens; the 8 MMA warps split each stage's 128 rows as
-// (k-slice, 16 tokens): with NKS = 128 / TT k-slices a stage holds NKS x 64
-// columns of x for the tile, so small token counts still spread over many SMs
-// (split-K across warps; slice partials summed in a fixed order).
+// Token tiles of TT tokens; the 8 MMA warps split each tile as (k-slice, 16
+// tokens): NKS = 128 / TT k-slices (split-K across warps; slice partials summed
+// in a fixed order).  A stage holds NKS x NB consecutive 64-column blocks of x
+// for the tile (NB = 1 or 2 blocks per k-slice), so a stage covers NKS*NB*128
+// contiguous bytes of each token row (in a plain read probe on GB300, stages of
+// 32 KB streamed at 7.1 TB/s and stages of 16 KB at 4.4).
 //
 // Persistent CTAs (one per SM), three roles:
 //   warp 8      TMA producer: 128B-swizzled boxes of x ({64 columns, TT rows}
@@ -225,6 +371,8 @@ struct RouteTma {
     RouteOut o;
     int* status;
     int stages;
+    int nb;          // 64-column blocks per k-slice per stage
+    float aux_coef;
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int col) {   // byte offset in a 128B-swizzled box
@@ -237,11 +385,12 @@ template <int NT, int TT>  // NT = E_pad / 8 tensor-core n-tiles; TT tokens per 
 __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __grid_constant__ RouteTma P)
 {
     constexpr int E_PAD = NT * 8;
-    constexpr int NKS = RT_TOK / TT;                 // k-slices per stage
+    constexpr int NKS = RT_TOK / TT;                 // k-slices per tile
     constexpr int LDL = E_PAD + 1;
-    constexpr uint32_t X_BYTES = RT_TOK * 128;       // 16 KB
-    constexpr uint32_t W_BYTES = (NKS * E_PAD * 128 + 1023) / 1024 * 1024;
-    constexpr uint32_t STAGE = X_BYTES + W_BYTES;
+    const int NB = P.nb;
+    const uint32_t X_BYTES = (uint32_t)NB * RT_TOK * 128;                        // 16 or 32 KB
+    const uint32_t W_BYTES = ((uint32_t)NB * NKS * E_PAD * 128 + 1023) / 1024 * 1024;
+    const uint32_t STAGE = X_BYTES + W_BYTES;
     const RouteOut& o = P.o;
     const int S = P.stages;
     extern __shared__ uint8_t smem_raw[];
@@ -251,7 +400,8 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
     int* sSel = reinterpret_cast<int*>(sLogB + 2 * TT * LDL);            // [TT*8]
     float* sEnt = reinterpret_cast<float*>(sSel + TT * 8);
     int* sBad = reinterpret_cast<int*>(sEnt + TT);
-    uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sBad + TT) + 15) & ~uintptr_t(15));
+    float* sAcc = reinterpret_cast<float*>(sBad + TT);                   // [ACC_FLOATS]
+    uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sAcc + ACC_FLOATS) + 15) & ~uintptr_t(15));
     uint64_t* full = bars;
     uint64_t* empty = full + S;
     uint64_t* lfull = empty + S;     // [2] logits buffer written (256 arrivals)
@@ -260,7 +410,7 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = o.d;
-    const int nk = d / (RT_BK * NKS);
+    const int nk = d / (RT_BK * NKS * NB);
     const int ntiles = (o.T + TT - 1) / TT;
     const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const uint32_t ring0 = smem_u32(ring);
@@ -294,12 +444,11 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status)) { ok = false; break; }
                     const uint32_t bar = smem_u32(&full[s]);
                     const uint32_t sx = ring0 + s * STAGE, sw = sx + X_BYTES;
-                    mbar_expect_tx(bar, X_BYTES + NKS * E_PAD * 128);
-                    const int k0 = kc * RT_BK * NKS;
-#pragma unroll
-                    for (int ks = 0; ks < NKS; ++ks) {
-                        tma_load3(&P.tmX, sx + ks * TT * 128, bar, k0 + ks * RT_BK, t0, 0);
-                        tma_load3(&P.tmW, sw + ks * E_PAD * 128, bar, k0 + ks * RT_BK, 0, 0);
+                    mbar_expect_tx(bar, X_BYTES + (uint32_t)NB * NKS * E_PAD * 128);
+                    const int k0 = kc * RT_BK * NKS * NB;
+                    for (int j = 0; j < NKS * NB; ++j) {   // block j: k-slice j / NB, columns k0 + 64 j
+                        tma_load3(&P.tmX, sx + j * TT * 128, bar, k0 + j * RT_BK, t0, 0);
+                        tma_load3(&P.tmW, sw + j * E_PAD * 128, bar, k0 + j * RT_BK, 0, 0);
                     }
                 }
             }
@@ -312,6 +461,7 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
     if (warp >= 9) {
         // ------------------------------------------------ finish warps
         const int ftid = tid - 9 * 32;   // 0..127
+        for (int q = ftid; q < ACC_FLOATS; q += 128) sAcc[q] = 0.f;   // the CTA's running sums
         bool live = true;
         for (int i = 0; i < my_tiles; ++i) {
             const int tile = blockIdx.x + i * gridDim.x;
@@ -319,10 +469,32 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
             const int b = i & 1;
             if (live) live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&lfull[b]), (uint32_t)(i >> 1) & 1u,
                                                             abort_flag, P.status));
-            if (live) finish_tile(sLogB + b * TT * LDL, LDL, sSel, sEnt, sBad, t0, ntok, TT, tile, o, ftid, 128, 2);
+            if (live) finish_tile(sLogB + b * TT * LDL, LDL, sSel, sEnt, sBad, t0, ntok, TT, tile, o, ftid, 128, 2, sAcc);
             else named_sync(2, 128);
             named_sync(2, 128);          // sSel / sEnt / sBad read by all before reuse
             mbar_arrive(smem_u32(&lempty[b]));
+        }
+        named_sync(2, 128);              // every tile's sums are in sAcc
+        // one partial per CTA (pidx = blockIdx.x), its tiles summed in tile order
+        for (int e = ftid; e < o.E; e += 128) {
+            o.part_psum[(size_t)blockIdx.x * o.E + e] = sAcc[e];
+            o.part_counts[(size_t)blockIdx.x * o.E + e] = reinterpret_cast<int*>(sAcc + 64)[e];
+        }
+        if (ftid == 0) {
+            o.part_ent[blockIdx.x] = sAcc[128];
+            o.part_bad[blockIdx.x] = reinterpret_cast<int*>(sAcc)[129];
+            o.part_real[blockIdx.x] = reinterpret_cast<int*>(sAcc)[130];
+        }
+        // the last CTA to finish reduces every CTA's partials (in CTA order)
+        __shared__ int s_last;
+        __threadfence();
+        named_sync(2, 128);
+        if (ftid == 0) s_last = atomicAdd(o.ticket, 1) == (int)gridDim.x - 1;
+        named_sync(2, 128);
+        if (s_last) {
+            __threadfence();
+            finalize_stats(gridDim.x, o.E, o.k, P.aux_coef, o.part_counts, o.part_psum, o.part_ent,
+                           o.part_bad, o.part_real, o.counts, o.stats, P.status, ftid, 128, 2);
         }
         return;
     }
@@ -330,6 +502,7 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
     // ---------------------------------------------------- MMA warps 0-7
     const int g = lane >> 2, tq = lane & 3;
     const int my_ks = (warp * 16) / TT;
+    const int tok0 = (warp * 16) % TT + g;              // this lane's first token row in a block
     bool live = true;
     int it = 0;
     for (int i = 0; i < my_tiles; ++i) {
@@ -341,25 +514,27 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
             const uint32_t ph = (uint32_t)(it / S) & 1u;
             if (live) live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), ph, abort_flag, P.status));
             if (!live) continue;
-            const uint8_t* X = ring + (size_t)s * STAGE;
-            const uint8_t* W = X + X_BYTES + my_ks * E_PAD * 128;
-            const int r0 = warp * 16 + g;                  // stage row (k-slice, token)
+            for (int bb = 0; bb < NB; ++bb) {
+                const int j = my_ks * NB + bb;                 // this warp's block of the stage
+                const uint8_t* X = ring + (size_t)s * STAGE + (size_t)j * TT * 128;
+                const uint8_t* W = ring + (size_t)s * STAGE + X_BYTES + (size_t)j * E_PAD * 128;
 #pragma unroll
-            for (int k16 = 0; k16 < RT_BK / 16; ++k16) {
-                const int kk = k16 * 16 + 2 * tq;
-                const uint32_t a0 = *reinterpret_cast<const uint32_t*>(X + swz128(r0, kk));
-                const uint32_t a1 = *reinterpret_cast<const uint32_t*>(X + swz128(r0 + 8, kk));
-                const uint32_t a2 = *reinterpret_cast<const uint32_t*>(X + swz128(r0, kk + 8));
-                const uint32_t a3 = *reinterpret_cast<const uint32_t*>(X + swz128(r0 + 8, kk + 8));
+                for (int k16 = 0; k16 < RT_BK / 16; ++k16) {
+                    const int kk = k16 * 16 + 2 * tq;
+                    const uint32_t a0 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0, kk));
+                    const uint32_t a1 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0 + 8, kk));
+                    const uint32_t a2 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0, kk + 8));
+                    const uint32_t a3 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0 + 8, kk + 8));
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk));
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk + 8));
-                    asm volatile(
-                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-                        : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
-                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                    for (int n = 0; n < NT; ++n) {
+                        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk));
+                        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk + 8));
+                        asm volatile(
+                            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                            : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
+                            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                    }
                 }
             }
             __syncwarp();
@@ -443,102 +618,26 @@ __global__ void __launch_bounds__(256) route_f32_kernel(const float* __restrict_
 
 // Sum the per-CTA partials (a warp per expert, lane-strided, then a fixed
 // shuffle tree: deterministic); derive the statistics.  1024 threads.
+// fp32 path: the reduction as its own one-CTA kernel after the router
 __global__ void __launch_bounds__(1024) route_finalize_kernel(
     int nblk, int T, int E, int k, float aux_coef, const int32_t* __restrict__ part_counts,
     const float* __restrict__ part_psum, const float* __restrict__ part_ent,
     const int32_t* __restrict__ part_bad, const int32_t* __restrict__ part_real,
     int32_t* __restrict__ counts, float* __restrict__ stats, int* status)
 {
-    __shared__ float s_pbar[64];
-    __shared__ int s_cnt[64];
-    __shared__ float s_h[32];
-    __shared__ int s_b[32], s_r[32];
-    __shared__ float s_treal;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // routed tokens first: the means below run over them
-    {
-        int rl = 0;
-        for (int b = tid; b < nblk; b += blockDim.x) rl += part_real[b];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) rl += __shfl_xor_sync(0xffffffffu, rl, o);
-        if (lane == 0) s_r[warp] = rl;
-        __syncthreads();
-        if (tid == 0) {
-            int tr = 0;
-            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tr += s_r[w];
-            s_treal = (float)tr;
-            if (stats) stats[MOE_STAT_TOKENS] = (float)tr;
-        }
-        __syncthreads();
-    }
-    const float Tr = fmaxf(s_treal, 1.0f);
-    for (int e = warp; e < E; e += 32) {
-        int c = 0;
-        float ps = 0.f;
-        for (int b = lane; b < nblk; b += 32) {
-            c += part_counts[(size_t)b * E + e];
-            ps += part_psum[(size_t)b * E + e];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            c += __shfl_xor_sync(0xffffffffu, c, o);
-            ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        }
-        if (lane == 0) {
-            counts[e] = c;
-            s_cnt[e] = c;
-            s_pbar[e] = ps / Tr;
-            if (stats) stats[MOE_STAT_PBAR + e] = ps / Tr;
-        }
-    }
-    float h = 0.f;
-    int bad = 0;
-    for (int b = tid; b < nblk; b += blockDim.x) { h += part_ent[b]; bad += part_bad[b]; }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        h += __shfl_xor_sync(0xffffffffu, h, o);
-        bad += __shfl_xor_sync(0xffffffffu, bad, o);
-    }
-    if (lane == 0) { s_h[warp] = h; s_b[warp] = bad; }
-    __syncthreads();
-    if (tid == 0) {
-        h = 0.f;
-        bad = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) { h += s_h[w]; bad += s_b[w]; }
-        float aux = 0.f, sw = 0.f, cmean = 0.f, cmax = 0.f;
-        for (int q = 0; q < E; ++q) {
-            float dq = s_pbar[q] - 1.0f / (float)E;
-            aux += dq * dq;
-            sw += ((float)s_cnt[q] / (Tr * (float)k)) * s_pbar[q];
-            cmean += (float)s_cnt[q];
-            cmax = fmaxf(cmax, (float)s_cnt[q]);
-        }
-        cmean /= (float)E;
-        float var = 0.f;
-        for (int q = 0; q < E; ++q) var += ((float)s_cnt[q] - cmean) * ((float)s_cnt[q] - cmean);
-        if (stats) {
-            stats[MOE_STAT_AUX_LOSS] = aux_coef * aux;
-            stats[MOE_STAT_AUX_SWITCH] = (float)E * sw;
-            stats[MOE_STAT_ENTROPY] = h / Tr;
-            stats[MOE_STAT_NONFINITE] = (float)bad;
-            stats[MOE_STAT_DROPPED] = 0.f;
-            stats[MOE_STAT_MAX_OVER_MEAN_KEPT] = 0.f;
-            stats[MOE_STAT_COUNT_CV] = cmean > 0.f ? sqrtf(var / (float)E) / cmean : 0.f;
-            stats[MOE_STAT_MAX_OVER_MEAN_COUNT] = cmean > 0.f ? cmax / cmean : 0.f;
-        }
-        if (bad) set_status(status, MOE_ERR_NONFINITE);
-    }
+    finalize_stats(nblk, E, k, aux_coef, part_counts, part_psum, part_ent, part_bad, part_real,
+                   counts, stats, status, threadIdx.x, blockDim.x, 1);
 }
 
 }  // namespace
 
-// Tokens per tile of the bf16 router.  A stage always holds 128 (k-slice, token)
-// rows of 64 columns: TT = 64 reads two adjacent 128-byte chunks of 64 token
-// rows per stage, which streamed fastest on GB300 (of 16, 32, 64 and 128
-// tokens per tile: about 3.9 TB/s versus 2.5-3.7 TB/s with the compute removed).
-// Smaller tiles are used only when 64-token tiles would leave SMs idle.  TT must
-// keep the stage's W_r^T slices (NKS * E_pad rows of 128 B) within 16 KB and
-// split d / 64 evenly into NKS slices.
+// Tokens per tile of the bf16 router (16, 32 or 64): the largest tile that
+// still gives every SM at least one tile, else the smallest legal one.  On
+// GB300 64-token tiles routed fastest even where they leave the last wave
+// uneven (T = 16384, d = 2048, E = 8: 50 us at 64 tokens, 52 at 32, 60 at 16;
+// T = 65536, d = 4096, E = 16: 159 / 179 / 233 us).  A tile must split d / 64
+// evenly into NKS = 128 / TT k-slices and keep a k-slice's W_r^T block (NKS *
+// E_pad rows of 128 B) within 16 KB.
 int route_tile_tokens(const moe_config& c) {
     if (c.dtype != MOE_DTYPE_BF16) return RT_TOK;
     const int e_pad = c.E <= 8 ? 8 : c.E <= 16 ? 16 : c.E <= 32 ? 32 : 64;
@@ -552,6 +651,14 @@ int route_tile_tokens(const moe_config& c) {
     return smallest > 0 ? smallest : RT_TOK;
 }
 
+// 64-column blocks per k-slice in one stage: 2 (32 KB of x per stage) when d
+// splits evenly and the stage's W_r^T blocks stay within 32 KB, else 1.
+int route_stage_blocks(const moe_config& c, int tt, int e_pad) {
+    const int nks = RT_TOK / tt;
+    if ((c.d / RT_BK) % (2 * nks) == 0 && 2 * nks * e_pad <= 256) return 2;
+    return 1;
+}
+
 size_t route_ws_bytes(const moe_config& c) {
     const int tt = route_tile_tokens(c);
     const size_t nblk = (size_t)(c.T + tt - 1) / tt;
@@ -562,6 +669,7 @@ size_t route_ws_bytes(const moe_config& c) {
     b += align_up(nblk * 4);                // ent
     b += align_up(nblk * 4);                // bad
     b += align_up(nblk * 4);                // routed tokens
+    b += align_up(4);                       // CTA ticket
     if (c.dtype == MOE_DTYPE_BF16) b += align_up((size_t)e_pad * c.d * 2);  // W_r^T
     return b;
 }
@@ -581,17 +689,21 @@ template <int NT, int TT>
 int launch_route_bf16(const moe_config& c, const void* x, const __nv_bfloat16* WrT, int e_pad,
                       const RouteOut& o, int nblk, cudaStream_t st) {
     constexpr int E_PAD = NT * 8, NKS = RT_TOK / TT;
-    constexpr size_t STAGE = RT_TOK * 128 + (NKS * E_PAD * 128 + 1023) / 1024 * 1024;
+    const int nb = route_stage_blocks(c, TT, E_PAD);
+    const size_t STAGE = (size_t)nb * RT_TOK * 128 + ((size_t)nb * NKS * E_PAD * 128 + 1023) / 1024 * 1024;
     const size_t extra = (size_t)RT_TOK * E_PAD * 4 + 2 * (size_t)TT * (E_PAD + 1) * 4 +
-                        (size_t)TT * 8 * 4 + (size_t)TT * 4 * 2 + 16 + (2 * 16 + 4) * 8 + 64;
-    const size_t budget = 220 * 1024 - 1024 - extra;
+                        (size_t)TT * 8 * 4 + (size_t)TT * 4 * 2 + ACC_FLOATS * 4 + 16 + (2 * 16 + 4) * 8 + 64;
+    // dynamic shared memory: the 227 KB per-block limit less the kernel's ~1 KB of
+    // static shared memory (the statistics reduction), rounded down
+    constexpr size_t DYN_SMEM = 225 * 1024;
+    const size_t budget = DYN_SMEM - 1024 - extra;
     const int stages = (int)std::min<size_t>(16, budget / STAGE);
     const size_t smem = 1024 + stages * STAGE + extra;
     static bool attr_set = false;  // the largest size is fixed per instantiation
     if (!attr_set) {
         MOE_CUDA_TRY(cudaFuncSetAttribute(route_bf16_kernel<NT, TT>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          220 * 1024));
+                                          (int)DYN_SMEM));
         attr_set = true;
     }
     RouteTma P;
@@ -605,6 +717,9 @@ int launch_route_bf16(const moe_config& c, const void* x, const __nv_bfloat16* W
     P.o = o;
     P.status = device_status_ptr();
     P.stages = stages;
+    P.nb = nb;
+    P.aux_coef = c.aux_coef;
+    if (stages < 2) return MOE_ERR_UNSUPPORTED;
     // persistent: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
     const int grid = std::min(nblk, num_sms());
     route_bf16_kernel<NT, TT><<<grid, RTMA_THREADS, smem, st>>>(P);
@@ -631,11 +746,14 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
     o.part_ent = reinterpret_cast<float*>(w); w += align_up((size_t)nblk * 4);
     o.part_bad = reinterpret_cast<int32_t*>(w); w += align_up((size_t)nblk * 4);
     o.part_real = reinterpret_cast<int32_t*>(w); w += align_up((size_t)nblk * 4);
+    o.ticket = reinterpret_cast<int*>(w); w += align_up(4);
+    o.counts = counts;
+    o.stats = stats;
 
     if (c.dtype == MOE_DTYPE_BF16) {
         __nv_bfloat16* WrT = reinterpret_cast<__nv_bfloat16*>(w);
         transpose_router_kernel<<<64, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(Wr), WrT,
-                                                    c.d, c.E, e_pad);
+                                                    c.d, c.E, e_pad, o.ticket);
         MOE_LAUNCH_CHECK();
         const int key = (e_pad / 8) * 1000 + tt;
         int r = MOE_OK;
@@ -655,7 +773,7 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
             case 8128: r = launch_route_bf16<8, 128>(c, x, WrT, e_pad, o, nblk, st); break;
             default: return MOE_ERR_UNSUPPORTED;
         }
-        return r != MOE_OK ? r : finalize_route(c, o, nblk, counts, stats, st);
+        return r;   // the kernel's last CTA reduced the statistics
     }
     const size_t tail = (RT_TOK * 8) * 4 + RT_TOK * 4 * 2;  // sSel, sEnt, sBad
     const size_t smem = (size_t)RT_TOK * 33 * 4 + (size_t)32 * c.E * 4 +
