@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_pe
                                                       const T* __restrict__ y_shared, int Tn,
                                                       int d, int k, T* __restrict__ out)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     constexpr int V = 16 / sizeof(T), U = 4;
     const int nv = d / V;
     const int lane = threadIdx.x & 31;
@@ -88,13 +90,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_pe
 }
 
 // Row r of the permuted layout: dy_perm[r] = gate * dout[t]; dgate = <dout[t], y_perm[r]>.
+// Slots without a row (dropped or padding tokens) get dgate = 0 in a first
+// grid-stride pass over the Tn * k slots.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const T* __restrict__ dout, const T* __restrict__ y_perm, const float* __restrict__ gate,
     const int32_t* __restrict__ slot_of, const int32_t* __restrict__ perm_token,
-    const int32_t* __restrict__ offsets, int E, int d, int k, T* __restrict__ dy_perm,
+    const int32_t* __restrict__ offsets, int Tn, int E, int d, int k, T* __restrict__ dy_perm,
     float* __restrict__ dgate)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < Tn * k; i += gridDim.x * blockDim.x)
+        if (slot_of[i] < 0) dgate[i] = 0.f;
     constexpr int V = 16 / sizeof(T);
     const int rows = offsets[E];
     const int nv = d / V;
@@ -128,19 +136,13 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
     }
 }
 
-// dgate of dropped slots is zero
-__global__ void zero_dropped_dgate_kernel(const int32_t* __restrict__ slot_of, int n,
-                                          float* __restrict__ dgate)
-{
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
-        if (slot_of[i] < 0) dgate[i] = 0.f;
-}
-
 // W_r [d,E] -> W_rT [E,d] fp32 (router-backward operand)
 template <typename T>
 __global__ void transpose_wr_f32_kernel(const T* __restrict__ Wr, float* __restrict__ WrT, int d,
                                         int E)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     const size_t n = (size_t)E * d;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n;
          idx += (size_t)gridDim.x * blockDim.x) {
@@ -161,6 +163,8 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     int Tn, int d, int E, int k, int normalize, int st, float inv_tau, float aux_coef,
     float* __restrict__ dlogits, T* __restrict__ dx)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     constexpr int V = 16 / sizeof(T);
     __shared__ float s_dl[8][64];
     const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -273,6 +277,8 @@ __global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
     const __nv_bfloat16* __restrict__ dx_shared, int Tn, int d, int E, int k,
     __nv_bfloat16* __restrict__ dx)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     constexpr int E16 = KS * 16, LDW = E16 + 2, LDO = RDX_CW + 4;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __nv_bfloat16* sW = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [128][LDW]
@@ -419,6 +425,8 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
                                                       float* __restrict__ part,
                                                       float* __restrict__ part_db)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     constexpr int E16 = MT * 16, LDT = 16 + 8;  // dlT row: 16 tokens (+pad)
     __shared__ __align__(16) __nv_bfloat16 sX[DWM_STAGES][16][DWM_LDX];
     __shared__ __align__(16) __nv_bfloat16 sD[DWM_STAGES][E16][LDT];
@@ -534,6 +542,8 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(const T* __restrict__ 
                                                           float* __restrict__ part,
                                                           float* __restrict__ part_db)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     constexpr int V = 16 / sizeof(T);
     extern __shared__ __align__(16) float red[];          // [8][32][V*EB]
     // grid: x = expert group (fastest, so the groups of one x tile run together and
@@ -599,22 +609,55 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(const T* __restrict__ 
     }
 }
 
+// dW_r = sum of the nsplit token-chunk partials (and dbias likewise).  A CTA
+// covers 64 four-column vectors with 4 groups of lanes; each group sums every
+// fourth partial with all of its loads independent (one memory round trip for
+// up to 32 partials), then the 4 group sums are added in a fixed order.
+constexpr int DWR_RED_COLS = 64, DWR_RED_GROUPS = 4;
+
 template <typename T>
-__global__ void dwr_reduce_kernel(const float* __restrict__ part, const float* __restrict__ part_db,
-                                  int nsplit, int d, int E, T* __restrict__ dWr,
-                                  float* __restrict__ dbias)
+__global__ void __launch_bounds__(DWR_RED_COLS * DWR_RED_GROUPS) dwr_reduce_kernel(
+    const float* __restrict__ part, const float* __restrict__ part_db, int nsplit, int d, int E,
+    T* __restrict__ dWr, float* __restrict__ dbias)
 {
-    const size_t n = (size_t)d * E;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-         i += (size_t)gridDim.x * blockDim.x) {
-        float a = 0.f;
-        for (int s = 0; s < nsplit; ++s) a += part[(size_t)s * n + i];
-        dWr[i] = from_f<T>(a);
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
+    __shared__ float4 s_acc[DWR_RED_GROUPS][DWR_RED_COLS];
+    const int n4 = d * E / 4;                    // d * E is a multiple of 4 (d % 8 == 0)
+    const int col = threadIdx.x % DWR_RED_COLS, grp = threadIdx.x / DWR_RED_COLS;
+    const int i4 = blockIdx.x * DWR_RED_COLS + col;
+    const float4* p4 = reinterpret_cast<const float4*>(part);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i4 < n4) {
+        int s0 = grp;
+        for (; s0 + 7 * DWR_RED_GROUPS < nsplit; s0 += 8 * DWR_RED_GROUPS) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(p4 + (size_t)(s0 + u * DWR_RED_GROUPS) * n4 + i4);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) { a.x += v[u].x; a.y += v[u].y; a.z += v[u].z; a.w += v[u].w; }
+        }
+        for (; s0 < nsplit; s0 += DWR_RED_GROUPS) {
+            const float4 v = __ldg(p4 + (size_t)s0 * n4 + i4);
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        }
+    }
+    s_acc[grp][col] = a;
+    __syncthreads();
+    if (grp == 0 && i4 < n4) {
+#pragma unroll
+        for (int g = 1; g < DWR_RED_GROUPS; ++g) {
+            const float4 b = s_acc[g][col];
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+        }
+        const float o[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dWr[(size_t)i4 * 4 + q] = from_f<T>(o[q]);
     }
     if (dbias && blockIdx.x == 0 && threadIdx.x < E) {
-        float a = 0.f;
-        for (int s = 0; s < nsplit; ++s) a += part_db[(size_t)s * E + threadIdx.x];
-        dbias[threadIdx.x] = a;
+        float b = 0.f;
+        for (int s = 0; s < nsplit; ++s) b += part_db[(size_t)s * E + threadIdx.x];
+        dbias[threadIdx.x] = b;
     }
 }
 
@@ -656,15 +699,13 @@ int launch_combine(const moe_config& c, const void* y_perm, const int32_t* slot_
 {
     const int grid = row_grid(c.T);
     if (c.dtype == MOE_DTYPE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(y_perm), slot_of, gate,
+        MOE_LAUNCH(combine_kernel<__nv_bfloat16>, grid, 256, 0, st, static_cast<const __nv_bfloat16*>(y_perm), slot_of, gate,
             static_cast<const __nv_bfloat16*>(y_shared), c.T, c.d, c.k,
             static_cast<__nv_bfloat16*>(out));
     else
-        combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(y_perm), slot_of,
+        MOE_LAUNCH(combine_kernel<float>, grid, 256, 0, st, static_cast<const float*>(y_perm), slot_of,
                                                     gate, static_cast<const float*>(y_shared),
                                                     c.T, c.d, c.k, static_cast<float*>(out));
-    MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
@@ -672,20 +713,14 @@ int launch_combine_backward(const moe_config& c, const void* dout, const void* y
                             const float* gate, const int32_t* slot_of, const int32_t* perm_token,
                             const int32_t* offsets, void* dy_perm, float* dgate, cudaStream_t st)
 {
-    const int n = c.T * c.k;
-    zero_dropped_dgate_kernel<<<std::min(1024, (n + 255) / 256), 256, 0, st>>>(slot_of, n, dgate);
-    MOE_LAUNCH_CHECK();
     const int grid = row_grid(rows_cap_of(c));
     if (c.dtype == MOE_DTYPE_BF16)
-        combine_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(y_perm),
-            gate, slot_of, perm_token, offsets, c.E, c.d, c.k,
+        MOE_LAUNCH(combine_bwd_kernel<__nv_bfloat16>, grid, 256, 0, st, static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(y_perm),
+            gate, slot_of, perm_token, offsets, c.T, c.E, c.d, c.k,
             static_cast<__nv_bfloat16*>(dy_perm), dgate);
     else
-        combine_bwd_kernel<float><<<grid, 256, 0, st>>>(
-            static_cast<const float*>(dout), static_cast<const float*>(y_perm), gate, slot_of,
-            perm_token, offsets, c.E, c.d, c.k, static_cast<float*>(dy_perm), dgate);
-    MOE_LAUNCH_CHECK();
+        MOE_LAUNCH(combine_bwd_kernel<float>, grid, 256, 0, st, static_cast<const float*>(dout), static_cast<const float*>(y_perm), gate, slot_of,
+            perm_token, offsets, c.T, c.E, c.d, c.k, static_cast<float*>(dy_perm), dgate);
     return MOE_OK;
 }
 
@@ -712,9 +747,8 @@ int launch_router_dx_ks(const moe_config& c, const float* dl, const __nv_bfloat1
     const int tiles = (c.T + 15) / 16;
     // one wave: at most the resident CTA slots (2 per SM), no partial second wave
     const int gy = std::max(1, std::min((tiles + 7) / 8, (2 * num_sms()) / gx));
-    router_dx_bf16_kernel<KS><<<dim3(gx, gy), 256, smem, st>>>(dl, Wr, slot_of, dxp, dxs, c.T,
+    MOE_LAUNCH(router_dx_bf16_kernel<KS>, dim3(gx, gy), 256, smem, st, dl, Wr, slot_of, dxp, dxs, c.T,
                                                                c.d, c.E, c.k, dx);
-    MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 }  // namespace
@@ -769,43 +803,32 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
     }
     if (c.dtype == MOE_DTYPE_BF16) {
         using T = __nv_bfloat16;
-        router_bwd_token_kernel<T, false><<<grid, 256, 0, st>>>(
-            logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), nullptr,
+        MOE_LAUNCH(router_bwd_token_kernel<T, false>, grid, 256, 0, st, logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), nullptr,
             nullptr, c.T, c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau,
             c.aux_coef, dlogits, static_cast<T*>(dx));
-        MOE_LAUNCH_CHECK();
         MOE_TRY_R(launch_router_dx_bf16(c, dlogits, static_cast<const T*>(Wr), slot_of,
                                         static_cast<const T*>(dx_perm),
                                         static_cast<const T*>(dx_shared), static_cast<T*>(dx), st));
         const dim3 mgrid((c.d + 127) / 128, ns);
         if (c.E <= 16)
-            dwr_mma_kernel<1><<<mgrid, 128, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
+            MOE_LAUNCH(dwr_mma_kernel<1>, mgrid, 128, 0, st, static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
                                                      chunk, part, part_db);
         else if (c.E <= 32)
-            dwr_mma_kernel<2><<<mgrid, 128, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
+            MOE_LAUNCH(dwr_mma_kernel<2>, mgrid, 128, 0, st, static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
                                                      chunk, part, part_db);
         else
-            dwr_mma_kernel<4><<<mgrid, 128, 0, st>>>(static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
+            MOE_LAUNCH(dwr_mma_kernel<4>, mgrid, 128, 0, st, static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
                                                      chunk, part, part_db);
-        MOE_LAUNCH_CHECK();
-        dwr_reduce_kernel<T><<<std::min(1024, (c.d * c.E + 255) / 256), 256, 0, st>>>(
-            part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);
-        MOE_LAUNCH_CHECK();
+        MOE_LAUNCH(dwr_reduce_kernel<T>, (c.d * c.E / 4 + DWR_RED_COLS - 1) / DWR_RED_COLS, DWR_RED_COLS * DWR_RED_GROUPS, 0, st, part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);
     } else {
         using T = float;
-        transpose_wr_f32_kernel<T><<<64, 256, 0, st>>>(static_cast<const T*>(Wr), WrT, c.d, c.E);
-        MOE_LAUNCH_CHECK();
-        router_bwd_token_kernel<T, true><<<grid, 256, 0, st>>>(
-            logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm),
+        MOE_LAUNCH(transpose_wr_f32_kernel<T>, 64, 256, 0, st, static_cast<const T*>(Wr), WrT, c.d, c.E);
+        MOE_LAUNCH(router_bwd_token_kernel<T, true>, grid, 256, 0, st, logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm),
             static_cast<const T*>(dx_shared), WrT, c.T, c.d, c.E, c.k, c.normalize_gates,
             c.straight_through, inv_tau, c.aux_coef, dlogits, static_cast<T*>(dx));
-        MOE_LAUNCH_CHECK();
-        dwr_partial_kernel<T, DWR_EB><<<pgrid, 256, dwr_smem, st>>>(static_cast<const T*>(x), dlogits,
+        MOE_LAUNCH(dwr_partial_kernel<T, DWR_EB>, pgrid, 256, dwr_smem, st, static_cast<const T*>(x), dlogits,
                                                                    c.T, c.d, c.E, chunk, part, part_db);
-        MOE_LAUNCH_CHECK();
-        dwr_reduce_kernel<T><<<std::min(1024, (c.d * c.E + 255) / 256), 256, 0, st>>>(
-            part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);
-        MOE_LAUNCH_CHECK();
+        MOE_LAUNCH(dwr_reduce_kernel<T>, (c.d * c.E / 4 + DWR_RED_COLS - 1) / DWR_RED_COLS, DWR_RED_COLS * DWR_RED_GROUPS, 0, st, part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);
     }
     return MOE_OK;
 }

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -26,6 +28,71 @@ int num_sms();                      // SM count of the current device
             (void)cudaGetLastError();                       \
             return MOE_ERR_CUDA;                            \
         }                                                   \
+    } while (0)
+
+// ---- programmatic dependent launch ----
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may be scheduled while the kernel before it on the stream
+// is still finishing.  Each kernel therefore calls pdl_wait() before its first
+// global-memory access (it returns once the preceding grid has completed and
+// its writes are visible), then pdl_trigger() to let the next kernel be
+// scheduled early in turn.  Set-up that touches no global memory (barrier
+// init, TMEM allocation, tensor-map prefetch) may come before the wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                     cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// launch with arguments converted to the kernel's parameter types
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(grid, block, smem, st, attr);
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// launch a kernel whose single parameter is a const __grid_constant__ struct
+template <typename P>
+inline cudaError_t launch_pdl_param(void (*kernel)(const P), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t st, const P& param) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(grid, block, smem, st, attr);
+    void* args[] = {const_cast<P*>(&param)};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), args);
+}
+
+// launch, count the launch, and turn a failure into MOE_ERR_CUDA
+#define MOE_LAUNCH(...)                                                  \
+    do {                                                                 \
+        const cudaError_t _le = ::moe::launch_pdl(__VA_ARGS__);          \
+        ::moe::note_launch();                                            \
+        if (_le != cudaSuccess) {                                        \
+            (void)cudaGetLastError();                                    \
+            return MOE_ERR_CUDA;                                         \
+        }                                                                \
+    } while (0)
+
+#define MOE_LAUNCH_PARAM(...)                                            \
+    do {                                                                 \
+        const cudaError_t _le = ::moe::launch_pdl_param(__VA_ARGS__);    \
+        ::moe::note_launch();                                            \
+        if (_le != cudaSuccess) {                                        \
+            (void)cudaGetLastError();                                    \
+            return MOE_ERR_CUDA;                                         \
+        }                                                                \
     } while (0)
 
 // ---- element access (fp32 or bf16 stored as __nv_bfloat16) ----

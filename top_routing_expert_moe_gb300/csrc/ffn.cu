@@ -38,6 +38,8 @@ constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16;
 template <typename T>
 __global__ void __launch_bounds__(256) simt_seg_gemm_kernel(SimtGemm g)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     __shared__ float As[SG_BK][SG_BM + 4];
     __shared__ float Bs[SG_BK][SG_BN + 4];
     const int e = blockIdx.z;
@@ -106,6 +108,8 @@ __global__ void act_fwd_kernel(const T* __restrict__ h0, const T* __restrict__ h
                                const int32_t* __restrict__ offsets, int E, int rows, int f,
                                int swiglu)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     const long long n = (long long)(offsets ? offsets[E] : rows) * f;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
@@ -123,6 +127,8 @@ __global__ void act_bwd_kernel(const T* __restrict__ h0, const T* __restrict__ h
                                const int32_t* __restrict__ offsets, int E, int rows, int f,
                                int swiglu)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     const long long n = (long long)(offsets ? offsets[E] : rows) * f;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
@@ -144,8 +150,7 @@ int simt_gemm(const SimtGemm& g, int E, int max_seg_rows, cudaStream_t st)
     dim3 grid((g.N + SG_BN - 1) / SG_BN,
               g.mode == SEG_ROWS ? (max_seg_rows + SG_BM - 1) / SG_BM : (g.M + SG_BM - 1) / SG_BM,
               E);
-    simt_seg_gemm_kernel<T><<<grid, 256, 0, st>>>(g);
-    MOE_LAUNCH_CHECK();
+    MOE_LAUNCH(simt_seg_gemm_kernel<T>, grid, 256, 0, st, g);
     return MOE_OK;
 }
 
@@ -200,8 +205,7 @@ int ffn_forward_f32(const moe_config& c, const float* xp, const int32_t* off, co
     } else {
         if ((r = simt_gemm<float>(rows_gemm(xp, d, Wu, 1, f, (long long)d * f, h0, f, f, d, off, 0), E, msr, st))) return r;
     }
-    act_fwd_kernel<float><<<ew_grid(c), 256, 0, st>>>(h0, h1, act, off, E, 0, f, sw);
-    MOE_LAUNCH_CHECK();
+    MOE_LAUNCH(act_fwd_kernel<float>, ew_grid(c), 256, 0, st, h0, h1, act, off, E, 0, f, sw);
     return simt_gemm<float>(rows_gemm(act, f, Wd, 1, d, (long long)f * d, y, d, d, f, off, 0), E, msr, st);
 }
 
@@ -221,8 +225,7 @@ int ffn_backward_f32(const moe_config& c, const float* xp, const int32_t* off, c
     int r;
     // dact = dy W_down^T   (B(n=j,k=i) = W_down[j][i])
     if ((r = simt_gemm<float>(rows_gemm(dy, d, Wd, d, 1, (long long)f * d, dact, f, f, d, off, 0), E, msr, st))) return r;
-    act_bwd_kernel<float><<<ew_grid(c), 256, 0, st>>>(h0, h1, dh0, dh1, off, E, 0, f, sw);
-    MOE_LAUNCH_CHECK();
+    MOE_LAUNCH(act_bwd_kernel<float>, ew_grid(c), 256, 0, st, h0, h1, dh0, dh1, off, E, 0, f, sw);
     // weight gradients
     if ((r = simt_gemm<float>(wgrad_gemm(act, f, dy, d, dWd, f, d, off), E, 0, st))) return r;
     if (sw) {
@@ -255,8 +258,7 @@ int shared_forward_f32(const moe_config& c, const moe_shared_ffn& s, cudaStream_
     } else {
         if ((r = simt_gemm<float>(rows_gemm(x, d, s.W_up, 1, f, 0, h0, f, f, d, nullptr, 0, T), 1, T, st))) return r;
     }
-    act_fwd_kernel<float><<<ew_grid((long long)T * f), 256, 0, st>>>(h0, h1, act, nullptr, 0, T, f, sw);
-    MOE_LAUNCH_CHECK();
+    MOE_LAUNCH(act_fwd_kernel<float>, ew_grid((long long)T * f), 256, 0, st, h0, h1, act, nullptr, 0, T, f, sw);
     return simt_gemm<float>(rows_gemm(act, f, s.W_down, 1, d, 0, s.y, d, d, f, nullptr, 0, T), 1, T, st);
 }
 
@@ -273,8 +275,7 @@ int shared_backward_f32(const moe_config& c, const moe_shared_ffn& s, cudaStream
     float* dact = sw ? dh1 : dh0;
     int r;
     if ((r = simt_gemm<float>(rows_gemm(dy, d, s.W_down, d, 1, 0, dact, f, f, d, nullptr, 0, T), 1, T, st))) return r;
-    act_bwd_kernel<float><<<ew_grid((long long)T * f), 256, 0, st>>>(h0, h1, dh0, dh1, nullptr, 0, T, f, sw);
-    MOE_LAUNCH_CHECK();
+    MOE_LAUNCH(act_bwd_kernel<float>, ew_grid((long long)T * f), 256, 0, st, h0, h1, dh0, dh1, nullptr, 0, T, f, sw);
     if ((r = simt_gemm<float>(wgrad_gemm(s.act, f, dy, d, s.dW_down, f, d, nullptr, T), 1, 0, st))) return r;
     if (sw) {
         if ((r = simt_gemm<float>(wgrad_gemm(x, d, dh1, f, s.dW_up, d, f, nullptr, T), 1, 0, st))) return r;

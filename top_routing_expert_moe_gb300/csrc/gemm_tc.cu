@@ -259,6 +259,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    pdl_wait();      // the preceding kernel's writes (offsets, operands) are visible from here on
+    pdl_trigger();
     if (P.offsets && tid < P.E + 1) offs[tid] = P.offsets[tid];
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -561,8 +563,7 @@ int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* prob
     P.offsets = offsets;
     P.status = device_status_ptr();
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms()));
-    tc_grouped_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(P);
-    MOE_LAUNCH_CHECK();
+    MOE_LAUNCH_PARAM(tc_grouped_gemm_kernel, grid, NTHREADS, SMEM_BYTES, st, P);
     return MOE_OK;
 }
 

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(PT_TOK) tile_hist_kernel(const int32_t* __rest
                                                            int32_t* __restrict__ tile_counts,
                                                            int* status)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     __shared__ int h[64];
     if (threadIdx.x < E) h[threadIdx.x] = 0;
     __syncthreads();
@@ -48,6 +50,8 @@ __global__ void __launch_bounds__(1024) scan_layout_kernel(
     int32_t* __restrict__ tile_base, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm_token, float* __restrict__ stats)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     __shared__ int s_total[64], s_kept[64], s_off[65];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int e = warp; e < E; e += 32) {
@@ -103,6 +107,8 @@ __global__ void __launch_bounds__(PT_TOK) assign_kernel(
     const int32_t* __restrict__ tile_base, const int32_t* __restrict__ offsets,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     __shared__ int wcount[PT_TOK / 32][64];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t = blockIdx.x * PT_TOK + tid;
@@ -148,6 +154,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const T* __restrict__ 
                                                           const int32_t* __restrict__ offsets,
                                                           int E, int d, T* __restrict__ x_perm)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     constexpr int V = 16 / sizeof(T);
     const int rows = offsets[E];
     const int nv = d / V;
@@ -186,26 +194,21 @@ int launch_permute(const moe_config& c, const void* x, const int32_t* topk, void
     int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
                                                     align_up((size_t)ntiles * c.E * 4));
     const int C = capacity_of(c);
-    tile_hist_kernel<<<ntiles, PT_TOK, 0, st>>>(topk, c.T, c.E, c.k, tile_counts,
+    MOE_LAUNCH(tile_hist_kernel, ntiles, PT_TOK, 0, st, topk, c.T, c.E, c.k, tile_counts,
                                                 device_status_ptr());
-    MOE_LAUNCH_CHECK();
-    scan_layout_kernel<<<1, 1024, 0, st>>>(tile_counts, ntiles, c.E, C, c.pad_m, tile_base, kept,
+    MOE_LAUNCH(scan_layout_kernel, 1, 1024, 0, st, tile_counts, ntiles, c.E, C, c.pad_m, tile_base, kept,
                                           offsets, perm_token, stats);
-    MOE_LAUNCH_CHECK();
-    assign_kernel<<<ntiles, PT_TOK, 0, st>>>(topk, c.T, c.E, c.k, C, tile_base, offsets, slot_of,
+    MOE_LAUNCH(assign_kernel, ntiles, PT_TOK, 0, st, topk, c.T, c.E, c.k, C, tile_base, offsets, slot_of,
                                              perm_token);
-    MOE_LAUNCH_CHECK();
     const int64_t rows = rows_cap_of(c);
     const int grid = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 8);
     if (c.dtype == MOE_DTYPE_BF16)
-        gather_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(x), perm_token, offsets, c.E, c.d,
+        MOE_LAUNCH(gather_rows_kernel<__nv_bfloat16>, grid, 256, 0, st, static_cast<const __nv_bfloat16*>(x), perm_token, offsets, c.E, c.d,
             static_cast<__nv_bfloat16*>(x_perm));
     else
-        gather_rows_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), perm_token,
+        MOE_LAUNCH(gather_rows_kernel<float>, grid, 256, 0, st, static_cast<const float*>(x), perm_token,
                                                         offsets, c.E, c.d,
                                                         static_cast<float*>(x_perm));
-    MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 

@@ -339,6 +339,8 @@ __global__ void transpose_router_kernel(const __nv_bfloat16* __restrict__ Wr,
                                         __nv_bfloat16* __restrict__ WrT, int d, int E, int E_pad,
                                         int* ticket)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;
     const size_t n = (size_t)E_pad * d;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n;
@@ -428,6 +430,8 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    pdl_wait();      // the preceding kernel's writes (x, W_r^T, the ticket) are visible from here on
+    pdl_trigger();
 
     if (warp == 8) {
         // ------------------------------------------------ TMA producer
@@ -572,6 +576,8 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
 __global__ void __launch_bounds__(256) route_f32_kernel(const float* __restrict__ x,
                                                         const float* __restrict__ Wr, RouteOut o)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     constexpr int BK = 32;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int E = o.E, d = o.d;
@@ -625,6 +631,8 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(
     const int32_t* __restrict__ part_bad, const int32_t* __restrict__ part_real,
     int32_t* __restrict__ counts, float* __restrict__ stats, int* status)
 {
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
     finalize_stats(nblk, E, k, aux_coef, part_counts, part_psum, part_ent, part_bad, part_real,
                    counts, stats, status, threadIdx.x, blockDim.x, 1);
 }
@@ -677,11 +685,10 @@ size_t route_ws_bytes(const moe_config& c) {
 namespace {
 int finalize_route(const moe_config& c, const RouteOut& o, int nblk, int32_t* counts,
                    float* stats, cudaStream_t st) {
-    route_finalize_kernel<<<1, 1024, 0, st>>>(nblk, c.T, c.E, c.k, c.aux_coef, o.part_counts,
+    MOE_LAUNCH(route_finalize_kernel, 1, 1024, 0, st, nblk, c.T, c.E, c.k, c.aux_coef, o.part_counts,
                                             o.part_psum, o.part_ent, o.part_bad, o.part_real,
                                             counts, stats,
                                             device_status_ptr());
-    MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
@@ -722,8 +729,7 @@ int launch_route_bf16(const moe_config& c, const void* x, const __nv_bfloat16* W
     if (stages < 2) return MOE_ERR_UNSUPPORTED;
     // persistent: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
     const int grid = std::min(nblk, num_sms());
-    route_bf16_kernel<NT, TT><<<grid, RTMA_THREADS, smem, st>>>(P);
-    MOE_LAUNCH_CHECK();
+    MOE_LAUNCH_PARAM(route_bf16_kernel<NT, TT>, grid, RTMA_THREADS, smem, st, P);
     return MOE_OK;
 }
 }  // namespace
@@ -752,9 +758,8 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
 
     if (c.dtype == MOE_DTYPE_BF16) {
         __nv_bfloat16* WrT = reinterpret_cast<__nv_bfloat16*>(w);
-        transpose_router_kernel<<<64, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(Wr), WrT,
+        MOE_LAUNCH(transpose_router_kernel, 64, 256, 0, st, static_cast<const __nv_bfloat16*>(Wr), WrT,
                                                     c.d, c.E, e_pad, o.ticket);
-        MOE_LAUNCH_CHECK();
         const int key = (e_pad / 8) * 1000 + tt;
         int r = MOE_OK;
         switch (key) {
@@ -780,9 +785,8 @@ int launch_route(const moe_config& c, const void* x, const void* Wr, const float
                         (size_t)RT_TOK * (c.E + 1) * 4 + tail;
     MOE_CUDA_TRY(cudaFuncSetAttribute(route_f32_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    route_f32_kernel<<<nblk, 256, smem, st>>>(static_cast<const float*>(x),
+    MOE_LAUNCH(route_f32_kernel, nblk, 256, smem, st, static_cast<const float*>(x),
                                               static_cast<const float*>(Wr), o);
-    MOE_LAUNCH_CHECK();
     return finalize_route(c, o, nblk, counts, stats, st);
 }
 
