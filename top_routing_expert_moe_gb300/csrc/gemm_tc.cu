@@ -49,12 +49,12 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + 256 * BK * 2;  // 48 KB
+constexpr int RING_BYTES = 192 * 1024;        // 4 stages of 48 KB (one CTA) or 6 of 32 KB (a pair)
 constexpr int GUARD_BYTES = 16 * 1024;        // slack after the ring
 constexpr int CTRL_BYTES = 3072;   // barriers, TMEM slot, offsets[65], prefix[6*64+1], slot bases
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + GUARD_BYTES + CTRL_BYTES;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + GUARD_BYTES + CTRL_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
@@ -114,17 +114,6 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dtmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -182,8 +171,14 @@ __device__ __forceinline__ float dsilu_fast(float z) {
 }
 
 // ---------------------------------------------------------------- schedule
+// A tile is CG * 128 rows (CG = 1: one CTA; CG = 2: a CTA pair, 128 rows each)
+// by bn columns.  Tiles are counted in these units; within a pair each CTA
+// takes its 128-row half, and a half that falls past the segment (an odd
+// number of 128-row blocks) computes but stores nothing.
 struct Tile {
     int p, e, m0, n0, krow0, nk;
+    int mb;        // index of the tile's first 128-row block within its segment
+    int mb_e;      // 128-row blocks of the segment (SCHED_ROWS) or of M (SCHED_KSEG)
 };
 
 __device__ __forceinline__ int seg_m_blocks(const TcProblem& q, const int* offs, int e) {
@@ -194,6 +189,7 @@ __device__ __forceinline__ int seg_m_blocks(const TcProblem& q, const int* offs,
 // Slots: problem p's segments (E of them, or 1 for a fixed-rows problem) are
 // slots sbase[p] .. sbase[p+1]-1.  prefix[s] = first tile of slot s;
 // prefix[sbase[nprob]] = total.  Binary search for the slot holding tile tix.
+template <int CG>
 __device__ __forceinline__ void decode_tile(const TcParams& P, const int* offs, const int* prefix,
                                             const int* sbase, int tix, Tile& t) {
     int lo = 0, hi = sbase[P.nprob] - 1;
@@ -207,35 +203,91 @@ __device__ __forceinline__ void decode_tile(const TcParams& P, const int* offs, 
     const TcProblem& q = P.prob[pi];
     const int local = tix - prefix[lo];
     const int mb_e = seg_m_blocks(q, offs, e);
-    const int gsz = RASTER_GM * q.n_blocks;
+    const int mt_e = (mb_e + CG - 1) / CG;                 // tiles along M
+    constexpr int RG = RASTER_GM / CG;
+    const int gsz = RG * q.n_blocks;
     const int grp = local / gsz;
-    const int first = grp * RASTER_GM;
-    const int gm = min(RASTER_GM, mb_e - first);
+    const int first = grp * RG;
+    const int gm = min(RG, mt_e - first);
     const int r = local - grp * gsz;
-    const int mb = first + r % gm, nb = r / gm;
+    const int mt = first + r % gm, nb = r / gm;
     t.p = pi;
     t.e = e;
     t.n0 = nb * q.bn;
+    t.mb = mt * CG;
+    t.mb_e = mb_e;
     if (q.sched == SCHED_ROWS) {
-        t.m0 = (q.fixed_rows ? 0 : offs[e]) + mb * BM;
+        t.m0 = (q.fixed_rows ? 0 : offs[e]) + t.mb * BM;
         t.krow0 = 0;
         t.nk = q.k_blocks * q.kconcat;
     } else {
-        t.m0 = mb * BM;
+        t.m0 = t.mb * BM;
         t.krow0 = q.fixed_rows ? 0 : offs[e];
         t.nk = (q.fixed_rows ? q.fixed_rows : offs[e + 1] - offs[e]) / BK;
     }
 }
 
+template <int CG>
+__device__ __forceinline__ void mma_issue(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    if constexpr (CG == 1) {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dtmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+    } else {
+        asm volatile(
+            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dtmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+    }
+}
+// arrive on `bar` once the MMAs issued so far complete: in this CTA (CG = 1),
+// or at the same offset in both CTAs of the pair (CG = 2)
+template <int CG>
+__device__ __forceinline__ void mma_commit_all(uint32_t bar) {
+    if constexpr (CG == 1) {
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+            "h"((uint16_t)0x3)
+            : "memory");
+    }
+}
+template <int CG>
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+}
+
 // ---------------------------------------------------------------- kernel
+// CG = 1: every CTA works alone on 128 x bn tiles (M = 128 MMAs).
+// CG = 2: clusters of two CTAs (a pair) work on 256 x bn tiles with M = 256
+// tcgen05.mma.cta_group::2 issued by the even CTA.  Each CTA stages its own
+// 128 rows of A and half of B's columns (32 KB per stage instead of 48, so six
+// stages fit instead of four and each CTA reads a third less from L2); both
+// halves' TMA loads complete on the even CTA's "full" barrier, the MMA
+// completions are multicast to both CTAs' "empty" and "accumulator full"
+// barriers, and both CTAs' epilogue warps release an accumulator on the even
+// CTA's "accumulator empty" barrier.  Each CTA drains its own 128 TMEM lanes.
+template <int CG>
 __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams P)
 {
+    constexpr int S = CG == 1 ? 4 : 6;                       // ring stages
+    constexpr int SB = CG == 1 ? 48 * 1024 : 32 * 1024;      // stage bytes per CTA
+    static_assert(S * SB == RING_BYTES, "ring size");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* ctrl = base + STAGES * STAGE_BYTES + GUARD_BYTES;
+    uint8_t* ctrl = base + RING_BYTES + GUARD_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-    uint64_t* empty = full + STAGES;
-    uint64_t* tfull = empty + STAGES;
+    uint64_t* empty = full + 8;
+    uint64_t* tfull = empty + 8;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -245,27 +297,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     int* sbase = prefix + MAX_PROBLEMS * 64 + 4;        // [nprob+1] first slot of each problem
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = CG == 1 ? 0u : cluster_rank();
+    const bool leader = rank == 0;
+    const int unit = (int)blockIdx.x / CG, nunits = (int)gridDim.x / CG;
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull[a]), 1);
-            mbar_init(smem_u32(&tempty[a]), NUM_EPI_WARPS);
+            mbar_init(smem_u32(&tempty[a]), CG * NUM_EPI_WARPS);
         }
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if constexpr (CG == 2) cluster_sync_all();   // both CTAs' barriers exist before any cross-CTA use
     pdl_wait();      // the preceding kernel's writes (offsets, operands) are visible from here on
     pdl_trigger();
     if (P.offsets && tid < P.E + 1) offs[tid] = P.offsets[tid];
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        if constexpr (CG == 1) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        } else {   // one warp of each CTA of the pair, collectively
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -277,7 +339,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const int nseg = P.prob[pi].fixed_rows ? 1 : P.E;
             for (int e = 0; e < nseg; ++e, ++sl) {
                 prefix[sl] = acc;
-                acc += seg_m_blocks(P.prob[pi], offs, e) * P.prob[pi].n_blocks;
+                acc += (seg_m_blocks(P.prob[pi], offs, e) + CG - 1) / CG * P.prob[pi].n_blocks;
             }
         }
         sbase[P.nprob] = sl;
@@ -289,127 +351,155 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     const uint32_t smem0 = smem_u32(base);
 
     if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (each CTA)
         for (int pi = 0; pi < P.nprob; ++pi) {   // the descriptors this launch uses
             const TcProblem& q = P.prob[pi];
-            const CUtensorMap* m[4] = {&q.tmA0, &q.tmB0, &q.tmA1, &q.tmB1};
-            const int used = q.kconcat == 2 ? 4 : q.dual ? 2 : 2;
-            for (int i = 0; i < used; ++i)
-                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m[i])) : "memory");
-            if (q.dual && q.kconcat != 2)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmA0)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmB0)) : "memory");
+            if (q.kconcat == 2)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmA1)) : "memory");
+            if (q.kconcat == 2 || q.dual)
                 asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmB1)) : "memory");
         }
         int it = 0;
         bool ok = true;
-        for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x) {
+        for (int tix = unit; ok && tix < total; tix += nunits) {
             Tile t;
-            decode_tile(P, offs, prefix, sbase, tix, t);
+            decode_tile<CG>(P, offs, prefix, sbase, tix, t);
             // per-tile copies of the problem's fields (registers, not re-read after each
             // "memory"-clobbering wait)
             const TcProblem& q = P.prob[t.p];
             const int q_kseg = q.sched == SCHED_KSEG, q_kb = q.k_blocks, q_dual = q.dual;
-            const int q_bmn = q.b_mn, q_nb64 = q.bn / 64;
+            const int q_bmn = q.b_mn;
             const CUtensorMap* tA0 = &q.tmA0;
             const CUtensorMap* tA1 = &q.tmA1;
             const CUtensorMap* tB0 = &q.tmB0;
             const CUtensorMap* tB1 = &q.tmB1;
-            const uint32_t b_bytes = q_dual ? 2u * 128u * BK * 2u : (uint32_t)q.bn * BK * 2u;
-            const uint32_t stage_tx = (uint32_t)A_BYTES + b_bytes;
+            // this CTA's rows of A and columns of B
+            const int am0 = t.m0 + (int)rank * BM;
+            const int bcols = (q_dual ? 128 : q.bn) / CG;        // per operand
+            const int bn0 = t.n0 + (int)rank * bcols;
+            const int nbox = bcols / 64;
+            const uint32_t b_bytes = (uint32_t)(q_dual ? 2 : 1) * bcols * BK * 2u;
+            const uint32_t stage_tx = CG * ((uint32_t)A_BYTES + b_bytes);   // both CTAs' bytes
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
-                const int s = it % STAGES;
-                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                const int s = it % S;
+                const uint32_t ph = (uint32_t)(it / S) & 1u;
                 if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status)) { ok = false; break; }
-                const uint32_t bar = smem_u32(&full[s]);
-                const uint32_t sA = smem0 + s * STAGE_BYTES, sB = sA + A_BYTES;
-                mbar_expect_tx(bar, stage_tx);
+                const uint32_t sA = smem0 + s * SB, sB = sA + A_BYTES;
+                uint32_t bar;
+                if constexpr (CG == 1) {
+                    bar = smem_u32(&full[s]);
+                    mbar_expect_tx(bar, stage_tx);
+                } else {
+                    bar = mapa_shared(smem_u32(&full[s]), 0);
+                    if (leader) mbar_expect_tx(smem_u32(&full[s]), stage_tx);
+                }
+                auto ld = [&](const CUtensorMap* m, uint32_t dst, int c0, int c1, int c2) {
+                    if constexpr (CG == 1) tma_load3(m, dst, bar, c0, c1, c2);
+                    else tma_load3_pair(m, dst, bar, c0, c1, c2);
+                };
                 if (q_kseg) {
                     const int kr = t.krow0 + kb * BK;
-                    tma_load3(tA0, sA, bar, t.m0, kr, 0);
-                    tma_load3(tA0, sA + 8192, bar, t.m0 + 64, kr, 0);
-                    for (int c = 0; c < q_nb64; ++c) tma_load3(tB0, sB + c * 8192, bar, t.n0 + 64 * c, kr, 0);
+                    ld(tA0, sA, am0, kr, 0);
+                    ld(tA0, sA + 8192, am0 + 64, kr, 0);
+                    for (int c = 0; c < nbox; ++c) ld(tB0, sB + c * 8192, bn0 + 64 * c, kr, 0);
                 } else {
                     const int phase = kb >= q_kb ? 1 : 0;
                     const int k0 = (kb - phase * q_kb) * BK;
-                    tma_load3(phase ? tA1 : tA0, sA, bar, k0, t.m0, 0);
+                    ld(phase ? tA1 : tA0, sA, k0, am0, 0);
                     if (q_dual) {
-                        tma_load3(tB0, sB, bar, t.n0, k0, t.e);
-                        tma_load3(tB0, sB + 8192, bar, t.n0 + 64, k0, t.e);
-                        tma_load3(tB1, sB + 16384, bar, t.n0, k0, t.e);
-                        tma_load3(tB1, sB + 24576, bar, t.n0 + 64, k0, t.e);
+                        for (int c = 0; c < nbox; ++c) ld(tB0, sB + c * 8192, bn0 + 64 * c, k0, t.e);
+                        for (int c = 0; c < nbox; ++c)
+                            ld(tB1, sB + (nbox + c) * 8192, bn0 + 64 * c, k0, t.e);
                     } else if (q_bmn) {
-                        for (int c = 0; c < q_nb64; ++c)
-                            tma_load3(tB0, sB + c * 8192, bar, t.n0 + 64 * c, k0, t.e);
-                    } else {
-                        tma_load3(phase ? tB1 : tB0, sB, bar, k0, t.n0, t.e);
+                        for (int c = 0; c < nbox; ++c) ld(tB0, sB + c * 8192, bn0 + 64 * c, k0, t.e);
+                    } else {   // K-major weights: boxes of 64 rows (N) x 64 k
+                        for (int c = 0; c < nbox; ++c)
+                            ld(phase ? tB1 : tB0, sB + c * 8192, k0, bn0 + 64 * c, t.e);
                     }
                 }
             }
         }
-        // drain: every load issued has landed before the CTA may exit
-        for (int i = max(0, it - STAGES); i < it; ++i)
-            mbar_drain(smem_u32(&full[i % STAGES]), (uint32_t)(i / STAGES) & 1u);
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
+        // drain: every load issued has landed before the CTA may exit (for a
+        // pair, the even CTA's "full" barriers count both CTAs' loads)
+        if (CG == 1 || leader)
+            for (int i = max(0, it - S); i < it; ++i) {
+                if constexpr (CG == 1) mbar_drain(smem_u32(&full[i % S]), (uint32_t)(i / S) & 1u);
+                else mbar_drain_cl(smem_u32(&full[i % S]), (uint32_t)(i / S) & 1u);
+            }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------ MMA issuer (the pair's even CTA)
         int it = 0, tcount = 0;
         bool ok = true;
-        for (int tix = blockIdx.x; ok && tix < total; tix += gridDim.x, ++tcount) {
+        for (int tix = unit; ok && tix < total; tix += nunits, ++tcount) {
             Tile t;
-            decode_tile(P, offs, prefix, sbase, tix, t);
+            decode_tile<CG>(P, offs, prefix, sbase, tix, t);
             const TcProblem& q = P.prob[t.p];
             const int q_dual = q.dual, q_amn = q.a_mn, q_bmn = q.b_mn;
-            const uint32_t idesc = idesc_bf16(BM, q_dual ? 128 : q.bn, q_amn, q_bmn);
+            const uint32_t idesc = idesc_bf16(BM * CG, q_dual ? 128 : q.bn, q_amn, q_bmn);
+            const uint32_t gate_bytes = (uint32_t)(128 / CG) * BK * 2u;   // dual: the up operand's offset
             const int acc = tcount & 1;
             const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-            if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, P.status)) { ok = false; break; }
+            const bool got = CG == 1 ? mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, P.status)
+                                     : mbar_wait_cl(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, P.status);
+            if (!got) { ok = false; break; }
             tc_fence_after();
             const uint32_t dt = tmem_base + (uint32_t)(acc * 256);
             uint32_t accum = 0;
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
-                const int s = it % STAGES;
-                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, P.status)) { ok = false; break; }
+                const int s = it % S;
+                const uint32_t ph = (uint32_t)(it / S) & 1u;
+                const bool in = CG == 1 ? mbar_wait(smem_u32(&full[s]), ph, abort_flag, P.status)
+                                        : mbar_wait_cl(smem_u32(&full[s]), ph, abort_flag, P.status);
+                if (!in) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sA = smem0 + s * STAGE_BYTES, sB = sA + A_BYTES;
+                const uint32_t sA = smem0 + s * SB, sB = sA + A_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BK / 16; ++ks) {
                     const uint64_t ad = q_amn ? sdesc(sA + ks * 2048, 8192, 1024) : sdesc(sA + ks * 32, 16, 1024);
                     if (q_dual) {
-                        mma_bf16(dt, ad, sdesc(sB + ks * 2048, 8192, 1024), idesc, accum);
-                        mma_bf16(dt + 128, ad, sdesc(sB + 16384 + ks * 2048, 8192, 1024), idesc, accum);
+                        mma_issue<CG>(dt, ad, sdesc(sB + ks * 2048, 8192, 1024), idesc, accum);
+                        mma_issue<CG>(dt + 128, ad, sdesc(sB + gate_bytes + ks * 2048, 8192, 1024), idesc, accum);
                     } else {
                         const uint64_t bd = q_bmn ? sdesc(sB + ks * 2048, 8192, 1024) : sdesc(sB + ks * 32, 16, 1024);
-                        mma_bf16(dt, ad, bd, idesc, accum);
+                        mma_issue<CG>(dt, ad, bd, idesc, accum);
                     }
                     accum = 1;
                 }
-                mma_commit(smem_u32(&empty[s]));  // stage free once these MMAs finish
+                mma_commit_all<CG>(smem_u32(&empty[s]));  // stage free (both CTAs) once these MMAs finish
             }
             if (!ok) break;
-            mma_commit(smem_u32(&tfull[acc]));    // accumulator ready
+            mma_commit_all<CG>(smem_u32(&tfull[acc]));    // accumulator ready (both CTAs)
         }
-        mma_commit(smem_u32(drain));
-        mbar_drain(smem_u32(drain), 0);
+        mma_commit_local<CG>(smem_u32(drain));
+        if constexpr (CG == 1) mbar_drain(smem_u32(drain), 0);
+        else mbar_drain_cl(smem_u32(drain), 0);
     } else if (warp >= 2) {
-        // ------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue (each CTA, its 128 rows)
         const int qd = warp & 3;                  // TMEM lane quarter this warp may access
         const int half = (warp - 2) / 4;          // which half of the tile's columns
         const int row_in_tile = qd * 32 + lane;
+        const uint32_t tempty_leader0 = CG == 1 ? smem_u32(&tempty[0]) : mapa_shared(smem_u32(&tempty[0]), 0);
         int tcount = 0;
-        for (int tix = blockIdx.x; tix < total; tix += gridDim.x, ++tcount) {
+        for (int tix = unit; tix < total; tix += nunits, ++tcount) {
             Tile t;
-            decode_tile(P, offs, prefix, sbase, tix, t);
+            decode_tile<CG>(P, offs, prefix, sbase, tix, t);
             const TcProblem& q = P.prob[t.p];
             const int width = q.dual ? 128 : q.bn;
             const int c_lo = half * (width / 64), c_hi = c_lo + width / 64;  // 32-column chunks
             const int acc = tcount & 1;
             const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, P.status)) break;
+            const bool got = CG == 1 ? mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, P.status)
+                                     : mbar_wait_cl(smem_u32(&tfull[acc]), aph, abort_flag, P.status);
+            if (!got) break;
             tc_fence_after();
-            const long long row = (long long)t.m0 + row_in_tile;
+            const bool valid = t.mb + (int)rank < t.mb_e;   // this CTA's half lies in the segment
+            const long long row = (long long)t.m0 + (long long)rank * BM + row_in_tile;
             const long long obase = (q.sched == SCHED_KSEG ? (long long)t.e * q.out_estride : 0) +
                                     row * q.ldo + t.n0;
             const uint32_t taddr = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(qd * 32) << 16);
-            for (int c = c_lo; c < c_hi; ++c) {
+            for (int c = c_lo; valid && c < c_hi; ++c) {
                 float v[32];
                 if (t.nk == 0) {
 #pragma unroll
@@ -457,14 +547,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+            if (lane == 0) {   // release the accumulator (on the even CTA's barrier)
+                if constexpr (CG == 1) mbar_arrive(smem_u32(&tempty[acc]));
+                else mbar_arrive_remote(tempty_leader0 + (uint32_t)(acc * 8));
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
+    // a pair ends together: no CTA leaves while the other may still reach its
+    // shared memory (the MMAs read both CTAs' stages; arrivals cross CTAs)
+    if constexpr (CG == 2) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+        if constexpr (CG == 1)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+        else
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
     }
 }
 
@@ -518,10 +617,11 @@ int act_map(CUtensorMap* m, const void* ptr, int64_t rows_cap, int cols, bool mn
     return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows_cap, 1, (uint64_t)cols * 2,
                     (uint64_t)cols * 2 * rows_cap, 64, mn_major ? 64 : BM);
 }
-// expert weights [E, rows, cols]: MN-major box {64, 64} or K-major box {64, bn}
-int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool mn_major, int bn) {
+// expert weights [E, rows, cols]: boxes {64, 64} (MN-major: 64 N x 64 k; K-major:
+// 64 k x 64 rows of N, several boxes per stage)
+int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool, int) {
     return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)E, (uint64_t)cols * 2,
-                    (uint64_t)cols * 2 * rows, 64, mn_major ? 64 : (uint32_t)bn);
+                    (uint64_t)cols * 2 * rows, 64, 64);
 }
 
 int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
@@ -532,12 +632,49 @@ int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
         if (_r != MOE_OK) return _r; \
     } while (0)
 
-// Upper bound of a problem's tile count (grid sizing only; the kernel counts
-// the real tiles from the device offsets).
-int64_t max_tiles(const moe_config& c, const TcProblem& q) {
-    if (q.sched == SCHED_ROWS)
-        return (q.fixed_rows ? q.fixed_rows / BM : rows_cap_of(c) / BM) * q.n_blocks;
-    return (int64_t)(q.fixed_rows ? 1 : c.E) * q.m_blocks * q.n_blocks;
+// Upper bound of a problem's tile count in cg * 128-row tiles (grid sizing
+// only; the kernel counts the real tiles from the device offsets).
+int64_t max_tiles(const moe_config& c, const TcProblem& q, int cg) {
+    if (q.sched == SCHED_ROWS) {
+        const int64_t mb = q.fixed_rows ? q.fixed_rows / BM : rows_cap_of(c) / BM;
+        // each segment may round up by one pair tile
+        return ((mb + cg - 1) / cg + (q.fixed_rows ? 0 : (cg - 1) * c.E)) * q.n_blocks;
+    }
+    return (int64_t)(q.fixed_rows ? 1 : c.E) * ((q.m_blocks + cg - 1) / cg) * q.n_blocks;
+}
+
+// CTA pairs the device can hold at once (0: pairs unusable)
+int max_pairs() {
+    static int cached[64] = {};
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!done[dev]) {
+        done[dev] = true;
+        if (cudaFuncSetAttribute(tc_grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms() / 2));
+        cfg.blockDim = dim3(NTHREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_gemm_kernel<2>, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        cached[dev] = std::min(n, num_sms() / 2);
+    }
+    return cached[dev];
 }
 
 int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* probs, int nprob,
@@ -546,24 +683,50 @@ int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* prob
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 64 && !attr_done[dev]) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(tc_grouped_gemm_kernel,
+        MOE_CUDA_TRY(cudaFuncSetAttribute(tc_grouped_gemm_kernel<1>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
         attr_done[dev] = true;
     }
     if (nprob < 1 || nprob > MAX_PROBLEMS) return MOE_ERR_INVALID_ARG;
     TcParams P;
     memset(&P, 0, sizeof(P));
-    int64_t tiles = 0;
-    for (int i = 0; i < nprob; ++i) {
-        P.prob[i] = probs[i];
-        tiles += max_tiles(c, probs[i]);
-    }
+    for (int i = 0; i < nprob; ++i) P.prob[i] = probs[i];
     P.nprob = nprob;
     P.E = c.E;
     P.offsets = offsets;
     P.status = device_status_ptr();
+    const int pairs = max_pairs();
+    if (pairs > 0) {   // CTA pairs: 256-row tiles, M = 256 MMAs across the pair
+        int64_t tiles = 0;
+        for (int i = 0; i < nprob; ++i) tiles += max_tiles(c, probs[i], 2);
+        const int units = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, pairs));
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * units);
+        cfg.blockDim = dim3(NTHREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        void* args[] = {&P};
+        const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(tc_grouped_gemm_kernel<2>), args);
+        note_launch();
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        return MOE_OK;
+    }
+    int64_t tiles = 0;
+    for (int i = 0; i < nprob; ++i) tiles += max_tiles(c, probs[i], 1);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms()));
-    MOE_LAUNCH_PARAM(tc_grouped_gemm_kernel, grid, NTHREADS, SMEM_BYTES, st, P);
+    MOE_LAUNCH_PARAM(tc_grouped_gemm_kernel<1>, grid, NTHREADS, SMEM_BYTES, st, P);
     return MOE_OK;
 }
 

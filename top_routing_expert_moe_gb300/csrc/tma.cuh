@@ -70,6 +70,71 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
         if (gtimer() - t0 > DRAIN_NS) break;
 }
 
+// ---- CTA-pair (cluster of 2) helpers ----
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// arrive on an mbarrier in another CTA of the cluster (release at cluster scope)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// try_wait with cluster-scope acquire (barriers that other CTAs of the cluster arrive on)
+__device__ __forceinline__ bool mbar_try_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait, cluster-scope acquire (as mbar_wait)
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             int* status) {
+    if (mbar_try_cl(bar, parity)) return true;
+    const unsigned long long t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_cl(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (*abort_flag) return false;
+            if (gtimer() - t0 > WAIT_NS) {
+                set_status(status, MOE_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void mbar_drain_cl(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = gtimer();
+    while (!mbar_try_cl(bar, parity))
+        if (gtimer() - t0 > DRAIN_NS) break;
+}
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (bar: a shared::cluster address)
+__device__ __forceinline__ void tma_load3_pair(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                               int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load3(const CUtensorMap* map, uint32_t dst, uint32_t bar, int c0,
                                           int c1, int c2) {
     asm volatile(
