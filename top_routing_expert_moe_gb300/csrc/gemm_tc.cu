@@ -52,9 +52,10 @@ namespace {
 constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int RING_BYTES = 192 * 1024;        // 4 stages of 48 KB (one CTA) or 6 of 32 KB (a pair)
-constexpr int GUARD_BYTES = 16 * 1024;        // slack after the ring
-constexpr int CTRL_BYTES = 3072;   // barriers, TMEM slot, offsets[65], prefix[6*64+1], slot bases
-constexpr int SMEM_BYTES = 1024 + RING_BYTES + GUARD_BYTES + CTRL_BYTES;
+constexpr int STAGING_BYTES = 32 * 1024;      // epilogue: two 2 KB output boxes per epilogue warp
+constexpr int CTRL_BYTES = 2048;   // barriers, TMEM slot, offsets[65], prefix[6*64+1], slot bases
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + STAGING_BYTES + CTRL_BYTES;
+static_assert(SMEM_BYTES <= 232448, "227 KB of dynamic shared memory per block");
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
@@ -71,6 +72,7 @@ enum Sched { SCHED_ROWS = 0, SCHED_KSEG = 1 };
 // expert index 0 (the shared FFN, which every token passes through).
 struct TcProblem {
     CUtensorMap tmA0, tmB0, tmA1, tmB1;
+    CUtensorMap tmO[3];     // outputs out0..out2: boxes of 32 rows x 32 columns, 64-byte swizzle
     __nv_bfloat16* out0;
     __nv_bfloat16* out1;
     __nv_bfloat16* out2;
@@ -84,7 +86,7 @@ struct TcProblem {
     int kconcat;            // SCHED_ROWS: 2 = K loop continues over (A1, B1)
     int a_mn, b_mn;         // operand is MN-major in global memory
     int bn;                 // 128 or 256
-    int dual;               // two accumulators (B0 -> cols 0..127, B1 -> 128..255)
+    int dual;               // SwiGLU GEMM1: B = [B0 tile | B1 tile], accumulator columns 0..127 / 128..255
     int epi;
     int ldo;
     int fixed_rows;         // > 0: one segment [0, fixed_rows) (a multiple of BM)
@@ -97,7 +99,7 @@ struct TcParams {
     int* status;
     int nprob, E;
 };
-static_assert(sizeof(TcParams) <= 4096, "kernel parameters stay within 4 KB");
+static_assert(sizeof(TcParams) <= 32764, "kernel parameters within the 32 KB launch limit");
 
 // mbarrier / TMA / timer helpers: tma.cuh
 
@@ -134,20 +136,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 32 fp32 -> 32 bf16 at p (64 bytes)
-__device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float* v) {
-    uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
-            w[j] = *reinterpret_cast<uint32_t*>(&b);
-        }
-        q[i] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
 __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float* v) {
     const uint4* q = reinterpret_cast<const uint4*>(p);
 #pragma unroll
@@ -284,7 +272,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     static_assert(S * SB == RING_BYTES, "ring size");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* ctrl = base + RING_BYTES + GUARD_BYTES;
+    uint8_t* ctrl = base + RING_BYTES + STAGING_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
     uint64_t* empty = full + 8;
     uint64_t* tfull = empty + 8;
@@ -360,6 +348,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                 asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmA1)) : "memory");
             if (q.kconcat == 2 || q.dual)
                 asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmB1)) : "memory");
+            const __nv_bfloat16* outs[3] = {q.out0, q.out1, q.out2};
+            for (int i = 0; i < 3; ++i)
+                if (outs[i])
+                    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmO[i])) : "memory");
         }
         int it = 0;
         bool ok = true;
@@ -377,10 +369,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const CUtensorMap* tB1 = &q.tmB1;
             // this CTA's rows of A and columns of B
             const int am0 = t.m0 + (int)rank * BM;
-            const int bcols = (q_dual ? 128 : q.bn) / CG;        // per operand
-            const int bn0 = t.n0 + (int)rank * bcols;
+            // SwiGLU's gate and up tiles form one 256-column B operand [gate | up]:
+            // one CTA stages both (CG = 1), or the even CTA the gate and the odd
+            // CTA the up tile (CG = 2)
+            const int bcols = (q_dual ? 256 : q.bn) / CG;
+            const int bn0 = t.n0 + (q_dual ? 0 : (int)rank * bcols);
             const int nbox = bcols / 64;
-            const uint32_t b_bytes = (uint32_t)(q_dual ? 2 : 1) * bcols * BK * 2u;
+            const uint32_t b_bytes = (uint32_t)bcols * BK * 2u;
             const uint32_t stage_tx = CG * ((uint32_t)A_BYTES + b_bytes);   // both CTAs' bytes
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
                 const int s = it % S;
@@ -409,9 +404,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     const int k0 = (kb - phase * q_kb) * BK;
                     ld(phase ? tA1 : tA0, sA, k0, am0, 0);
                     if (q_dual) {
-                        for (int c = 0; c < nbox; ++c) ld(tB0, sB + c * 8192, bn0 + 64 * c, k0, t.e);
-                        for (int c = 0; c < nbox; ++c)
-                            ld(tB1, sB + (nbox + c) * 8192, bn0 + 64 * c, k0, t.e);
+                        for (int c = 0; c < 4 / CG; ++c) {   // 64-column boxes of [gate | up]
+                            const int g = c + (int)rank * (4 / CG);        // 0,1: gate; 2,3: up
+                            ld(g < 2 ? tB0 : tB1, sB + c * 8192, bn0 + 64 * (g & 1), k0, t.e);
+                        }
                     } else if (q_bmn) {
                         for (int c = 0; c < nbox; ++c) ld(tB0, sB + c * 8192, bn0 + 64 * c, k0, t.e);
                     } else {   // K-major weights: boxes of 64 rows (N) x 64 k
@@ -437,8 +433,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             decode_tile<CG>(P, offs, prefix, sbase, tix, t);
             const TcProblem& q = P.prob[t.p];
             const int q_dual = q.dual, q_amn = q.a_mn, q_bmn = q.b_mn;
-            const uint32_t idesc = idesc_bf16(BM * CG, q_dual ? 128 : q.bn, q_amn, q_bmn);
-            const uint32_t gate_bytes = (uint32_t)(128 / CG) * BK * 2u;   // dual: the up operand's offset
+            const uint32_t idesc = idesc_bf16(BM * CG, q_dual ? 256 : q.bn, q_amn, q_bmn);
             const int acc = tcount & 1;
             const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
             const bool got = CG == 1 ? mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, P.status)
@@ -458,13 +453,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
 #pragma unroll
                 for (int ks = 0; ks < BK / 16; ++ks) {
                     const uint64_t ad = q_amn ? sdesc(sA + ks * 2048, 8192, 1024) : sdesc(sA + ks * 32, 16, 1024);
-                    if (q_dual) {
-                        mma_issue<CG>(dt, ad, sdesc(sB + ks * 2048, 8192, 1024), idesc, accum);
-                        mma_issue<CG>(dt + 128, ad, sdesc(sB + gate_bytes + ks * 2048, 8192, 1024), idesc, accum);
-                    } else {
-                        const uint64_t bd = q_bmn ? sdesc(sB + ks * 2048, 8192, 1024) : sdesc(sB + ks * 32, 16, 1024);
-                        mma_issue<CG>(dt, ad, bd, idesc, accum);
-                    }
+                    // (dual: one N = 256 MMA, gate -> columns 0..127, up -> 128..255)
+                    const uint64_t bd = (q_bmn || q_dual) ? sdesc(sB + ks * 2048, 8192, 1024)
+                                                          : sdesc(sB + ks * 32, 16, 1024);
+                    mma_issue<CG>(dt, ad, bd, idesc, accum);
                     accum = 1;
                 }
                 mma_commit_all<CG>(smem_u32(&empty[s]));  // stage free (both CTAs) once these MMAs finish
@@ -477,10 +469,42 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         else mbar_drain_cl(smem_u32(drain), 0);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue (each CTA, its 128 rows)
+        // Each warp drains 32 TMEM lanes (rows) x 32 columns at a time and writes
+        // every output box through one of its two 2 KB shared-memory buffers with a
+        // TMA store (64-byte swizzle: lane r's 16-byte chunk j goes to chunk
+        // j ^ ((r >> 1) & 3), conflict-free), so global writes leave as whole
+        // 64-byte row pieces instead of 16-byte partial stores.
         const int qd = warp & 3;                  // TMEM lane quarter this warp may access
         const int half = (warp - 2) / 4;          // which half of the tile's columns
         const int row_in_tile = qd * 32 + lane;
         const uint32_t tempty_leader0 = CG == 1 ? smem_u32(&tempty[0]) : mapa_shared(smem_u32(&tempty[0]), 0);
+        uint8_t* stg = base + RING_BYTES + (warp - 2) * 4096;
+        int nst = 0;                              // boxes this warp has stored
+        auto put = [&](const CUtensorMap* m, const float* v, int c0, int c1, int c2) {
+            uint8_t* buf = stg + (nst & 1) * 2048;
+            if (nst >= 2) {                       // the store that last used buf has read it
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+                    w[i] = *reinterpret_cast<uint32_t*>(&b2);
+                }
+                *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store3(m, smem_u32(buf), c0, c1, c2);
+                bulk_commit();
+            }
+            ++nst;
+        };
         int tcount = 0;
         for (int tix = unit; tix < total; tix += nunits, ++tcount) {
             Tile t;
@@ -498,13 +522,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const long long row = (long long)t.m0 + (long long)rank * BM + row_in_tile;
             const long long obase = (q.sched == SCHED_KSEG ? (long long)t.e * q.out_estride : 0) +
                                     row * q.ldo + t.n0;
+            // box coordinates of this warp's 32 rows: (column, row or M index, expert)
+            const int brow = t.m0 + (int)rank * BM + qd * 32;
+            const int bz = q.sched == SCHED_KSEG ? t.e : 0;
             const uint32_t taddr = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(qd * 32) << 16);
             for (int c = c_lo; valid && c < c_hi; ++c) {
+                const int bcol = t.n0 + c * 32;
                 float v[32];
                 if (t.nk == 0) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                    store32_bf16(q.out0 + obase + c * 32, v);
+                    put(&q.tmO[0], v, bcol, brow, bz);
                     continue;
                 }
                 tmem_ld32(taddr + c * 32, v);
@@ -512,37 +540,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     float u[32];
                     tmem_ld32(taddr + 128 + c * 32, u);
                     tmem_wait_ld();
-                    store32_bf16(q.out0 + obase + c * 32, v);
-                    store32_bf16(q.out1 + obase + c * 32, u);
+                    put(&q.tmO[0], v, bcol, brow, bz);
+                    put(&q.tmO[1], u, bcol, brow, bz);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = silu_fast(v[i]) * u[i];
-                    store32_bf16(q.out2 + obase + c * 32, v);
+                    put(&q.tmO[2], v, bcol, brow, bz);
                     continue;
                 }
                 tmem_wait_ld();
                 if (q.epi == EPI_STORE) {
-                    store32_bf16(q.out0 + obase + c * 32, v);
+                    put(&q.tmO[0], v, bcol, brow, bz);
                 } else if (q.epi == EPI_SILU_FWD) {
-                    store32_bf16(q.out0 + obase + c * 32, v);
+                    put(&q.tmO[0], v, bcol, brow, bz);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = silu_fast(v[i]);
-                    store32_bf16(q.out1 + obase + c * 32, v);
+                    put(&q.tmO[1], v, bcol, brow, bz);
                 } else if (q.epi == EPI_SILU_BWD) {
                     float h[32];
                     load32_bf16(q.in0 + obase + c * 32, h);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= dsilu_fast(h[i]);
-                    store32_bf16(q.out0 + obase + c * 32, v);
+                    put(&q.tmO[0], v, bcol, brow, bz);
                 } else {  // EPI_SWIGLU_BWD: v = dact
                     float g[32], u[32], o[32];
                     load32_bf16(q.in0 + obase + c * 32, g);
                     load32_bf16(q.in1 + obase + c * 32, u);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = v[i] * u[i] * dsilu_fast(g[i]);
-                    store32_bf16(q.out0 + obase + c * 32, o);
+                    put(&q.tmO[0], o, bcol, brow, bz);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = v[i] * silu_fast(g[i]);
-                    store32_bf16(q.out1 + obase + c * 32, o);
+                    put(&q.tmO[1], o, bcol, brow, bz);
                 }
             }
             tc_fence_before();
@@ -552,6 +580,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                 else mbar_arrive_remote(tempty_leader0 + (uint32_t)(acc * 8));
             }
         }
+        if (lane == 0) bulk_wait_all();           // every output box written before exit
     }
     tc_fence_before();
     __syncthreads();
@@ -592,7 +621,7 @@ EncodeTiledFn encode_fn() {
 // 3-D bf16 map with 128-byte swizzle: dims {d0 (contiguous), d1, d2}, byte strides
 // {s1, s2}, box {b0, b1, 1}
 int encode_bf16_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
-                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1) {
+                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return MOE_ERR_CUDA;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -600,7 +629,7 @@ int encode_bf16_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, u
     cuuint32_t box[3] = {b0, b1, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -750,6 +779,18 @@ struct Family {
     const void *Wu, *Wg, *Wd;
 };
 
+// Output maps of a row-segmented problem: out_i [rows_total, ldo], boxes of
+// 32 columns x 32 rows with 64-byte swizzle (the epilogue's TMA stores)
+int out_maps_rows(TcProblem& q, int64_t rows_total) {
+    __nv_bfloat16* outs[3] = {q.out0, q.out1, q.out2};
+    for (int i = 0; i < 3; ++i)
+        if (outs[i])
+            MOE_TRY(encode_bf16_map(&q.tmO[i], outs[i], (uint64_t)q.ldo, (uint64_t)rows_total, 1,
+                                    (uint64_t)q.ldo * 2, (uint64_t)q.ldo * 2 * rows_total, 32, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_64B));
+    return MOE_OK;
+}
+
 // Row-segmented problem: C[rows, N] = A[rows, K] (K-major) x B_e (expert weights)
 int rows_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, int K, int N) {
     q.sched = SCHED_ROWS;
@@ -776,7 +817,10 @@ int wgrad_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, 
     q.ldo = N;
     q.out_estride = (long long)M * N;
     MOE_TRY(act_map(&q.tmA0, A, a_rows, M, true));
-    return act_map(&q.tmB0, B, b_rows, N, true);
+    MOE_TRY(act_map(&q.tmB0, B, b_rows, N, true));
+    // out [E][M][N]: boxes of 32 columns x 32 rows of one expert
+    return encode_bf16_map(&q.tmO[0], out, (uint64_t)N, (uint64_t)M, (uint64_t)F.E, (uint64_t)N * 2,
+                           (uint64_t)N * 2 * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // GEMM1 with the activation fused: h|g,u = x W_up|W_gate; act = silu(h) | silu(g) u
@@ -801,7 +845,7 @@ int gemm1_problem(TcProblem& q, const moe_config& c, const Family& F, void* h, v
         q.out0 = static_cast<bf*>(h);
         q.out1 = static_cast<bf*>(act);
     }
-    return MOE_OK;
+    return out_maps_rows(q, F.rows);
 }
 
 // GEMM2: y = act W_down
@@ -811,7 +855,7 @@ int gemm2_problem(TcProblem& q, const moe_config& c, const Family& F, const void
     MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, F.f, c.d, true, 0));
     q.epi = EPI_STORE;
     q.out0 = static_cast<__nv_bfloat16*>(y);
-    return MOE_OK;
+    return out_maps_rows(q, F.rows);
 }
 
 // dgrad2 with the activation derivative fused: dact = dy W_down^T -> dh (SiLU) or dg, du (SwiGLU)
@@ -830,7 +874,7 @@ int dgrad2_problem(TcProblem& q, const moe_config& c, const Family& F, const voi
     } else {
         q.epi = EPI_SILU_BWD;
     }
-    return MOE_OK;
+    return out_maps_rows(q, F.rows);
 }
 
 // dgrad1: dx = dh W_up^T  (SwiGLU: du W_up^T + dg W_gate^T, one K loop over both)
@@ -848,7 +892,7 @@ int dgrad1_problem(TcProblem& q, const moe_config& c, const Family& F, const voi
     }
     q.epi = EPI_STORE;
     q.out0 = static_cast<bf*>(dx);
-    return MOE_OK;
+    return out_maps_rows(q, F.rows);
 }
 
 // weight gradients: dW_down = act^T dy; dW_up = x^T dh (du); dW_gate = x^T dg

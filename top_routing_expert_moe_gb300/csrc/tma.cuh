@@ -8,10 +8,11 @@
 
 namespace moe {
 
-// 3-D bf16 tensor map with 128-byte swizzle (host; defined in gemm_tc.cu):
-// dims {d0 (contiguous), d1, d2}, byte strides {s1, s2}, box {b0, b1, 1}.
+// 3-D bf16 tensor map (host; defined in gemm_tc.cu): dims {d0 (contiguous), d1,
+// d2}, byte strides {s1, s2}, box {b0, b1, 1}, 128-byte swizzle unless stated.
 int encode_bf16_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
-                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1);
+                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 constexpr unsigned long long WAIT_NS = 4000000000ull;   // bounded waits give up after 4 s
 constexpr unsigned long long DRAIN_NS = 500000000ull;   // draining gives up after 0.5 s
@@ -133,6 +134,21 @@ __device__ __forceinline__ void tma_load3_pair(const CUtensorMap* map, uint32_t 
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+// TMA store of a shared-memory box (bulk-group completion)
+__device__ __forceinline__ void tma_store3(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_load3(const CUtensorMap* map, uint32_t dst, uint32_t bar, int c0,
