@@ -15,6 +15,11 @@ Under torchrun each rank runs an independent replica on its own GPU (the
 layer has no exchange step on one GPU); rank 0 prints one JSON line with the
 whole-job tokens/s (max step time over ranks).
 
+`e2e` is the same step through the public layer API with pinned host buffers,
+every transfer inside the timed region: x copied in, the forward, dout copied
+in on a copy stream during the forward, out copied back during the backward,
+dx copied back at the end.
+
 --impl reference times the fp64 CPU oracle (the layer's plain definition) on
 the host cores, on a bounded token sample of the same workload per step.
 """
@@ -411,18 +416,29 @@ def run_ours(args, w):
         dx_h = torch.empty_like(L.out, device="cpu").pin_memory()
         x_d = torch.empty_like(x)
         dout_d = torch.empty_like(dout)
+        cs = torch.cuda.Stream(dev)       # copies that overlap compute: dout in, out back
         torch.cuda.synchronize(dev)
         e2e = []
         for i in range(args.steps):
             flush.zero_()
             e0, e1 = ev(), ev()
+            ev_dout, ev_fwd, ev_out = ev(), ev(), ev()
             e0.record(st)
             x_d.copy_(x_h, non_blocking=True)
-            dout_d.copy_(dout_h, non_blocking=True)
+            cs.wait_event(e0)
+            with torch.cuda.stream(cs):
+                dout_d.copy_(dout_h, non_blocking=True)   # during the forward
+                ev_dout.record(cs)
             L.forward(x_d, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, stream=st, shared=shared_w)
+            ev_fwd.record(st)
+            cs.wait_event(ev_fwd)
+            with torch.cuda.stream(cs):
+                out_h.copy_(L.out, non_blocking=True)     # during the backward
+                ev_out.record(cs)
+            st.wait_event(ev_dout)
             gg = L.backward(dout_d, stream=st)
-            out_h.copy_(L.out, non_blocking=True)
             dx_h.copy_(gg["dx"], non_blocking=True)
+            st.wait_event(ev_out)
             e1.record(st)
             e2e.append((e0, e1))
         torch.cuda.synchronize(dev)
