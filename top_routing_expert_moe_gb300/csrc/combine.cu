@@ -31,8 +31,10 @@ __host__ __device__ constexpr size_t align_up_dev(size_t b) { return (b + 255) /
 
 // out[t] = sum_j gate[t,j] * y_perm[slot_of[t,j]] (kept slots, j ascending),
 // plus y_shared[t] (the shared experts, weight 1) when given.
-// One warp per token; each lane keeps 4 vectors of 16 bytes per slot in flight.
-template <typename T>
+// One warp per token; for each group of U 16-byte vectors per lane the loads of
+// all k slots are issued before any is used (k * U = 8 loads in flight per
+// lane), then summed in slot order.
+template <typename T, int KMAX, int U>
 __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_of,
                                                       const float* __restrict__ gate,
@@ -41,19 +43,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_pe
 {
     pdl_wait();      // the preceding kernel's writes are visible from here on
     pdl_trigger();
-    constexpr int V = 16 / sizeof(T), U = 4;
+    constexpr int V = 16 / sizeof(T);
     const int nv = d / V;
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
     for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < Tn; t += warps) {
-        int slot[8];
-        float g[8];
+        int slot[KMAX];
+        float g[KMAX];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
             slot[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
             g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
         }
         for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+            uint4 raw[KMAX][U];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    raw[j][u] = (slot[j] >= 0 && v0 + 32 * u < nv)
+                                    ? __ldg(reinterpret_cast<const uint4*>(y_perm + (size_t)slot[j] * d) + v0 + 32 * u)
+                                    : make_uint4(0, 0, 0, 0);
             float acc[U][V];
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -66,18 +76,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_pe
                     if (v0 + 32 * u < nv) load16_f<T>(row + (v0 + 32 * u) * V, acc[u]);
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < KMAX; ++j) {
                 if (slot[j] < 0) continue;
-                const T* row = y_perm + (size_t)slot[j] * d;
-                uint4 raw[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    raw[u] = (v0 + 32 * u < nv) ? __ldg(reinterpret_cast<const uint4*>(row) + v0 + 32 * u)
-                                                : make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     float y[V];
-                    load16_f<T>(reinterpret_cast<const T*>(&raw[u]), y);
+                    load16_f<T>(reinterpret_cast<const T*>(&raw[j][u]), y);
 #pragma unroll
                     for (int q = 0; q < V; ++q) acc[u][q] = fmaf(g[j], y[q], acc[u][q]);
                 }
@@ -347,21 +351,15 @@ __global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
             so[(g + 8) * LDO + nt * 8 + 2 * tq + 1] = c[3];
         }
         __syncwarp();
-        // round trip 2 (per pair of slots): 16 row loads in flight per lane;
-        // a half-warp covers the chunk's 128 columns for 8 tokens
+        // round trip 2 (per pair of slots): 16 row loads in flight per lane (and the
+        // shared experts' rows with the last pair); a half-warp covers the chunk's
+        // 128 columns for 8 tokens.  The router term waits in shared memory, so
+        // only the loads occupy registers; partial sums of k > 2 go back there.
         if (col < d) {
-            float acc[8][8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = hw + 2 * i;
-                const float4 s0 = *reinterpret_cast<const float4*>(so + r * LDO + hl * 8);
-                const float4 s1 = *reinterpret_cast<const float4*>(so + r * LDO + hl * 8 + 4);
-                acc[i][0] = s0.x; acc[i][1] = s0.y; acc[i][2] = s0.z; acc[i][3] = s0.w;
-                acc[i][4] = s1.x; acc[i][5] = s1.y; acc[i][6] = s1.z; acc[i][7] = s1.w;
-            }
             for (int j0 = 0; j0 < k; j0 += 2) {
                 if (j0 > 0) load_slots(j0);
-                uint4 y[2][8];
+                const bool last = j0 + 2 >= k;
+                uint4 y[2][8], ys[8];
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
@@ -370,39 +368,37 @@ __global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
                                        ? __ldg(reinterpret_cast<const uint4*>(dx_perm + (size_t)sl[jj][i] * d + col))
                                        : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t w4[4] = {y[jj][i].x, y[jj][i].y, y[jj][i].z, y[jj][i].w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            acc[i][2 * q] += __uint_as_float(w4[q] << 16);
-                            acc[i][2 * q + 1] += __uint_as_float(w4[q] & 0xFFFF0000u);
-                        }
-                    }
-            }
-            if (dx_shared) {   // the shared experts' input gradient
-                uint4 y[8];
-#pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int t = t0 + hw + 2 * i;
-                    y[i] = t < Tn ? __ldg(reinterpret_cast<const uint4*>(dx_shared + (size_t)t * d + col))
-                                  : make_uint4(0, 0, 0, 0);
+                    ys[i] = (last && dx_shared && t < Tn)
+                                ? __ldg(reinterpret_cast<const uint4*>(dx_shared + (size_t)t * d + col))
+                                : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t w4[4] = {y[i].x, y[i].y, y[i].z, y[i].w};
+                    const int r = hw + 2 * i;
+                    float* sp = so + r * LDO + hl * 8;
+                    const float4 s0 = *reinterpret_cast<const float4*>(sp);
+                    const float4 s1 = *reinterpret_cast<const float4*>(sp + 4);
+                    float a8[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                    const uint4 src[3] = {y[0][i], y[1][i], ys[i]};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[i][2 * q] += __uint_as_float(w4[q] << 16);
-                        acc[i][2 * q + 1] += __uint_as_float(w4[q] & 0xFFFF0000u);
+                    for (int m = 0; m < 3; ++m) {
+                        const uint32_t w4[4] = {src[m].x, src[m].y, src[m].z, src[m].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            a8[2 * q] += __uint_as_float(w4[q] << 16);
+                            a8[2 * q + 1] += __uint_as_float(w4[q] & 0xFFFF0000u);
+                        }
+                    }
+                    if (last) {
+                        const int t = t0 + r;
+                        if (t < Tn) store16_f<__nv_bfloat16>(dx + (size_t)t * d + col, a8);
+                    } else {
+                        *reinterpret_cast<float4*>(sp) = make_float4(a8[0], a8[1], a8[2], a8[3]);
+                        *reinterpret_cast<float4*>(sp + 4) = make_float4(a8[4], a8[5], a8[6], a8[7]);
                     }
                 }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = t0 + hw + 2 * i;
-                if (t < Tn) store16_f<__nv_bfloat16>(dx + (size_t)t * d + col, acc[i]);
             }
         }
         __syncwarp();
@@ -427,16 +423,21 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
 {
     pdl_wait();      // the preceding kernel's writes are visible from here on
     pdl_trigger();
-    constexpr int E16 = MT * 16, LDT = 16 + 8;  // dlT row: 16 tokens (+pad)
+    constexpr int E16 = MT * 16;
     __shared__ __align__(16) __nv_bfloat16 sX[DWM_STAGES][16][DWM_LDX];
-    __shared__ __align__(16) __nv_bfloat16 sD[DWM_STAGES][E16][LDT];
+    __shared__ __align__(16) float sDf[DWM_STAGES][16][E16];   // dlogits tile [token][expert], fp32
     __shared__ float sDb[128];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
     const int c0 = blockIdx.x * 128;
     const int tbeg = blockIdx.y * chunk, tend = min(Tn, tbeg + chunk);
     const int nblk16 = (tend - tbeg + 15) / 16;
-    float db = 0.f;  // this thread's dbias share (expert tid % E16), column chunk 0 only
+    // dlogits rows stream with cp.async too when they are 16-byte granular (E % 4
+    // == 0), so no synchronous load stalls the ring; columns E..E16 stay zero
+    const bool async_dl = (E & 3) == 0;
+    for (int i = tid; i < DWM_STAGES * 16 * E16; i += 128) (&sDf[0][0][0])[i] = 0.f;
+    __syncthreads();
+    float db = 0.f;  // this thread's dbias share (expert tid, tid < E16), column chunk 0 only
     auto load = [&](int b, int st) {
         const int t0 = tbeg + b * 16;
         // x tile: 16 rows x 128 columns = 256 vectors of 16 bytes, two per thread
@@ -451,14 +452,28 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                          "r"(ok ? 16 : 0));
         }
-        // dlogits tile transposed to [e][t] in bf16
-        for (int i = tid; i < 16 * E16; i += 128) {
-            const int row = i / E16, e = i % E16;
-            const int t = t0 + row;
-            const float v = (t < tend && e < E) ? __ldg(dlogits + (size_t)t * E + e) : 0.f;
-            sD[st][e][row] = __float2bfloat16_rn(v);
-            if (blockIdx.x == 0) db += v;
+        if (async_dl) {
+            const int q4 = E >> 2;                       // 16-byte pieces per token row
+            for (int i = tid; i < 16 * q4; i += 128) {
+                const int row = i / q4, c4 = i % q4;
+                const int t = t0 + row;
+                const bool ok = t < tend;
+                const float* src = ok ? dlogits + (size_t)t * E + c4 * 4 : dlogits;
+                const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&sDf[st][row][c4 * 4]);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                             "r"(ok ? 16 : 0));
+            }
+        } else {
+            for (int i = tid; i < 16 * E; i += 128) {
+                const int row = i / E, e = i % E;
+                const int t = t0 + row;
+                sDf[st][row][e] = t < tend ? __ldg(dlogits + (size_t)t * E + e) : 0.f;
+            }
         }
+    };
+    auto pack2 = [](float lo, float hi) -> uint32_t {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&b2);
     };
     float acc[MT][4][4];
 #pragma unroll
@@ -474,14 +489,19 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
         asm volatile("cp.async.wait_group %0;\n" ::"n"(DWM_STAGES - 2));
         __syncthreads();
         const int st = b % DWM_STAGES;
+        // A = dlogits^T (rows experts, k = tokens), bf16 pairs of consecutive tokens
         uint32_t af[MT][4];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            af[m][0] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g][2 * tq]);
-            af[m][1] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g + 8][2 * tq]);
-            af[m][2] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g][2 * tq + 8]);
-            af[m][3] = *reinterpret_cast<const uint32_t*>(&sD[st][m * 16 + g + 8][2 * tq + 8]);
+            const int e0 = m * 16 + g;
+            af[m][0] = pack2(sDf[st][2 * tq][e0], sDf[st][2 * tq + 1][e0]);
+            af[m][1] = pack2(sDf[st][2 * tq][e0 + 8], sDf[st][2 * tq + 1][e0 + 8]);
+            af[m][2] = pack2(sDf[st][2 * tq + 8][e0], sDf[st][2 * tq + 9][e0]);
+            af[m][3] = pack2(sDf[st][2 * tq + 8][e0 + 8], sDf[st][2 * tq + 9][e0 + 8]);
         }
+        if (blockIdx.x == 0 && tid < E16)
+#pragma unroll
+            for (int r = 0; r < 16; ++r) db += sDf[st][r][tid];
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
             // B (k = token, n = column) from the row-major [token][col] tile
@@ -498,6 +518,8 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
                     : "+f"(acc[m][n][0]), "+f"(acc[m][n][1]), "+f"(acc[m][n][2]), "+f"(acc[m][n][3])
                     : "r"(af[m][0]), "r"(af[m][1]), "r"(af[m][2]), "r"(af[m][3]), "r"(b0), "r"(b1));
         }
+        // the refill targets the stage read in the previous iteration (all threads
+        // passed this iteration's barrier after reading it)
         const int nxt = b + DWM_STAGES - 1;
         if (nxt < nblk16) load(nxt, nxt % DWM_STAGES);
         asm volatile("cp.async.commit_group;\n" ::);
@@ -694,19 +716,29 @@ int row_grid(int64_t rows) {
 
 }  // namespace
 
+template <typename T, int KMAX, int U>
+int launch_combine_t(const moe_config& c, const void* y_perm, const int32_t* slot_of,
+                     const float* gate, const void* y_shared, void* out, cudaStream_t st) {
+    MOE_LAUNCH(combine_kernel<T, KMAX, U>, row_grid(c.T), 256, 0, st, static_cast<const T*>(y_perm),
+               slot_of, gate, static_cast<const T*>(y_shared), c.T, c.d, c.k, static_cast<T*>(out));
+    return MOE_OK;
+}
+
+template <typename T>
+int launch_combine_k(const moe_config& c, const void* y_perm, const int32_t* slot_of,
+                     const float* gate, const void* y_shared, void* out, cudaStream_t st) {
+    if (c.k <= 1) return launch_combine_t<T, 1, 8>(c, y_perm, slot_of, gate, y_shared, out, st);
+    if (c.k <= 2) return launch_combine_t<T, 2, 4>(c, y_perm, slot_of, gate, y_shared, out, st);
+    if (c.k <= 4) return launch_combine_t<T, 4, 2>(c, y_perm, slot_of, gate, y_shared, out, st);
+    return launch_combine_t<T, 8, 1>(c, y_perm, slot_of, gate, y_shared, out, st);
+}
+
 int launch_combine(const moe_config& c, const void* y_perm, const int32_t* slot_of,
                    const float* gate, const void* y_shared, void* out, cudaStream_t st)
 {
-    const int grid = row_grid(c.T);
     if (c.dtype == MOE_DTYPE_BF16)
-        MOE_LAUNCH(combine_kernel<__nv_bfloat16>, grid, 256, 0, st, static_cast<const __nv_bfloat16*>(y_perm), slot_of, gate,
-            static_cast<const __nv_bfloat16*>(y_shared), c.T, c.d, c.k,
-            static_cast<__nv_bfloat16*>(out));
-    else
-        MOE_LAUNCH(combine_kernel<float>, grid, 256, 0, st, static_cast<const float*>(y_perm), slot_of,
-                                                    gate, static_cast<const float*>(y_shared),
-                                                    c.T, c.d, c.k, static_cast<float*>(out));
-    return MOE_OK;
+        return launch_combine_k<__nv_bfloat16>(c, y_perm, slot_of, gate, y_shared, out, st);
+    return launch_combine_k<float>(c, y_perm, slot_of, gate, y_shared, out, st);
 }
 
 int launch_combine_backward(const moe_config& c, const void* dout, const void* y_perm,
