@@ -51,6 +51,23 @@ GEMM_SOURCE = os.path.join(ROOT, "top_routing_expert_moe_gb300", "csrc", "gemm_t
 
 
 # ----------------------------------------------------------------------------- helpers
+def max_over_ranks(values, device, world):
+    """Per-rank timings -> their maximum over all ranks (the job ends with the
+    slowest replica); identity on one rank."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job rate: every rank processed units_per_rank in (at most) ms."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
@@ -445,12 +462,7 @@ def run_ours(args, w):
         e2e_ms = float(np.mean([a.elapsed_time(c) for a, c in e2e]))
 
     # max over ranks
-    if world > 1:
-        t = torch.tensor([ms_local, fwd_ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, fwd_ms, e2e_ms = (float(v) for v in t.tolist())
-    else:
-        ms = ms_local
+    ms, fwd_ms, e2e_ms = max_over_ranks([ms_local, fwd_ms, e2e_ms], dev, world)
     if rank == 0:
         peaks, src = load_peaks()
         gemm_ms = float(stage_ms[2] + stage_ms[5])
@@ -469,7 +481,7 @@ def run_ours(args, w):
                    "kind": "oracle",
                    "sample": f"oracle fp64 fwd+bwd on a {T_s}-token batch of {w.name} "
                              f"(same d, f, E, k, capacity factor), {t_cpu:.1f} s"}
-        tok = w.T * world / (ms * 1e-3)
+        tok = job_rate(w.T, world, ms)
         es = 2 if dt == "bf16" else 4
         line = {
             "metric": METRIC, "value": tok, "unit": "tokens/s", "n_gpus": world,
@@ -483,14 +495,14 @@ def run_ours(args, w):
                          "kernel": "tc_grouped_gemm_kernel (all grouped-GEMM launches of a step)",
                          "peak_source": f"{src} bf16 burst"},
             "cpu_baseline": cpu,
-            "e2e": {"value": w.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": job_rate(w.T, world, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": (x.numel() + dout.numel()) * es,
                     "d2h_bytes_per_step": 2 * L.out.numel() * es},
             "clocks": clocks,
             "gpu_launches": int(launches_per_step * args.steps),
             "launches_per_step": int(launches_per_step),
             "eager_ms_per_step": eager_ms,
-            "fwd_tokens_per_s": w.T * world / (fwd_ms * 1e-3),
+            "fwd_tokens_per_s": job_rate(w.T, world, fwd_ms),
             "stages_ms": {n: float(v) for n, v in zip(
                 ["route", "permute", "grouped_ffn", "combine", "combine_bwd", "grouped_ffn_bwd",
                  "router_bwd"], stage_ms)},

@@ -1,0 +1,55 @@
+"""Host-side logic of bench.py (CPU only): the multi-rank reduction over gloo
+with two ranks, the whole-job rate, and the reference arm's non-zero ranks."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r timed (1 + r, 10 - r, 5) ms: the job takes the slowest of each
+        got = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 5.0], torch.device("cpu"), world)
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    world, port = 2, _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+    for r in range(world):
+        assert out[r] == [2.0, 10.0, 5.0]
+
+
+def test_single_rank_and_job_rate():
+    assert bench.max_over_ranks([3, 4.5], None, 1) == [3.0, 4.5]
+    # two replicas of 2048 tokens each in 0.5 ms (the slowest): 8.192 M tokens/s
+    assert bench.job_rate(2048, 2, 0.5) == pytest.approx(8.192e6)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "1"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
