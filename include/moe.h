@@ -306,6 +306,14 @@ MOE_API int moe_last_device_status(moe_stream_t stream, int* status);
 /* Number of kernels this library has launched in this process (host counter). */
 MOE_API uint64_t moe_launch_count(void);
 
+/* Self-test of the failure path (no counterpart in the pages): launches one
+ * kernel that waits, with the bounded wait every TMA-fed kernel uses, on an
+ * mbarrier that nothing arrives on.  The wait gives up after limit_ns
+ * nanoseconds (1 ns .. 1 s, else MOE_ERR_INVALID_ARG), records MOE_ERR_TIMEOUT
+ * in the device status word and the kernel returns; read it with
+ * moe_last_device_status.  The GPU context stays usable.                     */
+MOE_API int moe_selftest_bounded_wait(unsigned long long limit_ns, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

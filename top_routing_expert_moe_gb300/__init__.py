@@ -113,6 +113,7 @@ _SIGS = {
     "moe_router_backward": [ctypes.c_void_p] * 17,
     "moe_backward": [ctypes.c_void_p] * 27,
     "moe_last_device_status": [ctypes.c_void_p, ctypes.c_void_p],
+    "moe_selftest_bounded_wait": [ctypes.c_ulonglong, ctypes.c_void_p],
 }
 
 
@@ -198,6 +199,12 @@ def workspace_size(cfg: MoEConfig) -> int:
 
 def launch_count() -> int:
     return int(load_library().moe_launch_count())
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Run the device-side timeout self-test (the status is read with
+    last_device_status())."""
+    _call("moe_selftest_bounded_wait", ctypes.c_ulonglong(int(limit_ns)), _s(stream))
 
 
 def last_device_status(stream=None) -> int:

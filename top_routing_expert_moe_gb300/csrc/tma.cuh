@@ -49,14 +49,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 // Bounded wait.  Returns false when the wait gave up (timeout or another
 // role's abort); the first to time out records the status and raises abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, unsigned long long limit_ns = WAIT_NS) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
         if ((it & 15) == 0) {
             if (*abort_flag) return false;
-            if (gtimer() - t0 > WAIT_NS) {
+            if (gtimer() - t0 > limit_ns) {
                 set_status(status, MOE_ERR_TIMEOUT);
                 *abort_flag = 1;
                 return false;
