@@ -6,11 +6,13 @@
 //
 // A stable counting sort, deterministic (no order-dependent atomics):
 //   1. tile histogram: per 256-token tile, selections per expert;
-//   2. one CTA scans the tiles per expert (rank base of each tile), applies the
-//      capacity, lays out padded segments (offsets) and marks padding rows;
-//   3. per tile, warp ballots give each assignment its rank among the expert's
-//      assignments in token order; rank < C keeps it at row offsets[e] + rank;
-//   4. gather: one warp per destination row copies the token's x row with
+//   2. per tile (one CTA each): the expert's tokens in earlier tiles and in all
+//      tiles (every CTA sums the small histogram itself, so no separate scan
+//      launch), the capacity and the padded segments (offsets); then warp
+//      ballots give each assignment its rank among the expert's assignments in
+//      token order; rank < C keeps it at row offsets[e] + rank; padding rows
+//      are marked, each CTA a strided share of them;
+//   3. gather: one warp per destination row copies the token's x row with
 //      16-byte vectors (zeros on padding rows), rows read from device offsets.
 #include "common.cuh"
 #include "kernels.h"
@@ -42,35 +44,37 @@ __global__ void __launch_bounds__(PT_TOK) tile_hist_kernel(const int32_t* __rest
     if (threadIdx.x < E) tile_counts[(size_t)blockIdx.x * E + threadIdx.x] = h[threadIdx.x];
 }
 
-// One CTA (1024 threads).  A warp per expert scans that expert's tile counts
-// 32 tiles at a time (exclusive prefix = the tile's first rank); thread 0 then
-// applies the capacity and lays out the padded segments.
-__global__ void __launch_bounds__(1024) scan_layout_kernel(
-    const int32_t* __restrict__ tile_counts, int ntiles, int E, int C, int pad_m,
-    int32_t* __restrict__ tile_base, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ perm_token, float* __restrict__ stats)
+// One CTA per 256-token tile.  A warp per expert sums the expert's counts over
+// the earlier tiles (this tile's first rank) and over all tiles; thread 0 then
+// applies the capacity and lays out the padded segments (every CTA finds the
+// same layout; CTA 0 writes offsets, kept and the statistics).
+__global__ void __launch_bounds__(PT_TOK) scan_assign_kernel(
+    const int32_t* __restrict__ topk, int T, int E, int k, int C, int pad_m,
+    const int32_t* __restrict__ tile_counts, int ntiles, int32_t* __restrict__ kept,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token,
+    float* __restrict__ stats)
 {
     pdl_wait();      // the preceding kernel's writes are visible from here on
     pdl_trigger();
-    __shared__ int s_total[64], s_kept[64], s_off[65];
+    __shared__ int s_base[64], s_total[64], s_off[65];
+    __shared__ int wcount[PT_TOK / 32][64];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = warp; e < E; e += 32) {
-        int run = 0;
-        for (int b0 = 0; b0 < ntiles; b0 += 32) {
-            const int b = b0 + lane;
-            const int v = b < ntiles ? tile_counts[(size_t)b * E + e] : 0;
-            int incl = v;
+    const int blk = blockIdx.x;
+    for (int e = warp; e < E; e += PT_TOK / 32) {
+        int before = 0, total = 0;
+        for (int b = lane; b < ntiles; b += 32) {
+            const int v = tile_counts[(size_t)b * E + e];
+            total += v;
+            if (b < blk) before += v;
+        }
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += u;
-            }
-            if (b < ntiles) tile_base[(size_t)b * E + e] = run + incl - v;
-            run += __shfl_sync(0xffffffffu, incl, 31);
+        for (int o = 16; o > 0; o >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, o);
+            total += __shfl_xor_sync(0xffffffffu, total, o);
         }
         if (lane == 0) {
-            s_total[e] = run;
-            s_kept[e] = min(run, C);
+            s_base[e] = before;
+            s_total[e] = total;
         }
     }
     __syncthreads();
@@ -78,40 +82,36 @@ __global__ void __launch_bounds__(1024) scan_layout_kernel(
         int off = 0, kmax = 0;
         long ksum = 0, dropped = 0;
         for (int e = 0; e < E; ++e) {
+            const int ke = min(s_total[e], C);
             s_off[e] = off;
-            offsets[e] = off;
-            kept[e] = s_kept[e];
-            off += (s_kept[e] + pad_m - 1) / pad_m * pad_m;
-            kmax = max(kmax, s_kept[e]);
-            ksum += s_kept[e];
-            dropped += s_total[e] - s_kept[e];
+            if (blk == 0) {
+                offsets[e] = off;
+                kept[e] = ke;
+            }
+            off += (ke + pad_m - 1) / pad_m * pad_m;
+            kmax = max(kmax, ke);
+            ksum += ke;
+            dropped += s_total[e] - ke;
         }
         s_off[E] = off;
-        offsets[E] = off;
-        if (stats) {
-            stats[MOE_STAT_DROPPED] = (float)dropped;
-            stats[MOE_STAT_MAX_OVER_MEAN_KEPT] =
-                ksum > 0 ? (float)kmax / ((float)ksum / (float)E) : 0.f;
+        if (blk == 0) {
+            offsets[E] = off;
+            if (stats) {
+                stats[MOE_STAT_DROPPED] = (float)dropped;
+                stats[MOE_STAT_MAX_OVER_MEAN_KEPT] =
+                    ksum > 0 ? (float)kmax / ((float)ksum / (float)E) : 0.f;
+            }
         }
     }
     __syncthreads();
-    // padding rows carry token -1
+    // padding rows carry token -1 (this CTA: every ntiles-th group of 256 rows)
     for (int e = 0; e < E; ++e) {
-        const int b = s_off[e] + s_kept[e], end = s_off[e + 1];
-        for (int r = b + tid; r < end; r += blockDim.x) perm_token[r] = -1;
+        const int end = s_off[e + 1];
+        for (int r = s_off[e] + min(s_total[e], C) + blk * PT_TOK + tid; r < end; r += ntiles * PT_TOK)
+            perm_token[r] = -1;
     }
-}
-
-__global__ void __launch_bounds__(PT_TOK) assign_kernel(
-    const int32_t* __restrict__ topk, int T, int E, int k, int C,
-    const int32_t* __restrict__ tile_base, const int32_t* __restrict__ offsets,
-    int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_token)
-{
-    pdl_wait();      // the preceding kernel's writes are visible from here on
-    pdl_trigger();
-    __shared__ int wcount[PT_TOK / 32][64];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t = blockIdx.x * PT_TOK + tid;
+    // ranks within the tile: per expert, a ballot over each warp's tokens
+    const int t = blk * PT_TOK + tid;
     int sel[8];
     int inrank[8];
 #pragma unroll
@@ -135,10 +135,10 @@ __global__ void __launch_bounds__(PT_TOK) assign_kernel(
     for (int j = 0; j < k; ++j) {
         const int e = sel[j];
         if (e < 0 || e >= E) { slot_of[(size_t)t * k + j] = -1; continue; }
-        int r = tile_base[(size_t)blockIdx.x * E + e] + inrank[j];
+        int r = s_base[e] + inrank[j];
         for (int w = 0; w < warp; ++w) r += wcount[w][e];
         if (r < C) {
-            const int row = offsets[e] + r;
+            const int row = s_off[e] + r;
             slot_of[(size_t)t * k + j] = row;
             perm_token[row] = t;
         } else {
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const T* __restrict__ 
 
 size_t permute_ws_bytes(const moe_config& c) {
     const size_t ntiles = (size_t)(c.T + PT_TOK - 1) / PT_TOK;
-    return 2 * align_up(ntiles * c.E * 4);
+    return align_up(ntiles * c.E * 4);
 }
 
 int launch_permute(const moe_config& c, const void* x, const int32_t* topk, void* x_perm,
@@ -191,15 +191,11 @@ int launch_permute(const moe_config& c, const void* x, const int32_t* topk, void
 {
     const int ntiles = (c.T + PT_TOK - 1) / PT_TOK;
     int32_t* tile_counts = static_cast<int32_t*>(ws);
-    int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
-                                                    align_up((size_t)ntiles * c.E * 4));
     const int C = capacity_of(c);
     MOE_LAUNCH(tile_hist_kernel, ntiles, PT_TOK, 0, st, topk, c.T, c.E, c.k, tile_counts,
                                                 device_status_ptr());
-    MOE_LAUNCH(scan_layout_kernel, 1, 1024, 0, st, tile_counts, ntiles, c.E, C, c.pad_m, tile_base, kept,
-                                          offsets, perm_token, stats);
-    MOE_LAUNCH(assign_kernel, ntiles, PT_TOK, 0, st, topk, c.T, c.E, c.k, C, tile_base, offsets, slot_of,
-                                             perm_token);
+    MOE_LAUNCH(scan_assign_kernel, ntiles, PT_TOK, 0, st, topk, c.T, c.E, c.k, C, c.pad_m, tile_counts,
+               ntiles, kept, offsets, slot_of, perm_token, stats);
     const int64_t rows = rows_cap_of(c);
     const int grid = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 8);
     if (c.dtype == MOE_DTYPE_BF16)
