@@ -157,7 +157,7 @@ __global__ void transpose_wr_f32_kernel(const T* __restrict__ Wr, float* __restr
 
 // One warp per token: dlogits (gate Jacobian + aux term); with WITH_DX also
 // dx[t] = sum_kept dx_perm[slot] + dlogits[t] . W_r^T (the fp32 path; the bf16
-// path forms dx in router_dx_bf16_kernel on the tensor cores).
+// path forms dx in router_dx_dwr_kernel on the tensor cores).
 template <typename T, bool WITH_DX>
 __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ topk,
@@ -274,23 +274,21 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
 // tile, then half-warps add the kept dx_perm rows (16-byte vectors) and store.
 constexpr int RDX_CW = 128;  // columns per CTA
 
+// CTA (bx, by) of a gx x gy grid: column chunk bx, 16-token tiles by, by + gy, ...
 template <int KS>  // KS = ceil(E / 16) k-steps
-__global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
+__device__ __forceinline__ void router_dx_body(
     const float* __restrict__ dlogits, const __nv_bfloat16* __restrict__ Wr,
     const int32_t* __restrict__ slot_of, const __nv_bfloat16* __restrict__ dx_perm,
     const __nv_bfloat16* __restrict__ dx_shared, int Tn, int d, int E, int k,
-    __nv_bfloat16* __restrict__ dx)
+    __nv_bfloat16* __restrict__ dx, int bx, int by, int gy, uint8_t* smem_raw)
 {
-    pdl_wait();      // the preceding kernel's writes are visible from here on
-    pdl_trigger();
     constexpr int E16 = KS * 16, LDW = E16 + 2, LDO = RDX_CW + 4;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
     __nv_bfloat16* sW = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [128][LDW]
     float* sOut = reinterpret_cast<float*>(smem_raw + align_up_dev(RDX_CW * LDW * 2)); // [8][16][LDO]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
     const int hl = lane & 15, hw = lane >> 4;
-    const int c0 = blockIdx.x * RDX_CW;
+    const int c0 = bx * RDX_CW;
     const int col = c0 + hl * 8;
     for (int i = tid; i < RDX_CW * E16; i += 256) {
         const int cc = i / E16, e = i % E16;
@@ -300,7 +298,7 @@ __global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
     __syncthreads();
     float* so = sOut + warp * 16 * LDO;
     const int ntiles = (Tn + 15) / 16;
-    for (int wt = blockIdx.y * 8 + warp; wt < ntiles; wt += gridDim.y * 8) {
+    for (int wt = by * 8 + warp; wt < ntiles; wt += gy * 8) {
         const int t0 = wt * 16;
         // round trip 1: this tile's dlogits (A fragments) and the half-warp's
         // first two slot indices for its 8 tokens, all independent loads
@@ -414,29 +412,39 @@ __global__ void __launch_bounds__(256, 2) router_dx_bf16_kernel(
 // dlogits over the chunk for dbias.
 constexpr int DWM_STAGES = 4, DWM_LDX = 128 + 8;
 
+// shared memory of one 128-thread dW_r unit: x ring, dlogits ring, dbias partials
+template <int MT>
+constexpr size_t dwr_unit_smem() {
+    return (size_t)DWM_STAGES * 16 * DWM_LDX * 2 + (size_t)DWM_STAGES * 16 * MT * 16 * 4 + 128 * 4;
+}
+
+// 128 threads (tid 0..127, named barrier `bar`) on column chunk bx, token chunk by
 template <int MT>  // MT = ceil(E / 16) expert m-tiles
-__global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __restrict__ x,
-                                                      const float* __restrict__ dlogits, int Tn,
-                                                      int d, int E, int chunk,
-                                                      float* __restrict__ part,
-                                                      float* __restrict__ part_db)
+__device__ __forceinline__ void dwr_mma_body(const __nv_bfloat16* __restrict__ x,
+                                             const float* __restrict__ dlogits, int Tn, int d, int E,
+                                             int chunk, float* __restrict__ part,
+                                             float* __restrict__ part_db, int bx, int by, int tid,
+                                             uint8_t* smem, int bar)
 {
-    pdl_wait();      // the preceding kernel's writes are visible from here on
-    pdl_trigger();
     constexpr int E16 = MT * 16;
-    __shared__ __align__(16) __nv_bfloat16 sX[DWM_STAGES][16][DWM_LDX];
-    __shared__ __align__(16) float sDf[DWM_STAGES][16][E16];   // dlogits tile [token][expert], fp32
-    __shared__ float sDb[128];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto sX = reinterpret_cast<__nv_bfloat16 (*)[16][DWM_LDX]>(smem);
+    auto sDf = reinterpret_cast<float (*)[16][E16]>(smem + (size_t)DWM_STAGES * 16 * DWM_LDX * 2);  // [token][expert]
+    float* sDb = reinterpret_cast<float*>(smem + (size_t)DWM_STAGES * 16 * DWM_LDX * 2 +
+                                          (size_t)DWM_STAGES * 16 * E16 * 4);
+    auto hsync = [bar]() {   // immediate barrier ids: the CTA uses barriers 0-2 only
+        if (bar == 1) asm volatile("bar.sync 1, 128;" ::: "memory");
+        else asm volatile("bar.sync 2, 128;" ::: "memory");
+    };
+    const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;
-    const int c0 = blockIdx.x * 128;
-    const int tbeg = blockIdx.y * chunk, tend = min(Tn, tbeg + chunk);
+    const int c0 = bx * 128;
+    const int tbeg = by * chunk, tend = min(Tn, tbeg + chunk);
     const int nblk16 = (tend - tbeg + 15) / 16;
     // dlogits rows stream with cp.async too when they are 16-byte granular (E % 4
     // == 0), so no synchronous load stalls the ring; columns E..E16 stay zero
     const bool async_dl = (E & 3) == 0;
     for (int i = tid; i < DWM_STAGES * 16 * E16; i += 128) (&sDf[0][0][0])[i] = 0.f;
-    __syncthreads();
+    hsync();
     float db = 0.f;  // this thread's dbias share (expert tid, tid < E16), column chunk 0 only
     auto load = [&](int b, int st) {
         const int t0 = tbeg + b * 16;
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
     }
     for (int b = 0; b < nblk16; ++b) {
         asm volatile("cp.async.wait_group %0;\n" ::"n"(DWM_STAGES - 2));
-        __syncthreads();
+        hsync();
         const int st = b % DWM_STAGES;
         // A = dlogits^T (rows experts, k = tokens), bf16 pairs of consecutive tokens
         uint32_t af[MT][4];
@@ -499,7 +507,7 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
             af[m][2] = pack2(sDf[st][2 * tq + 8][e0], sDf[st][2 * tq + 9][e0]);
             af[m][3] = pack2(sDf[st][2 * tq + 8][e0 + 8], sDf[st][2 * tq + 9][e0 + 8]);
         }
-        if (blockIdx.x == 0 && tid < E16)
+        if (bx == 0 && tid < E16)
 #pragma unroll
             for (int r = 0; r < 16; ++r) db += sDf[st][r][tid];
 #pragma unroll
@@ -536,20 +544,47 @@ __global__ void __launch_bounds__(128) dwr_mma_kernel(const __nv_bfloat16* __res
             for (int h = 0; h < 2; ++h) {
                 const int cc = colb + h;
                 if (cc >= d) continue;
-                float* dst = part + ((size_t)blockIdx.y * d + cc) * E;
+                float* dst = part + ((size_t)by * d + cc) * E;
                 if (e_lo < E) dst[e_lo] = acc[m][n][h];
                 if (e_hi < E) dst[e_hi] = acc[m][n][2 + h];
             }
         }
-    if (blockIdx.x == 0) {
+    if (bx == 0) {
         sDb[tid] = db;
-        __syncthreads();
+        hsync();
         if (tid < E) {
             float a = 0.f;
             for (int i = tid; i < 128; i += E16) a += sDb[i];
-            part_db[(size_t)blockIdx.y * E + tid] = a;
+            part_db[(size_t)by * E + tid] = a;
         }
     }
+}
+
+// dX and the dW_r partials in one launch (both read dlogits only; they run side
+// by side): CTAs 0 .. n_dx - 1 form the gx x gy grid of the dX body, the rest run
+// two 128-thread dW_r units each over the gxm x ns grid of (column, token) chunks.
+template <int KS>
+__global__ void __launch_bounds__(256, 2) router_dx_dwr_kernel(
+    const float* __restrict__ dlogits, const __nv_bfloat16* __restrict__ Wr,
+    const int32_t* __restrict__ slot_of, const __nv_bfloat16* __restrict__ dx_perm,
+    const __nv_bfloat16* __restrict__ dx_shared, const __nv_bfloat16* __restrict__ x, int Tn,
+    int d, int E, int k, __nv_bfloat16* __restrict__ dx, int gx, int gy, int chunk, int gxm,
+    int ns, float* __restrict__ part, float* __restrict__ part_db)
+{
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int bid = blockIdx.x, n_dx = gx * gy;
+    if (bid < n_dx) {
+        router_dx_body<KS>(dlogits, Wr, slot_of, dx_perm, dx_shared, Tn, d, E, k, dx, bid % gx,
+                           bid / gx, gy, smem_raw);
+        return;
+    }
+    const int half = threadIdx.x >> 7;
+    const int u = 2 * (bid - n_dx) + half;   // this unit's (column chunk, token chunk)
+    if (u >= gxm * ns) return;               // (its barrier is its own: the other unit runs on)
+    dwr_mma_body<KS>(x, dlogits, Tn, d, E, chunk, part, part_db, u % gxm, u / gxm, threadIdx.x & 127,
+                     smem_raw + half * dwr_unit_smem<KS>(), 1 + half);
 }
 
 // Partial dW_r over a token chunk: part[s][i][e] = sum_{t in chunk s} x[t,i] dlogits[t,e].
@@ -763,35 +798,32 @@ int launch_combine_backward(const moe_config& c, const void* dout, const void* y
     } while (0)
 
 namespace {
+// dX and the dW_r partials (bf16): one launch of router_dx_dwr_kernel
 template <int KS>
-int launch_router_dx_ks(const moe_config& c, const float* dl, const __nv_bfloat16* Wr,
-                        const int32_t* slot_of, const __nv_bfloat16* dxp,
-                        const __nv_bfloat16* dxs, __nv_bfloat16* dx, cudaStream_t st) {
+int launch_router_dx_dwr_ks(const moe_config& c, const float* dl, const __nv_bfloat16* Wr,
+                            const int32_t* slot_of, const __nv_bfloat16* dxp,
+                            const __nv_bfloat16* dxs, const __nv_bfloat16* x, __nv_bfloat16* dx,
+                            int chunk, int ns, float* part, float* part_db, cudaStream_t st) {
     constexpr int LDW = KS * 16 + 2;
-    const size_t smem = align_up_dev((size_t)RDX_CW * LDW * 2) + (size_t)8 * 16 * (RDX_CW + 4) * 4;
+    const size_t smem_dx = align_up_dev((size_t)RDX_CW * LDW * 2) + (size_t)8 * 16 * (RDX_CW + 4) * 4;
+    const size_t smem = std::max(smem_dx, 2 * dwr_unit_smem<KS>());
     static bool attr = false;
     if (!attr) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(router_dx_bf16_kernel<KS>,
+        MOE_CUDA_TRY(cudaFuncSetAttribute(router_dx_dwr_kernel<KS>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         attr = true;
     }
     const int gx = (c.d + RDX_CW - 1) / RDX_CW;
     const int tiles = (c.T + 15) / 16;
-    // one wave: at most the resident CTA slots (2 per SM), no partial second wave
+    // the dX part: one wave of the resident CTA slots (2 per SM) at most
     const int gy = std::max(1, std::min((tiles + 7) / 8, (2 * num_sms()) / gx));
-    MOE_LAUNCH(router_dx_bf16_kernel<KS>, dim3(gx, gy), 256, smem, st, dl, Wr, slot_of, dxp, dxs, c.T,
-                                                               c.d, c.E, c.k, dx);
+    const int gxm = (c.d + 127) / 128;
+    const int n_dwr = (gxm * ns + 1) / 2;   // two dW_r units per CTA
+    MOE_LAUNCH(router_dx_dwr_kernel<KS>, gx * gy + n_dwr, 256, smem, st, dl, Wr, slot_of, dxp, dxs, x,
+               c.T, c.d, c.E, c.k, dx, gx, gy, chunk, gxm, ns, part, part_db);
     return MOE_OK;
 }
 }  // namespace
-
-int launch_router_dx_bf16(const moe_config& c, const float* dl, const __nv_bfloat16* Wr,
-                          const int32_t* slot_of, const __nv_bfloat16* dxp,
-                          const __nv_bfloat16* dxs, __nv_bfloat16* dx, cudaStream_t st) {
-    if (c.E <= 16) return launch_router_dx_ks<1>(c, dl, Wr, slot_of, dxp, dxs, dx, st);
-    if (c.E <= 32) return launch_router_dx_ks<2>(c, dl, Wr, slot_of, dxp, dxs, dx, st);
-    return launch_router_dx_ks<4>(c, dl, Wr, slot_of, dxp, dxs, dx, st);
-}
 
 size_t router_bwd_ws_bytes(const moe_config& c) {
     const int ns = dwr_nsplit(c);
@@ -838,19 +870,17 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
         MOE_LAUNCH(router_bwd_token_kernel<T, false>, grid, 256, 0, st, logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), nullptr,
             nullptr, c.T, c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau,
             c.aux_coef, dlogits, static_cast<T*>(dx));
-        MOE_TRY_R(launch_router_dx_bf16(c, dlogits, static_cast<const T*>(Wr), slot_of,
-                                        static_cast<const T*>(dx_perm),
-                                        static_cast<const T*>(dx_shared), static_cast<T*>(dx), st));
-        const dim3 mgrid((c.d + 127) / 128, ns);
+        const T* Wr_ = static_cast<const T*>(Wr);
+        const T* dxp_ = static_cast<const T*>(dx_perm);
+        const T* dxs_ = static_cast<const T*>(dx_shared);
+        const T* x_ = static_cast<const T*>(x);
+        T* dx_ = static_cast<T*>(dx);
         if (c.E <= 16)
-            MOE_LAUNCH(dwr_mma_kernel<1>, mgrid, 128, 0, st, static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
-                                                     chunk, part, part_db);
+            MOE_TRY_R(launch_router_dx_dwr_ks<1>(c, dlogits, Wr_, slot_of, dxp_, dxs_, x_, dx_, chunk, ns, part, part_db, st));
         else if (c.E <= 32)
-            MOE_LAUNCH(dwr_mma_kernel<2>, mgrid, 128, 0, st, static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
-                                                     chunk, part, part_db);
+            MOE_TRY_R(launch_router_dx_dwr_ks<2>(c, dlogits, Wr_, slot_of, dxp_, dxs_, x_, dx_, chunk, ns, part, part_db, st));
         else
-            MOE_LAUNCH(dwr_mma_kernel<4>, mgrid, 128, 0, st, static_cast<const T*>(x), dlogits, c.T, c.d, c.E,
-                                                     chunk, part, part_db);
+            MOE_TRY_R(launch_router_dx_dwr_ks<4>(c, dlogits, Wr_, slot_of, dxp_, dxs_, x_, dx_, chunk, ns, part, part_db, st));
         MOE_LAUNCH(dwr_reduce_kernel<T>, (c.d * c.E / 4 + DWR_RED_COLS - 1) / DWR_RED_COLS, DWR_RED_COLS * DWR_RED_GROUPS, 0, st, part, part_db, ns, c.d, c.E, static_cast<T*>(dWr), dbias);
     } else {
         using T = float;
