@@ -807,12 +807,8 @@ int launch_router_dx_dwr_ks(const moe_config& c, const float* dl, const __nv_bfl
     constexpr int LDW = KS * 16 + 2;
     const size_t smem_dx = align_up_dev((size_t)RDX_CW * LDW * 2) + (size_t)8 * 16 * (RDX_CW + 4) * 4;
     const size_t smem = std::max(smem_dx, 2 * dwr_unit_smem<KS>());
-    static bool attr = false;
-    if (!attr) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(router_dx_dwr_kernel<KS>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        attr = true;
-    }
+    static bool attr[64] = {};
+    if (const int r = smem_attr_once(router_dx_dwr_kernel<KS>, smem, attr)) return r;
     const int gx = (c.d + RDX_CW - 1) / RDX_CW;
     const int tiles = (c.T + 15) / 16;
     // the dX part: one wave of the resident CTA slots (2 per SM) at most
@@ -851,19 +847,11 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
     // reduction buffer: 8 token lanes x 32 vectors x (V * EB) floats, V = 16 / sizeof(T)
     const size_t dwr_smem = (size_t)8 * 32 * (c.dtype == MOE_DTYPE_BF16 ? 8 : 4) * DWR_EB * sizeof(float);
     if (c.dtype == MOE_DTYPE_BF16) {
-        static bool attr = false;
-        if (!attr) {
-            MOE_CUDA_TRY(cudaFuncSetAttribute(dwr_partial_kernel<__nv_bfloat16, DWR_EB>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dwr_smem));
-            attr = true;
-        }
+        static bool attr[64] = {};
+        if (const int r = smem_attr_once(dwr_partial_kernel<__nv_bfloat16, DWR_EB>, dwr_smem, attr)) return r;
     } else {
-        static bool attr = false;
-        if (!attr) {
-            MOE_CUDA_TRY(cudaFuncSetAttribute(dwr_partial_kernel<float, DWR_EB>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dwr_smem));
-            attr = true;
-        }
+        static bool attr[64] = {};
+        if (const int r = smem_attr_once(dwr_partial_kernel<float, DWR_EB>, dwr_smem, attr)) return r;
     }
     if (c.dtype == MOE_DTYPE_BF16) {
         using T = __nv_bfloat16;

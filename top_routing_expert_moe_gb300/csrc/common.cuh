@@ -75,6 +75,23 @@ inline cudaError_t launch_pdl_param(void (*kernel)(const P), dim3 grid, dim3 blo
 }
 
 // launch, count the launch, and turn a failure into MOE_ERR_CUDA
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `kernel` on the current
+// device, once per device (function attributes belong to a device's context;
+// `done` is the call site's static per-device flags)
+template <class F>
+inline int smem_attr_once(F* kernel, size_t bytes, bool (&done)[64]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && done[dev]) return MOE_OK;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    if (dev >= 0 && dev < 64) done[dev] = true;
+    return MOE_OK;
+}
+
 #define MOE_LAUNCH(...)                                                  \
     do {                                                                 \
         const cudaError_t _le = ::moe::launch_pdl(__VA_ARGS__);          \

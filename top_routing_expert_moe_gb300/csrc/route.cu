@@ -706,13 +706,8 @@ int launch_route_bf16(const moe_config& c, const void* x, const __nv_bfloat16* W
     const size_t budget = DYN_SMEM - 1024 - extra;
     const int stages = (int)std::min<size_t>(16, budget / STAGE);
     const size_t smem = 1024 + stages * STAGE + extra;
-    static bool attr_set = false;  // the largest size is fixed per instantiation
-    if (!attr_set) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(route_bf16_kernel<NT, TT>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)DYN_SMEM));
-        attr_set = true;
-    }
+    static bool attr_set[64] = {};  // the largest size is fixed per instantiation
+    if (const int ra = smem_attr_once(route_bf16_kernel<NT, TT>, DYN_SMEM, attr_set)) return ra;
     RouteTma P;
     memset(&P, 0, sizeof(P));
     int r = encode_bf16_map(&P.tmX, x, (uint64_t)c.d, (uint64_t)c.T, 1, (uint64_t)c.d * 2,
