@@ -141,8 +141,15 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
+        with open(self.path) as fh:
+            lines = fh.readlines()
+        if not os.environ.get("MOE_BENCH_CLOCKS_DIR"):
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         rows = []
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
