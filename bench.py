@@ -174,32 +174,53 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- oracle leg
-def oracle_step(w, T_s: int, seed: int = 0):
+def router_variant(args=None) -> dict:
+    """The router options of a run (softmax temperature, raw or renormalised gates, a
+    padding mask, Gumbel top-k with the straight-through estimator)."""
+    if args is None:
+        return dict(temperature=1.0, normalize=True, mask=False, straight_through=False)
+    return dict(temperature=args.temperature, normalize=not args.raw_gates,
+                mask=args.padding_mask, straight_through=args.straight_through)
+
+
+def variant_inputs(w, v: dict, seed: int):
+    """Seeded selection noise (Gumbel draws) and token mask of a router variant."""
+    gum = moe_inputs.gumbel(seed, w.T, w.E) if v["straight_through"] else None
+    mask = moe_inputs.padding_mask(seed, w.T) if v["mask"] else None
+    return gum, mask
+
+
+def oracle_step(w, T_s: int, seed: int = 0, v: dict | None = None):
     """One oracle forward + backward on a T_s-token batch of workload w (fp64)."""
     import oracle
     from dataclasses import replace
+    v = v or router_variant()
     ws = replace(w, T=T_s)
     inp = moe_inputs.make_inputs(ws, seed)
-    f64 = {k: moe_inputs.as_f64(v, ws.dtype if k not in ("bias", "noise") else "fp32")
-           for k, v in inp.items()}
+    f64 = {k: moe_inputs.as_f64(v_, ws.dtype if k not in ("bias", "noise") else "fp32")
+           for k, v_ in inp.items()}
+    gum, mask = variant_inputs(ws, v, seed)
+    noise = moe_inputs.as_f64(gum, "fp32") if gum is not None else f64["noise"]
     cfg = oracle.OracleConfig(T=T_s, d=w.d, f=w.f, E=w.E, k=w.k,
                               capacity_factor=float(np.float32(w.capacity_factor)),
                               swiglu=w.swiglu, aux_coef=w.aux_coef, pad_m=128,
-                              f_shared=w.f_shared)
+                              f_shared=w.f_shared, normalize_gates=v["normalize"],
+                              temperature=float(np.float32(v["temperature"])),
+                              straight_through=v["straight_through"])
     sh = dict(Wup_s=f64.get("W_up_s"), Wdown_s=f64.get("W_down_s"), Wgate_s=f64.get("W_gate_s"))
     t0 = time.perf_counter()
     o = oracle.forward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], Wgate=f64["W_gate"],
-                       bias=f64["bias"], noise=f64["noise"], **sh)
+                       bias=f64["bias"], noise=noise, mask=mask, **sh)
     oracle.backward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], o["logits"],
                     o["topk_idx"], o["gate"], o["slot_of"], f64["dout"], Wgate=f64["W_gate"],
                     with_bias=f64["bias"] is not None, **sh)
     return time.perf_counter() - t0
 
 
-def oracle_sample_tokens(w, budget_s: float):
+def oracle_sample_tokens(w, budget_s: float, v: dict | None = None):
     """Token count whose oracle fwd+bwd takes about budget_s on this host."""
     pilot = min(64, w.T)
-    t = max(oracle_step(w, pilot), 1e-3)
+    t = max(oracle_step(w, pilot, v=v), 1e-3)
     return int(max(pilot, min(w.T, pilot * budget_s / t)))
 
 
@@ -214,10 +235,11 @@ def run_reference(args, w):
         return 0
     import oracle
     oracle.build()
-    T_s = oracle_sample_tokens(w, args.ref_budget_s)
+    v = router_variant(args)
+    T_s = oracle_sample_tokens(w, args.ref_budget_s, v)
     for _ in range(args.warmup):
-        oracle_step(w, T_s)
-    times = [oracle_step(w, T_s) for _ in range(args.steps)]
+        oracle_step(w, T_s, v=v)
+    times = [oracle_step(w, T_s, v=v) for _ in range(args.steps)]
     tok_s = T_s / statistics.mean(times)
     sample = (f"oracle fp64 fwd+bwd on a {T_s}-token batch of {w.name} (same d, f, E, k, "
               f"capacity factor), per step")
@@ -225,7 +247,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.mean(times) * w.T / T_s,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, "n/a (CPU)"),
+            "data": "synthetic", "config": workload_config(w, "n/a (CPU)", v),
             "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": oracle_cores(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -234,11 +256,14 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, l2):
+def workload_config(w, l2, v: dict | None = None):
+    v = v or router_variant()
     return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E,
             "top_k": w.k, "capacity_factor": w.capacity_factor,
             "ffn": "swiglu" if w.swiglu else "silu", "gate_noise_std": w.noise_std,
             "zipf_router_bias": w.zipf_bias, "aux_coef": w.aux_coef, "f_shared": w.f_shared,
+            "router": {"temperature": v["temperature"], "normalize_gates": v["normalize"],
+                       "padding_mask": v["mask"], "gumbel_straight_through": v["straight_through"]},
             "l2": l2,
             "parallelism": "replicas (one independent layer per GPU)"}
 
@@ -258,8 +283,11 @@ def run_ours(args, w):
     moe.load_library()
 
     from tests.parity import gpu_cfg, to_torch   # seeded-input marshalling only
-    cfg = gpu_cfg(w)
+    v = router_variant(args)
+    cfg = gpu_cfg(w, normalize=v["normalize"], temperature=v["temperature"],
+                  straight_through=v["straight_through"])
     inp = moe_inputs.make_inputs(w, args.seed + rank)
+    gum, mask_np = variant_inputs(w, v, args.seed + rank)
     dt = w.dtype
     x = to_torch(inp["x"], dt, dev)
     Wr = to_torch(inp["W_r"], dt, dev)
@@ -267,7 +295,8 @@ def run_ours(args, w):
     Wg = to_torch(inp["W_gate"], dt, dev)
     Wd = to_torch(inp["W_down"], dt, dev)
     b = to_torch(inp["bias"], "fp32", dev)
-    nz = to_torch(inp["noise"], "fp32", dev)
+    nz = to_torch(gum if gum is not None else inp["noise"], "fp32", dev)
+    mk = torch.from_numpy(mask_np).to(dev) if mask_np is not None else None
     dout = to_torch(inp["dout"], dt, dev)
     L = moe.MoELayer(cfg, device=dev)
     g = L.grads()
@@ -305,7 +334,7 @@ def run_ours(args, w):
     # one step through the C ABI; optional events around each call (all on `st`)
     def forward(evs=None):
         rec(evs, 0)
-        moe.moe_route(cfg, x, Wr, b, nz, None, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
+        moe.moe_route(cfg, x, Wr, b, nz, mk, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
         rec(evs, 1)
         moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept, L.offsets,
                         L.stats, L.ws, st)
@@ -394,7 +423,7 @@ def run_ours(args, w):
         # per-stage breakdown: each C-ABI call captured as its own CUDA graph and
         # replayed between events (device time, no host launch overhead)
         stage_fns = [
-            lambda: moe.moe_route(cfg, x, Wr, b, nz, None, L.logits, L.topk_idx, L.gate, L.counts,
+            lambda: moe.moe_route(cfg, x, Wr, b, nz, mk, L.logits, L.topk_idx, L.gate, L.counts,
                                   L.stats, L.ws, st),
             lambda: moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept,
                                     L.offsets, L.stats, L.ws, st),
@@ -456,7 +485,8 @@ def run_ours(args, w):
             with torch.cuda.stream(cs):
                 dout_d.copy_(dout_h, non_blocking=True)   # during the forward
                 ev_dout.record(cs)
-            L.forward(x_d, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, stream=st, shared=shared_w)
+            L.forward(x_d, Wr, Wu, Wd, W_gate=Wg, bias=b, noise=nz, token_mask=mk, stream=st,
+                      shared=shared_w)
             ev_fwd.record(st)
             cs.wait_event(ev_fwd)
             with torch.cuda.stream(cs):
@@ -485,8 +515,8 @@ def run_ours(args, w):
         if world == 1 and not args.no_cpu_baseline:
             import oracle
             oracle.build()
-            T_s = oracle_sample_tokens(w, args.cpu_budget_s)
-            t_cpu = oracle_step(w, T_s)
+            T_s = oracle_sample_tokens(w, args.cpu_budget_s, v)
+            t_cpu = oracle_step(w, T_s, v=v)
             cpu = {"value": T_s / t_cpu, "unit": "tokens/s", "cores": oracle_cores(),
                    "kind": "oracle",
                    "sample": f"oracle fp64 fwd+bwd on a {T_s}-token batch of {w.name} "
@@ -498,7 +528,7 @@ def run_ours(args, w):
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dt, "data": "synthetic (seeded normals, random-init weights)",
-            "config": workload_config(w, "flushed before every step (512 MB write)"),
+            "config": workload_config(w, "flushed before every step (512 MB write)", v),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "traffic": None if traffic is None else traffic / launches_gemm,
@@ -545,11 +575,29 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--f-shared", type=int, default=0,
                     help="add shared experts: a dense FFN of this hidden width on every token")
+    ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count")
+    ap.add_argument("--top-k", type=int, default=0, help="override the workload's top-k")
+    ap.add_argument("--temperature", type=float, default=1.0, help="router softmax temperature")
+    ap.add_argument("--raw-gates", action="store_true",
+                    help="gates = softmax probabilities of the selected experts (no renormalising)")
+    ap.add_argument("--padding-mask", action="store_true",
+                    help="right-padded sequences of 128 tokens: padding tokens select no expert")
+    ap.add_argument("--straight-through", action="store_true",
+                    help="Gumbel top-k selection, gates 1, straight-through router gradient")
     args = ap.parse_args(argv)
+    from dataclasses import replace
     w = moe_inputs.get(args.workload)
+    if args.experts:
+        w = replace(w, E=args.experts, name=f"{w.name}+E{args.experts}")
+    if args.top_k:
+        w = replace(w, k=args.top_k, name=f"{w.name}+k{args.top_k}")
     if args.f_shared:
-        from dataclasses import replace
         w = replace(w, f_shared=args.f_shared, name=f"{w.name}+shared{args.f_shared}")
+    tags = ([f"tau{args.temperature:g}"] if args.temperature != 1.0 else []) + \
+           (["rawgates"] if args.raw_gates else []) + (["mask"] if args.padding_mask else []) + \
+           (["gumbelST"] if args.straight_through else [])
+    if tags:
+        w = replace(w, name=w.name + "+" + "+".join(tags))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
