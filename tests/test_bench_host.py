@@ -77,3 +77,24 @@ def test_reference_arm_json_line_on_rank_zero():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("opts,router,name", [
+    (["--straight-through"], {"gumbel_straight_through": True}, "tiny_fp32+gumbelST"),
+    (["--padding-mask", "--temperature", "0.5"], {"padding_mask": True, "temperature": 0.5},
+     "tiny_fp32+tau0.5+mask"),
+    (["--raw-gates", "--top-k", "1"], {"normalize_gates": False}, "tiny_fp32+k1+rawgates"),
+])
+def test_reference_arm_router_variants(opts, router, name):
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_fp32", "--steps", "1", "--warmup", "1", *opts],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    import json
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["config"]["workload"] == name and d["value"] > 0
+    for k, v in router.items():
+        assert d["config"]["router"][k] == v, k
