@@ -77,6 +77,16 @@ def test_ragged_tokens_bf16_top1():
     _report("ragged_top1_bf16", rep)
 
 
+def test_odd_dwr_unit_count_bf16():
+    """d = 384 and 200 tokens: 3 column chunks x 13 token chunks of dW_r, an odd
+    number of 128-thread units, so the last CTA of the router-backward launch runs
+    one unit and its other half returns at once; d also gives three 128-row blocks
+    in dW_up."""
+    w = _w("small_bf16", T=200, d=384, f=256)
+    rep, _ = parity.full_check(w, _edge_inputs(w, seed=61))
+    _report("odd_dwr_units_bf16", rep)
+
+
 def test_k_equals_E_bf16():
     w = _w("small_bf16", T=200, E=4, k=4, d=256, f=256, capacity_factor=0.0)
     rep, _ = parity.full_check(w, _edge_inputs(w))
