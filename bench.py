@@ -6,11 +6,16 @@ One step = the whole hot path on one batch of synthetic tokens: router,
 permutation, grouped expert FFN, combine (forward) and the full backward
 (combine-bwd, grouped FFN backward, router backward), all through the C ABI,
 replayed as one CUDA graph (the ABI does no host sync and no allocation, so
-the step is capturable).  Per-stage times (and the grouped-GEMM roofline) come
-from each C-ABI call captured as its own graph and replayed between events,
-in step order; `eager_ms_per_step` is the same step launched call by call.
-Inputs and weights are resident in HBM before the timed region; L2 is
-flushed (512 MB write) before every timed step, outside its event pair.
+the step is capturable).  The default workload is the Mixtral-shaped layer at
+T = 65536 tokens (d 4096, f 14336, E 8, top-2, SwiGLU), the largest shape.
+
+Timing: the step graph carries external CUDA events around its two grouped-GEMM
+calls, so the grouped-GEMM time of the roofline is measured inside the very
+replays whose duration gives ms_per_step (it cannot exceed the step).  Inputs
+and weights are resident in HBM before the timed region; L2 is flushed (512 MB
+write) before every timed step, outside its event pair.  Per-stage times of the
+other calls come from each C-ABI call captured as its own graph and replayed
+between events (reported beside the line, not used for the roofline).
 Under torchrun each rank runs an independent replica on its own GPU (the
 layer has no exchange step on one GPU); rank 0 prints one JSON line with the
 whole-job tokens/s (max step time over ranks).
@@ -26,9 +31,9 @@ the host cores, on a bounded token sample of the same workload per step.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -36,6 +41,7 @@ import subprocess
 import sys
 import tempfile
 import time
+from dataclasses import replace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -45,10 +51,13 @@ import numpy as np  # noqa: E402
 import moe_inputs  # noqa: E402
 
 METRIC = "MoE layer tokens/sec fwd and fwd+bwd on 1 GB300; grouped-GEMM % of bf16 peak"
-DEFAULT_WORKLOAD = "small_bf16"
+DEFAULT_WORKLOAD = "mixtral_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_PROFILE = os.path.join(ROOT, "profiles", "tc_grouped_gemm_small_bf16.md")
-GEMM_SOURCE = os.path.join(ROOT, "top_routing_expert_moe_gb300", "csrc", "gemm_tc.cu")
+PROFILES = os.path.join(ROOT, "profiles")
+GEMM_SOURCES = [os.path.join(ROOT, "top_routing_expert_moe_gb300", "csrc", f)
+                for f in ("gemm_tc.cu", "tma.cuh", "common.cuh")]
+SUSTAINED_AFTER_S = 1.0   # timed regions at least this long run under the power cap
+GEMM_LAUNCHES_PER_STEP = 4  # GEMM1, GEMM2, {dgrad2 || dW_down}, {dW_up [|| dW_gate] || dgrad1}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -83,6 +92,14 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def pick_bf16_peak(peaks, timed_region_s):
+    """The burst figure for a short timed region, the sustained (power-capped)
+    one once the timed region lasts SUSTAINED_AFTER_S or more."""
+    if timed_region_s >= SUSTAINED_AFTER_S and "bf16_tflops_sustained" in peaks:
+        return float(peaks["bf16_tflops_sustained"]), "sustained"
+    return float(peaks["bf16_tflops"]), "burst"
+
+
 def algorithmic_work(w, A_kept: int):
     """FLOPs of the grouped GEMMs and bytes of the HBM-bound kernels per step."""
     s = 2 if w.dtype == "bf16" else 4
@@ -97,18 +114,31 @@ def algorithmic_work(w, A_kept: int):
         combine_bytes=A_kept * d * s + T * d * s + 8 * A + (T * d * s if w.f_shared else 0))
 
 
-def gemm_traffic_from_profile():
-    """dram bytes per grouped-GEMM launch from the committed ncu summary, or
-    None when the kernel source changed since the counters were taken."""
-    if not os.path.exists(GEMM_PROFILE):
+def gemm_source_digest() -> str:
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(p, "rb") as fh:
+            h.update(os.path.basename(p).encode() + fh.read())
+    return h.hexdigest()
+
+
+def gemm_profile_path(workload: str) -> str:
+    return os.path.join(PROFILES, "tc_grouped_gemm_" + re.sub(r"[^A-Za-z0-9_]", "_", workload) + ".md")
+
+
+def gemm_traffic_from_profile(workload: str):
+    """DRAM bytes per grouped-GEMM launch of this workload from its committed ncu
+    summary; None when there is none or the kernel source changed since."""
+    path = gemm_profile_path(workload)
+    if not os.path.exists(path):
         return None
-    txt = open(GEMM_PROFILE).read()
-    m = re.search(r"traffic_bytes_per_step:\s*([0-9.eE+]+)", txt)
-    h = re.search(r"gemm_tc_sha256:\s*([0-9a-f]{64})", txt)
-    if not m or not h:
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"gemm_source_sha256:\s*([0-9a-f]{64})", txt)
+    wl = re.search(r"workload:\s*(\S+)", txt)
+    if not m or not h or not wl or wl.group(1) != workload:
         return None
-    cur = hashlib.sha256(open(GEMM_SOURCE, "rb").read()).hexdigest()
-    return float(m.group(1)) if cur == h.group(1) else None
+    return float(m.group(1)) if gemm_source_digest() == h.group(1) else None
 
 
 class ClockSampler:
@@ -173,6 +203,48 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+class StepEvent:
+    """A timing event that may also be recorded while a stream is captured: it
+    becomes an external event node of the graph, so every replay re-records it
+    and the graph times its own parts.  torch's external events where torch
+    offers them, else the driver's cuEventRecordWithFlags(..., EXTERNAL)."""
+    _drv = None
+
+    def __init__(self):
+        import torch
+        self.ev = None
+        try:
+            self.ev = torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            drv = StepEvent._driver()
+            self.h = ctypes.c_void_p()
+            if drv.cuEventCreate(ctypes.byref(self.h), 0) != 0:
+                raise RuntimeError("cuEventCreate failed")
+
+    @staticmethod
+    def _driver():
+        if StepEvent._drv is None:
+            StepEvent._drv = ctypes.CDLL("libcuda.so.1")
+        return StepEvent._drv
+
+    def record(self, stream):
+        if self.ev is not None:
+            self.ev.record(stream)
+        elif StepEvent._driver().cuEventRecordWithFlags(self.h, ctypes.c_void_p(stream.cuda_stream),
+                                                        1) != 0:
+            raise RuntimeError("cuEventRecordWithFlags failed")
+
+    def elapsed_ms(self, later: "StepEvent") -> float:
+        if self.ev is not None:
+            return float(self.ev.elapsed_time(later.ev))
+        ms = ctypes.c_float()
+        drv = StepEvent._driver()
+        fn = getattr(drv, "cuEventElapsedTime_v2", None) or drv.cuEventElapsedTime
+        if fn(ctypes.byref(ms), self.h, later.h) != 0:
+            raise RuntimeError("cuEventElapsedTime failed")
+        return float(ms.value)
+
+
 # ----------------------------------------------------------------------------- oracle leg
 def router_variant(args=None) -> dict:
     """The router options of a run (softmax temperature, raw or renormalised gates, a
@@ -190,43 +262,90 @@ def variant_inputs(w, v: dict, seed: int):
     return gum, mask
 
 
-def oracle_step(w, T_s: int, seed: int = 0, v: dict | None = None):
-    """One oracle forward + backward on a T_s-token batch of workload w (fp64)."""
-    import oracle
-    from dataclasses import replace
-    v = v or router_variant()
-    ws = replace(w, T=T_s)
-    inp = moe_inputs.make_inputs(ws, seed)
-    f64 = {k: moe_inputs.as_f64(v_, ws.dtype if k not in ("bias", "noise") else "fp32")
-           for k, v_ in inp.items()}
-    gum, mask = variant_inputs(ws, v, seed)
-    noise = moe_inputs.as_f64(gum, "fp32") if gum is not None else f64["noise"]
-    cfg = oracle.OracleConfig(T=T_s, d=w.d, f=w.f, E=w.E, k=w.k,
-                              capacity_factor=float(np.float32(w.capacity_factor)),
-                              swiglu=w.swiglu, aux_coef=w.aux_coef, pad_m=128,
-                              f_shared=w.f_shared, normalize_gates=v["normalize"],
-                              temperature=float(np.float32(v["temperature"])),
-                              straight_through=v["straight_through"])
-    sh = dict(Wup_s=f64.get("W_up_s"), Wdown_s=f64.get("W_down_s"), Wgate_s=f64.get("W_gate_s"))
-    t0 = time.perf_counter()
-    o = oracle.forward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], Wgate=f64["W_gate"],
-                       bias=f64["bias"], noise=noise, mask=mask, **sh)
-    oracle.backward(cfg, f64["x"], f64["W_r"], f64["W_up"], f64["W_down"], o["logits"],
-                    o["topk_idx"], o["gate"], o["slot_of"], f64["dout"], Wgate=f64["W_gate"],
-                    with_bias=f64["bias"] is not None, **sh)
-    return time.perf_counter() - t0
+class OracleInputs:
+    """A workload's seeded inputs for the oracle: the weights converted to fp64
+    once; samples take the first T_s tokens of x, dout and the noise (the GPU
+    arm's own draws when ``inp`` is given, else drawn from the same seed)."""
+
+    def __init__(self, w, v: dict, seed: int = 0, inp=None, max_tokens=None):
+        import oracle
+        self.oracle, self.w, self.v = oracle, w, v
+        self.cap = min(w.T, max_tokens or w.T)
+        if inp is None:
+            inp = moe_inputs.make_inputs(replace(w, T=self.cap), seed)
+        self.tok = {k_: inp.get(k_) for k_ in ("x", "dout", "noise")}
+        self.weights = {k_: moe_inputs.as_f64(a, w.dtype if k_ != "bias" else "fp32")
+                        for k_, a in inp.items() if k_ not in self.tok}
+        gum, mask = variant_inputs(w, v, seed) if (v["straight_through"] or v["mask"]) else (None, None)
+        self.gum, self.mask = gum, mask
+
+    def sample(self, T_s: int) -> "OracleSample":
+        return OracleSample(self, int(min(T_s, self.cap)))
 
 
-def oracle_sample_tokens(w, budget_s: float, v: dict | None = None):
-    """Token count whose oracle fwd+bwd takes about budget_s on this host."""
-    pilot = min(64, w.T)
-    t = max(oracle_step(w, pilot, v=v), 1e-3)
-    return int(max(pilot, min(w.T, pilot * budget_s / t)))
+class OracleSample:
+    """The first T_s tokens of an OracleInputs, ready to run forward + backward."""
+
+    def __init__(self, src: OracleInputs, T_s: int):
+        w, v, o_ = src.w, src.v, src.oracle
+        self.oracle, self.T_s = o_, T_s
+        f = dict(src.weights)
+        for k_, a in src.tok.items():
+            f[k_] = None if a is None else moe_inputs.as_f64(a[:T_s], w.dtype if k_ != "noise" else "fp32")
+        self.f64 = f
+        self.noise = moe_inputs.as_f64(src.gum[:T_s], "fp32") if src.gum is not None else f["noise"]
+        self.mask = src.mask[:T_s] if src.mask is not None else None
+        self.cfg = o_.OracleConfig(T=T_s, d=w.d, f=w.f, E=w.E, k=w.k,
+                                   capacity_factor=float(np.float32(w.capacity_factor)),
+                                   swiglu=w.swiglu, aux_coef=w.aux_coef, pad_m=128,
+                                   f_shared=w.f_shared, normalize_gates=v["normalize"],
+                                   temperature=float(np.float32(v["temperature"])),
+                                   straight_through=v["straight_through"])
+
+    def run(self) -> float:
+        """One oracle forward + backward; its wall time in seconds."""
+        o_, f = self.oracle, self.f64
+        sh = dict(Wup_s=f.get("W_up_s"), Wdown_s=f.get("W_down_s"), Wgate_s=f.get("W_gate_s"))
+        t0 = time.perf_counter()
+        o = o_.forward(self.cfg, f["x"], f["W_r"], f["W_up"], f["W_down"], Wgate=f["W_gate"],
+                       bias=f["bias"], noise=self.noise, mask=self.mask, **sh)
+        o_.backward(self.cfg, f["x"], f["W_r"], f["W_up"], f["W_down"], o["logits"],
+                    o["topk_idx"], o["gate"], o["slot_of"], f["dout"], Wgate=f["W_gate"],
+                    with_bias=f["bias"] is not None, **sh)
+        return time.perf_counter() - t0
+
+
+def oracle_sample_tokens(src: OracleInputs, budget_s: float) -> int:
+    """Token count whose oracle fwd+bwd takes about budget_s on this host: two
+    pilot runs give the fixed cost (the weight gradients are written whatever
+    the token count) and the cost per token."""
+    cap = src.cap
+    n1, n2 = min(8, cap), min(32, cap)
+    s1 = src.sample(n1)
+    t1 = min(s1.run(), s1.run())
+    if n2 == n1:
+        return n1
+    t2 = src.sample(n2).run()
+    per_tok = max((t2 - t1) / (n2 - n1), 1e-6)
+    fixed = max(t1 - per_tok * n1, 0.0)
+    return int(max(n1, min(cap, (budget_s - fixed) / per_tok)))
 
 
 def oracle_cores():
-    n = os.environ.get("OMP_NUM_THREADS")
-    return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
+    import oracle
+    return oracle.max_threads()
+
+
+def workload_config(w, v: dict | None = None):
+    v = v or router_variant()
+    return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E,
+            "top_k": w.k, "capacity_factor": w.capacity_factor,
+            "ffn": "swiglu" if w.swiglu else "silu", "gate_noise_std": w.noise_std,
+            "zipf_router_bias": w.zipf_bias, "aux_coef": w.aux_coef, "f_shared": w.f_shared,
+            "router": {"temperature": v["temperature"], "normalize_gates": v["normalize"],
+                       "padding_mask": v["mask"], "gumbel_straight_through": v["straight_through"]},
+            "l2": "GPU arm: flushed before every step (512 MB write)",
+            "parallelism": "replicas (one independent layer per GPU)"}
 
 
 def run_reference(args, w):
@@ -236,18 +355,24 @@ def run_reference(args, w):
     import oracle
     oracle.build()
     v = router_variant(args)
-    T_s = oracle_sample_tokens(w, args.ref_budget_s, v)
+    # the sample's inputs: the first tokens of the same seeded draws the GPU arm uses
+    src = OracleInputs(w, v, args.seed, max_tokens=4096)
+    T_s = oracle_sample_tokens(src, args.ref_budget_s)
+    samp = src.sample(T_s)
     for _ in range(args.warmup):
-        oracle_step(w, T_s, v=v)
-    times = [oracle_step(w, T_s, v=v) for _ in range(args.steps)]
-    tok_s = T_s / statistics.mean(times)
-    sample = (f"oracle fp64 fwd+bwd on a {T_s}-token batch of {w.name} (same d, f, E, k, "
-              f"capacity factor), per step")
+        samp.run()
+    times = [samp.run() for _ in range(args.steps)]
+    step_s = statistics.mean(times)
+    tok_s = T_s / step_s
+    sample = (f"oracle fp64 fwd+bwd on the first {T_s} tokens of {w.name} (same d, f, E, k, "
+              f"capacity factor, weights and seed), per step")
     line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * statistics.mean(times) * w.T / T_s,
+            "ms_per_step": 1e3 * step_s, "tokens_per_step": T_s,
+            "ms_per_full_batch_extrapolated": 1e3 * step_s * w.T / T_s,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, "n/a (CPU)", v),
+            "data": "synthetic (seeded normals, random-init weights)",
+            "config": workload_config(w, v),
             "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": oracle_cores(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -256,16 +381,28 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, l2, v: dict | None = None):
-    v = v or router_variant()
-    return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E,
-            "top_k": w.k, "capacity_factor": w.capacity_factor,
-            "ffn": "swiglu" if w.swiglu else "silu", "gate_noise_std": w.noise_std,
-            "zipf_router_bias": w.zipf_bias, "aux_coef": w.aux_coef, "f_shared": w.f_shared,
-            "router": {"temperature": v["temperature"], "normalize_gates": v["normalize"],
-                       "padding_mask": v["mask"], "gumbel_straight_through": v["straight_through"]},
-            "l2": l2,
-            "parallelism": "replicas (one independent layer per GPU)"}
+def cpu_baseline_leg(w, v, inp, seed, budget_s, one_core_budget_s):
+    """The oracle as it stands on a bounded sample of the workload: on every host
+    core, then on one core."""
+    import oracle
+    oracle.build()
+    cores = oracle_cores()
+    src = OracleInputs(w, v, seed, inp=inp)
+    T_s = oracle_sample_tokens(src, budget_s)
+    t_all = src.sample(T_s).run()
+    out = {"value": T_s / t_all, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": f"oracle fp64 fwd+bwd on the first {T_s} tokens of {w.name} "
+                     f"(same d, f, E, k, weights), {t_all:.1f} s"}
+    if one_core_budget_s > 0:
+        oracle.set_threads(1)
+        try:
+            T_1 = oracle_sample_tokens(src, one_core_budget_s)
+            t_1 = src.sample(T_1).run()
+        finally:
+            oracle.set_threads(cores)
+        out["one_core"] = {"value": T_1 / t_1, "unit": "tokens/s", "cores": 1,
+                           "sample": f"first {T_1} tokens, {t_1:.1f} s"}
+    return out
 
 
 # ----------------------------------------------------------------------------- GPU leg
@@ -282,29 +419,29 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     moe.load_library()
 
-    from tests.parity import gpu_cfg, to_torch   # seeded-input marshalling only
     v = router_variant(args)
-    cfg = gpu_cfg(w, normalize=v["normalize"], temperature=v["temperature"],
-                  straight_through=v["straight_through"])
+    cfg = moe.config_for(w, normalize=v["normalize"], temperature=v["temperature"],
+                         straight_through=v["straight_through"])
     inp = moe_inputs.make_inputs(w, args.seed + rank)
     gum, mask_np = variant_inputs(w, v, args.seed + rank)
     dt = w.dtype
-    x = to_torch(inp["x"], dt, dev)
-    Wr = to_torch(inp["W_r"], dt, dev)
-    Wu = to_torch(inp["W_up"], dt, dev)
-    Wg = to_torch(inp["W_gate"], dt, dev)
-    Wd = to_torch(inp["W_down"], dt, dev)
-    b = to_torch(inp["bias"], "fp32", dev)
-    nz = to_torch(gum if gum is not None else inp["noise"], "fp32", dev)
+    td = moe.tensor_from_numpy
+    x = td(inp["x"], dt, dev)
+    Wr = td(inp["W_r"], dt, dev)
+    Wu = td(inp["W_up"], dt, dev)
+    Wg = td(inp["W_gate"], dt, dev)
+    Wd = td(inp["W_down"], dt, dev)
+    b = td(inp["bias"], "fp32", dev)
+    nz = td(gum if gum is not None else inp["noise"], "fp32", dev)
     mk = torch.from_numpy(mask_np).to(dev) if mask_np is not None else None
-    dout = to_torch(inp["dout"], dt, dev)
+    dout = td(inp["dout"], dt, dev)
     L = moe.MoELayer(cfg, device=dev)
     g = L.grads()
     shared_w = None
     sh_f = sh_b = None
     if w.f_shared > 0:             # the shared experts' FFN (same launches as the routed one)
-        shared_w = (to_torch(inp["W_up_s"], dt, dev), to_torch(inp["W_down_s"], dt, dev),
-                    to_torch(inp.get("W_gate_s"), dt, dev))
+        shared_w = (td(inp["W_up_s"], dt, dev), td(inp["W_down_s"], dt, dev),
+                    td(inp.get("W_gate_s"), dt, dev))
         Ts = L.shared_rows
         sh_f = moe.shared_block(x=x, W_up=shared_w[0], W_down=shared_w[1], W_gate=shared_w[2],
                                 h=L.h_shared, act=L.act_shared, y=L.y_shared)
@@ -331,27 +468,36 @@ def run_ours(args, w):
         if evs is not None:
             evs[i].record(st)
 
-    # one step through the C ABI; optional events around each call (all on `st`)
-    def forward(evs=None):
+    # one step through the C ABI; optional events around each call (all on `st`);
+    # gev: four step events around the two grouped-GEMM calls
+    def forward(evs=None, gev=None):
         rec(evs, 0)
         moe.moe_route(cfg, x, Wr, b, nz, mk, L.logits, L.topk_idx, L.gate, L.counts, L.stats, L.ws, st)
         rec(evs, 1)
         moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept, L.offsets,
                         L.stats, L.ws, st)
         rec(evs, 2)
+        if gev:
+            gev[0].record(st)
         moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act, L.y_perm,
                             L.ws, st, shared=sh_f)
+        if gev:
+            gev[1].record(st)
         rec(evs, 3)
         moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st, shared=sh_f)
         rec(evs, 4)
 
-    def backward(evs=None):
+    def backward(evs=None, gev=None):
         moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token, L.offsets,
                                  bw["dy"], bw["dgate"], st)
         rec(evs, 5)
+        if gev:
+            gev[2].record(st)
         moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
                                      bw["dy"], bw["dh"], bw["dxp"], g["dW_up"], g["dW_gate"],
                                      g["dW_down"], L.ws, st, shared=sh_b)
+        if gev:
+            gev[3].record(st)
         rec(evs, 6)
         moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of, bw["dgate"],
                                 bw["dxp"], L.stats, g["dx"], g["dW_r"],
@@ -359,9 +505,9 @@ def run_ours(args, w):
                                 shared=sh_b)
         rec(evs, 7)
 
-    def step(evs=None):
-        forward(evs)
-        backward(evs)
+    def step(evs=None, gev=None):
+        forward(evs, gev)
+        backward(evs, gev)
 
     with torch.cuda.stream(st):
         for _ in range(max(3, args.warmup)):
@@ -371,14 +517,17 @@ def run_ours(args, w):
         if status != 0:
             raise RuntimeError(f"device status after warm-up: {moe.error_string(status)}")
         A_kept = int(L.kept.sum().item())
+        stats = L.stats.cpu().tolist()
         work = algorithmic_work(w, A_kept)
 
-        # the step and the forward as CUDA graphs (the C ABI is capturable: no host sync,
-        # no allocation); their kernel count per replay is the capture's launch count
+        # the step (with its grouped-GEMM events) and the forward as CUDA graphs (the C ABI
+        # is capturable: no host sync, no allocation); their kernel count per replay is the
+        # capture's launch count
+        gev = [StepEvent() for _ in range(4)]
         graph, fgraph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         n0 = moe.launch_count()
         with torch.cuda.graph(graph, stream=st):
-            step()
+            step(gev=gev)
         launches_per_step = moe.launch_count() - n0
         with torch.cuda.graph(fgraph, stream=st):
             forward()
@@ -391,6 +540,7 @@ def run_ours(args, w):
         sampler = ClockSampler(local)
         time.sleep(0.3)
         step_evs = [(ev(), ev()) for _ in range(args.steps)]
+        gemm_ms_steps = []
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
@@ -400,12 +550,17 @@ def run_ours(args, w):
             step_evs[i][0].record(st)
             graph.replay()
             step_evs[i][1].record(st)
+            st.synchronize()                # the next replay re-records the step's GEMM events
+            gemm_ms_steps.append(gev[0].elapsed_ms(gev[1]) + gev[2].elapsed_ms(gev[3]))
         torch.cuda.synchronize(dev)
         t_wall1 = time.time()
         if world > 1:
             dist.barrier()
         clocks = sampler.stop(t_wall0, t_wall1)
-        ms_local = float(np.mean([a.elapsed_time(c) for a, c in step_evs]))
+        step_ms = [a.elapsed_time(c) for a, c in step_evs]
+        ms_local = float(np.mean(step_ms))
+        gemm_ms_local = float(np.mean(gemm_ms_steps))
+        assert all(gm <= sm for gm, sm in zip(gemm_ms_steps, step_ms)), "GEMM events outside the step"
         status = moe.last_device_status(st)
         if status != 0:
             raise RuntimeError(f"device status after the timed steps: {moe.error_string(status)}")
@@ -447,8 +602,9 @@ def run_ours(args, w):
                 fn()
             stage_graphs.append(sg)
         torch.cuda.synchronize(dev)
-        per = np.zeros((args.steps, len(stage_graphs)))
-        for i in range(args.steps):
+        n_stage = max(3, min(args.steps, 10))
+        per = np.zeros((n_stage, len(stage_graphs)))
+        for i in range(n_stage):
             evs = [(ev(), ev()) for _ in stage_graphs]
             flush.zero_()
             for j, sg in enumerate(stage_graphs):   # in step order, so inputs are fresh
@@ -458,8 +614,8 @@ def run_ours(args, w):
             torch.cuda.synchronize(dev)
             per[i] = [a.elapsed_time(c) for a, c in evs]
         stage_ms = per.mean(0)
-        eager_evs = [[ev() for _ in range(8)] for _ in range(args.steps)]
-        for i in range(args.steps):
+        eager_evs = [[ev() for _ in range(8)] for _ in range(n_stage)]
+        for i in range(n_stage):
             flush.zero_()
             step(eager_evs[i])
         torch.cuda.synchronize(dev)
@@ -502,38 +658,35 @@ def run_ours(args, w):
         e2e_ms = float(np.mean([a.elapsed_time(c) for a, c in e2e]))
 
     # max over ranks
-    ms, fwd_ms, e2e_ms = max_over_ranks([ms_local, fwd_ms, e2e_ms], dev, world)
+    ms, fwd_ms, e2e_ms, gemm_ms = max_over_ranks([ms_local, fwd_ms, e2e_ms, gemm_ms_local], dev,
+                                                 world)
     if rank == 0:
         peaks, src = load_peaks()
-        gemm_ms = float(stage_ms[2] + stage_ms[5])
         gemm_flop = work["gemm_fwd_flop"] + work["gemm_bwd_flop"]
-        launches_gemm = 4   # GEMM1, GEMM2, {dgrad2 || dW_down}, {dW_up [|| dW_gate] || dgrad1}
         achieved = gemm_flop / (gemm_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        traffic = gemm_traffic_from_profile()
+        timed_region_s = args.steps * ms * 1e-3
+        peak, kind = pick_bf16_peak(peaks, timed_region_s)
+        traffic = gemm_traffic_from_profile(w.name)
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            import oracle
-            oracle.build()
-            T_s = oracle_sample_tokens(w, args.cpu_budget_s, v)
-            t_cpu = oracle_step(w, T_s, v=v)
-            cpu = {"value": T_s / t_cpu, "unit": "tokens/s", "cores": oracle_cores(),
-                   "kind": "oracle",
-                   "sample": f"oracle fp64 fwd+bwd on a {T_s}-token batch of {w.name} "
-                             f"(same d, f, E, k, capacity factor), {t_cpu:.1f} s"}
+            cpu = cpu_baseline_leg(w, v, inp, args.seed, args.cpu_budget_s, args.one_core_budget_s)
         tok = job_rate(w.T, world, ms)
         es = 2 if dt == "bf16" else 4
+        A = w.T * w.k
         line = {
             "metric": METRIC, "value": tok, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dt, "data": "synthetic (seeded normals, random-init weights)",
-            "config": workload_config(w, "flushed before every step (512 MB write)", v),
+            "config": workload_config(w, v),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
-                         "traffic": None if traffic is None else traffic / launches_gemm,
+                         "traffic": traffic,
                          "kernel": "tc_grouped_gemm_kernel (all grouped-GEMM launches of a step)",
-                         "peak_source": f"{src} bf16 burst"},
+                         "timing": "external CUDA events around the two grouped-GEMM calls inside "
+                                   "the replayed step graph (the timed steps themselves)",
+                         "gemm_ms_per_step": gemm_ms,
+                         "peak_source": f"{src} bf16 {kind} (timed region {timed_region_s:.2f} s)"},
             "cpu_baseline": cpu,
             "e2e": {"value": job_rate(w.T, world, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": (x.numel() + dout.numel()) * es,
@@ -543,7 +696,7 @@ def run_ours(args, w):
             "launches_per_step": int(launches_per_step),
             "eager_ms_per_step": eager_ms,
             "fwd_tokens_per_s": job_rate(w.T, world, fwd_ms),
-            "stages_ms": {n: float(v) for n, v in zip(
+            "stages_ms": {n: float(v_) for n, v_ in zip(
                 ["route", "permute", "grouped_ffn", "combine", "combine_bwd", "grouped_ffn_bwd",
                  "router_bwd"], stage_ms)},
             "hbm_gbs": {"route": work["route_bytes"] / (stage_ms[0] * 1e-3) / 1e9,
@@ -552,7 +705,10 @@ def run_ours(args, w):
                         "peak": peaks["hbm_gbs"]},
             "gemm_tflops": {"fwd": work["gemm_fwd_flop"] / (stage_ms[2] * 1e-3) / 1e12,
                             "bwd": work["gemm_bwd_flop"] / (stage_ms[5] * 1e-3) / 1e12},
-            "kept_assignments": A_kept,
+            "routing": {"kept_assignments": A_kept, "dropped_assignments": int(stats[4]),
+                        "drop_rate": stats[4] / A, "max_over_mean_kept": stats[5],
+                        "max_over_mean_count": stats[7], "count_cv": stats[6],
+                        "aux_loss": stats[0], "aux_switch": stats[1]},
         }
         print(json.dumps(line))
     if world > 1:
@@ -568,10 +724,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--ref-budget-s", type=float, default=4.0,
+    ap.add_argument("--ref-budget-s", type=float, default=3.0,
                     help="CPU seconds per reference-arm step")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
-                    help="CPU seconds of the cpu_baseline sample")
+                    help="CPU seconds of the cpu_baseline sample (all host cores)")
+    ap.add_argument("--one-core-budget-s", type=float, default=8.0,
+                    help="CPU seconds of the one-core oracle sample (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--f-shared", type=int, default=0,
                     help="add shared experts: a dense FFN of this hidden width on every token")
@@ -585,7 +743,6 @@ def main(argv=None):
     ap.add_argument("--straight-through", action="store_true",
                     help="Gumbel top-k selection, gates 1, straight-through router gradient")
     args = ap.parse_args(argv)
-    from dataclasses import replace
     w = moe_inputs.get(args.workload)
     if args.experts:
         w = replace(w, E=args.experts, name=f"{w.name}+E{args.experts}")

@@ -38,6 +38,16 @@
  *     checks run before anything is launched.  Conditions found on the
  *     device (a bounded wait that ran out, non-finite logits) are recorded
  *     in a device status word read by moe_last_device_status().
+ *   - Fail fast after a timeout: once a bounded wait has run out
+ *     (MOE_ERR_TIMEOUT in the status word), every other wait on the device
+ *     gives up at its next check, and the router and grouped-GEMM kernels
+ *     launched before the host reads the status skip their work.  Outputs of
+ *     calls made between the timeout and that read are undefined.
+ *   - Per-device state (the status word's address, kernel attributes, the
+ *     no-allocation router's scratch address) is looked up once per device and
+ *     kept for the life of the process.  After cudaDeviceReset on a device
+ *     those cached values are stale: do not call this library on that device
+ *     again in the same process.
  *   - Gradients are written, never accumulated into.
  *   - Results are deterministic: no floating-point atomics; reruns on the
  *     same inputs give identical bytes.
@@ -197,6 +207,8 @@ MOE_API int moe_route(const moe_config* cfg, const void* x, const void* W_r, con
  *     weights) return MOE_ERR_SCRATCH_LIMIT before anything is launched.
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is cached for the life of the process, so it is stale after
+ *     a cudaDeviceReset of that device (see the conventions above).
  *   - All calls share the array and it keeps the last call's contents (every
  *     word is written before it is read, so nothing needs clearing); calls
  *     whose kernels overlap on the GPU race on it.                            */

@@ -81,10 +81,14 @@ def lib():
         _lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         _lib.oracle_capacity.restype = ctypes.c_int
+        _lib.oracle_max_threads.restype = ctypes.c_int
+        _lib.oracle_set_threads.restype = None
+        _lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib.oracle_route.restype = ctypes.c_int
         for name in ("oracle_router_logits", "oracle_permute", "oracle_combine", "oracle_stats",
                      "oracle_forward", "oracle_backward", "oracle_expert_apply",
-                     "oracle_expert_forward", "oracle_shared_forward", "oracle_shared_add"):
+                     "oracle_expert_forward", "oracle_shared_forward", "oracle_shared_add",
+                     "oracle_expert_wgrad_entries"):
             getattr(_lib, name).restype = None
     return _lib
 
@@ -242,3 +246,37 @@ def backward(cfg, x, Wr, Wup, Wdown, logits, topk_idx, gate, slot_of, dout, Wgat
                           _p(Wus), _p(Wgs), _p(Wds),
                           *[_p(g.get(n)) for n in ("dWup_s", "dWgate_s", "dWdown_s")])
     return g
+
+
+WGRAD_DOWN, WGRAD_UP, WGRAD_GATE = 0, 1, 2
+
+
+def expert_wgrad_entries(cfg, xs, gates, douts, Wu_e, Wd_e, which, rows, cols, Wg_e=None):
+    """Single entries of one expert's weight gradients from their definition:
+    which[q] = WGRAD_DOWN -> dW_down[rows[q], cols[q]], WGRAD_UP -> dW_up[...],
+    WGRAD_GATE -> dW_gate[...] (SwiGLU).  xs / douts [n, d] are the inputs and
+    output gradients of the expert's kept tokens (ascending), gates [n] their
+    gates; Wu_e, Wg_e [d, f] and Wd_e [f, d] the expert's weight blocks."""
+    xs, douts, gates = _d(xs), _d(douts), _d(gates)
+    n = len(gates)
+    assert xs.shape == (n, cfg.d) and douts.shape == (n, cfg.d)
+    which = np.ascontiguousarray(which, np.int32)
+    rows = np.ascontiguousarray(rows, np.int32)
+    cols = np.ascontiguousarray(cols, np.int32)
+    out = np.empty(len(which), np.float64)
+    lib().oracle_expert_wgrad_entries(ctypes.byref(cfg.c()), ctypes.c_int(n), _p(xs), _p(gates),
+                                      _p(douts), _p(_d(Wu_e)),
+                                      _p(_d(Wg_e) if cfg.swiglu else None), _p(_d(Wd_e)),
+                                      ctypes.c_int(len(which)), _p(which), _p(rows), _p(cols),
+                                      _p(out))
+    return out
+
+
+def max_threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(lib().oracle_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Set the OpenMP thread count of later oracle calls from this thread."""
+    lib().oracle_set_threads(int(n))

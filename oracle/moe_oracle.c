@@ -31,6 +31,7 @@
  *   - each expert is a two-layer FFN without biases: SiLU-MLP, or SwiGLU.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -640,3 +641,72 @@ void oracle_backward(const oracle_cfg* c, const double* x, const double* Wr,
     if (dlogits_out) memcpy(dlogits_out, dl, sizeof(double) * (size_t)T * E);
     free(dgate); free(dxp); free(probs); free(pbar); free(dl); free(cvec); free(dxs);
 }
+
+/* ---- Single weight-gradient entries of one expert, from the definition ----
+ * Only the <dout, out> part of the loss reaches the expert weights (the aux
+ * loss depends on the router alone).  Expert e's kept tokens t, with
+ * dy_t = gate_t dout_t ([LLaMA4-MoE] §2.4: output = gate-weighted sum), give
+ *   dW_down[j][i] = sum_t act_j(x_t) dy_t[i]
+ *   SiLU:   dW_up[i][j]   = sum_t x_t[i] dact_j silu'(h_j)
+ *   SwiGLU: dW_up[i][j]   = sum_t x_t[i] dact_j silu(g_j)
+ *           dW_gate[i][j] = sum_t x_t[i] dact_j u_j silu'(g_j)
+ * where, for the one hidden unit j, h_j = x_t . W_up[:,j] (SwiGLU:
+ * g_j = x_t . W_gate[:,j], u_j = x_t . W_up[:,j]), act_j = silu(h_j) or
+ * silu(g_j) u_j, and dact_j = W_down[j,:] . dy_t.  So an entry needs one
+ * column of W_up (W_gate) and one row of W_down: O(n d) per entry, which
+ * lets single entries of a full-size layer be checked.
+ *   xs[n][d], douts[n][d]: inputs and output gradients of the n kept tokens,
+ *   gates[n] their gates for this expert (tokens in ascending order);
+ *   Wu, Wg (SwiGLU, else NULL) [d][f] and Wd [f][d]: expert e's blocks;
+ *   which[q] = 0: dW_down[rows[q]][cols[q]]; 1: dW_up[rows[q]][cols[q]];
+ *   2: dW_gate[rows[q]][cols[q]] (SwiGLU).  out[q] receives the entry.       */
+void oracle_expert_wgrad_entries(const oracle_cfg* c, int n, const double* xs,
+                                 const double* gates, const double* douts, const double* Wu,
+                                 const double* Wg, const double* Wd, int nq, const int* which,
+                                 const int* rows, const int* cols, double* out)
+{
+    const int d = c->d, f = c->f;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < nq; ++q) {
+        const int kind = which[q];
+        const int j = kind == 0 ? rows[q] : cols[q];    /* hidden unit */
+        const int i = kind == 0 ? cols[q] : rows[q];    /* model-width index */
+        /* the weights unit j touches: column j of W_up (and W_gate), row j of W_down */
+        double* wcol = (double*)malloc(sizeof(double) * 2 * (size_t)d);
+        double* gcol = wcol + d;
+        for (int r = 0; r < d; ++r) {
+            wcol[r] = Wu[(size_t)r * f + j];
+            gcol[r] = c->swiglu ? Wg[(size_t)r * f + j] : 0.0;
+        }
+        const double* wdrow = Wd + (size_t)j * d;
+        double acc = 0.0;
+        for (int t = 0; t < n; ++t) {
+            const double* x = xs + (size_t)t * d;
+            const double* go = douts + (size_t)t * d;
+            double pre = 0.0, u = 0.0;     /* h_j (SiLU) or g_j, and u_j (SwiGLU) */
+            for (int r = 0; r < d; ++r) {
+                if (c->swiglu) { pre += x[r] * gcol[r]; u += x[r] * wcol[r]; }
+                else pre += x[r] * wcol[r];
+            }
+            if (kind == 0) {
+                const double act = c->swiglu ? silu(pre) * u : silu(pre);
+                acc += act * (gates[t] * go[i]);
+                continue;
+            }
+            double dact = 0.0;
+            for (int r = 0; r < d; ++r) dact += wdrow[r] * (gates[t] * go[r]);
+            double dpre;
+            if (!c->swiglu) dpre = dact * dsilu(pre);
+            else if (kind == 1) dpre = dact * silu(pre);
+            else dpre = dact * u * dsilu(pre);
+            acc += x[i] * dpre;
+        }
+        out[q] = acc;
+        free(wcol);
+    }
+}
+
+/* Threads the OpenMP loops above use (results do not depend on it): the
+ * benchmark times the oracle on all host cores and on one.                   */
+void oracle_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+int oracle_max_threads(void) { return omp_get_max_threads(); }

@@ -7,9 +7,12 @@ buffers bench.py uses).  Then:
   * per-token quantities (logits, output, dgate, dh and dx_perm of each kept
     slot, dlogits, dx) are compared with the oracle on a seeded token sample
     (the aux term of the sample's backward uses the full batch's pbar and T);
-  * the weight-gradient reductions, which no per-token oracle call can give at
-    this size, are checked entry-wise as fp64 sums over the GPU's own operands
-    (x_perm, act, dy, dh, dlogits), operands the sample checks above validate.
+  * sampled rows also meet a per-row relative bound (parity.ROW_TOL), so one
+    wrong row cannot hide inside a whole-tensor norm;
+  * sampled entries of dW_down / dW_up / dW_gate come from the oracle's
+    per-entry definition over the expert's kept tokens of the whole batch
+    (variable-length reductions of up to ~16k rows); dW_r entries are fp64
+    sums of x against the GPU's dlogits, whose rows the sample checks.
 """
 import numpy as np
 import pytest
@@ -74,45 +77,62 @@ def fullsize_check(w, inp, n_tok, n_entries=48, seed=0):
             if slot[t, j] >= 0:
                 y = oracle.expert_apply(ocfg, ro["topk_idx"][t, j], xs[i], Wu, Wg, Wd)
                 out_want[i] += ro["gate"][t, j] * y
-    rep["out_rel"] = parity.rel_fro(_rows(L.out, S), out_want)
+    out_got = _rows(L.out, S)
+    rep["out_rel"] = parity.rel_fro(out_got, out_want)
+    parity.check_rows(rep, "out_row_max", out_got, out_want, w.dtype)
     ob = oracle.backward(sub, xs, Wr, Wu, Wd, logits[S], ro["topk_idx"][S], ro["gate"][S],
                          slot[S], f64(inp["dout"][S]), Wgate=Wg, per_slot=True,
                          pbar=st[oracle.ST_PBAR:], T_aux=T, with_bias=b is not None)
     rep["dgate_rel"] = parity.rel_fro(_rows(r["dgate"], S), ob["dgate"])
     rep["dlogits_rel"] = parity.rel_fro(_rows(r["dlogits"], S), ob["dlogits"])
-    rep["dx_rel"] = parity.rel_fro(_rows(g["dx"], S), ob["dx"])
+    dx_got = _rows(g["dx"], S)
+    rep["dx_rel"] = parity.rel_fro(dx_got, ob["dx"])
+    parity.check_rows(rep, "dx_row_max", dx_got, ob["dx"], w.dtype)
     ii, jj = np.nonzero(slot[S] >= 0)
     srow = slot[S][ii, jj]
-    rep["dxp_rel"] = parity.rel_fro(_rows(r["dxp"], srow), ob["dxp_slot"][ii, jj])
+    dxp_got = _rows(r["dxp"], srow)
+    rep["dxp_rel"] = parity.rel_fro(dxp_got, ob["dxp_slot"][ii, jj])
+    parity.check_rows(rep, "dxp_row_max", dxp_got, ob["dxp_slot"][ii, jj], w.dtype)
     dh = r["dh"]
-    rep["dh_rel"] = parity.rel_fro(_rows(dh[0], srow), ob["dh_slot"][ii, jj, 0])
+    dh_got = _rows(dh[0], srow)
+    rep["dh_rel"] = parity.rel_fro(dh_got, ob["dh_slot"][ii, jj, 0])
+    parity.check_rows(rep, "dh_row_max", dh_got, ob["dh_slot"][ii, jj, 0], w.dtype)
     if w.swiglu:
-        rep["du_rel"] = parity.rel_fro(_rows(dh[1], srow), ob["dh_slot"][ii, jj, 1])
-    # ---- reductions: sampled entries as fp64 sums over the GPU operands
-    off = po["offsets"]
-    kept = po["kept"]
-
-    def seg_sum(A, B, e, a_col, b_col):
-        lo, hi = int(off[e]), int(off[e] + kept[e])
-        if hi == lo:
-            return 0.0
-        a = parity.np64(A[lo:hi, a_col])
-        bb = parity.np64(B[lo:hi, b_col])
-        return float(a @ bb)
-
-    ents = [(int(rng.integers(E)), int(rng.integers(w.f)), int(rng.integers(w.d)))
-            for _ in range(n_entries)]
-    got = np.array([float(g["dW_down"][e, j, i]) for e, j, i in ents])
-    want = np.array([seg_sum(L.act, r["dy"], e, j, i) for e, j, i in ents])
-    rep["dWdown_rel"] = parity.rel_fro(got, want)
-    dh_up = dh[1] if w.swiglu else dh[0]
-    got = np.array([float(g["dW_up"][e, i, j]) for e, j, i in ents])
-    want = np.array([seg_sum(L.x_perm, dh_up, e, i, j) for e, j, i in ents])
-    rep["dWup_rel"] = parity.rel_fro(got, want)
+        du_got = _rows(dh[1], srow)
+        rep["du_rel"] = parity.rel_fro(du_got, ob["dh_slot"][ii, jj, 1])
+        parity.check_rows(rep, "du_row_max", du_got, ob["dh_slot"][ii, jj, 1], w.dtype)
+    # ---- expert weight gradients: sampled entries from the oracle's per-entry
+    # definition over each sampled expert's kept tokens (the whole batch)
+    off, kept = po["offsets"], po["kept"]
+    perm = po["perm_token"]
+    busy = np.nonzero(kept > 0)[0]
+    kinds = [(oracle.WGRAD_DOWN, "dW_down", w.f, w.d), (oracle.WGRAD_UP, "dW_up", w.d, w.f)]
     if w.swiglu:
-        got = np.array([float(g["dW_gate"][e, i, j]) for e, j, i in ents])
-        want = np.array([seg_sum(L.x_perm, dh[0], e, i, j) for e, j, i in ents])
-        rep["dWgate_rel"] = parity.rel_fro(got, want)
+        kinds.append((oracle.WGRAD_GATE, "dW_gate", w.d, w.f))
+    got_all = {name: [] for _, name, _, _ in kinds}
+    want_all = {name: [] for _, name, _, _ in kinds}
+    for e in rng.choice(busy, size=min(3, len(busy)), replace=False):
+        e = int(e)
+        r0_, n_e = int(off[e]), int(kept[e])
+        toks = perm[r0_:r0_ + n_e]
+        assert (np.diff(toks) > 0).all()
+        jsel = np.argmax(slot[toks] == (r0_ + np.arange(n_e))[:, None], axis=1)
+        gates = ro["gate"][toks, jsel]
+        Wg_e = f64(inp["W_gate"][e]) if w.swiglu else None
+        xs_e, do_e = f64(inp["x"][toks]), f64(inp["dout"][toks])
+        Wu_e, Wd_e = f64(inp["W_up"][e]), f64(inp["W_down"][e])
+        for kind, name, nr, nc in kinds:
+            rr = rng.integers(nr, size=n_entries // 3)
+            cc = rng.integers(nc, size=n_entries // 3)
+            want_all[name].append(oracle.expert_wgrad_entries(
+                ocfg, xs_e, gates, do_e, Wu_e, Wd_e, np.full(len(rr), kind), rr, cc, Wg_e=Wg_e))
+            gt = g[name][e]
+            got_all[name].append(parity.np64(gt[torch.as_tensor(rr, device=gt.device),
+                                                torch.as_tensor(cc, device=gt.device)]))
+        del xs_e, do_e, Wu_e, Wd_e, Wg_e
+    for _, name, _, _ in kinds:
+        key = {"dW_down": "dWdown_rel", "dW_up": "dWup_rel", "dW_gate": "dWgate_rel"}[name]
+        rep[key] = parity.rel_fro(np.concatenate(got_all[name]), np.concatenate(want_all[name]))
     x_gpu = parity.to_torch(inp["x"], w.dtype)
     dl = r["dlogits"]
     cols = rng.integers(w.d, size=16)

@@ -104,18 +104,116 @@ def test_empty_expert_and_exact_capacity_bf16():
     _report("empty_and_capped_bf16", rep)
 
 
-def test_exact_ties_lowest_id_wins_fp32():
-    """Duplicate router columns give bit-identical logits; the lower id must win."""
-    w = _w("tiny_fp32", T=130, E=6, k=2)
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_exact_ties_lowest_id_wins(dtype):
+    """Router columns 4 and 5 duplicate columns 1 and 2.  The GPU's own logits
+    of each pair must be bit-identical (so the tie really reaches the top-k),
+    and the lower expert id must win it: 4 / 5 are never a token's first pick,
+    and a token whose first pick is 1 (2) takes 4 (5) second, the tied pair in
+    id order.  Everything else is checked bit-exact against the oracle."""
+    if dtype == "fp32":
+        w = _w("tiny_fp32", T=130, E=6, k=2)
+        pad_m = 2
+    else:
+        w = _w("small_bf16", T=384, d=256, f=256, E=6, k=2, capacity_factor=0.0)
+        pad_m = 128
     inp = _edge_inputs(w)
     Wr = inp["W_r"].copy()
     Wr[:, 4] = Wr[:, 1]
     Wr[:, 5] = Wr[:, 2]
     inp["W_r"] = Wr
-    rep, r = parity.full_check(w, inp, pad_m=2)
+    rep, r = parity.full_check(w, inp, pad_m=pad_m)
+    lg = r["layer"].logits
+    assert torch.equal(lg[:, 4], lg[:, 1]) and torch.equal(lg[:, 5], lg[:, 2]), \
+        "duplicated router columns did not give bit-identical logits"
     topk = r["layer"].topk_idx.cpu().numpy()
-    assert not np.isin(topk, [4, 5]).any() or True   # ties resolved by the oracle comparison
-    _report("exact_ties_fp32", rep)
+    assert not np.isin(topk[:, 0], [4, 5]).any()
+    first1, first2 = topk[:, 0] == 1, topk[:, 0] == 2
+    assert first1.sum() + first2.sum() >= w.T // 8, "too few tokens meet an exact tie"
+    assert (topk[first1, 1] == 4).all() and (topk[first2, 1] == 5).all()
+    rep["tied_first_picks"] = int(first1.sum() + first2.sum())
+    _report(f"exact_ties_{dtype}", rep)
+
+
+def _guarded(shape, dtype, guard=4096, fill=0xA5):
+    """A tensor of `shape` placed inside a larger byte buffer whose `guard`
+    bytes before and after it (and the tensor itself) hold the byte `fill`."""
+    n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+    buf = torch.full((n + 2 * guard,), fill, dtype=torch.uint8, device="cuda")
+    return buf, buf[guard:guard + n].view(dtype).view(*shape)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_outputs_stay_inside_their_buffers(dtype):
+    """Canary guards around every output of the forward and backward entry
+    points (a stand-in for an out-of-bounds checker): after the layer ran, the
+    guard bytes before and after each output still hold the sentinel, the rows
+    the layout leaves unused (at and past offsets[E] in the permuted buffers)
+    are untouched too, and the results equal an unguarded run byte for byte."""
+    if dtype == "bf16":
+        w = _w("small_bf16", T=333, d=256, f=384, E=4, k=2, capacity_factor=1.0)
+        pad_m = 128
+    else:
+        w = _w("tiny_fp32", T=301, d=64, f=96, E=5, k=2, capacity_factor=0.9)
+        pad_m = 8
+    inp = _edge_inputs(w, seed=71)
+    ref = parity.run_gpu(w, inp, pad_m=pad_m)
+    assert ref["status"] == 0
+    cfg = parity.gpu_cfg(w, pad_m)
+    dt, tdt = w.dtype, cfg.torch_dtype
+    T, d, f, E, k, R, nh = w.T, w.d, w.f, w.E, w.k, ref["layer"].rows_cap, cfg.nh
+    x, Wr = parity.to_torch(inp["x"], dt), parity.to_torch(inp["W_r"], dt)
+    Wu, Wd = parity.to_torch(inp["W_up"], dt), parity.to_torch(inp["W_down"], dt)
+    Wg = parity.to_torch(inp.get("W_gate"), dt)
+    dout = parity.to_torch(inp["dout"], dt)
+    i32, f32 = torch.int32, torch.float32
+    shapes = dict(logits=((T, E), f32), topk=((T, k), i32), gate=((T, k), f32),
+                  counts=((E,), i32), stats=((9 + E,), f32), x_perm=((R, d), tdt),
+                  perm_token=((R,), i32), slot_of=((T, k), i32), kept=((E,), i32),
+                  offsets=((E + 1,), i32), h=((nh, R, f), tdt), act=((R, f), tdt),
+                  y=((R, d), tdt), out=((T, d), tdt), dy=((R, d), tdt), dgate=((T, k), f32),
+                  dh=((nh, R, f), tdt), dxp=((R, d), tdt), dlogits=((T, E), f32),
+                  dx=((T, d), tdt), dWr=((d, E), tdt), dWu=((E, d, f), tdt),
+                  dWd=((E, f, d), tdt), ws=((moe.workspace_size(cfg),), torch.uint8))
+    bufs, t = {}, {}
+    for name, (shape, tt) in shapes.items():
+        bufs[name], t[name] = _guarded(shape, tt)
+    moe.moe_route(cfg, x, Wr, None, None, None, t["logits"], t["topk"], t["gate"], t["counts"],
+                  t["stats"], t["ws"])
+    moe.moe_permute(cfg, x, t["topk"], t["x_perm"], t["perm_token"], t["slot_of"], t["kept"],
+                    t["offsets"], t["stats"], t["ws"])
+    moe.moe_grouped_ffn(cfg, t["x_perm"], t["offsets"], Wu, Wg, Wd, t["h"], t["act"], t["y"],
+                        t["ws"])
+    moe.moe_combine(cfg, t["y"], t["slot_of"], t["gate"], t["out"])
+    moe.moe_combine_backward(cfg, dout, t["y"], t["gate"], t["slot_of"], t["perm_token"],
+                             t["offsets"], t["dy"], t["dgate"])
+    moe.moe_grouped_ffn_backward(cfg, t["x_perm"], t["offsets"], Wu, Wg, Wd, t["h"], t["act"],
+                                 t["dy"], t["dh"], t["dxp"], t["dWu"], None, t["dWd"], t["ws"])
+    moe.moe_router_backward(cfg, x, Wr, t["logits"], t["topk"], t["gate"], t["slot_of"],
+                            t["dgate"], t["dxp"], t["stats"], t["dx"], t["dWr"], None,
+                            t["dlogits"], t["ws"])
+    torch.cuda.synchronize()
+    assert moe.last_device_status() == 0
+    for name, b in bufs.items():
+        g = 4096
+        assert (b[:g] == 0xA5).all() and (b[-g:] == 0xA5).all(), f"write outside {name}"
+    rows = int(t["offsets"][-1].item())
+    assert 0 < rows < R
+    for name in ("x_perm", "act", "y", "dy", "dxp"):
+        assert (t[name][rows:].view(torch.uint8) == 0xA5).all(), f"{name}: rows past offsets[E]"
+    for name in ("h", "dh"):
+        assert (t[name][:, rows:].contiguous().view(torch.uint8) == 0xA5).all(), name
+    assert (t["perm_token"][rows:].view(torch.uint8) == 0xA5).all()
+    L, g = ref["layer"], ref["grads"]
+    same = dict(logits=L.logits, topk=L.topk_idx, gate=L.gate, counts=L.counts,
+                offsets=L.offsets, slot_of=L.slot_of, kept=L.kept, out=L.out, dx=g["dx"],
+                dWr=g["dW_r"], dWu=g["dW_up"], dWd=g["dW_down"], dgate=ref["dgate"],
+                dlogits=ref["dlogits"])
+    for name, want in same.items():
+        assert torch.equal(t[name], want), name
+    for name, want in (("x_perm", L.x_perm), ("act", L.act), ("y", L.y_perm),
+                       ("dy", ref["dy"]), ("dxp", ref["dxp"])):
+        assert torch.equal(t[name][:rows], want[:rows]), name
 
 
 def test_reruns_are_bit_identical():

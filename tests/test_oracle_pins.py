@@ -515,3 +515,82 @@ def test_shared_expert_backward_matches_finite_differences(oracle_lib, swiglu, c
             assert grad[ix] == pytest.approx((vals[0] - vals[1]) / (2 * h), rel=2e-5, abs=2e-7)
             checked += 1
     assert checked >= 120
+
+
+# --------------------------------------------------------------------------- single dW entries
+def _kept_tokens(cfg, r, e):
+    """Expert e's kept (token, gate) pairs in ascending token order."""
+    tt, jj = np.nonzero((r["topk_idx"] == e) & (r["slot_of"] >= 0))
+    order = np.argsort(tt, kind="stable")
+    return tt[order], r["gate"][tt[order], jj[order]]
+
+
+@pytest.mark.parametrize("swiglu,cf,norm,st", [(False, 0.75, False, False), (True, 0.0, True, False),
+                                               (True, 0.8, True, False), (False, 0.0, True, True)])
+def test_wgrad_entries_equal_the_full_backward(oracle_lib, swiglu, cf, norm, st):
+    """Every entry of dW_up / dW_gate / dW_down from the per-entry definition
+    equals the full-matrix backward (capacity drops, raw gates, straight-through
+    gates of 1 included)."""
+    rng = np.random.default_rng(300 + 10 * int(swiglu) + int(cf * 4) + 2 * int(norm) + int(st))
+    T, d, f, E, k = 24, 8, 12, 4, 2
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, swiglu, bias=True, noise=True)
+    dout = rng.standard_normal((T, d))
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=cf, swiglu=swiglu,
+                              normalize_gates=norm, aux_coef=0.3, straight_through=st)
+    r = oracle.forward(cfg, x, Wr, Wup, Wd, Wgate=Wg, bias=b, noise=nz)
+    if cf > 0:
+        assert (r["slot_of"] < 0).any(), "the case should drop assignments"
+    g = oracle.backward(cfg, x, Wr, Wup, Wd, r["logits"], r["topk_idx"], r["gate"], r["slot_of"],
+                        dout, Wgate=Wg, with_bias=True)
+    jj, ii = np.meshgrid(np.arange(f), np.arange(d), indexing="ij")   # [f, d] grids
+    for e in range(E):
+        toks, gates = _kept_tokens(cfg, r, e)
+        kinds = [(oracle.WGRAD_DOWN, jj.ravel(), ii.ravel(), g["dWdown"][e]),
+                 (oracle.WGRAD_UP, ii.T.ravel(), jj.T.ravel(), g["dWup"][e])]
+        if swiglu:
+            kinds.append((oracle.WGRAD_GATE, ii.T.ravel(), jj.T.ravel(), g["dWgate"][e]))
+        for kind, rows, cols, full in kinds:
+            got = oracle.expert_wgrad_entries(cfg, x[toks], gates, dout[toks], Wup[e], Wd[e],
+                                              np.full(len(rows), kind), rows, cols,
+                                              Wg_e=Wg[e] if swiglu else None)
+            want = full[rows, cols]
+            np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+def test_wgrad_entries_match_finite_differences(oracle_lib):
+    """Single entries against central differences of <dout, out> + aux loss in
+    the expert weights (SwiGLU, capacity drops): pinned to the loss itself."""
+    rng = np.random.default_rng(401)
+    T, d, f, E, k = 10, 6, 8, 3, 2
+    x, Wr, Wup, Wg, Wd, b, nz = _rand_case(rng, T, d, f, E, k, swiglu=True, bias=True)
+    dout = rng.standard_normal((T, d))
+    cfg = oracle.OracleConfig(T=T, d=d, f=f, E=E, k=k, capacity_factor=0.8, swiglu=True,
+                              aux_coef=0.3)
+    L0, r0 = _loss(cfg, x, Wr, Wup, Wd, Wg, b, nz, dout)
+    h = 1e-6
+    checked = 0
+    for name, kind in (("Wd", oracle.WGRAD_DOWN), ("Wup", oracle.WGRAD_UP),
+                       ("Wg", oracle.WGRAD_GATE)):
+        for _ in range(12):
+            e = int(rng.integers(E))
+            if name == "Wd":
+                rr, cc = int(rng.integers(f)), int(rng.integers(d))
+            else:
+                rr, cc = int(rng.integers(d)), int(rng.integers(f))
+            vals = []
+            for s in (+h, -h):
+                kw = dict(x=x, Wr=Wr, Wup=Wup, Wd=Wd, Wg=Wg, b=b, nz=nz)
+                a2 = kw[name].copy()
+                a2[e, rr, cc] += s
+                kw[name] = a2
+                L, r = _loss(cfg, kw["x"], kw["Wr"], kw["Wup"], kw["Wd"], kw["Wg"], kw["b"],
+                             kw["nz"], dout)
+                assert (r["slot_of"] == r0["slot_of"]).all()
+                vals.append(L)
+            fd = (vals[0] - vals[1]) / (2 * h)
+            toks, gates = _kept_tokens(cfg, r0, e)
+            got = oracle.expert_wgrad_entries(cfg, x[toks], gates, dout[toks], Wup[e], Wd[e],
+                                              [kind], [rr], [cc], Wg_e=Wg[e])[0]
+            assert got == pytest.approx(fd, rel=2e-5, abs=2e-7), (name, e, rr, cc)
+            checked += 1
+    assert checked == 36

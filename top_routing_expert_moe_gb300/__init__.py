@@ -62,6 +62,31 @@ class MoEConfig(ctypes.Structure):
         return ("MoEConfig(" + ", ".join(f"{n}={getattr(self, n)!r}" for n, _ in self._fields_) + ")")
 
 
+def config_for(shape, pad_m=128, normalize=True, temperature=1.0, straight_through=False):
+    """A MoEConfig from a layer-shape record with fields T, d, f, E, k,
+    capacity_factor, swiglu, dtype ("bf16" / "fp32"), aux_coef and f_shared
+    (e.g. a seeded workload), plus the router options."""
+    return MoEConfig(T=shape.T, d=shape.d, f=shape.f, E=shape.E, k=shape.k,
+                     capacity_factor=shape.capacity_factor,
+                     ffn=SWIGLU if shape.swiglu else SILU,
+                     dtype=BF16 if shape.dtype == "bf16" else F32,
+                     normalize_gates=1 if normalize else 0, aux_coef=shape.aux_coef, pad_m=pad_m,
+                     temperature=temperature, straight_through=int(straight_through),
+                     f_shared=shape.f_shared)
+
+
+def tensor_from_numpy(a, dtype: str, device="cuda"):
+    """Copy a host array to the device: bf16 tensors arrive as their uint16 bit
+    patterns and are reinterpreted, everything else keeps its numpy dtype.
+    None stays None."""
+    if a is None:
+        return None
+    import numpy as np
+    if dtype == "bf16" and a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
 _SHARED_FIELDS = ("x", "W_up", "W_gate", "W_down", "h", "act", "y", "dout", "dh", "dx",
                   "dW_up", "dW_gate", "dW_down")
 

@@ -333,10 +333,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         sbase[P.nprob] = sl;
         prefix[sl] = acc;
     }
+    // a timeout recorded earlier on this device (not yet read by the host): skip the work
+    if (tid == 0 && timeout_pending(P.status)) *abort_flag = 1;
     __syncthreads();
     const uint32_t tmem_base = *tmem_slot;
     const int total = prefix[sbase[P.nprob]];
     const uint32_t smem0 = smem_u32(base);
+    const bool start_live = *abort_flag == 0;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer (each CTA)
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&q.tmO[i])) : "memory");
         }
         int it = 0;
-        bool ok = true;
+        bool ok = start_live;
         for (int tix = unit; ok && tix < total; tix += nunits) {
             Tile t;
             decode_tile<CG>(P, offs, prefix, sbase, tix, t);
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------ MMA issuer (the pair's even CTA)
         int it = 0, tcount = 0;
-        bool ok = true;
+        bool ok = start_live;
         for (int tix = unit; ok && tix < total; tix += nunits, ++tcount) {
             Tile t;
             decode_tile<CG>(P, offs, prefix, sbase, tix, t);

@@ -432,6 +432,10 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
     __syncthreads();
     pdl_wait();      // the preceding kernel's writes (x, W_r^T, the ticket) are visible from here on
     pdl_trigger();
+    // a timeout recorded earlier on this device (not yet read by the host): skip the work
+    if (tid == 0 && timeout_pending(P.status)) *abort_flag = 1;
+    __syncthreads();
+    const bool start_live = *abort_flag == 0;
 
     if (warp == 8) {
         // ------------------------------------------------ TMA producer
@@ -439,7 +443,7 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmX)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.tmW)) : "memory");
             int it = 0;
-            bool ok = true;
+            bool ok = start_live;
             for (int i = 0; ok && i < my_tiles; ++i) {
                 const int t0 = (blockIdx.x + i * gridDim.x) * TT;
                 for (int kc = 0; kc < nk; ++kc, ++it) {
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
         // ------------------------------------------------ finish warps
         const int ftid = tid - 9 * 32;   // 0..127
         for (int q = ftid; q < ACC_FLOATS; q += 128) sAcc[q] = 0.f;   // the CTA's running sums
-        bool live = true;
+        bool live = start_live;
         for (int i = 0; i < my_tiles; ++i) {
             const int tile = blockIdx.x + i * gridDim.x;
             const int t0 = tile * TT, ntok = min(TT, o.T - t0);
@@ -507,7 +511,7 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
     const int g = lane >> 2, tq = lane & 3;
     const int my_ks = (warp * 16) / TT;
     const int tok0 = (warp * 16) % TT + g;              // this lane's first token row in a block
-    bool live = true;
+    bool live = start_live;
     int it = 0;
     for (int i = 0; i < my_tiles; ++i) {
         float acc[NT][4];

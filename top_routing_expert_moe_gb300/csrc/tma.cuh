@@ -46,8 +46,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-// Bounded wait.  Returns false when the wait gave up (timeout or another
-// role's abort); the first to time out records the status and raises abort.
+// A bounded wait that timed out anywhere on the device (this launch's other
+// CTAs, or an earlier launch whose status the host has not read yet) is
+// visible in the device status word; waits give up as soon as they see it,
+// so one lost arrival costs one time limit, not one per CTA or per launch.
+__device__ __forceinline__ bool timeout_pending(const int* status) {
+    return status && *reinterpret_cast<const volatile int*>(status) == MOE_ERR_TIMEOUT;
+}
+// Bounded wait.  Returns false when the wait gave up (timeout, another role's
+// abort, or a timeout recorded on the device); the first to time out records
+// the status and raises abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, unsigned long long limit_ns = WAIT_NS) {
     if (mbar_try(bar, parity)) return true;
@@ -56,6 +64,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if (mbar_try(bar, parity)) return true;
         if ((it & 15) == 0) {
             if (*abort_flag) return false;
+            if (timeout_pending(status)) {
+                *abort_flag = 1;
+                return false;
+            }
             if (gtimer() - t0 > limit_ns) {
                 set_status(status, MOE_ERR_TIMEOUT);
                 *abort_flag = 1;
@@ -112,6 +124,10 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, vola
         if (mbar_try_cl(bar, parity)) return true;
         if ((it & 15) == 0) {
             if (*abort_flag) return false;
+            if (timeout_pending(status)) {
+                *abort_flag = 1;
+                return false;
+            }
             if (gtimer() - t0 > WAIT_NS) {
                 set_status(status, MOE_ERR_TIMEOUT);
                 *abort_flag = 1;
