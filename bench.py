@@ -12,8 +12,9 @@ T = 65536 tokens (d 4096, f 14336, E 8, top-2, SwiGLU), the largest shape.
 Timing: the step graph carries external CUDA events around its two grouped-GEMM
 calls, so the grouped-GEMM time of the roofline is measured inside the very
 replays whose duration gives ms_per_step (it cannot exceed the step).  Inputs
-and weights are resident in HBM before the timed region; L2 is flushed (512 MB
-write) before every timed step, outside its event pair.  Per-stage times of the
+and weights are resident in HBM before the timed region; L2 is flushed before
+every timed step, outside its event pair (a 512 MB write, then a 1 GB read that
+also pushes the written lines back to DRAM before the step starts).  Per-stage times of the
 other calls come from each C-ABI call captured as its own graph and replayed
 between events (reported beside the line, not used for the roofline).
 Under torchrun each rank runs an independent replica on its own GPU (the
@@ -344,7 +345,7 @@ def workload_config(w, v: dict | None = None):
             "zipf_router_bias": w.zipf_bias, "aux_coef": w.aux_coef, "f_shared": w.f_shared,
             "router": {"temperature": v["temperature"], "normalize_gates": v["normalize"],
                        "padding_mask": v["mask"], "gumbel_straight_through": v["straight_through"]},
-            "l2": "GPU arm: flushed before every step (512 MB write)",
+            "l2": "GPU arm: flushed before every step (512 MB write, then 1 GB read)",
             "parallelism": "replicas (one independent layer per GPU)"}
 
 
@@ -452,7 +453,15 @@ def run_ours(args, w):
             dx=torch.empty(Ts, w.d, dtype=cfg.torch_dtype, device=dev),
             dW_up=g["dW_up_s"], dW_gate=g["dW_gate_s"], dW_down=g["dW_down_s"])
     st = torch.cuda.Stream(dev)           # a side stream: graphs cannot capture the default one
-    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(256 * 2**20, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        """Evict L2 before a timed step: write 512 MB, then read 1 GB of another
+        buffer so the written lines are also written back to DRAM here, outside
+        the step's events (otherwise the first timed kernel pays for them)."""
+        flush_w.zero_()
+        flush_r.sum()
     R = L.rows_cap
     bw = dict(dy=torch.empty(R, w.d, dtype=cfg.torch_dtype, device=dev),
               dgate=torch.empty(w.T, w.k, dtype=torch.float32, device=dev),
@@ -546,7 +555,7 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         t_wall0 = time.time()
         for i in range(args.steps):
-            flush.zero_()                   # L2 flush, outside the step's events
+            flush_l2()                      # outside the step's events
             step_evs[i][0].record(st)
             graph.replay()
             step_evs[i][1].record(st)
@@ -568,7 +577,7 @@ def run_ours(args, w):
         # forward only (graph)
         fwd_evs = [(ev(), ev()) for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             fwd_evs[i][0].record(st)
             fgraph.replay()
             fwd_evs[i][1].record(st)
@@ -606,7 +615,7 @@ def run_ours(args, w):
         per = np.zeros((n_stage, len(stage_graphs)))
         for i in range(n_stage):
             evs = [(ev(), ev()) for _ in stage_graphs]
-            flush.zero_()
+            flush_l2()
             for j, sg in enumerate(stage_graphs):   # in step order, so inputs are fresh
                 evs[j][0].record(st)
                 sg.replay()
@@ -616,7 +625,7 @@ def run_ours(args, w):
         stage_ms = per.mean(0)
         eager_evs = [[ev() for _ in range(8)] for _ in range(n_stage)]
         for i in range(n_stage):
-            flush.zero_()
+            flush_l2()
             step(eager_evs[i])
         torch.cuda.synchronize(dev)
         eager_ms = float(np.mean([e_[0].elapsed_time(e_[7]) for e_ in eager_evs]))
@@ -632,7 +641,7 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         e2e = []
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             e0, e1 = ev(), ev()
             ev_dout, ev_fwd, ev_out = ev(), ev(), ev()
             e0.record(st)

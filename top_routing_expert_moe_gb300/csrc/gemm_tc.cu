@@ -38,6 +38,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -60,6 +61,15 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
 constexpr int RASTER_GM = 16;
+// Progress sync of the units (CTA pairs) of a long launch: a unit's TMA producer
+// counts the k-steps it has issued in chunks of SYNC_CHUNK and does not start
+// chunk g before every unit has issued chunk g - SYNC_SLACK (or has no tiles
+// left).  Units then stay within a few chunks of each other, so tiles that
+// share an operand's k-slices ask for them while L2 still holds them.
+constexpr bool GEMM_SYNC = false;
+constexpr uint32_t SYNC_CHUNK = 16, SYNC_SLACK = 1;
+constexpr int SYNC_MAX_CHUNKS = 65536;
+constexpr int SPLIT_MIN_WAVES = 16;   // "many waves of tiles": a launch this long is split / synced
 
 enum Epi { EPI_STORE = 0, EPI_SILU_FWD = 1, EPI_SWIGLU_FWD = 2, EPI_SILU_BWD = 3, EPI_SWIGLU_BWD = 4 };
 enum Sched { SCHED_ROWS = 0, SCHED_KSEG = 1 };
@@ -98,6 +108,10 @@ struct TcParams {
     const int32_t* offsets;
     int* status;
     int nprob, E;
+    // progress counters that keep the CTA pairs of a long launch together (zeroed
+    // before the launch; NULL: off): [0] units done, [1 .. 1 + sync_n) chunk arrivals
+    uint32_t* sync;
+    int sync_n;
 };
 static_assert(sizeof(TcParams) <= 32764, "kernel parameters within the 32 KB launch limit");
 
@@ -136,18 +150,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float* v) {
-    const uint4* q = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 u = q[i];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-            v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
-    }
+// element i (0..31) of 32 consecutive bf16 values held in four 16-byte words
+__device__ __forceinline__ float bf16_at(const uint4 (&w)[4], int i) {
+    const uint4 q = w[i >> 3];
+    const uint32_t x = ((i >> 1) & 3) == 0 ? q.x : ((i >> 1) & 3) == 1 ? q.y : ((i >> 1) & 3) == 2 ? q.z : q.w;
+    return __uint_as_float((i & 1) ? (x & 0xFFFF0000u) : (x << 16));
 }
 
 // bf16-path activations: fast exp and approximate divide (no slow-path
@@ -156,6 +163,31 @@ __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f 
 __device__ __forceinline__ float dsilu_fast(float z) {
     const float s = __fdividef(1.0f, 1.0f + __expf(-z));
     return s * (1.0f + z * (1.0f - s));
+}
+
+// Bounded wait until arrive + done >= need (both counters only grow).
+__device__ __forceinline__ bool sync_wait(const uint32_t* arrive, const uint32_t* done, uint32_t need,
+                                          volatile int* abort_flag, int* status) {
+    const volatile uint32_t* a = arrive;
+    const volatile uint32_t* d = done;
+    if (*a + *d >= need) return true;
+    const unsigned long long t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(64);
+        if (*a + *d >= need) return true;
+        if ((it & 15) == 0) {
+            if (*abort_flag) return false;
+            if (timeout_pending(status)) {
+                *abort_flag = 1;
+                return false;
+            }
+            if (gtimer() - t0 > WAIT_NS) {
+                set_status(status, MOE_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------- schedule
@@ -358,6 +390,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         }
         int it = 0;
         bool ok = start_live;
+        // progress sync: the unit's k-steps issued so far (one CTA of each unit counts)
+        const bool sync_on = GEMM_SYNC && P.sync != nullptr && (CG == 1 || leader);
+        uint32_t* const sync_done = P.sync;
+        uint32_t* const sync_arrive = P.sync + 1;
+        uint32_t ks = 0;
         for (int tix = unit; ok && tix < total; tix += nunits) {
             Tile t;
             decode_tile<CG>(P, offs, prefix, sbase, tix, t);
@@ -381,6 +418,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const uint32_t b_bytes = (uint32_t)bcols * BK * 2u;
             const uint32_t stage_tx = CG * ((uint32_t)A_BYTES + b_bytes);   // both CTAs' bytes
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
+                if (sync_on && ks % SYNC_CHUNK == 0) {   // chunk g = ks / SYNC_CHUNK starts here
+                    const uint32_t g = ks / SYNC_CHUNK;
+                    if (g >= SYNC_SLACK && g - SYNC_SLACK < (uint32_t)P.sync_n &&
+                        !sync_wait(sync_arrive + (g - SYNC_SLACK), sync_done, (uint32_t)nunits,
+                                   abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 const int s = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status)) { ok = false; break; }
@@ -418,8 +464,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                             ld(phase ? tB1 : tB0, sB + c * 8192, k0, bn0 + 64 * c, t.e);
                     }
                 }
+                ++ks;
+                if (sync_on && ks % SYNC_CHUNK == 0 && ks / SYNC_CHUNK - 1 < (uint32_t)P.sync_n)
+                    atomicAdd(sync_arrive + (ks / SYNC_CHUNK - 1), 1u);   // chunk done
             }
         }
+        if (sync_on) atomicAdd(sync_done, 1u);   // no further chunks from this unit
         // drain: every load issued has landed before the CTA may exit (for a
         // pair, the even CTA's "full" barriers count both CTAs' loads)
         if (CG == 1 || leader)
@@ -517,14 +567,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const int c_lo = half * (width / 64), c_hi = c_lo + width / 64;  // 32-column chunks
             const int acc = tcount & 1;
             const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
-            const bool got = CG == 1 ? mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, P.status)
-                                     : mbar_wait_cl(smem_u32(&tfull[acc]), aph, abort_flag, P.status);
-            if (!got) break;
-            tc_fence_after();
             const bool valid = t.mb + (int)rank < t.mb_e;   // this CTA's half lies in the segment
             const long long row = (long long)t.m0 + (long long)rank * BM + row_in_tile;
             const long long obase = (q.sched == SCHED_KSEG ? (long long)t.e * q.out_estride : 0) +
                                     row * q.ldo + t.n0;
+            // The backward epilogues' inputs (h, or g and u) do not depend on the
+            // accumulator: the first chunk's are fetched before waiting for it, each
+            // later chunk's while the one before is processed (kept as packed bf16).
+            const int n_in = q.epi == EPI_SWIGLU_BWD ? 2 : (q.epi == EPI_SILU_BWD ? 1 : 0);
+            uint4 nxt[2][4];
+            auto fetch = [&](int c) {
+                const uint4* p0 = reinterpret_cast<const uint4*>(q.in0 + obase + c * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) nxt[0][j] = p0[j];
+                if (n_in == 2) {
+                    const uint4* p1 = reinterpret_cast<const uint4*>(q.in1 + obase + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) nxt[1][j] = p1[j];
+                }
+            };
+            if (valid && n_in) fetch(c_lo);
+            const bool got = CG == 1 ? mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, P.status)
+                                     : mbar_wait_cl(smem_u32(&tfull[acc]), aph, abort_flag, P.status);
+            if (!got) break;
+            tc_fence_after();
             // box coordinates of this warp's 32 rows: (column, row or M index, expert)
             const int brow = t.m0 + (int)rank * BM + qd * 32;
             const int bz = q.sched == SCHED_KSEG ? t.e : 0;
@@ -550,6 +616,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     put(&q.tmO[2], v, bcol, brow, bz);
                     continue;
                 }
+                uint4 cur[2][4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) { cur[0][j] = nxt[0][j]; cur[1][j] = nxt[1][j]; }
+                if (n_in && c + 1 < c_hi) fetch(c + 1);
                 tmem_wait_ld();
                 if (q.epi == EPI_STORE) {
                     put(&q.tmO[0], v, bcol, brow, bz);
@@ -559,21 +629,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     for (int i = 0; i < 32; ++i) v[i] = silu_fast(v[i]);
                     put(&q.tmO[1], v, bcol, brow, bz);
                 } else if (q.epi == EPI_SILU_BWD) {
-                    float h[32];
-                    load32_bf16(q.in0 + obase + c * 32, h);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= dsilu_fast(h[i]);
+                    for (int i = 0; i < 32; ++i) v[i] *= dsilu_fast(bf16_at(cur[0], i));
                     put(&q.tmO[0], v, bcol, brow, bz);
-                } else {  // EPI_SWIGLU_BWD: v = dact
-                    float g[32], u[32], o[32];
-                    load32_bf16(q.in0 + obase + c * 32, g);
-                    load32_bf16(q.in1 + obase + c * 32, u);
+                } else {  // EPI_SWIGLU_BWD: v = dact; dg = dact u silu'(g), du = dact silu(g)
+                    float o[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = v[i] * u[i] * dsilu_fast(g[i]);
+                    for (int i = 0; i < 32; ++i) {
+                        const float g = bf16_at(cur[0], i), u = bf16_at(cur[1], i);
+                        const float sg = __fdividef(1.0f, 1.0f + __expf(-g));   // sigmoid(g), once
+                        o[i] = v[i] * u * (sg * (1.0f + g * (1.0f - sg)));
+                        v[i] = v[i] * (g * sg);
+                    }
                     put(&q.tmO[0], o, bcol, brow, bz);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = v[i] * silu_fast(g[i]);
-                    put(&q.tmO[1], o, bcol, brow, bz);
+                    put(&q.tmO[1], v, bcol, brow, bz);
                 }
             }
             tc_fence_before();
@@ -709,8 +778,25 @@ int max_pairs() {
     return cached[dev];
 }
 
+// Chunk counters a launch's progress sync needs: every unit's k-steps, in chunks,
+// bounded by its tile count times the longest tile (NOT the launch's real work,
+// which only the device knows); 0 when that exceeds SYNC_MAX_CHUNKS.
+int64_t sync_chunks(const moe_config& c, const TcProblem* probs, int nprob, int cg, int units) {
+    int64_t tiles = 0, nk_max = 1;
+    for (int i = 0; i < nprob; ++i) {
+        const TcProblem& q = probs[i];
+        tiles += max_tiles(c, q, cg);
+        const int64_t nk = q.sched == SCHED_ROWS ? (int64_t)q.k_blocks * q.kconcat
+                                                 : (q.fixed_rows ? q.fixed_rows : (int64_t)c.T) / BK + 1;
+        nk_max = std::max(nk_max, nk);
+    }
+    const int64_t per_unit = (tiles + units - 1) / units;
+    const int64_t n = per_unit * ((nk_max + SYNC_CHUNK - 1) / SYNC_CHUNK) + 2;
+    return n <= SYNC_MAX_CHUNKS ? n : 0;
+}
+
 int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* probs, int nprob,
-              cudaStream_t st) {
+              cudaStream_t st, void* sync_ws = nullptr) {
     static bool attr_done[64] = {};
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
@@ -732,6 +818,15 @@ int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* prob
         int64_t tiles = 0;
         for (int i = 0; i < nprob; ++i) tiles += max_tiles(c, probs[i], 2);
         const int units = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, pairs));
+        // long launches (many waves of tiles) keep their units together
+        if (GEMM_SYNC && sync_ws && tiles >= (int64_t)SPLIT_MIN_WAVES * units) {
+            const int64_t n = sync_chunks(c, probs, nprob, 2, units);
+            if (n > 0) {
+                P.sync = static_cast<uint32_t*>(sync_ws);
+                P.sync_n = (int)n;
+                MOE_CUDA_TRY(cudaMemsetAsync(sync_ws, 0, (size_t)(n + 1) * 4, st));
+            }
+        }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * units);
         cfg.blockDim = dim3(NTHREADS);
@@ -759,6 +854,50 @@ int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* prob
     for (int i = 0; i < nprob; ++i) tiles += max_tiles(c, probs[i], 1);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms()));
     MOE_LAUNCH_PARAM(tc_grouped_gemm_kernel<1>, grid, NTHREADS, SMEM_BYTES, st, P);
+    return MOE_OK;
+}
+
+// Estimated 64-deep k-steps of one tile of a problem: the routed experts'
+// segments at their mean size (their exact sizes are known on the device only).
+int64_t est_ksteps(const moe_config& c, const TcProblem& q) {
+    if (q.sched == SCHED_ROWS) return (int64_t)q.k_blocks * q.kconcat;
+    const int64_t rows = q.fixed_rows ? q.fixed_rows : (int64_t)c.T * c.k / c.E;
+    return std::max<int64_t>(1, rows / BK);
+}
+
+// The CTA pairs of a persistent launch take tiles in a fixed stride.  When the
+// launch mixes problems whose tiles differ in length (the backward's dgrad with
+// K = d next to a weight gradient with K = an expert's rows), the pairs cross
+// from one problem to the next at different times and stay offset from each
+// other by up to a tile.  Tiles that share an operand's k-slices then ask for
+// them tens of microseconds apart, longer than L2 keeps them once the launch
+// streams from DRAM, and the operands are fetched from DRAM again and again.
+// So a launch that holds many waves of tiles is issued as one launch per class
+// of tile length (k-steps within a factor of about 1.4), problems in their
+// given order; small launches stay whole (a launch's tail costs more there).
+int launch_tc_classes(const moe_config& c, const int32_t* offsets, const TcProblem* probs,
+                      int nprob, cudaStream_t st, void* sync_ws) {
+    const int cg = max_pairs() > 0 ? 2 : 1;
+    const int units = std::max(1, cg == 2 ? max_pairs() : num_sms());
+    int64_t tiles = 0;
+    for (int i = 0; i < nprob; ++i) tiles += max_tiles(c, probs[i], cg);
+    if (nprob < 2 || tiles < (int64_t)SPLIT_MIN_WAVES * units)
+        return launch_tc(c, offsets, probs, nprob, st, sync_ws);
+    int cls[MAX_PROBLEMS];
+    bool done[MAX_PROBLEMS] = {};
+    for (int i = 0; i < nprob; ++i) cls[i] = (int)std::lround(std::log2((double)est_ksteps(c, probs[i])));
+    for (int i = 0; i < nprob; ++i) {
+        if (done[i]) continue;
+        TcProblem g[MAX_PROBLEMS];
+        int n = 0;
+        for (int j = i; j < nprob; ++j)
+            if (!done[j] && cls[j] == cls[i]) {
+                g[n++] = probs[j];
+                done[j] = true;
+            }
+        const int r = launch_tc(c, offsets, g, n, st, sync_ws);
+        if (r != MOE_OK) return r;
+    }
     return MOE_OK;
 }
 
@@ -917,11 +1056,11 @@ Family shared_family(const moe_config& c, const moe_shared_ffn& s) {
 
 }  // namespace
 
-size_t tc_ws_bytes(const moe_config&) { return 0; }
+size_t tc_ws_bytes(const moe_config&) { return GEMM_SYNC ? (size_t)(SYNC_MAX_CHUNKS + 1) * 4 : 0; }
 
 int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                    const void* W_up, const void* W_gate, const void* W_down, void* h_saved,
-                   void* act, void* y_perm, const moe_shared_ffn* sh, void*, cudaStream_t st)
+                   void* act, void* y_perm, const moe_shared_ffn* sh, void* ws, cudaStream_t st)
 {
     const Family R = routed_family(c, x_perm, W_up, W_gate, W_down);
     TcProblem q[2];
@@ -932,7 +1071,7 @@ int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offse
         q[1] = new_problem();
         MOE_TRY(gemm1_problem(q[1], c, shared_family(c, *sh), sh->h, sh->act));
     }
-    MOE_TRY(launch_tc(c, offsets, q, sh ? 2 : 1, st));
+    MOE_TRY(launch_tc(c, offsets, q, sh ? 2 : 1, st, ws));
     // GEMM2
     q[0] = new_problem();
     MOE_TRY(gemm2_problem(q[0], c, R, act, y_perm));
@@ -940,14 +1079,14 @@ int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offse
         q[1] = new_problem();
         MOE_TRY(gemm2_problem(q[1], c, shared_family(c, *sh), sh->act, sh->y));
     }
-    return launch_tc(c, offsets, q, sh ? 2 : 1, st);
+    return launch_tc(c, offsets, q, sh ? 2 : 1, st, ws);
 }
 
 int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                     const void* W_up, const void* W_gate, const void* W_down,
                     const void* h_saved, const void* act, const void* dy_perm, void* dh,
                     void* dx_perm, void* dW_up, void* dW_gate, void* dW_down,
-                    const moe_shared_ffn* sh, void*, cudaStream_t st)
+                    const moe_shared_ffn* sh, void* ws, cudaStream_t st)
 {
     using bf = __nv_bfloat16;
     const bool sw = c.ffn == MOE_FFN_SWIGLU;
@@ -967,7 +1106,7 @@ int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offs
         q[n] = new_problem();
         MOE_TRY(wgrads_down(q[n++], c, S, sh->act, sh->dout, c.T, sh->dW_down));
     }
-    MOE_TRY(launch_tc(c, offsets, q, n, st));
+    MOE_TRY(launch_tc_classes(c, offsets, q, n, st, ws));
     // launch 2: dW_up = x^T dh (du)  ||  [dW_gate = x^T dg]  ||  dx = dh W_up^T (+ dg W_gate^T)
     n = 0;
     auto second = [&](const Family& F, const void* dhF, void* dWu, void* dWg, void* dx) -> int {
@@ -984,7 +1123,7 @@ int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offs
     };
     MOE_TRY(second(R, dh, dW_up, dW_gate, dx_perm));
     if (sh) MOE_TRY(second(shared_family(c, *sh), sh->dh, sh->dW_up, sh->dW_gate, sh->dx));
-    return launch_tc(c, offsets, q, n, st);
+    return launch_tc_classes(c, offsets, q, n, st, ws);
 }
 
 }  // namespace moe

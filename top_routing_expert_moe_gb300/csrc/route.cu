@@ -103,11 +103,21 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
             m = fmaxf(m, __shfl_xor_sync(mask, m, off));
             bad |= __shfl_xor_sync(mask, (int)bad, off) != 0;
         }
-        float z = 0.f;
-        for (int e = sub; e < E; e += G) z += expf((l[e] - m) * itau);
+        // z = sum exp((l - m) / tau); zl = sum exp((l - m) / tau) (l - m) / tau gives the
+        // entropy without a logarithm per expert: -sum p log p = log z - zl / z
+        float z = 0.f, zl = 0.f;
+        for (int e = sub; e < E; e += G) {
+            const float dl = (l[e] - m) * itau;
+            const float ex = __expf(dl);
+            z += ex;
+            zl += ex * dl;
+        }
 #pragma unroll
-        for (int off = G / 2; off > 0; off >>= 1) z += __shfl_xor_sync(mask, z, off);
-        const float inv = 1.0f / z;
+        for (int off = G / 2; off > 0; off >>= 1) {
+            z += __shfl_xor_sync(mask, z, off);
+            zl += __shfl_xor_sync(mask, zl, off);
+        }
+        const float inv = __fdividef(1.0f, z);
         // top-k: k rounds; each lane proposes its best unselected expert, the
         // group keeps the one that ranks highest (larger key, NaN lowest, lower id).
         // The key is the logit, or logit + Gumbel draw in straight-through mode.
@@ -148,20 +158,16 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
                 float ms = lsel[0];
                 for (int j = 1; j < k; ++j) ms = fmaxf(ms, lsel[j]);
                 float zs = 0.f;
-                for (int j = 0; j < k; ++j) zs += expf((lsel[j] - ms) * itau);
-                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = expf((lsel[j] - ms) * itau) / zs;
+                for (int j = 0; j < k; ++j) zs += __expf((lsel[j] - ms) * itau);
+                const float izs = __fdividef(1.0f, zs);
+                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = __expf((lsel[j] - ms) * itau) * izs;
             } else {
-                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = expf((lsel[j] - m) * itau) * inv;
+                for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = __expf((lsel[j] - m) * itau) * inv;
             }
         }
-        float h = 0.f;
-        for (int e = sub; e < E; e += G) {
-            const float pe = routed ? expf((l[e] - m) * itau) * inv : 0.f;
-            l[e] = pe;  // the tile now holds probabilities (0 for padding tokens)
-            if (pe > 0.f) h -= pe * logf(pe);
-        }
-#pragma unroll
-        for (int off = G / 2; off > 0; off >>= 1) h += __shfl_xor_sync(mask, h, off);
+        for (int e = sub; e < E; e += G)   // the tile now holds probabilities (0 for padding tokens)
+            l[e] = routed ? __expf((l[e] - m) * itau) * inv : 0.f;
+        const float h = (routed && !bad) ? __logf(z) - zl * inv : 0.f;   // non-finite rows: none
         if (sub == 0) {
             sEnt[tok] = routed ? h : 0.f;
             sBad[tok] = (routed && bad) ? 1 : 0;
@@ -257,34 +263,49 @@ __device__ void finalize_stats(int nblk, int E, int k, float aux_coef,
     __shared__ float s_h[32];
     __shared__ int s_b[32], s_r[32];
     const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
-    // per-tile scalars: routed tokens, entropy, non-finite tokens
-    int rl = 0, bad = 0;
-    float h = 0.f;
-    for (int b = tid; b < nblk; b += nthr) {
+    // every load of the pass issued before any is used: per-tile scalars (routed
+    // tokens, entropy, non-finite tokens) for up to 4 partials per thread, and
+    // per expert R lanes x 16 partials
+    int R = 32;
+    while (R > 1 && R * E > nthr) R >>= 1;
+    const int e = tid / R, r = tid % R;
+    int rl = 0, bad = 0, c = 0;
+    float h = 0.f, ps = 0.f;
+    {   // first round: every load in flight at once
+        int rv[4], bv[4];
+        float hv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int b = tid + u * nthr;
+            rv[u] = b < nblk ? __ldcg(part_real + b) : 0;
+            hv[u] = b < nblk ? __ldcg(part_ent + b) : 0.f;
+            bv[u] = b < nblk ? __ldcg(part_bad + b) : 0;
+        }
+        float pv[16];
+        int cv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int bb = r + u * R;
+            const bool in = e < E && bb < nblk;
+            pv[u] = in ? __ldcg(part_psum + (size_t)bb * E + e) : 0.f;
+            cv[u] = in ? __ldcg(part_counts + (size_t)bb * E + e) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) { rl += rv[u]; h += hv[u]; bad += bv[u]; }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) { ps += pv[u]; c += cv[u]; }
+    }
+    // more partials than one round covers
+    for (int b = tid + 4 * nthr; b < nblk; b += nthr) {
         rl += __ldcg(part_real + b);
         h += __ldcg(part_ent + b);
         bad += __ldcg(part_bad + b);
     }
-    // per-expert sums: lanes (e, r), r < R, take partials r, r + R, ...
-    int R = 32;
-    while (R > 1 && R * E > nthr) R >>= 1;
-    const int e = tid / R, r = tid % R;
-    float ps = 0.f;
-    int c = 0;
-    if (e < E) {
-        for (int b0 = r; b0 < nblk; b0 += 16 * R) {
-            float pv[16];
-            int cv[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int bb = b0 + u * R;
-                pv[u] = bb < nblk ? __ldcg(part_psum + (size_t)bb * E + e) : 0.f;
-                cv[u] = bb < nblk ? __ldcg(part_counts + (size_t)bb * E + e) : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) { ps += pv[u]; c += cv[u]; }
+    if (e < E)
+        for (int bb = r + 16 * R; bb < nblk; bb += R) {
+            ps += __ldcg(part_psum + (size_t)bb * E + e);
+            c += __ldcg(part_counts + (size_t)bb * E + e);
         }
-    }
     for (int off = R / 2; off > 0; off >>= 1) {
         ps += __shfl_xor_sync(0xffffffffu, ps, off);
         c += __shfl_xor_sync(0xffffffffu, c, off);
@@ -298,38 +319,58 @@ __device__ void finalize_stats(int nblk, int E, int k, float aux_coef,
     }
     if (lane == 0) { s_r[warp] = rl; s_h[warp] = h; s_b[warp] = bad; }
     named_sync(bar_id, nthr);
-    if (tid == 0) {
+    // warp 0: lanes e and e + 32 take the experts; fixed shuffle trees (deterministic)
+    if (warp == 0) {
         int tr = 0;
         h = 0.f;
         bad = 0;
         for (int w = 0; w < nwarps; ++w) { tr += s_r[w]; h += s_h[w]; bad += s_b[w]; }
         const float Tr = fmaxf((float)tr, 1.0f);   // means over the routed tokens
-        float aux = 0.f, sw = 0.f, cmean = 0.f, cmax = 0.f;
-        for (int q = 0; q < E; ++q) {
-            const float pbar = s_psum[q] / Tr;
-            counts[q] = s_cnt[q];
-            if (stats) stats[MOE_STAT_PBAR + q] = pbar;
-            const float dq = pbar - 1.0f / (float)E;
-            aux += dq * dq;
-            sw += ((float)s_cnt[q] / (Tr * (float)k)) * pbar;
-            cmean += (float)s_cnt[q];
-            cmax = fmaxf(cmax, (float)s_cnt[q]);
+        float aux = 0.f, sw = 0.f, csum = 0.f, cmax = 0.f;
+        float cnt_l[2] = {0.f, 0.f};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int q = lane + 32 * hh;
+            if (q < E) {
+                const float pbar = s_psum[q] / Tr;
+                counts[q] = s_cnt[q];
+                if (stats) stats[MOE_STAT_PBAR + q] = pbar;
+                const float dq = pbar - 1.0f / (float)E;
+                aux += dq * dq;
+                sw += ((float)s_cnt[q] / (Tr * (float)k)) * pbar;
+                cnt_l[hh] = (float)s_cnt[q];
+                csum += cnt_l[hh];
+                cmax = fmaxf(cmax, cnt_l[hh]);
+            }
         }
-        cmean /= (float)E;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            aux += __shfl_xor_sync(0xffffffffu, aux, o);
+            sw += __shfl_xor_sync(0xffffffffu, sw, o);
+            csum += __shfl_xor_sync(0xffffffffu, csum, o);
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+        }
+        const float cmean = csum / (float)E;
         float var = 0.f;
-        for (int q = 0; q < E; ++q) var += ((float)s_cnt[q] - cmean) * ((float)s_cnt[q] - cmean);
-        if (stats) {
-            stats[MOE_STAT_TOKENS] = (float)tr;
-            stats[MOE_STAT_AUX_LOSS] = aux_coef * aux;
-            stats[MOE_STAT_AUX_SWITCH] = (float)E * sw;
-            stats[MOE_STAT_ENTROPY] = h / Tr;
-            stats[MOE_STAT_NONFINITE] = (float)bad;
-            stats[MOE_STAT_DROPPED] = 0.f;
-            stats[MOE_STAT_MAX_OVER_MEAN_KEPT] = 0.f;
-            stats[MOE_STAT_COUNT_CV] = cmean > 0.f ? sqrtf(var / (float)E) / cmean : 0.f;
-            stats[MOE_STAT_MAX_OVER_MEAN_COUNT] = cmean > 0.f ? cmax / cmean : 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+            if (lane + 32 * hh < E) var += (cnt_l[hh] - cmean) * (cnt_l[hh] - cmean);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) var += __shfl_xor_sync(0xffffffffu, var, o);
+        if (lane == 0) {
+            if (stats) {
+                stats[MOE_STAT_TOKENS] = (float)tr;
+                stats[MOE_STAT_AUX_LOSS] = aux_coef * aux;
+                stats[MOE_STAT_AUX_SWITCH] = (float)E * sw;
+                stats[MOE_STAT_ENTROPY] = h / Tr;
+                stats[MOE_STAT_NONFINITE] = (float)bad;
+                stats[MOE_STAT_DROPPED] = 0.f;
+                stats[MOE_STAT_MAX_OVER_MEAN_KEPT] = 0.f;
+                stats[MOE_STAT_COUNT_CV] = cmean > 0.f ? sqrtf(var / (float)E) / cmean : 0.f;
+                stats[MOE_STAT_MAX_OVER_MEAN_COUNT] = cmean > 0.f ? cmax / cmean : 0.f;
+            }
+            if (bad) set_status(status, MOE_ERR_NONFINITE);
         }
-        if (bad) set_status(status, MOE_ERR_NONFINITE);
     }
 }
 
