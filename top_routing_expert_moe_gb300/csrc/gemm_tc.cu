@@ -8,28 +8,33 @@
 //             dW    = x^T dh, act^T dy     (reduction over each expert's rows)
 //             dx    = dh W_up^T (+ dg W_gate^T)
 //
-// Design (one CTA per SM, 320 threads, warp-specialised):
-//   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
-//               (BN x 64) into a 4-stage shared-memory ring (mbarrier tx).
-//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
-//               (M=128, N=BN, K=16, bf16 in, fp32 accumulate) and commits to
-//               the ring's "empty" barriers and to a double-buffered TMEM
-//               accumulator's "full" barrier.
-//   warps 2-9   epilogue: two warps per TMEM lane quarter, each taking half
-//               the tile's columns; tcgen05.ld 32 columns at a time, fused
-//               activation math (branch-free fast exp / divide so the 32
-//               elements of a chunk pipeline), bf16 stores; frees the
-//               accumulator so the next tile's MMAs overlap this epilogue.
-// Tiles come from a static persistent schedule whose per-expert tile counts
-// are read from the device-side segment offsets, so no host sync separates
-// routing from the GEMMs.  Within an expert, tiles are visited in groups of
-// 16 M-blocks so the A rows and B columns in flight stay L2-resident.
+// Design (clusters of two CTAs -- a pair -- one CTA per SM, 320 threads each):
+//   warp 0      TMA producer of each CTA: its 128 rows of A and its half of B's
+//               columns, 128B-swizzled, into a ring of six 32 KB stages; the
+//               loads of both CTAs complete on the even CTA's "full" barrier.
+//   warp 1      allocates 512 TMEM columns (both CTAs, collectively); the even
+//               CTA's thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+//               K = 16, bf16 in, fp32 accumulate) and commits, multicast to both
+//               CTAs, to the ring's "empty" barriers and to one of two TMEM
+//               accumulators' "full" barriers.
+//   warps 2-9   epilogue of each CTA's 128 accumulator lanes: two warps per TMEM
+//               lane quarter, tcgen05.ld 32 columns at a time, the fused
+//               activation (or its derivative), 32 x 32 output boxes written by
+//               TMA stores; the accumulator is released to the even CTA so the
+//               next tile's MMAs overlap this epilogue.
+// A one-CTA variant (M = 128, four 48 KB stages) serves devices that cannot
+// hold pairs.  Tiles come from a static persistent schedule whose per-expert
+// tile counts are read from the device-side segment offsets, so no host sync
+// separates routing from the GEMMs; within an expert, tiles are visited in
+// groups of 16 row blocks so the A rows and B columns in flight stay
+// L2-resident.  A launch may hold up to six independent problems (the
+// backward's dgrad || weight gradient pairs, the shared experts' FFN).
 //
 // Shared-memory operand layouts (canonical 128B-swizzle layouts):
 //   K-major   rows of 64 bf16 (128 B); 8-row groups 1024 B apart (SBO);
 //             the K=16 step advances the start address by 32 B.
-//   MN-major  boxes of 64 k-rows x 64 MN-elements (8 KB); 8-k-row groups
-//             1024 B apart (SBO); MN boxes 8 KB apart (LBO); the K=16 step
+//   MN-major  blocks of 64 k-rows x 64 MN-elements (8 KB); 8-k-row groups
+//             1024 B apart (SBO); MN blocks 8 KB apart (LBO); the K=16 step
 //             advances the start address by 2048 B.
 //
 // Every mbarrier wait is bounded (globaltimer): on expiry the kernel records
@@ -61,6 +66,11 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
 constexpr int RASTER_GM = 16;
+// 64-wide blocks one TMA load brings of an MN-major operand (a 3-D / 4-D view of the
+// tensor whose outermost coordinate steps between the blocks): fewer, larger TMA
+// operations per stage load faster (measured on the K-major weights: two 64-row
+// boxes -> one 128-row box took the Mixtral dgrad launches 5-7 % faster)
+constexpr int MN_BLOCKS_PER_LOAD = 2;
 // Progress sync of the units (CTA pairs) of a long launch: a unit's TMA producer
 // counts the k-steps it has issued in chunks of SYNC_CHUNK and does not start
 // chunk g before every unit has issued chunk g - SYNC_SLACK (or has no tiles
@@ -100,6 +110,8 @@ struct TcProblem {
     int epi;
     int ldo;
     int fixed_rows;         // > 0: one segment [0, fixed_rows) (a multiple of BM)
+    int a_blk, b_blk;       // MN-major operands: 64-wide blocks per TMA load (1 or 2)
+    int b_box_rows;         // K-major weights: rows of N per TMA box (64 or 128)
 };
 constexpr int MAX_PROBLEMS = 6;
 
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             // "memory"-clobbering wait)
             const TcProblem& q = P.prob[t.p];
             const int q_kseg = q.sched == SCHED_KSEG, q_kb = q.k_blocks, q_dual = q.dual;
-            const int q_bmn = q.b_mn;
+            const int q_bmn = q.b_mn, q_ablk = q.a_blk, q_bblk = q.b_blk, q_brows = q.b_box_rows;
             const CUtensorMap* tA0 = &q.tmA0;
             const CUtensorMap* tA1 = &q.tmA1;
             const CUtensorMap* tB0 = &q.tmB0;
@@ -443,24 +455,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     if constexpr (CG == 1) tma_load3(m, dst, bar, c0, c1, c2);
                     else tma_load3_pair(m, dst, bar, c0, c1, c2);
                 };
-                if (q_kseg) {
+                auto ld4 = [&](const CUtensorMap* m, uint32_t dst, int c0, int c1, int c2, int c3) {
+                    if constexpr (CG == 1) tma_load4(m, dst, bar, c0, c1, c2, c3);
+                    else tma_load4_pair(m, dst, bar, c0, c1, c2, c3);
+                };
+                if (q_kseg) {   // both operands MN-major (block views when blk > 1)
                     const int kr = t.krow0 + kb * BK;
-                    ld(tA0, sA, am0, kr, 0);
-                    ld(tA0, sA + 8192, am0 + 64, kr, 0);
-                    for (int c = 0; c < nbox; ++c) ld(tB0, sB + c * 8192, bn0 + 64 * c, kr, 0);
+                    for (int c = 0; c < 2; c += q_ablk) {
+                        if (q_ablk > 1) ld(tA0, sA + c * 8192, 0, kr, am0 / 64 + c);
+                        else ld(tA0, sA + c * 8192, am0 + 64 * c, kr, 0);
+                    }
+                    for (int c = 0; c < nbox; c += q_bblk) {
+                        if (q_bblk > 1) ld(tB0, sB + c * 8192, 0, kr, bn0 / 64 + c);
+                        else ld(tB0, sB + c * 8192, bn0 + 64 * c, kr, 0);
+                    }
                 } else {
                     const int phase = kb >= q_kb ? 1 : 0;
                     const int k0 = (kb - phase * q_kb) * BK;
                     ld(phase ? tA1 : tA0, sA, k0, am0, 0);
-                    if (q_dual) {
-                        for (int c = 0; c < 4 / CG; ++c) {   // 64-column boxes of [gate | up]
+                    if (q_dual) {   // 64-column blocks of [gate | up], 4-D views {64, k, blocks, E}
+                        for (int c = 0; c < 4 / CG; c += q_bblk) {
                             const int g = c + (int)rank * (4 / CG);        // 0,1: gate; 2,3: up
-                            ld(g < 2 ? tB0 : tB1, sB + c * 8192, bn0 + 64 * (g & 1), k0, t.e);
+                            if (q_bblk > 1) ld4(g < 2 ? tB0 : tB1, sB + c * 8192, 0, k0, bn0 / 64 + (g & 1), t.e);
+                            else ld(g < 2 ? tB0 : tB1, sB + c * 8192, bn0 + 64 * (g & 1), k0, t.e);
                         }
                     } else if (q_bmn) {
-                        for (int c = 0; c < nbox; ++c) ld(tB0, sB + c * 8192, bn0 + 64 * c, k0, t.e);
-                    } else {   // K-major weights: boxes of 64 rows (N) x 64 k
-                        for (int c = 0; c < nbox; ++c)
+                        for (int c = 0; c < nbox; c += q_bblk) {
+                            if (q_bblk > 1) ld4(tB0, sB + c * 8192, 0, k0, bn0 / 64 + c, t.e);
+                            else ld(tB0, sB + c * 8192, bn0 + 64 * c, k0, t.e);
+                        }
+                    } else {   // K-major weights: boxes of b_box_rows rows (N) x 64 k
+                        for (int c = 0; c < nbox; c += q_brows / 64)
                             ld(phase ? tB1 : tB0, sB + c * 8192, k0, bn0 + 64 * c, t.e);
                     }
                 }
@@ -713,17 +738,62 @@ int make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t
     return encode_bf16_map(m, ptr, d0, d1, d2, s1, s2, b0, b1);
 }
 
-// activations [rows_cap, cols]: K-major box {64, 128} or MN-major box {64, 64}
-int act_map(CUtensorMap* m, const void* ptr, int64_t rows_cap, int cols, bool mn_major) {
+// bf16 map of rank 3 or 4 with 128-byte swizzle: dims[0] contiguous, strides[i] the
+// byte stride of dims[i + 1] (any order: the outer dimensions may step by less than
+// an inner one, as in the block views below)
+int make_map_nd(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return MOE_ERR_CUDA;
+    cuuint64_t d[4], st[3];
+    cuuint32_t b[4], es[4] = {1, 1, 1, 1};
+    for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), d, st,
+                    b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// activations [rows_cap, cols].  K-major: box {64 k, 128 rows}.  MN-major with blk = 2:
+// the view {64, rows_cap, cols / 64} (64-column blocks 128 B apart), box {64, 64 k, 2}:
+// one load brings two 64-column blocks, each 64 k-rows x 128 B, 8 KB apart in shared
+// memory -- the same image as two {64, 64} boxes.  If the driver declines that view,
+// blk falls back to 1: boxes {64 columns, 64 k} of the plain layout.
+int act_map(CUtensorMap* m, const void* ptr, int64_t rows_cap, int cols, bool mn_major, int& blk) {
+    if (!mn_major)
+        return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows_cap, 1, (uint64_t)cols * 2,
+                        (uint64_t)cols * 2 * rows_cap, 64, BM);
+    if (blk > 1) {
+        const uint64_t dims[3] = {64, (uint64_t)rows_cap, (uint64_t)cols / 64};
+        const uint64_t st[2] = {(uint64_t)cols * 2, 128};
+        const uint32_t box[3] = {64, 64, (uint32_t)blk};
+        if (make_map_nd(m, ptr, 3, dims, st, box) == MOE_OK) return MOE_OK;
+        blk = 1;
+    }
     return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows_cap, 1, (uint64_t)cols * 2,
-                    (uint64_t)cols * 2 * rows_cap, 64, mn_major ? 64 : BM);
+                    (uint64_t)cols * 2 * rows_cap, 64, 64);
 }
-// expert weights [E, rows, cols]: boxes {64, 64} (MN-major: 64 N x 64 k; K-major:
-// 64 k x 64 rows of N, several boxes per stage)
-int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool, int) {
+// expert weights [E, rows, cols].  MN-major (N = cols), box > 1: the view
+// {64, rows, cols / 64, E}, box {64, 64 k, box, 1} (box 64-column blocks per load; falls
+// back to box = 1, plain boxes {64, 64, 1}).  K-major (N = rows, K = cols): box {64 k,
+// box rows of N, 1}.
+int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool mn, int& box) {
+    if (mn && box > 1) {
+        const uint64_t dims[4] = {64, (uint64_t)rows, (uint64_t)cols / 64, (uint64_t)E};
+        const uint64_t st[3] = {(uint64_t)cols * 2, 128, (uint64_t)cols * 2 * rows};
+        const uint32_t b[4] = {64, 64, (uint32_t)box, 1};
+        if (make_map_nd(m, ptr, 4, dims, st, b) == MOE_OK) return MOE_OK;
+        box = 1;
+    }
     return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)E, (uint64_t)cols * 2,
-                    (uint64_t)cols * 2 * rows, 64, 64);
+                    (uint64_t)cols * 2 * rows, 64, mn ? 64 : (uint32_t)box);
 }
+
+int max_pairs();
+int cta_group() { return max_pairs() > 0 ? 2 : 1; }
+// 64-wide blocks per load of an MN-major operand whose CTA share is `cols` wide
+int mn_blocks(int cols) { return std::min(MN_BLOCKS_PER_LOAD, std::max(1, cols / 64)); }
 
 int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
 
@@ -941,7 +1011,8 @@ int rows_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, i
     q.bn = pick_bn(N);
     q.n_blocks = N / q.bn;
     q.ldo = N;
-    return act_map(&q.tmA0, A, a_rows, K, false);
+    int blk = 0;   // K-major: unused
+    return act_map(&q.tmA0, A, a_rows, K, false, blk);
 }
 
 // Weight-gradient problem: out_e[M, N] = A_e^T B_e over the segment's rows (both MN-major)
@@ -958,8 +1029,10 @@ int wgrad_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, 
     q.out0 = static_cast<__nv_bfloat16*>(out);
     q.ldo = N;
     q.out_estride = (long long)M * N;
-    MOE_TRY(act_map(&q.tmA0, A, a_rows, M, true));
-    MOE_TRY(act_map(&q.tmB0, B, b_rows, N, true));
+    q.a_blk = mn_blocks(BM);
+    q.b_blk = mn_blocks(q.bn / cta_group());
+    MOE_TRY(act_map(&q.tmA0, A, a_rows, M, true, q.a_blk));
+    MOE_TRY(act_map(&q.tmB0, B, b_rows, N, true, q.b_blk));
     // out [E][M][N]: boxes of 32 columns x 32 rows of one expert
     return encode_bf16_map(&q.tmO[0], out, (uint64_t)N, (uint64_t)M, (uint64_t)F.E, (uint64_t)N * 2,
                            (uint64_t)N * 2 * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -975,14 +1048,24 @@ int gemm1_problem(TcProblem& q, const moe_config& c, const Family& F, void* h, v
         q.dual = 1;
         q.bn = 128;
         q.n_blocks = f / 128;
-        MOE_TRY(weight_map(&q.tmB0, F.Wg, F.E, d, f, true, 0));
-        MOE_TRY(weight_map(&q.tmB1, F.Wu, F.E, d, f, true, 0));
+        // a CTA's share: 128 columns of the gate or the up tile; both maps take the
+        // same form (if either view is declined, both use the plain boxes)
+        int b0 = mn_blocks(128), b1 = b0;
+        MOE_TRY(weight_map(&q.tmB0, F.Wg, F.E, d, f, true, b0));
+        MOE_TRY(weight_map(&q.tmB1, F.Wu, F.E, d, f, true, b1));
+        if (b0 != b1) {
+            b0 = b1 = 1;
+            MOE_TRY(weight_map(&q.tmB0, F.Wg, F.E, d, f, true, b0));
+            MOE_TRY(weight_map(&q.tmB1, F.Wu, F.E, d, f, true, b1));
+        }
+        q.b_blk = b0;
         q.epi = EPI_SWIGLU_FWD;
         q.out0 = static_cast<bf*>(h);
         q.out1 = static_cast<bf*>(h) + F.rows * f;
         q.out2 = static_cast<bf*>(act);
     } else {
-        MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, d, f, true, 0));
+        q.b_blk = mn_blocks(q.bn / cta_group());
+        MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, d, f, true, q.b_blk));
         q.epi = EPI_SILU_FWD;
         q.out0 = static_cast<bf*>(h);
         q.out1 = static_cast<bf*>(act);
@@ -994,7 +1077,8 @@ int gemm1_problem(TcProblem& q, const moe_config& c, const Family& F, void* h, v
 int gemm2_problem(TcProblem& q, const moe_config& c, const Family& F, const void* act, void* y) {
     MOE_TRY(rows_problem(q, F, act, F.rows, F.f, c.d));
     q.b_mn = 1;
-    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, F.f, c.d, true, 0));
+    q.b_blk = mn_blocks(q.bn / cta_group());
+    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, F.f, c.d, true, q.b_blk));
     q.epi = EPI_STORE;
     q.out0 = static_cast<__nv_bfloat16*>(y);
     return out_maps_rows(q, F.rows);
@@ -1006,7 +1090,8 @@ int dgrad2_problem(TcProblem& q, const moe_config& c, const Family& F, const voi
     using bf = __nv_bfloat16;
     const int f = F.f;
     MOE_TRY(rows_problem(q, F, dy, dy_rows, c.d, f));
-    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, f, c.d, false, q.bn));
+    q.b_box_rows = q.bn / cta_group() >= 128 ? 128 : 64;
+    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, f, c.d, false, q.b_box_rows));
     q.in0 = static_cast<const bf*>(h);
     q.out0 = static_cast<bf*>(dh);
     if (c.ffn == MOE_FFN_SWIGLU) {
@@ -1026,11 +1111,13 @@ int dgrad1_problem(TcProblem& q, const moe_config& c, const Family& F, const voi
     const bf* dh0 = static_cast<const bf*>(dh);
     const bf* dh1 = sw ? dh0 + F.rows * F.f : nullptr;
     MOE_TRY(rows_problem(q, F, sw ? dh1 : dh0, F.rows, F.f, c.d));
-    MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, c.d, F.f, false, q.bn));
+    q.b_box_rows = q.bn / cta_group() >= 128 ? 128 : 64;
+    MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, c.d, F.f, false, q.b_box_rows));
     if (sw) {
         q.kconcat = 2;
-        MOE_TRY(act_map(&q.tmA1, dh0, F.rows, F.f, false));
-        MOE_TRY(weight_map(&q.tmB1, F.Wg, F.E, c.d, F.f, false, q.bn));
+        int blk = 0;   // K-major: unused
+        MOE_TRY(act_map(&q.tmA1, dh0, F.rows, F.f, false, blk));
+        MOE_TRY(weight_map(&q.tmB1, F.Wg, F.E, c.d, F.f, false, q.b_box_rows));
     }
     q.epi = EPI_STORE;
     q.out0 = static_cast<bf*>(dx);

@@ -152,6 +152,25 @@ __device__ __forceinline__ void tma_load3_pair(const CUtensorMap* map, uint32_t 
         : "memory");
 }
 
+// 4-D TMA load into this CTA's shared memory, completion counted on an mbarrier of
+// either CTA of the pair (bar: a shared::cluster address)
+__device__ __forceinline__ void tma_load4_pair(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                               int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load4(const CUtensorMap* map, uint32_t dst, uint32_t bar, int c0,
+                                          int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
 // TMA store of a shared-memory box (bulk-group completion)
 __device__ __forceinline__ void tma_store3(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
