@@ -55,9 +55,9 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int RING_BYTES = 192 * 1024;        // 4 stages of 48 KB (one CTA) or 6 of 32 KB (a pair)
+constexpr int BM = 128, BK = 128;             // k per stage: two 64-wide k-blocks (128-byte rows)
+constexpr int A_BYTES = BM * BK * 2;          // 32 KB
+constexpr int RING_BYTES = 192 * 1024;        // 2 stages of 96 KB (one CTA) or 3 of 64 KB (a pair)
 constexpr int STAGING_BYTES = 32 * 1024;      // epilogue: two 2 KB output boxes per epilogue warp
 constexpr int CTRL_BYTES = 2048;   // barriers, TMEM slot, offsets[65], prefix[6*64+1], slot bases
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + STAGING_BYTES + CTRL_BYTES;
@@ -66,11 +66,11 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
 constexpr int RASTER_GM = 16;
-// 64-wide blocks one TMA load brings of an MN-major operand (a 3-D / 4-D view of the
-// tensor whose outermost coordinate steps between the blocks): fewer, larger TMA
-// operations per stage load faster (measured on the K-major weights: two 64-row
-// boxes -> one 128-row box took the Mixtral dgrad launches 5-7 % faster)
-constexpr int MN_BLOCKS_PER_LOAD = 2;
+// Every operand share of a stage arrives with one TMA load: the TMA unit's cost
+// follows its instructions more than its bytes (on the Mixtral step, one load per
+// share instead of two took the grouped GEMMs about 8 % faster; adding L2
+// prefetch instructions beside the loads made them 40 % slower).  So a stage is
+// 128 deep in k -- a share is a {64, 128, 2} box of a block view of the tensor.
 // Progress sync of the units (CTA pairs) of a long launch: a unit's TMA producer
 // counts the k-steps it has issued in chunks of SYNC_CHUNK and does not start
 // chunk g before every unit has issued chunk g - SYNC_SLACK (or has no tiles
@@ -110,8 +110,6 @@ struct TcProblem {
     int epi;
     int ldo;
     int fixed_rows;         // > 0: one segment [0, fixed_rows) (a multiple of BM)
-    int a_blk, b_blk;       // MN-major operands: 64-wide blocks per TMA load (1 or 2)
-    int b_box_rows;         // K-major weights: rows of N per TMA box (64 or 128)
 };
 constexpr int MAX_PROBLEMS = 6;
 
@@ -311,8 +309,8 @@ __device__ __forceinline__ void mma_commit_local(uint32_t bar) {
 template <int CG>
 __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __grid_constant__ TcParams P)
 {
-    constexpr int S = CG == 1 ? 4 : 6;                       // ring stages
-    constexpr int SB = CG == 1 ? 48 * 1024 : 32 * 1024;      // stage bytes per CTA
+    constexpr int S = CG == 1 ? 2 : 3;                       // ring stages
+    constexpr int SB = CG == 1 ? 96 * 1024 : 64 * 1024;      // stage bytes per CTA
     static_assert(S * SB == RING_BYTES, "ring size");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -414,7 +412,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             // "memory"-clobbering wait)
             const TcProblem& q = P.prob[t.p];
             const int q_kseg = q.sched == SCHED_KSEG, q_kb = q.k_blocks, q_dual = q.dual;
-            const int q_bmn = q.b_mn, q_ablk = q.a_blk, q_bblk = q.b_blk, q_brows = q.b_box_rows;
+            const int q_bmn = q.b_mn;
             const CUtensorMap* tA0 = &q.tmA0;
             const CUtensorMap* tA1 = &q.tmA1;
             const CUtensorMap* tB0 = &q.tmB0;
@@ -426,7 +424,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             // CTA the up tile (CG = 2)
             const int bcols = (q_dual ? 256 : q.bn) / CG;
             const int bn0 = t.n0 + (q_dual ? 0 : (int)rank * bcols);
-            const int nbox = bcols / 64;
             const uint32_t b_bytes = (uint32_t)bcols * BK * 2u;
             const uint32_t stage_tx = CG * ((uint32_t)A_BYTES + b_bytes);   // both CTAs' bytes
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
@@ -459,34 +456,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                     if constexpr (CG == 1) tma_load4(m, dst, bar, c0, c1, c2, c3);
                     else tma_load4_pair(m, dst, bar, c0, c1, c2, c3);
                 };
-                if (q_kseg) {   // both operands MN-major (block views when blk > 1)
+                // one load per operand share; every view is {64, rows, 64-column blocks[, E]}
+                if (q_kseg) {   // both MN-major: 128 k-rows x the share's 64-column blocks
                     const int kr = t.krow0 + kb * BK;
-                    for (int c = 0; c < 2; c += q_ablk) {
-                        if (q_ablk > 1) ld(tA0, sA + c * 8192, 0, kr, am0 / 64 + c);
-                        else ld(tA0, sA + c * 8192, am0 + 64 * c, kr, 0);
-                    }
-                    for (int c = 0; c < nbox; c += q_bblk) {
-                        if (q_bblk > 1) ld(tB0, sB + c * 8192, 0, kr, bn0 / 64 + c);
-                        else ld(tB0, sB + c * 8192, bn0 + 64 * c, kr, 0);
-                    }
+                    ld(tA0, sA, 0, kr, am0 / 64);
+                    ld(tB0, sB, 0, kr, bn0 / 64);
                 } else {
                     const int phase = kb >= q_kb ? 1 : 0;
                     const int k0 = (kb - phase * q_kb) * BK;
-                    ld(phase ? tA1 : tA0, sA, k0, am0, 0);
-                    if (q_dual) {   // 64-column blocks of [gate | up], 4-D views {64, k, blocks, E}
-                        for (int c = 0; c < 4 / CG; c += q_bblk) {
-                            const int g = c + (int)rank * (4 / CG);        // 0,1: gate; 2,3: up
-                            if (q_bblk > 1) ld4(g < 2 ? tB0 : tB1, sB + c * 8192, 0, k0, bn0 / 64 + (g & 1), t.e);
-                            else ld(g < 2 ? tB0 : tB1, sB + c * 8192, bn0 + 64 * (g & 1), k0, t.e);
+                    ld(phase ? tA1 : tA0, sA, 0, am0, k0 / 64);   // K-major: 128 rows x 2 k-blocks
+                    if (q_dual) {   // [gate | up]: two 64-column blocks of one of them per load
+                        for (int c = 0; c < 4 / CG; c += 2) {
+                            const int g = c + (int)rank * (4 / CG);        // 0: gate; 2: up
+                            ld4(g < 2 ? tB0 : tB1, sB + c * (BK * 128), 0, k0, bn0 / 64, t.e);
                         }
-                    } else if (q_bmn) {
-                        for (int c = 0; c < nbox; c += q_bblk) {
-                            if (q_bblk > 1) ld4(tB0, sB + c * 8192, 0, k0, bn0 / 64 + c, t.e);
-                            else ld(tB0, sB + c * 8192, bn0 + 64 * c, k0, t.e);
-                        }
-                    } else {   // K-major weights: boxes of b_box_rows rows (N) x 64 k
-                        for (int c = 0; c < nbox; c += q_brows / 64)
-                            ld(phase ? tB1 : tB0, sB + c * 8192, k0, bn0 + 64 * c, t.e);
+                    } else if (q_bmn) {   // MN-major weights: 128 k-rows x the share's blocks
+                        ld4(tB0, sB, 0, k0, bn0 / 64, t.e);
+                    } else {              // K-major weights: the share's rows of N x 2 k-blocks
+                        ld4(phase ? tB1 : tB0, sB, 0, bn0, k0 / 64, t.e);
                     }
                 }
                 ++ks;
@@ -512,6 +499,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const TcProblem& q = P.prob[t.p];
             const int q_dual = q.dual, q_amn = q.a_mn, q_bmn = q.b_mn;
             const uint32_t idesc = idesc_bf16(BM * CG, q_dual ? 256 : q.bn, q_amn, q_bmn);
+            // K-major B: stride between the stage's two k-blocks (the CTA's rows of B x 128 B)
+            const uint32_t b_kblk = (uint32_t)((q_dual ? 256 : q.bn) / CG) * 128u;
             const int acc = tcount & 1;
             const uint32_t aph = (uint32_t)(tcount >> 1) & 1u;
             const bool got = CG == 1 ? mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort_flag, P.status)
@@ -530,10 +519,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                 const uint32_t sA = smem0 + s * SB, sB = sA + A_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BK / 16; ++ks) {
-                    const uint64_t ad = q_amn ? sdesc(sA + ks * 2048, 8192, 1024) : sdesc(sA + ks * 32, 16, 1024);
+                    // K-major: 128-byte rows, k-block (ks / 4) at a fixed stride, 32 B per K = 16;
+                    // MN-major: 64-column blocks of 128 k-rows (16 KB apart), 2048 B per K = 16
+                    const uint64_t ad = q_amn ? sdesc(sA + ks * 2048, 16384, 1024)
+                                              : sdesc(sA + (ks >> 2) * (BM * 128) + (ks & 3) * 32, 16, 1024);
                     // (dual: one N = 256 MMA, gate -> columns 0..127, up -> 128..255)
-                    const uint64_t bd = (q_bmn || q_dual) ? sdesc(sB + ks * 2048, 8192, 1024)
-                                                          : sdesc(sB + ks * 32, 16, 1024);
+                    const uint64_t bd = (q_bmn || q_dual) ? sdesc(sB + ks * 2048, 16384, 1024)
+                                                          : sdesc(sB + (ks >> 2) * b_kblk + (ks & 3) * 32, 16, 1024);
                     mma_issue<CG>(dt, ad, bd, idesc, accum);
                     accum = 1;
                 }
@@ -733,11 +725,6 @@ int encode_bf16_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, u
 
 namespace {
 
-int make_map(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-             uint64_t s2, uint32_t b0, uint32_t b1) {
-    return encode_bf16_map(m, ptr, d0, d1, d2, s1, s2, b0, b1);
-}
-
 // bf16 map of rank 3 or 4 with 128-byte swizzle: dims[0] contiguous, strides[i] the
 // byte stride of dims[i + 1] (any order: the outer dimensions may step by less than
 // an inner one, as in the block views below)
@@ -755,45 +742,28 @@ int make_map_nd(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// activations [rows_cap, cols].  K-major: box {64 k, 128 rows}.  MN-major with blk = 2:
-// the view {64, rows_cap, cols / 64} (64-column blocks 128 B apart), box {64, 64 k, 2}:
-// one load brings two 64-column blocks, each 64 k-rows x 128 B, 8 KB apart in shared
-// memory -- the same image as two {64, 64} boxes.  If the driver declines that view,
-// blk falls back to 1: boxes {64 columns, 64 k} of the plain layout.
-int act_map(CUtensorMap* m, const void* ptr, int64_t rows_cap, int cols, bool mn_major, int& blk) {
-    if (!mn_major)
-        return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows_cap, 1, (uint64_t)cols * 2,
-                        (uint64_t)cols * 2 * rows_cap, 64, BM);
-    if (blk > 1) {
-        const uint64_t dims[3] = {64, (uint64_t)rows_cap, (uint64_t)cols / 64};
-        const uint64_t st[2] = {(uint64_t)cols * 2, 128};
-        const uint32_t box[3] = {64, 64, (uint32_t)blk};
-        if (make_map_nd(m, ptr, 3, dims, st, box) == MOE_OK) return MOE_OK;
-        blk = 1;
-    }
-    return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows_cap, 1, (uint64_t)cols * 2,
-                    (uint64_t)cols * 2 * rows_cap, 64, 64);
+// activations [rows_cap, cols] as the block view {64, rows_cap, cols / 64} (64-column
+// blocks 128 B apart).  K-major share: box {64, 128 rows, 2 k-blocks}; MN-major share:
+// box {64, 128 k-rows, blocks 64-column blocks}.  Shared memory: the box's blocks one
+// after the other, each its rows of 128 B (the canonical 128B-swizzled layouts).
+int act_map(CUtensorMap* m, const void* ptr, int64_t rows_cap, int cols, bool mn_major, int blocks) {
+    const uint64_t dims[3] = {64, (uint64_t)rows_cap, (uint64_t)cols / 64};
+    const uint64_t st[2] = {(uint64_t)cols * 2, 128};
+    const uint32_t box[3] = {64, mn_major ? (uint32_t)BK : (uint32_t)BM, mn_major ? (uint32_t)blocks : 2u};
+    return make_map_nd(m, ptr, 3, dims, st, box);
 }
-// expert weights [E, rows, cols].  MN-major (N = cols), box > 1: the view
-// {64, rows, cols / 64, E}, box {64, 64 k, box, 1} (box 64-column blocks per load; falls
-// back to box = 1, plain boxes {64, 64, 1}).  K-major (N = rows, K = cols): box {64 k,
-// box rows of N, 1}.
-int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool mn, int& box) {
-    if (mn && box > 1) {
-        const uint64_t dims[4] = {64, (uint64_t)rows, (uint64_t)cols / 64, (uint64_t)E};
-        const uint64_t st[3] = {(uint64_t)cols * 2, 128, (uint64_t)cols * 2 * rows};
-        const uint32_t b[4] = {64, 64, (uint32_t)box, 1};
-        if (make_map_nd(m, ptr, 4, dims, st, b) == MOE_OK) return MOE_OK;
-        box = 1;
-    }
-    return make_map(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)E, (uint64_t)cols * 2,
-                    (uint64_t)cols * 2 * rows, 64, mn ? 64 : (uint32_t)box);
+// expert weights [E, rows, cols] as the view {64, rows, cols / 64, E}.  MN-major (N =
+// cols): box {64, 128 k-rows, n_blocks, 1}; K-major (N = rows, K = cols): box {64,
+// n_rows, 2 k-blocks, 1}.
+int weight_map(CUtensorMap* m, const void* ptr, int E, int rows, int cols, bool mn, int share) {
+    const uint64_t dims[4] = {64, (uint64_t)rows, (uint64_t)cols / 64, (uint64_t)E};
+    const uint64_t st[3] = {(uint64_t)cols * 2, 128, (uint64_t)cols * 2 * rows};
+    const uint32_t b[4] = {64, mn ? (uint32_t)BK : (uint32_t)share, mn ? (uint32_t)share : 2u, 1};
+    return make_map_nd(m, ptr, 4, dims, st, b);
 }
 
 int max_pairs();
 int cta_group() { return max_pairs() > 0 ? 2 : 1; }
-// 64-wide blocks per load of an MN-major operand whose CTA share is `cols` wide
-int mn_blocks(int cols) { return std::min(MN_BLOCKS_PER_LOAD, std::max(1, cols / 64)); }
 
 int pick_bn(int n) { return n % 256 == 0 ? 256 : 128; }
 
@@ -1011,8 +981,7 @@ int rows_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, i
     q.bn = pick_bn(N);
     q.n_blocks = N / q.bn;
     q.ldo = N;
-    int blk = 0;   // K-major: unused
-    return act_map(&q.tmA0, A, a_rows, K, false, blk);
+    return act_map(&q.tmA0, A, a_rows, K, false, 0);
 }
 
 // Weight-gradient problem: out_e[M, N] = A_e^T B_e over the segment's rows (both MN-major)
@@ -1029,10 +998,8 @@ int wgrad_problem(TcProblem& q, const Family& F, const void* A, int64_t a_rows, 
     q.out0 = static_cast<__nv_bfloat16*>(out);
     q.ldo = N;
     q.out_estride = (long long)M * N;
-    q.a_blk = mn_blocks(BM);
-    q.b_blk = mn_blocks(q.bn / cta_group());
-    MOE_TRY(act_map(&q.tmA0, A, a_rows, M, true, q.a_blk));
-    MOE_TRY(act_map(&q.tmB0, B, b_rows, N, true, q.b_blk));
+    MOE_TRY(act_map(&q.tmA0, A, a_rows, M, true, BM / 64));
+    MOE_TRY(act_map(&q.tmB0, B, b_rows, N, true, q.bn / cta_group() / 64));
     // out [E][M][N]: boxes of 32 columns x 32 rows of one expert
     return encode_bf16_map(&q.tmO[0], out, (uint64_t)N, (uint64_t)M, (uint64_t)F.E, (uint64_t)N * 2,
                            (uint64_t)N * 2 * M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -1048,24 +1015,15 @@ int gemm1_problem(TcProblem& q, const moe_config& c, const Family& F, void* h, v
         q.dual = 1;
         q.bn = 128;
         q.n_blocks = f / 128;
-        // a CTA's share: 128 columns of the gate or the up tile; both maps take the
-        // same form (if either view is declined, both use the plain boxes)
-        int b0 = mn_blocks(128), b1 = b0;
-        MOE_TRY(weight_map(&q.tmB0, F.Wg, F.E, d, f, true, b0));
-        MOE_TRY(weight_map(&q.tmB1, F.Wu, F.E, d, f, true, b1));
-        if (b0 != b1) {
-            b0 = b1 = 1;
-            MOE_TRY(weight_map(&q.tmB0, F.Wg, F.E, d, f, true, b0));
-            MOE_TRY(weight_map(&q.tmB1, F.Wu, F.E, d, f, true, b1));
-        }
-        q.b_blk = b0;
+        // a CTA's load: two 64-column blocks of the gate or of the up tile
+        MOE_TRY(weight_map(&q.tmB0, F.Wg, F.E, d, f, true, 2));
+        MOE_TRY(weight_map(&q.tmB1, F.Wu, F.E, d, f, true, 2));
         q.epi = EPI_SWIGLU_FWD;
         q.out0 = static_cast<bf*>(h);
         q.out1 = static_cast<bf*>(h) + F.rows * f;
         q.out2 = static_cast<bf*>(act);
     } else {
-        q.b_blk = mn_blocks(q.bn / cta_group());
-        MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, d, f, true, q.b_blk));
+        MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, d, f, true, q.bn / cta_group() / 64));
         q.epi = EPI_SILU_FWD;
         q.out0 = static_cast<bf*>(h);
         q.out1 = static_cast<bf*>(act);
@@ -1077,8 +1035,7 @@ int gemm1_problem(TcProblem& q, const moe_config& c, const Family& F, void* h, v
 int gemm2_problem(TcProblem& q, const moe_config& c, const Family& F, const void* act, void* y) {
     MOE_TRY(rows_problem(q, F, act, F.rows, F.f, c.d));
     q.b_mn = 1;
-    q.b_blk = mn_blocks(q.bn / cta_group());
-    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, F.f, c.d, true, q.b_blk));
+    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, F.f, c.d, true, q.bn / cta_group() / 64));
     q.epi = EPI_STORE;
     q.out0 = static_cast<__nv_bfloat16*>(y);
     return out_maps_rows(q, F.rows);
@@ -1090,8 +1047,7 @@ int dgrad2_problem(TcProblem& q, const moe_config& c, const Family& F, const voi
     using bf = __nv_bfloat16;
     const int f = F.f;
     MOE_TRY(rows_problem(q, F, dy, dy_rows, c.d, f));
-    q.b_box_rows = q.bn / cta_group() >= 128 ? 128 : 64;
-    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, f, c.d, false, q.b_box_rows));
+    MOE_TRY(weight_map(&q.tmB0, F.Wd, F.E, f, c.d, false, q.bn / cta_group()));
     q.in0 = static_cast<const bf*>(h);
     q.out0 = static_cast<bf*>(dh);
     if (c.ffn == MOE_FFN_SWIGLU) {
@@ -1111,13 +1067,11 @@ int dgrad1_problem(TcProblem& q, const moe_config& c, const Family& F, const voi
     const bf* dh0 = static_cast<const bf*>(dh);
     const bf* dh1 = sw ? dh0 + F.rows * F.f : nullptr;
     MOE_TRY(rows_problem(q, F, sw ? dh1 : dh0, F.rows, F.f, c.d));
-    q.b_box_rows = q.bn / cta_group() >= 128 ? 128 : 64;
-    MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, c.d, F.f, false, q.b_box_rows));
+    MOE_TRY(weight_map(&q.tmB0, F.Wu, F.E, c.d, F.f, false, q.bn / cta_group()));
     if (sw) {
         q.kconcat = 2;
-        int blk = 0;   // K-major: unused
-        MOE_TRY(act_map(&q.tmA1, dh0, F.rows, F.f, false, blk));
-        MOE_TRY(weight_map(&q.tmB1, F.Wg, F.E, c.d, F.f, false, q.b_box_rows));
+        MOE_TRY(act_map(&q.tmA1, dh0, F.rows, F.f, false, 0));
+        MOE_TRY(weight_map(&q.tmB1, F.Wg, F.E, c.d, F.f, false, q.bn / cta_group()));
     }
     q.epi = EPI_STORE;
     q.out0 = static_cast<bf*>(dx);
