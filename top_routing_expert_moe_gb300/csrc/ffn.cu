@@ -289,9 +289,7 @@ int shared_backward_f32(const moe_config& c, const moe_shared_ffn& s, cudaStream
 
 }  // namespace
 
-size_t ffn_ws_bytes(const moe_config& c) {
-    return c.dtype == MOE_DTYPE_BF16 ? tc_ws_bytes(c) : 0;
-}
+size_t ffn_ws_bytes(const moe_config&) { return 0; }   // the expert FFN needs no scratch
 
 int launch_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                        const void* W_up, const void* W_gate, const void* W_down, void* h_saved,
@@ -300,7 +298,7 @@ int launch_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* o
 {
     if (c.dtype == MOE_DTYPE_BF16)
         return tc_ffn_forward(c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, y_perm,
-                              shared, ws, st);
+                              shared, st);
     int r = ffn_forward_f32(c, static_cast<const float*>(x_perm), offsets,
                             static_cast<const float*>(W_up), static_cast<const float*>(W_gate),
                             static_cast<const float*>(W_down), static_cast<float*>(h_saved),
@@ -317,7 +315,7 @@ int launch_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* 
 {
     if (c.dtype == MOE_DTYPE_BF16)
         return tc_ffn_backward(c, x_perm, offsets, W_up, W_gate, W_down, h_saved, act, dy_perm,
-                               dh, dx_perm, dW_up, dW_gate, dW_down, shared, ws, st);
+                               dh, dx_perm, dW_up, dW_gate, dW_down, shared, st);
     int r = ffn_backward_f32(c, static_cast<const float*>(x_perm), offsets,
                             static_cast<const float*>(W_up), static_cast<const float*>(W_gate),
                             static_cast<const float*>(W_down), static_cast<const float*>(h_saved),

@@ -65,21 +65,13 @@ static_assert(SMEM_BYTES <= 232448, "227 KB of dynamic shared memory per block")
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
-constexpr int RASTER_GM = 16;
+constexpr int RASTER_GM = 32;
 // Every operand share of a stage arrives with one TMA load: the TMA unit's cost
 // follows its instructions more than its bytes (on the Mixtral step, one load per
 // share instead of two took the grouped GEMMs about 8 % faster; adding L2
 // prefetch instructions beside the loads made them 40 % slower).  So a stage is
 // 128 deep in k -- a share is a {64, 128, 2} box of a block view of the tensor.
-// Progress sync of the units (CTA pairs) of a long launch: a unit's TMA producer
-// counts the k-steps it has issued in chunks of SYNC_CHUNK and does not start
-// chunk g before every unit has issued chunk g - SYNC_SLACK (or has no tiles
-// left).  Units then stay within a few chunks of each other, so tiles that
-// share an operand's k-slices ask for them while L2 still holds them.
-constexpr bool GEMM_SYNC = false;
-constexpr uint32_t SYNC_CHUNK = 16, SYNC_SLACK = 1;
-constexpr int SYNC_MAX_CHUNKS = 65536;
-constexpr int SPLIT_MIN_WAVES = 16;   // "many waves of tiles": a launch this long is split / synced
+constexpr int SPLIT_MIN_WAVES = 16;   // "many waves of tiles": a launch this long is split by tile length
 
 enum Epi { EPI_STORE = 0, EPI_SILU_FWD = 1, EPI_SWIGLU_FWD = 2, EPI_SILU_BWD = 3, EPI_SWIGLU_BWD = 4 };
 enum Sched { SCHED_ROWS = 0, SCHED_KSEG = 1 };
@@ -102,7 +94,7 @@ struct TcProblem {
     int sched;
     int n_blocks;           // N / bn
     int m_blocks;           // SCHED_KSEG: M / 128
-    int k_blocks;           // SCHED_ROWS: K / 64 (per operand pair)
+    int k_blocks;           // SCHED_ROWS: K / BK (per operand pair)
     int kconcat;            // SCHED_ROWS: 2 = K loop continues over (A1, B1)
     int a_mn, b_mn;         // operand is MN-major in global memory
     int bn;                 // 128 or 256
@@ -118,10 +110,6 @@ struct TcParams {
     const int32_t* offsets;
     int* status;
     int nprob, E;
-    // progress counters that keep the CTA pairs of a long launch together (zeroed
-    // before the launch; NULL: off): [0] units done, [1 .. 1 + sync_n) chunk arrivals
-    uint32_t* sync;
-    int sync_n;
 };
 static_assert(sizeof(TcParams) <= 32764, "kernel parameters within the 32 KB launch limit");
 
@@ -173,31 +161,6 @@ __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f 
 __device__ __forceinline__ float dsilu_fast(float z) {
     const float s = __fdividef(1.0f, 1.0f + __expf(-z));
     return s * (1.0f + z * (1.0f - s));
-}
-
-// Bounded wait until arrive + done >= need (both counters only grow).
-__device__ __forceinline__ bool sync_wait(const uint32_t* arrive, const uint32_t* done, uint32_t need,
-                                          volatile int* abort_flag, int* status) {
-    const volatile uint32_t* a = arrive;
-    const volatile uint32_t* d = done;
-    if (*a + *d >= need) return true;
-    const unsigned long long t0 = gtimer();
-    for (uint32_t it = 1;; ++it) {
-        __nanosleep(64);
-        if (*a + *d >= need) return true;
-        if ((it & 15) == 0) {
-            if (*abort_flag) return false;
-            if (timeout_pending(status)) {
-                *abort_flag = 1;
-                return false;
-            }
-            if (gtimer() - t0 > WAIT_NS) {
-                set_status(status, MOE_ERR_TIMEOUT);
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
 }
 
 // ---------------------------------------------------------------- schedule
@@ -400,11 +363,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
         }
         int it = 0;
         bool ok = start_live;
-        // progress sync: the unit's k-steps issued so far (one CTA of each unit counts)
-        const bool sync_on = GEMM_SYNC && P.sync != nullptr && (CG == 1 || leader);
-        uint32_t* const sync_done = P.sync;
-        uint32_t* const sync_arrive = P.sync + 1;
-        uint32_t ks = 0;
         for (int tix = unit; ok && tix < total; tix += nunits) {
             Tile t;
             decode_tile<CG>(P, offs, prefix, sbase, tix, t);
@@ -427,15 +385,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
             const uint32_t b_bytes = (uint32_t)bcols * BK * 2u;
             const uint32_t stage_tx = CG * ((uint32_t)A_BYTES + b_bytes);   // both CTAs' bytes
             for (int kb = 0; kb < t.nk; ++kb, ++it) {
-                if (sync_on && ks % SYNC_CHUNK == 0) {   // chunk g = ks / SYNC_CHUNK starts here
-                    const uint32_t g = ks / SYNC_CHUNK;
-                    if (g >= SYNC_SLACK && g - SYNC_SLACK < (uint32_t)P.sync_n &&
-                        !sync_wait(sync_arrive + (g - SYNC_SLACK), sync_done, (uint32_t)nunits,
-                                   abort_flag, P.status)) {
-                        ok = false;
-                        break;
-                    }
-                }
                 const int s = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, P.status)) { ok = false; break; }
@@ -476,12 +425,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                         ld4(phase ? tB1 : tB0, sB, 0, bn0, k0 / 64, t.e);
                     }
                 }
-                ++ks;
-                if (sync_on && ks % SYNC_CHUNK == 0 && ks / SYNC_CHUNK - 1 < (uint32_t)P.sync_n)
-                    atomicAdd(sync_arrive + (ks / SYNC_CHUNK - 1), 1u);   // chunk done
             }
         }
-        if (sync_on) atomicAdd(sync_done, 1u);   // no further chunks from this unit
         // drain: every load issued has landed before the CTA may exit (for a
         // pair, the even CTA's "full" barriers count both CTAs' loads)
         if (CG == 1 || leader)
@@ -818,25 +763,8 @@ int max_pairs() {
     return cached[dev];
 }
 
-// Chunk counters a launch's progress sync needs: every unit's k-steps, in chunks,
-// bounded by its tile count times the longest tile (NOT the launch's real work,
-// which only the device knows); 0 when that exceeds SYNC_MAX_CHUNKS.
-int64_t sync_chunks(const moe_config& c, const TcProblem* probs, int nprob, int cg, int units) {
-    int64_t tiles = 0, nk_max = 1;
-    for (int i = 0; i < nprob; ++i) {
-        const TcProblem& q = probs[i];
-        tiles += max_tiles(c, q, cg);
-        const int64_t nk = q.sched == SCHED_ROWS ? (int64_t)q.k_blocks * q.kconcat
-                                                 : (q.fixed_rows ? q.fixed_rows : (int64_t)c.T) / BK + 1;
-        nk_max = std::max(nk_max, nk);
-    }
-    const int64_t per_unit = (tiles + units - 1) / units;
-    const int64_t n = per_unit * ((nk_max + SYNC_CHUNK - 1) / SYNC_CHUNK) + 2;
-    return n <= SYNC_MAX_CHUNKS ? n : 0;
-}
-
 int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* probs, int nprob,
-              cudaStream_t st, void* sync_ws = nullptr) {
+              cudaStream_t st) {
     static bool attr_done[64] = {};
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
@@ -858,15 +786,6 @@ int launch_tc(const moe_config& c, const int32_t* offsets, const TcProblem* prob
         int64_t tiles = 0;
         for (int i = 0; i < nprob; ++i) tiles += max_tiles(c, probs[i], 2);
         const int units = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, pairs));
-        // long launches (many waves of tiles) keep their units together
-        if (GEMM_SYNC && sync_ws && tiles >= (int64_t)SPLIT_MIN_WAVES * units) {
-            const int64_t n = sync_chunks(c, probs, nprob, 2, units);
-            if (n > 0) {
-                P.sync = static_cast<uint32_t*>(sync_ws);
-                P.sync_n = (int)n;
-                MOE_CUDA_TRY(cudaMemsetAsync(sync_ws, 0, (size_t)(n + 1) * 4, st));
-            }
-        }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * units);
         cfg.blockDim = dim3(NTHREADS);
@@ -916,13 +835,13 @@ int64_t est_ksteps(const moe_config& c, const TcProblem& q) {
 // of tile length (k-steps within a factor of about 1.4), problems in their
 // given order; small launches stay whole (a launch's tail costs more there).
 int launch_tc_classes(const moe_config& c, const int32_t* offsets, const TcProblem* probs,
-                      int nprob, cudaStream_t st, void* sync_ws) {
+                      int nprob, cudaStream_t st) {
     const int cg = max_pairs() > 0 ? 2 : 1;
     const int units = std::max(1, cg == 2 ? max_pairs() : num_sms());
     int64_t tiles = 0;
     for (int i = 0; i < nprob; ++i) tiles += max_tiles(c, probs[i], cg);
     if (nprob < 2 || tiles < (int64_t)SPLIT_MIN_WAVES * units)
-        return launch_tc(c, offsets, probs, nprob, st, sync_ws);
+        return launch_tc(c, offsets, probs, nprob, st);
     int cls[MAX_PROBLEMS];
     bool done[MAX_PROBLEMS] = {};
     for (int i = 0; i < nprob; ++i) cls[i] = (int)std::lround(std::log2((double)est_ksteps(c, probs[i])));
@@ -935,7 +854,7 @@ int launch_tc_classes(const moe_config& c, const int32_t* offsets, const TcProbl
                 g[n++] = probs[j];
                 done[j] = true;
             }
-        const int r = launch_tc(c, offsets, g, n, st, sync_ws);
+        const int r = launch_tc(c, offsets, g, n, st);
         if (r != MOE_OK) return r;
     }
     return MOE_OK;
@@ -1097,11 +1016,9 @@ Family shared_family(const moe_config& c, const moe_shared_ffn& s) {
 
 }  // namespace
 
-size_t tc_ws_bytes(const moe_config&) { return GEMM_SYNC ? (size_t)(SYNC_MAX_CHUNKS + 1) * 4 : 0; }
-
 int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                    const void* W_up, const void* W_gate, const void* W_down, void* h_saved,
-                   void* act, void* y_perm, const moe_shared_ffn* sh, void* ws, cudaStream_t st)
+                   void* act, void* y_perm, const moe_shared_ffn* sh, cudaStream_t st)
 {
     const Family R = routed_family(c, x_perm, W_up, W_gate, W_down);
     TcProblem q[2];
@@ -1112,7 +1029,7 @@ int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offse
         q[1] = new_problem();
         MOE_TRY(gemm1_problem(q[1], c, shared_family(c, *sh), sh->h, sh->act));
     }
-    MOE_TRY(launch_tc(c, offsets, q, sh ? 2 : 1, st, ws));
+    MOE_TRY(launch_tc(c, offsets, q, sh ? 2 : 1, st));
     // GEMM2
     q[0] = new_problem();
     MOE_TRY(gemm2_problem(q[0], c, R, act, y_perm));
@@ -1120,14 +1037,14 @@ int tc_ffn_forward(const moe_config& c, const void* x_perm, const int32_t* offse
         q[1] = new_problem();
         MOE_TRY(gemm2_problem(q[1], c, shared_family(c, *sh), sh->act, sh->y));
     }
-    return launch_tc(c, offsets, q, sh ? 2 : 1, st, ws);
+    return launch_tc(c, offsets, q, sh ? 2 : 1, st);
 }
 
 int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offsets,
                     const void* W_up, const void* W_gate, const void* W_down,
                     const void* h_saved, const void* act, const void* dy_perm, void* dh,
                     void* dx_perm, void* dW_up, void* dW_gate, void* dW_down,
-                    const moe_shared_ffn* sh, void* ws, cudaStream_t st)
+                    const moe_shared_ffn* sh, cudaStream_t st)
 {
     using bf = __nv_bfloat16;
     const bool sw = c.ffn == MOE_FFN_SWIGLU;
@@ -1147,7 +1064,7 @@ int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offs
         q[n] = new_problem();
         MOE_TRY(wgrads_down(q[n++], c, S, sh->act, sh->dout, c.T, sh->dW_down));
     }
-    MOE_TRY(launch_tc_classes(c, offsets, q, n, st, ws));
+    MOE_TRY(launch_tc_classes(c, offsets, q, n, st));
     // launch 2: dW_up = x^T dh (du)  ||  [dW_gate = x^T dg]  ||  dx = dh W_up^T (+ dg W_gate^T)
     n = 0;
     auto second = [&](const Family& F, const void* dhF, void* dWu, void* dWg, void* dx) -> int {
@@ -1164,7 +1081,7 @@ int tc_ffn_backward(const moe_config& c, const void* x_perm, const int32_t* offs
     };
     MOE_TRY(second(R, dh, dW_up, dW_gate, dx_perm));
     if (sh) MOE_TRY(second(shared_family(c, *sh), sh->dh, sh->dW_up, sh->dW_gate, sh->dx));
-    return launch_tc_classes(c, offsets, q, n, st, ws);
+    return launch_tc_classes(c, offsets, q, n, st);
 }
 
 }  // namespace moe
