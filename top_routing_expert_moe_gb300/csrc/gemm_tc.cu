@@ -549,8 +549,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_grouped_gemm_kernel(const __gr
                 }
             };
             if (valid && n_in) fetch(c_lo);
-            const bool got = CG == 1 ? mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, P.status)
-                                     : mbar_wait_cl(smem_u32(&tfull[acc]), aph, abort_flag, P.status);
+            // every lane takes the same decision (the box stores below sync the warp)
+            const bool got = __all_sync(0xffffffffu,
+                                        CG == 1 ? mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, P.status)
+                                                : mbar_wait_cl(smem_u32(&tfull[acc]), aph, abort_flag, P.status));
             if (!got) break;
             tc_fence_after();
             // box coordinates of this warp's 32 rows: (column, row or M index, expert)
