@@ -128,13 +128,14 @@ def gemm_profile_path(workload: str) -> str:
 
 
 def gemm_traffic_from_profile(workload: str):
-    """DRAM bytes per grouped-GEMM launch of this workload from its committed ncu
-    summary; None when there is none or the kernel source changed since."""
+    """DRAM bytes of all grouped-GEMM launches of one step of this workload (the unit
+    of `achieved`) from its committed ncu summary; None when there is none or the
+    kernel source changed since."""
     path = gemm_profile_path(workload)
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m = re.search(r"traffic_bytes_per_step:\s*([0-9.eE+]+)", txt)
     h = re.search(r"gemm_source_sha256:\s*([0-9a-f]{64})", txt)
     wl = re.search(r"workload:\s*(\S+)", txt)
     if not m or not h or not wl or wl.group(1) != workload:
@@ -691,6 +692,8 @@ def run_ours(args, w):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "traffic": traffic,
+                         "traffic_scope": "ncu dram__bytes_read.sum + dram__bytes_write.sum over "
+                                          "the grouped-GEMM launches of one step (one-pass capture)",
                          "kernel": "tc_grouped_gemm_kernel (all grouped-GEMM launches of a step)",
                          "timing": "external CUDA events around the two grouped-GEMM calls inside "
                                    "the replayed step graph (the timed steps themselves)",
