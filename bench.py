@@ -14,9 +14,9 @@ calls, so the grouped-GEMM time of the roofline is measured inside the very
 replays whose duration gives ms_per_step (it cannot exceed the step).  Inputs
 and weights are resident in HBM before the timed region; L2 is flushed before
 every timed step, outside its event pair (a 512 MB write, then a 1 GB read that
-also pushes the written lines back to DRAM before the step starts).  Per-stage times of the
-other calls come from each C-ABI call captured as its own graph and replayed
-between events (reported beside the line, not used for the roofline).
+also pushes the written lines back to DRAM before the step starts).  Per-stage times
+come from a second capture of the step with an event between every two C-ABI calls,
+replayed after the same flush (reported beside the line, not used for the roofline).
 Under torchrun each rank runs an independent replica on its own GPU (the
 layer has no exchange step on one GPU); rank 0 prints one JSON line with the
 whole-job tokens/s (max step time over ranks).
@@ -585,44 +585,23 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         fwd_ms = float(np.mean([a.elapsed_time(c) for a, c in fwd_evs]))
 
-        # per-stage breakdown: each C-ABI call captured as its own CUDA graph and
-        # replayed between events (device time, no host launch overhead)
-        stage_fns = [
-            lambda: moe.moe_route(cfg, x, Wr, b, nz, mk, L.logits, L.topk_idx, L.gate, L.counts,
-                                  L.stats, L.ws, st),
-            lambda: moe.moe_permute(cfg, x, L.topk_idx, L.x_perm, L.perm_token, L.slot_of, L.kept,
-                                    L.offsets, L.stats, L.ws, st),
-            lambda: moe.moe_grouped_ffn(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved, L.act,
-                                        L.y_perm, L.ws, st, shared=sh_f),
-            lambda: moe.moe_combine(cfg, L.y_perm, L.slot_of, L.gate, L.out, st, shared=sh_f),
-            lambda: moe.moe_combine_backward(cfg, dout, L.y_perm, L.gate, L.slot_of, L.perm_token,
-                                             L.offsets, bw["dy"], bw["dgate"], st),
-            lambda: moe.moe_grouped_ffn_backward(cfg, L.x_perm, L.offsets, Wu, Wg, Wd, L.h_saved,
-                                                 L.act, bw["dy"], bw["dh"], bw["dxp"], g["dW_up"],
-                                                 g["dW_gate"], g["dW_down"], L.ws, st, shared=sh_b),
-            lambda: moe.moe_router_backward(cfg, x, Wr, L.logits, L.topk_idx, L.gate, L.slot_of,
-                                            bw["dgate"], bw["dxp"], L.stats, g["dx"], g["dW_r"],
-                                            g["dbias"] if b is not None else None, bw["dlogits"],
-                                            L.ws, st, shared=sh_b),
-        ]
-        stage_graphs = []
-        for fn in stage_fns:
-            sg = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(sg, stream=st):
-                fn()
-            stage_graphs.append(sg)
+        # per-stage breakdown inside the step: a second capture of the same step with an
+        # event at every boundary between C-ABI calls, so each call is timed where it runs
+        # (inputs as the step leaves them, launch overlap inside a call kept, no graph
+        # start); the events keep consecutive calls from overlapping, so the stages sum
+        # to a little more than ms_per_step
+        sev = [StepEvent() for _ in range(8)]
+        sgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sgraph, stream=st):
+            step(evs=sev)
         torch.cuda.synchronize(dev)
         n_stage = max(3, min(args.steps, 10))
-        per = np.zeros((n_stage, len(stage_graphs)))
+        per = np.zeros((n_stage, 7))
         for i in range(n_stage):
-            evs = [(ev(), ev()) for _ in stage_graphs]
             flush_l2()
-            for j, sg in enumerate(stage_graphs):   # in step order, so inputs are fresh
-                evs[j][0].record(st)
-                sg.replay()
-                evs[j][1].record(st)
-            torch.cuda.synchronize(dev)
-            per[i] = [a.elapsed_time(c) for a, c in evs]
+            sgraph.replay()
+            st.synchronize()
+            per[i] = [sev[j].elapsed_ms(sev[j + 1]) for j in range(7)]
         stage_ms = per.mean(0)
         eager_evs = [[ev() for _ in range(8)] for _ in range(n_stage)]
         for i in range(n_stage):
@@ -708,6 +687,8 @@ def run_ours(args, w):
             "launches_per_step": int(launches_per_step),
             "eager_ms_per_step": eager_ms,
             "fwd_tokens_per_s": job_rate(w.T, world, fwd_ms),
+            "stages_timing": "events between the C-ABI calls inside one replayed step graph "
+                             "(L2 flushed before the step)",
             "stages_ms": {n: float(v_) for n, v_ in zip(
                 ["route", "permute", "grouped_ffn", "combine", "combine_bwd", "grouped_ffn_bwd",
                  "router_bwd"], stage_ms)},

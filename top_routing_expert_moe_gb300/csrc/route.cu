@@ -418,10 +418,6 @@ struct RouteTma {
     float aux_coef;
 };
 
-__device__ __forceinline__ uint32_t swz128(int row, int col) {   // byte offset in a 128B-swizzled box
-    return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2);
-}
-
 constexpr int RTMA_THREADS = 13 * 32;   // 8 MMA warps, 1 producer warp, 4 finish warps
 
 template <int NT, int TT>  // NT = E_pad / 8 tensor-core n-tiles; TT tokens per tile
@@ -551,7 +547,15 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
     // ---------------------------------------------------- MMA warps 0-7
     const int g = lane >> 2, tq = lane & 3;
     const int my_ks = (warp * 16) / TT;
-    const int tok0 = (warp * 16) % TT + g;              // this lane's first token row in a block
+    // ldmatrix row addresses (each 8 x 8 bf16 matrix = 8 rows of 16 bytes of a
+    // 128B-swizzled box: chunk c of row r sits at chunk c ^ (r & 7)).
+    // A (x4): lanes 0-15 rows 0-15 of the warp's 16 tokens at k 0-7, lanes 16-31 the
+    // same rows at k 8-15 -> the m16n8k16 A fragment {a0, a1, a2, a3}.
+    const int a_row = (warp * 16) % TT + (lane & 15), a_kh = lane >> 4;
+    // B (x4 over n-tiles n, n + 1; x2 for a last odd one): lanes 0-7 / 8-15 rows
+    // (experts) of tile n at k 0-7 / 8-15, lanes 16-31 the same for tile n + 1.
+    const int b_row = (lane & 7) + ((lane >> 4) << 3), b_kh = (lane >> 3) & 1;
+    const uint32_t ring_sa = smem_u32(ring);
     bool live = start_live;
     int it = 0;
     for (int i = 0; i < my_tiles; ++i) {
@@ -565,24 +569,34 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
             if (!live) continue;
             for (int bb = 0; bb < NB; ++bb) {
                 const int j = my_ks * NB + bb;                 // this warp's block of the stage
-                const uint8_t* X = ring + (size_t)s * STAGE + (size_t)j * TT * 128;
-                const uint8_t* W = ring + (size_t)s * STAGE + X_BYTES + (size_t)j * E_PAD * 128;
+                const uint32_t Xs = ring_sa + (uint32_t)s * STAGE + (uint32_t)j * TT * 128;
+                const uint32_t Ws = ring_sa + (uint32_t)s * STAGE + X_BYTES + (uint32_t)j * E_PAD * 128;
 #pragma unroll
                 for (int k16 = 0; k16 < RT_BK / 16; ++k16) {
-                    const int kk = k16 * 16 + 2 * tq;
-                    const uint32_t a0 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0, kk));
-                    const uint32_t a1 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0 + 8, kk));
-                    const uint32_t a2 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0, kk + 8));
-                    const uint32_t a3 = *reinterpret_cast<const uint32_t*>(X + swz128(tok0 + 8, kk + 8));
+                    uint32_t a0, a1, a2, a3;
+                    const uint32_t xa = Xs + (uint32_t)(a_row * 128 + (((k16 * 2 + a_kh) ^ (a_row & 7)) << 4));
+                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(xa));
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk));
-                        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(W + swz128(n * 8 + g, kk + 8));
-                        asm volatile(
-                            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-                            : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
-                            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                    for (int n = 0; n < NT; n += 2) {
+                        const int row = n * 8 + b_row;
+                        const uint32_t wa = Ws + (uint32_t)(row * 128 + (((k16 * 2 + b_kh) ^ (row & 7)) << 4));
+                        uint32_t b[4];
+                        if (n + 1 < NT)
+                            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                                         : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(wa));
+                        else
+                            asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n"
+                                         : "=r"(b[0]), "=r"(b[1]) : "r"(wa));
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (n + h >= NT) break;
+                            asm volatile(
+                                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                                "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                                : "+f"(acc[n + h][0]), "+f"(acc[n + h][1]), "+f"(acc[n + h][2]), "+f"(acc[n + h][3])
+                                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b[2 * h]), "r"(b[2 * h + 1]));
+                        }
                     }
                 }
             }
