@@ -10,8 +10,9 @@
 //
 // Design (clusters of two CTAs -- a pair -- one CTA per SM, 320 threads each):
 //   warp 0      TMA producer of each CTA: its 128 rows of A and its half of B's
-//               columns, 128B-swizzled, into a ring of six 32 KB stages; the
-//               loads of both CTAs complete on the even CTA's "full" barrier.
+//               columns, 128B-swizzled, into a ring of three 64 KB stages 128
+//               deep in k, one TMA load per operand share; the loads of both
+//               CTAs complete on the even CTA's "full" barrier.
 //   warp 1      allocates 512 TMEM columns (both CTAs, collectively); the even
 //               CTA's thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
 //               K = 16, bf16 in, fp32 accumulate) and commits, multicast to both
@@ -22,11 +23,11 @@
 //               activation (or its derivative), 32 x 32 output boxes written by
 //               TMA stores; the accumulator is released to the even CTA so the
 //               next tile's MMAs overlap this epilogue.
-// A one-CTA variant (M = 128, four 48 KB stages) serves devices that cannot
+// A one-CTA variant (M = 128, two 96 KB stages) serves devices that cannot
 // hold pairs.  Tiles come from a static persistent schedule whose per-expert
 // tile counts are read from the device-side segment offsets, so no host sync
 // separates routing from the GEMMs; within an expert, tiles are visited in
-// groups of 16 row blocks so the A rows and B columns in flight stay
+// groups of RASTER_GM row blocks so the A rows and B columns in flight stay
 // L2-resident.  A launch may hold up to six independent problems (the
 // backward's dgrad || weight gradient pairs, the shared experts' FFN).
 //
@@ -66,11 +67,14 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;                   // two per TMEM lane quarter
 constexpr int NTHREADS = 64 + 32 * NUM_EPI_WARPS;  // producer warp, MMA warp, epilogue
 constexpr int RASTER_GM = 32;
-// Every operand share of a stage arrives with one TMA load: the TMA unit's cost
-// follows its instructions more than its bytes (on the Mixtral step, one load per
-// share instead of two took the grouped GEMMs about 8 % faster; adding L2
-// prefetch instructions beside the loads made them 40 % slower).  So a stage is
-// 128 deep in k -- a share is a {64, 128, 2} box of a block view of the tensor.
+// Every operand share of a stage arrives with one TMA load: each TMA instruction
+// the producer issues costs mainloop time, more than the bytes it moves (on the
+// Mixtral step one load per share instead of two took the grouped GEMMs about 8 %
+// faster, and 128-deep stages, half the loads again, about 7 % more; L2 prefetch
+// instructions beside the loads made them slower).  So a stage is 128 deep in k
+// -- a share is a {64, 128, 2} box of a block view of the tensor.  Raster groups
+// of 32 row blocks: one pass over an expert's weights per 4096 rows (GEMM1 at
+// K = d reads 30 % less DRAM than with 16) while a group's A rows fit in L2.
 constexpr int SPLIT_MIN_WAVES = 16;   // "many waves of tiles": a launch this long is split by tile length
 
 enum Epi { EPI_STORE = 0, EPI_SILU_FWD = 1, EPI_SWIGLU_FWD = 2, EPI_SILU_BWD = 3, EPI_SWIGLU_BWD = 4 };
