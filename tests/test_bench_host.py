@@ -98,3 +98,35 @@ def test_reference_arm_router_variants(opts, router, name):
     assert d["config"]["workload"] == name and d["value"] > 0
     for k, v in router.items():
         assert d["config"]["router"][k] == v, k
+
+
+def test_roofline_traffic_comes_from_the_matching_profile(tmp_path, monkeypatch):
+    """`roofline.traffic` is read from the committed per-workload ncu summary only when
+    it names the same workload and the grouped-GEMM sources still hash to its digest."""
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    dig = bench.gemm_source_digest()
+    p = tmp_path / "tc_grouped_gemm_mixtral_bf16.md"
+    p.write_text(f"workload: mixtral_bf16\ntraffic_bytes_per_step: 175535728896\n"
+                 f"gemm_source_sha256: {dig}\n")
+    assert bench.gemm_traffic_from_profile("mixtral_bf16") == 175535728896.0
+    # another workload's profile, a stale digest, or no profile: no traffic figure
+    assert bench.gemm_traffic_from_profile("llama4_bf16") is None
+    p.write_text("workload: mixtral_bf16\ntraffic_bytes_per_step: 1\ngemm_source_sha256: " + "0" * 64 + "\n")
+    assert bench.gemm_traffic_from_profile("mixtral_bf16") is None
+    p.write_text(f"workload: llama4_bf16\ntraffic_bytes_per_step: 1\ngemm_source_sha256: {dig}\n")
+    assert bench.gemm_traffic_from_profile("mixtral_bf16") is None
+
+
+def test_committed_gemm_profiles_name_their_workload():
+    """Every committed GEMM traffic summary is parseable and keyed by its own workload."""
+    import re
+    for name in os.listdir(bench.PROFILES):
+        m = re.fullmatch(r"tc_grouped_gemm_(\w+)\.md", name)
+        if not m:
+            continue
+        txt = open(os.path.join(bench.PROFILES, name)).read()
+        if "traffic_bytes_per_step:" not in txt:
+            continue
+        wl = re.search(r"workload:\s*(\S+)", txt).group(1)
+        assert bench.gemm_profile_path(wl).endswith(name)
+        assert re.search(r"gemm_source_sha256:\s*[0-9a-f]{64}", txt)
