@@ -72,11 +72,15 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 // given, added to the running sums of this CTA's tiles.
 constexpr int ACC_FLOATS = 64 + 64 + 4;   // psum[64], counts[64] (int), h, bad (int), real (int)
 
-template <int G>
+// EP > 0: E <= EP is known at compile time, so each lane's expert loops (at most
+// EP / G slots) unroll and their loads and exponentials overlap; EP = 0: runtime loops.
+template <int G, int EP>
 __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, int* sBad, int t0,
                                 int ntok, int TT, int pidx, const RouteOut& o, int i, int nthr,
                                 int bar_id, float* acc)
 {
+    constexpr int QMAX = EP > 0 ? (EP + G - 1) / G : 64;   // expert slots of one lane
+    constexpr int UNR = EP > 0 ? QMAX : 1;
     const int E = o.E, k = o.k;
     const int sub = i % G, per_pass = nthr / G;
     const unsigned mask = 0xffffffffu;
@@ -89,7 +93,10 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
         bool bad = false;
         float m = -INFINITY;
         uint64_t taken = 0;                                  // my experts already selected
-        for (int e = sub; e < E; e += G) {
+#pragma unroll UNR
+        for (int q = 0; q < QMAX; ++q) {
+            const int e = sub + q * G;
+            if (e >= E) break;
             float v = l[e];
             if (o.bias) v += o.bias[e];
             if (o.noise && valid && !o.st) v += o.noise[(size_t)t * E + e];  // gate noise
@@ -106,7 +113,10 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
         // z = sum exp((l - m) / tau); zl = sum exp((l - m) / tau) (l - m) / tau gives the
         // entropy without a logarithm per expert: -sum p log p = log z - zl / z
         float z = 0.f, zl = 0.f;
-        for (int e = sub; e < E; e += G) {
+#pragma unroll UNR
+        for (int q = 0; q < QMAX; ++q) {
+            const int e = sub + q * G;
+            if (e >= E) break;
             const float dl = (l[e] - m) * itau;
             const float ex = __expf(dl);
             z += ex;
@@ -126,7 +136,10 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
         for (int j = 0; j < k; ++j) {
             int be = -1;
             float bv = 0.f;
-            for (int e = sub, q = 0; e < E; e += G, ++q) {
+#pragma unroll UNR
+            for (int q = 0; q < QMAX; ++q) {
+                const int e = sub + q * G;
+                if (e >= E) break;
                 if ((taken >> q) & 1ull) continue;
                 const float key = (o.st && o.noise && valid) ? l[e] + o.noise[(size_t)t * E + e] : l[e];
                 if (be < 0 || ranks_above(key, e, bv, be)) { be = e; bv = key; }
@@ -165,8 +178,12 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
                 for (int j = 0; j < k; ++j) o.gate[(size_t)t * k + j] = __expf((lsel[j] - m) * itau) * inv;
             }
         }
-        for (int e = sub; e < E; e += G)   // the tile now holds probabilities (0 for padding tokens)
+#pragma unroll UNR
+        for (int q = 0; q < QMAX; ++q) {   // the tile now holds probabilities (0 for padding tokens)
+            const int e = sub + q * G;
+            if (e >= E) break;
             l[e] = routed ? __expf((l[e] - m) * itau) * inv : 0.f;
+        }
         const float h = (routed && !bad) ? __logf(z) - zl * inv : 0.f;   // non-finite rows: none
         if (sub == 0) {
             sEnt[tok] = routed ? h : 0.f;
@@ -232,15 +249,16 @@ __device__ void finish_tile_seg(float* sLog, int ldl, int* sSel, float* sEnt, in
 }
 
 // G lanes per token for TT tokens on nthr threads (G <= 32, a power of two)
+template <int EP>
 __device__ __forceinline__ void finish_tile(float* sLog, int ldl, int* sSel, float* sEnt, int* sBad,
                                             int t0, int ntok, int TT, int pidx, const RouteOut& o,
                                             int i, int nthr, int bar_id, float* acc = nullptr)
 {
     const int G = nthr / TT;
-    if (G >= 8) finish_tile_seg<8>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
-    else if (G >= 4) finish_tile_seg<4>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
-    else if (G >= 2) finish_tile_seg<2>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
-    else finish_tile_seg<1>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
+    if (G >= 8) finish_tile_seg<8, EP>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
+    else if (G >= 4) finish_tile_seg<4, EP>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
+    else if (G >= 2) finish_tile_seg<2, EP>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
+    else finish_tile_seg<1, EP>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, TT, pidx, o, i, nthr, bar_id, acc);
 }
 
 // Reduce the per-tile (or per-CTA) partials into counts and the statistics,
@@ -514,7 +532,7 @@ __global__ void __launch_bounds__(RTMA_THREADS, 1) route_bf16_kernel(const __gri
             const int b = i & 1;
             if (live) live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&lfull[b]), (uint32_t)(i >> 1) & 1u,
                                                             abort_flag, P.status));
-            if (live) finish_tile(sLogB + b * TT * LDL, LDL, sSel, sEnt, sBad, t0, ntok, TT, tile, o, ftid, 128, 2, sAcc);
+            if (live) finish_tile<E_PAD>(sLogB + b * TT * LDL, LDL, sSel, sEnt, sBad, t0, ntok, TT, tile, o, ftid, 128, 2, sAcc);
             else named_sync(2, 128);
             named_sync(2, 128);          // sSel / sEnt / sBad read by all before reuse
             mbar_arrive(smem_u32(&lempty[b]));
@@ -678,7 +696,7 @@ __global__ void __launch_bounds__(256) route_f32_kernel(const float* __restrict_
     for (int q = 0; q < 32; ++q)
         if (e_begin + q < e_end) sLog[tok * ldl + e_begin + q] = acc[q];
     __syncthreads();
-    finish_tile(sLog, ldl, sSel, sEnt, sBad, t0, ntok, RT_TOK, blockIdx.x, o, threadIdx.x, 256, 1);
+    finish_tile<0>(sLog, ldl, sSel, sEnt, sBad, t0, ntok, RT_TOK, blockIdx.x, o, threadIdx.x, 256, 1);
 }
 
 // Sum the per-CTA partials (a warp per expert, lane-strided, then a fixed
