@@ -155,9 +155,10 @@ __global__ void transpose_wr_f32_kernel(const T* __restrict__ Wr, float* __restr
     }
 }
 
-// One warp per token: dlogits (gate Jacobian + aux term); with WITH_DX also
-// dx[t] = sum_kept dx_perm[slot] + dlogits[t] . W_r^T (the fp32 path; the bf16
-// path forms dx in router_dx_dwr_kernel on the tensor cores).
+// The fp32 path's router backward, one warp per token: dlogits (gate Jacobian +
+// aux term); with WITH_DX also dx[t] = sum_kept dx_perm[slot] + dlogits[t] . W_r^T.
+// (The bf16 path forms dlogits in router_dlogits_kernel and dx in
+// router_dx_dwr_kernel on the tensor cores.)
 template <typename T, bool WITH_DX>
 __global__ void __launch_bounds__(256) router_bwd_token_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ topk,
@@ -262,6 +263,114 @@ __global__ void __launch_bounds__(256) router_bwd_token_kernel(
             store16_f<T>(dx + (size_t)t * d + v * V, acc);
         }
         __syncwarp();
+    }
+}
+
+// dlogits for the bf16 path (dX and dW_r follow on the tensor cores): G lanes per
+// token (G = the expert count rounded up to a power of two, at most 32; a lane holds
+// experts sub and sub + G), 32 / G tokens per warp.  Every load of a token (logits,
+// its k picks, gates, slots and dgates) is issued before any is used, and the
+// softmax, gate Jacobian and aux term reduce over the token's G lanes; the token
+// loop and every shuffle are uniform across the warp.
+template <int G>
+__global__ void __launch_bounds__(256) router_dlogits_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ topk,
+    const float* __restrict__ gate, const int32_t* __restrict__ slot_of,
+    const float* __restrict__ dgate, const float* __restrict__ stats, int Tn, int E, int k,
+    int normalize, int st, float inv_tau, float aux_coef, float* __restrict__ dlogits)
+{
+    pdl_wait();      // the preceding kernel's writes are visible from here on
+    pdl_trigger();
+    constexpr int TPW = 32 / G;
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31, sub = lane % G, gbase = lane - sub;
+    const int e0 = sub, e1 = sub + G;
+    // the aux term's per-expert coefficients (the statistics are final)
+    float c0 = 0.f, c1 = 0.f;
+    if (aux_coef != 0.f) {
+        const float invE = 1.0f / (float)E;
+        const float sc = aux_coef * 2.0f / fmaxf(stats[MOE_STAT_TOKENS], 1.0f);
+        if (e0 < E) c0 = sc * (stats[MOE_STAT_PBAR + e0] - invE);
+        if (e1 < E) c1 = sc * (stats[MOE_STAT_PBAR + e1] - invE);
+    }
+    const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+    for (int tw = gw * TPW; tw < Tn; tw += nw * TPW) {      // uniform per warp
+        const int t = tw + lane / G;
+        const bool valid = t < Tn;
+        const size_t tb = (size_t)(valid ? t : 0);
+        const float x0 = (valid && e0 < E) ? logits[tb * E + e0] : 0.f;
+        const float x1 = (valid && e1 < E) ? logits[tb * E + e1] : 0.f;
+        int tk[8], so[8];
+        float gt[8], dgr[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const bool in = valid && j < k;
+            tk[j] = in ? topk[tb * k + j] : -1;
+            so[j] = in ? slot_of[tb * k + j] : -1;
+            gt[j] = in ? gate[tb * k + j] : 0.f;
+            dgr[j] = in ? dgate[tb * k + j] : 0.f;
+        }
+        // p = softmax(l / tau); every derivative through it carries 1 / tau
+        const float l0 = e0 < E ? x0 * inv_tau : -INFINITY;
+        const float l1 = e1 < E ? x1 * inv_tau : -INFINITY;
+        float m = fmaxf(l0, l1);
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(full, m, off));
+        float p0 = e0 < E ? expf(l0 - m) : 0.f;
+        float p1 = e1 < E ? expf(l1 - m) : 0.f;
+        float z = p0 + p1;
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) z += __shfl_xor_sync(full, z, off);
+        p0 /= z;
+        p1 /= z;
+        const bool routed = valid && tk[0] >= 0;   // padding tokens: no gradient
+        float dl0 = 0.f, dl1 = 0.f;
+        if (normalize && !st) {
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float dg = so[j] >= 0 ? dgr[j] : 0.f;
+                s += gt[j] * dg;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                const float dg = so[j] >= 0 ? dgr[j] : 0.f;
+                const float v = gt[j] * (dg - s);
+                if (tk[j] == e0) dl0 += v;
+                if (tk[j] == e1) dl1 += v;
+            }
+        } else {
+            // raw probabilities, and the straight-through estimator (gates 1 forward,
+            // gradient through p of the selected experts); p of a pick comes from the
+            // lane that holds it (every lane shuffles, whatever its token)
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                const int e = tk[j] >= 0 ? tk[j] : 0;
+                const int src = gbase + (e % G);
+                const float pa = __shfl_sync(full, p0, src);
+                const float pb = __shfl_sync(full, p1, src);
+                const float dg = so[j] >= 0 ? dgr[j] : 0.f;
+                s += dg * (e < G ? pa : pb);
+                if (tk[j] == e0) dl0 += dg * p0;
+                if (tk[j] == e1) dl1 += dg * p1;
+            }
+            dl0 -= p0 * s;
+            dl1 -= p1 * s;
+        }
+        float s2 = p0 * c0 + p1 * c1;
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) s2 += __shfl_xor_sync(full, s2, off);
+        if (aux_coef != 0.f) {
+            dl0 += p0 * (c0 - s2);
+            dl1 += p1 * (c1 - s2);
+        }
+        if (!routed) dl0 = dl1 = 0.f;
+        if (valid && e0 < E) dlogits[tb * E + e0] = dl0 * inv_tau;
+        if (valid && e1 < E) dlogits[tb * E + e1] = dl1 * inv_tau;
     }
 }
 
@@ -855,9 +964,21 @@ int launch_router_backward(const moe_config& c, const void* x, const void* Wr,
     }
     if (c.dtype == MOE_DTYPE_BF16) {
         using T = __nv_bfloat16;
-        MOE_LAUNCH(router_bwd_token_kernel<T, false>, grid, 256, 0, st, logits, topk, gate, slot_of, dgate, stats, static_cast<const T*>(dx_perm), nullptr,
-            nullptr, c.T, c.d, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau,
-            c.aux_coef, dlogits, static_cast<T*>(dx));
+        {
+            const int g = c.E <= 2 ? 2 : c.E <= 4 ? 4 : c.E <= 8 ? 8 : c.E <= 16 ? 16 : 32;
+            const int tok_per_cta = 8 * (32 / g);
+            const int grid_dl = std::max(1, std::min((c.T + tok_per_cta - 1) / tok_per_cta, 8 * num_sms()));
+#define MOE_DL(GG)                                                                                   \
+    MOE_LAUNCH(router_dlogits_kernel<GG>, grid_dl, 256, 0, st, logits, topk, gate, slot_of, dgate,   \
+               stats, c.T, c.E, c.k, c.normalize_gates, c.straight_through, inv_tau, c.aux_coef, \
+               dlogits)
+            if (g == 2) MOE_DL(2);
+            else if (g == 4) MOE_DL(4);
+            else if (g == 8) MOE_DL(8);
+            else if (g == 16) MOE_DL(16);
+            else MOE_DL(32);
+#undef MOE_DL
+        }
         const T* Wr_ = static_cast<const T*>(Wr);
         const T* dxp_ = static_cast<const T*>(dx_perm);
         const T* dxs_ = static_cast<const T*>(dx_shared);
