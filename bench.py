@@ -338,6 +338,24 @@ def oracle_cores():
     return oracle.max_threads()
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as the kernel reports it (lscpu's source), or the
+    architecture when the name is not listed (some Arm kernels omit it)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
 def workload_config(w, v: dict | None = None):
     v = v or router_variant()
     return {"workload": w.name, "T": w.T, "d_model": w.d, "d_ff": w.f, "experts": w.E,
@@ -376,7 +394,7 @@ def run_reference(args, w):
             "data": "synthetic (seeded normals, random-init weights)",
             "config": workload_config(w, v),
             "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": oracle_cores(),
-                             "kind": "oracle", "sample": sample},
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
             "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -392,7 +410,8 @@ def cpu_baseline_leg(w, v, inp, seed, budget_s, one_core_budget_s):
     src = OracleInputs(w, v, seed, inp=inp)
     T_s = oracle_sample_tokens(src, budget_s)
     t_all = src.sample(T_s).run()
-    out = {"value": T_s / t_all, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    out = {"value": T_s / t_all, "unit": "tokens/s", "cores": cores, "cpu_model": cpu_model(),
+           "kind": "oracle",
            "sample": f"oracle fp64 fwd+bwd on the first {T_s} tokens of {w.name} "
                      f"(same d, f, E, k, weights), {t_all:.1f} s"}
     if one_core_budget_s > 0:
