@@ -254,11 +254,13 @@ def test_nonfinite_logits_are_flagged():
     assert moe.last_device_status() == 0   # reading clears it
 
 
-@pytest.mark.parametrize("E,k,dtype", [(2, 1, "bf16"), (8, 1, "bf16"), (16, 4, "bf16"),
-                                       (32, 2, "bf16"), (64, 2, "bf16"), (64, 8, "bf16"),
+@pytest.mark.parametrize("E,k,dtype", [(2, 1, "bf16"), (8, 1, "bf16"), (12, 3, "bf16"),
+                                       (16, 4, "bf16"), (32, 2, "bf16"), (48, 4, "bf16"),
+                                       (64, 2, "bf16"), (64, 8, "bf16"),
                                        (12, 3, "fp32"), (64, 5, "fp32")])
 def test_expert_count_and_top_k_sweep(E, k, dtype):
-    """Top-k / expert-count sweep (top-1 routing, wide k, up to 64 experts)."""
+    """Top-k / expert-count sweep (top-1 routing, wide k, up to 64 experts, expert counts
+    that are not powers of two: padded expert slots in the router and its backward)."""
     base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
     w = _w(base, T=640, E=E, k=k, d=256 if dtype == "bf16" else 64,
            f=256 if dtype == "bf16" else 96, capacity_factor=1.1)
