@@ -371,3 +371,48 @@ def test_shared_experts_composite_backward_matches_substeps():
         if k == "dbias":
             continue
         assert torch.equal(v, g[k]), k
+
+
+@pytest.mark.parametrize("T", [384, 8192])   # one tile and many
+def test_out_of_range_expert_index_is_reported(T):
+    """An expert index outside [0, E) in a caller's top-k (a bad input to moe_permute) is
+    caught by the permutation kernels' own bounds checks: the device status reads
+    MOE_ERR_DEVICE_BOUNDS and the entry is dropped exactly as a -1 (no selection) there
+    would be — the permutation is byte-identical to that run, which reports nothing."""
+    E, k, d = 8, 2, 256
+    cfg = moe.MoEConfig(T=T, d=d, f=256, E=E, k=k, capacity_factor=1.25, dtype=moe.BF16,
+                        pad_m=128)
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(T)
+    topk = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    bad_t, bad_j = T // 3, 1
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16).to(dev)
+    rows = moe.rows_capacity(cfg)
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=dev)
+
+    def run(fill):
+        tk = topk.clone()
+        tk[bad_t, bad_j] = fill
+        tk = tk.to(dev)
+        out = dict(x_perm=torch.empty(rows, d, dtype=torch.bfloat16, device=dev),
+                   perm_token=torch.empty(rows, dtype=torch.int32, device=dev),
+                   slot_of=torch.empty(T, k, dtype=torch.int32, device=dev),
+                   kept=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   stats=torch.zeros(9 + E, dtype=torch.float32, device=dev))
+        moe.last_device_status()              # start from a clear status word
+        moe.moe_permute(cfg, x, tk, out["x_perm"], out["perm_token"], out["slot_of"], out["kept"],
+                        out["offsets"], out["stats"], ws)
+        status = moe.last_device_status()     # reading clears it
+        n = int(out["offsets"][E].item())
+        out["x_perm"] = out["x_perm"][:n]
+        out["perm_token"] = out["perm_token"][:n]
+        return status, out
+
+    st_bad, bad = run(E + 5)
+    st_none, none = run(-1)
+    assert st_bad == moe.ERR_DEVICE_BOUNDS and st_none == 0
+    assert int(bad["slot_of"][bad_t, bad_j].item()) == -1
+    for key in ("slot_of", "kept", "offsets", "perm_token", "x_perm"):
+        assert torch.equal(bad[key], none[key]), key
+    assert torch.equal(bad["stats"][moe.STAT_DROPPED], none["stats"][moe.STAT_DROPPED])
