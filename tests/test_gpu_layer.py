@@ -269,6 +269,19 @@ def test_expert_count_and_top_k_sweep(E, k, dtype):
     _report(f"sweep E{E} k{k} {dtype}", rep)
 
 
+@pytest.mark.parametrize("T,dtype", [(1, "bf16"), (3, "bf16"), (17, "bf16"), (1, "fp32"),
+                                     (5, "fp32")])
+def test_decode_sized_batches(T, dtype):
+    """A handful of tokens (decode-sized batches): one partly filled router tile, most
+    experts empty, weight gradients reduced over one or two rows."""
+    base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
+    w = _w(base, T=T, d=256 if dtype == "bf16" else 64, f=256 if dtype == "bf16" else 96,
+           E=8, k=2, capacity_factor=0.0)
+    rep, r = parity.full_check(w, _edge_inputs(w, seed=40 + T), pad_m=128 if dtype == "bf16" else 8)
+    assert int(r["layer"].kept.sum().item()) == 2 * T
+    _report(f"decode batch T{T} {dtype}", rep)
+
+
 # ------------------------------------------------------------------ router variants
 @pytest.mark.parametrize("tau,normalize,dtype", [(0.5, True, "bf16"), (2.0, False, "bf16"),
                                                  (0.7, True, "fp32"), (3.0, False, "fp32")])
