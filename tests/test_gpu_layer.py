@@ -254,7 +254,8 @@ def test_nonfinite_logits_are_flagged():
     assert moe.last_device_status() == 0   # reading clears it
 
 
-@pytest.mark.parametrize("E,k,dtype", [(2, 1, "bf16"), (8, 1, "bf16"), (12, 3, "bf16"),
+@pytest.mark.parametrize("E,k,dtype", [(1, 1, "bf16"), (1, 1, "fp32"), (2, 1, "bf16"),
+                                       (8, 1, "bf16"), (12, 3, "bf16"),
                                        (16, 4, "bf16"), (32, 2, "bf16"), (48, 4, "bf16"),
                                        (64, 2, "bf16"), (64, 8, "bf16"),
                                        (12, 3, "fp32"), (64, 5, "fp32")])
