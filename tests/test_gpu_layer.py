@@ -283,6 +283,23 @@ def test_decode_sized_batches(T, dtype):
     _report(f"decode batch T{T} {dtype}", rep)
 
 
+@pytest.mark.parametrize("cf,dtype", [(0.001, "bf16"), (0.0625, "bf16"), (0.001, "fp32")])
+def test_extreme_capacity(cf, dtype):
+    """Capacity 1 (cf = 0.001) and 10 (cf = 0.0625) per expert at 640 tokens, 8 experts, top-2:
+    nearly every assignment dropped, most tokens lose both slots (zero output rows), and the
+    backward reduces over a handful of kept rows."""
+    base = "small_bf16" if dtype == "bf16" else "tiny_fp32"
+    w = _w(base, T=640, d=256 if dtype == "bf16" else 64, f=256 if dtype == "bf16" else 96,
+           E=8, k=2, capacity_factor=cf)
+    rep, r = parity.full_check(w, _edge_inputs(w, seed=77), pad_m=128 if dtype == "bf16" else 8)
+    C = moe.capacity(parity.gpu_cfg(w))
+    assert C == (1 if cf < 0.01 else 10)
+    kept = r["layer"].kept.cpu().numpy()
+    assert (kept <= C).all() and kept.sum() <= 8 * C
+    assert (r["layer"].slot_of.cpu().numpy() < 0).all(1).sum() > 0   # fully dropped tokens exist
+    _report(f"extreme capacity cf{cf} {dtype}", rep)
+
+
 # ------------------------------------------------------------------ router variants
 @pytest.mark.parametrize("tau,normalize,dtype", [(0.5, True, "bf16"), (2.0, False, "bf16"),
                                                  (0.7, True, "fp32"), (3.0, False, "fp32")])
