@@ -5,8 +5,10 @@
 // gradient must flow through those weights into the router (no detach).
 // [ZeRO3-MoE] §3.2: variance-form aux loss on the mean routing probability.
 //
-// All kernels are HBM-bound row streams: one warp per row, 16-byte vectors,
-// fp32 accumulation, fixed summation order (deterministic).
+// All kernels are HBM-bound with fp32 accumulation in a fixed order
+// (deterministic): the combine and its backward stream rows (one warp per row,
+// 16-byte vectors); the router backward forms dlogits with a few lanes per token,
+// then dX and the dW_r partials on mma.sync tiles, reduced in one more pass.
 #include <algorithm>
 
 #include "common.cuh"

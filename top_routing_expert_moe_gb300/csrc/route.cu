@@ -11,10 +11,12 @@
 // router weights) with TMA into a ring of 128-row stages (mbarrier transaction
 // counts); warps 0-7 split each stage's rows into (k-slice, 16 tokens) and run
 // the router contraction on the tensor cores (mma.sync m16n8k16, fp32
-// accumulate), so the E flops/byte never throttle the HBM stream; warps 9-12
-// take the finished logit tile (double-buffered, so the next tile's loads and
-// MMAs overlap) and finish it with G lanes per token: bias, noise, softmax of
-// logits / tau, top-k, gates, entropy.  Each CTA sums its tiles' statistics;
+// accumulate, fragments fetched from the swizzled boxes with ldmatrix), so the
+// E flops/byte never throttle the HBM stream even at a power-capped clock;
+// warps 9-12 take the finished logit tile (double-buffered, so the next tile's
+// loads and MMAs overlap) and finish it with G lanes per token: bias, noise,
+// softmax of logits / tau, top-k, gates, entropy (each lane's expert loops
+// unrolled to the padded expert count).  Each CTA sums its tiles' statistics;
 // the last CTA to finish (an atomic ticket) reduces all CTAs' sums in CTA
 // order (deterministic), so no separate reduction launch follows.
 // fp32: plain FMA over 128-token tiles (k-chunks staged in shared memory),
